@@ -1,0 +1,429 @@
+/*
+ * oracle.c - plain, slow fp64 CPU definitions of the graph-attention path.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the checker, not the product: only
+ * the test suite, the smoke check and the benchmark's CPU-baseline leg load
+ * it. It shares no code, header, table or constant with the CUDA library and
+ * includes nothing from it.
+ *
+ * Every function is the textbook definition of its operation written out as
+ * loops, in the order the source pages state it, in double precision on the
+ * inputs exactly as the GPU receives them (fp32 values, or bf16 bit patterns
+ * widened exactly). Softmax is two-pass (max, then sum, then divide), never
+ * online. Nothing is blocked, fused or reordered.
+ *
+ * Sources (POPCORNBENCH transcripts of a PyTorch reference model being
+ * replaced by a CUDA kernel):
+ *   [P1] FW-GLM-5-1 l1_p6  - multi-head row-wise softmax over CSR edge scores
+ *   [P2] Kimi-K2.6 l2_p37  - CSR softmax + neighbourhood aggregation
+ *   [P3] FW-GLM-5-1 l1_p18 - multi-head weighted sparse aggregation
+ *   [P4] Kimi-K2.6 l2_p4   - scene-graph relation (dense-masked) attention block
+ *   [P5] FW-GLM-5-1 l1_p10 - edge-only SDDMM (gathered dot product)
+ *
+ * Return value of every entry point: 0 on success, -1 on a bad argument,
+ * -2 when a scratch allocation fails.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* dtype codes of the feature arguments */
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+
+static double widen_bf16(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double elem(const void *base, int dtype, int64_t i)
+{
+    if (dtype == ORACLE_F32)
+        return (double)((const float *)base)[i];
+    return widen_bf16(((const uint16_t *)base)[i]);
+}
+
+static int64_t max_degree(const int32_t *row_ptr, int64_t n_rows)
+{
+    int64_t m = 0;
+    for (int64_t i = 0; i < n_rows; ++i) {
+        int64_t d = (int64_t)row_ptr[i + 1] - row_ptr[i];
+        if (d > m)
+            m = d;
+    }
+    return m;
+}
+
+/*
+ * O1 - segmented edge softmax [P1, reference model: softmax over each node's
+ * edge range, per head]. For every row i and head h, over the edges
+ * e in [row_ptr[i], row_ptr[i+1]):
+ *     m = max_e s[e,h];  Z = sum_e exp(s[e,h] - m);  out[e,h] = exp(s[e,h] - m) / Z.
+ * A zero-degree row has no edges and writes nothing. A row whose scores are
+ * all -inf gives NaN (exp(-inf - -inf)), as the library softmax does.
+ * scores/out are [E, H] row-major (edge-major, heads contiguous).
+ */
+int oracle_edge_softmax(const int32_t *row_ptr, int64_t n_rows, int32_t H,
+                        const float *scores, double *out)
+{
+    if (!row_ptr || n_rows < 0 || H < 1 || (!scores && row_ptr[n_rows] > 0))
+        return -1;
+    for (int64_t i = 0; i < n_rows; ++i) {
+        int64_t e0 = row_ptr[i], e1 = row_ptr[i + 1];
+        for (int32_t h = 0; h < H; ++h) {
+            double m = -INFINITY;
+            for (int64_t e = e0; e < e1; ++e) {
+                double s = scores[e * H + h];
+                if (s > m)
+                    m = s;
+            }
+            double Z = 0.0;
+            for (int64_t e = e0; e < e1; ++e)
+                Z += exp((double)scores[e * H + h] - m);
+            for (int64_t e = e0; e < e1; ++e)
+                out[e * H + h] = exp((double)scores[e * H + h] - m) / Z;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Weighted SpMM [P3, reference model: for each destination node, sum of the
+ * per-edge, per-head weight times the source node's feature row; P2: the
+ * aggregation step, a zero-degree row stays zero]:
+ *     out[i,h,d] = sum_{e in row i} w[e,h] * feat[col_idx[e],h,d]
+ * w is [E,H] (fp64 so that the oracle's own softmax weights can be chained in
+ * without rounding), feat is [n_src,H,Dh] in `dtype`, out is [n_rows,H,Dh].
+ * cond (optional) receives sum_e |w[e,h] * feat[...]|, the conditioning scale
+ * of each output used by the tolerance.
+ */
+int oracle_spmm_weighted(const int32_t *row_ptr, const int32_t *col_idx,
+                         int64_t n_rows, int32_t H, int32_t Dh,
+                         const double *w, const void *feat, int dtype,
+                         double *out, double *cond)
+{
+    if (!row_ptr || n_rows < 0 || H < 1 || Dh < 1 || !out)
+        return -1;
+    const int64_t HD = (int64_t)H * Dh;
+    for (int64_t i = 0; i < n_rows; ++i) {
+        for (int64_t x = 0; x < HD; ++x) {
+            out[i * HD + x] = 0.0;
+            if (cond)
+                cond[i * HD + x] = 0.0;
+        }
+        for (int64_t e = row_ptr[i]; e < row_ptr[i + 1]; ++e) {
+            int64_t src = col_idx[e];
+            for (int32_t h = 0; h < H; ++h) {
+                double we = w[e * H + h];
+                for (int32_t d = 0; d < Dh; ++d) {
+                    double t = we * elem(feat, dtype, src * HD + (int64_t)h * Dh + d);
+                    out[i * HD + (int64_t)h * Dh + d] += t;
+                    if (cond)
+                        cond[i * HD + (int64_t)h * Dh + d] += fabs(t);
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * SDDMM [P5, reference model: gather the two endpoint feature rows of each
+ * edge and sum their elementwise product], generalised to heads and a scale:
+ *     out[e,h] = scale * sum_d src_feat[src(e),h,d] * dst_feat[dst(e),h,d]
+ * COO form (row_ptr == NULL): src(e) = src_idx[e], dst(e) = dst_idx[e].
+ * CSR form: dst(e) is the row i that owns edge e, src(e) = src_idx[e] (the
+ * column index); dst_idx is ignored.
+ * cond (optional) receives scale * sum_d |product|.
+ */
+int oracle_sddmm(const int32_t *row_ptr, const int32_t *src_idx,
+                 const int32_t *dst_idx, int64_t n_rows, int64_t n_edges,
+                 int32_t H, int32_t Dh, double scale, const void *src_feat,
+                 const void *dst_feat, int dtype, double *out, double *cond)
+{
+    if (H < 1 || Dh < 1 || n_edges < 0 || (!row_ptr && !dst_idx))
+        return -1;
+    const int64_t HD = (int64_t)H * Dh;
+    for (int64_t r = 0; r < (row_ptr ? n_rows : 1); ++r) {
+        int64_t e0 = row_ptr ? row_ptr[r] : 0;
+        int64_t e1 = row_ptr ? row_ptr[r + 1] : n_edges;
+        for (int64_t e = e0; e < e1; ++e) {
+            int64_t s = src_idx[e];
+            int64_t t = row_ptr ? r : dst_idx[e];
+            for (int32_t h = 0; h < H; ++h) {
+                double acc = 0.0, c = 0.0;
+                for (int32_t d = 0; d < Dh; ++d) {
+                    double p = elem(src_feat, dtype, s * HD + (int64_t)h * Dh + d) *
+                               elem(dst_feat, dtype, t * HD + (int64_t)h * Dh + d);
+                    acc += p;
+                    c += fabs(p);
+                }
+                out[e * H + h] = scale * acc;
+                if (cond)
+                    cond[e * H + h] = fabs(scale) * c;
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Fused multi-head graph-attention layer: the composition SDDMM -> segmented
+ * softmax -> weighted SpMM over one CSR graph, computed stage by stage with a
+ * two-pass softmax ([P5] score, [P1] softmax, [P3]/[P2] aggregation):
+ *     s[e,h]     = scale * sum_d q[i,h,d] * k[col_idx[e],h,d]
+ *     w[e,h]     = exp(s[e,h] - max_e s) / sum_e exp(s[e,h] - max_e s)
+ *     out[i,h,d] = sum_e w[e,h] * v[col_idx[e],h,d]      (0 for a zero-degree row)
+ * rows (optional) selects which destination rows to compute, n_sel of them;
+ * out/cond are then [n_sel,H,Dh]. cond receives sum_e w[e,h] * |v[...]|.
+ */
+int oracle_fused_layer(const int32_t *row_ptr, const int32_t *col_idx,
+                       int64_t n_rows, int32_t H, int32_t Dh, double scale,
+                       const void *q, const void *k, const void *v, int dtype,
+                       const int64_t *rows, int64_t n_sel, double *out,
+                       double *cond)
+{
+    if (!row_ptr || n_rows < 0 || H < 1 || Dh < 1 || !out)
+        return -1;
+    if (!rows)
+        n_sel = n_rows;
+    const int64_t HD = (int64_t)H * Dh;
+    int64_t dm = max_degree(row_ptr, n_rows);
+    double *s = (double *)malloc((size_t)(dm > 0 ? dm : 1) * sizeof(double));
+    if (!s)
+        return -2;
+    for (int64_t t = 0; t < n_sel; ++t) {
+        int64_t i = rows ? rows[t] : t;
+        if (i < 0 || i >= n_rows) {
+            free(s);
+            return -1;
+        }
+        int64_t e0 = row_ptr[i], e1 = row_ptr[i + 1];
+        for (int32_t h = 0; h < H; ++h) {
+            double *o = out + t * HD + (int64_t)h * Dh;
+            double *c = cond ? cond + t * HD + (int64_t)h * Dh : NULL;
+            for (int32_t d = 0; d < Dh; ++d) {
+                o[d] = 0.0;
+                if (c)
+                    c[d] = 0.0;
+            }
+            if (e1 == e0)
+                continue;
+            /* pass 0: scores */
+            for (int64_t e = e0; e < e1; ++e) {
+                int64_t src = col_idx[e];
+                double acc = 0.0;
+                for (int32_t d = 0; d < Dh; ++d)
+                    acc += elem(q, dtype, i * HD + (int64_t)h * Dh + d) *
+                           elem(k, dtype, src * HD + (int64_t)h * Dh + d);
+                s[e - e0] = scale * acc;
+            }
+            /* pass 1: max; pass 2: normaliser */
+            double m = -INFINITY;
+            for (int64_t e = e0; e < e1; ++e)
+                if (s[e - e0] > m)
+                    m = s[e - e0];
+            double Z = 0.0;
+            for (int64_t e = e0; e < e1; ++e)
+                Z += exp(s[e - e0] - m);
+            /* aggregation with the normalised weights */
+            for (int64_t e = e0; e < e1; ++e) {
+                int64_t src = col_idx[e];
+                double w = exp(s[e - e0] - m) / Z;
+                for (int32_t d = 0; d < Dh; ++d) {
+                    double val = elem(v, dtype, src * HD + (int64_t)h * Dh + d);
+                    o[d] += w * val;
+                    if (c)
+                        c[d] += w * fabs(val);
+                }
+            }
+        }
+    }
+    free(s);
+    return 0;
+}
+
+/*
+ * Dense-masked small-graph attention block [P4, reference model]. Per graph b
+ * (nodes x[N,D], pair feats [N,N,P], mask [N,N]), with head h owning feature
+ * dims [h*dh, (h+1)*dh), dh = D/H:
+ *   xn      = (x - mean) / sqrt(biased_var + eps) * ln_w + ln_b   (per node)
+ *   Q,K,V   = xn Wq^T, xn Wk^T, xn Wv^T          (Linear(D,D), no bias)
+ *   hid     = SiLU(W1 pair[i,j] + b1),  SiLU(t) = t / (1 + exp(-t))
+ *   r[h]    = (W2 hid + b2)[h]                   (relation bias, per pair)
+ *   logit   = Q_i^h . K_j^h / sqrt(dh) + r[h];  -inf where mask[i,j] < 0.5
+ *   a[i,j]  = softmax_j(logit)                   (all -inf row -> NaN)
+ *   ctx_i^h = sum_j a[i,j] V_j^h
+ *   out_i   = x_i + Wout ctx_i                   (Linear(D,D), no bias; residual)
+ * graphs (optional) selects n_sel graphs; out is then [n_sel,N,D].
+ */
+int oracle_dense_block(int32_t B, int32_t N, int32_t D, int32_t H, int32_t P,
+                       const float *nodes, const float *pair, const float *mask,
+                       const float *ln_w, const float *ln_b, double eps,
+                       const float *Wq, const float *Wk, const float *Wv,
+                       const float *W1, const float *b1, const float *W2,
+                       const float *b2, const float *Wout,
+                       const int64_t *graphs, int64_t n_sel, double *out)
+{
+    if (B < 0 || N < 1 || D < 1 || H < 1 || P < 1 || D % H != 0 || !out)
+        return -1;
+    if (!graphs)
+        n_sel = B;
+    const int32_t dh = D / H;
+    const double inv_sqrt_dh = 1.0 / sqrt((double)dh);
+    size_t nd = (size_t)N * D;
+    double *xn = (double *)malloc(nd * sizeof(double));
+    double *Q = (double *)malloc(nd * sizeof(double));
+    double *K = (double *)malloc(nd * sizeof(double));
+    double *V = (double *)malloc(nd * sizeof(double));
+    double *ctx = (double *)malloc(nd * sizeof(double));
+    double *logit = (double *)malloc((size_t)N * sizeof(double));
+    double *hid = (double *)malloc((size_t)P * sizeof(double));
+    double *rel = (double *)malloc((size_t)N * N * H * sizeof(double));
+    int rc = 0;
+    if (!xn || !Q || !K || !V || !ctx || !logit || !hid || !rel) {
+        rc = -2;
+        goto done;
+    }
+    for (int64_t t = 0; t < n_sel; ++t) {
+        int64_t b = graphs ? graphs[t] : t;
+        if (b < 0 || b >= B) {
+            rc = -1;
+            goto done;
+        }
+        const float *x = nodes + b * (int64_t)nd;
+        /* LayerNorm, biased variance */
+        for (int32_t n = 0; n < N; ++n) {
+            double mean = 0.0, var = 0.0;
+            for (int32_t d = 0; d < D; ++d)
+                mean += x[n * D + d];
+            mean /= D;
+            for (int32_t d = 0; d < D; ++d)
+                var += (x[n * D + d] - mean) * (x[n * D + d] - mean);
+            var /= D;
+            double rstd = 1.0 / sqrt(var + eps);
+            for (int32_t d = 0; d < D; ++d)
+                xn[n * D + d] = (x[n * D + d] - mean) * rstd * ln_w[d] + ln_b[d];
+        }
+        /* Q, K, V projections: y[o] = sum_c W[o][c] xn[c] */
+        for (int32_t n = 0; n < N; ++n)
+            for (int32_t o = 0; o < D; ++o) {
+                double aq = 0.0, ak = 0.0, av = 0.0;
+                for (int32_t c = 0; c < D; ++c) {
+                    aq += (double)Wq[o * D + c] * xn[n * D + c];
+                    ak += (double)Wk[o * D + c] * xn[n * D + c];
+                    av += (double)Wv[o * D + c] * xn[n * D + c];
+                }
+                Q[n * D + o] = aq;
+                K[n * D + o] = ak;
+                V[n * D + o] = av;
+            }
+        /* relation MLP bias per pair (i, j), all heads */
+        for (int32_t i = 0; i < N; ++i)
+            for (int32_t j = 0; j < N; ++j) {
+                const float *pf = pair + (((b * N) + i) * (int64_t)N + j) * P;
+                for (int32_t p = 0; p < P; ++p) {
+                    double a = b1[p];
+                    for (int32_t c = 0; c < P; ++c)
+                        a += (double)W1[p * P + c] * pf[c];
+                    hid[p] = a / (1.0 + exp(-a));
+                }
+                for (int32_t h = 0; h < H; ++h) {
+                    double a = b2[h];
+                    for (int32_t p = 0; p < P; ++p)
+                        a += (double)W2[h * P + p] * hid[p];
+                    rel[((size_t)i * N + j) * H + h] = a;
+                }
+            }
+        /* masked softmax attention per head and query row */
+        for (int32_t h = 0; h < H; ++h)
+            for (int32_t i = 0; i < N; ++i) {
+                for (int32_t j = 0; j < N; ++j) {
+                    double dot = 0.0;
+                    for (int32_t c = 0; c < dh; ++c)
+                        dot += Q[i * D + h * dh + c] * K[j * D + h * dh + c];
+                    double l = dot * inv_sqrt_dh + rel[((size_t)i * N + j) * H + h];
+                    if (mask[((b * N) + i) * (int64_t)N + j] < 0.5f)
+                        l = -INFINITY;
+                    logit[j] = l;
+                }
+                double m = -INFINITY;
+                for (int32_t j = 0; j < N; ++j)
+                    if (logit[j] > m)
+                        m = logit[j];
+                double Z = 0.0;
+                for (int32_t j = 0; j < N; ++j)
+                    Z += exp(logit[j] - m);
+                for (int32_t c = 0; c < dh; ++c) {
+                    double a = 0.0;
+                    for (int32_t j = 0; j < N; ++j)
+                        a += exp(logit[j] - m) / Z * V[j * D + h * dh + c];
+                    ctx[i * D + h * dh + c] = a;
+                }
+            }
+        /* out_proj + residual */
+        double *o = out + t * (int64_t)nd;
+        for (int32_t n = 0; n < N; ++n)
+            for (int32_t r = 0; r < D; ++r) {
+                double a = 0.0;
+                for (int32_t c = 0; c < D; ++c)
+                    a += (double)Wout[r * D + c] * ctx[n * D + c];
+                o[n * D + r] = (double)x[n * D + r] + a;
+            }
+    }
+done:
+    free(xn);
+    free(Q);
+    free(K);
+    free(V);
+    free(ctx);
+    free(logit);
+    free(hid);
+    free(rel);
+    return rc;
+}
+
+/*
+ * Degree-bucket plan (the scheduling table of the CUDA path, defined here
+ * from its specification so its integers can be compared bit for bit):
+ *   deg(i)      = row_ptr[i+1] - row_ptr[i]
+ *   heavy rows  = the rows with deg(i) > heavy_threshold, ascending
+ *   chunks(i)   = ceil(deg(i) / chunk) for a heavy row i
+ *   chunk_start = exclusive prefix sum of chunks over the heavy rows [n_heavy+1]
+ *   chunk_row   = for each chunk, the index (into heavy rows) of its row
+ * Chunk c of heavy row r covers edges [row_ptr[row] + j*chunk,
+ * min(row_ptr[row] + (j+1)*chunk, row_ptr[row+1])) with j = c - chunk_start[r].
+ * With NULL output arrays only the counts are produced.
+ */
+int oracle_plan(const int32_t *row_ptr, int64_t n_rows, int32_t heavy_threshold,
+                int32_t chunk, int64_t *n_heavy, int64_t *n_chunks,
+                int32_t *heavy_rows, int32_t *chunk_start, int32_t *chunk_row)
+{
+    if (!row_ptr || n_rows < 0 || heavy_threshold < 0 || chunk < 1 || !n_heavy || !n_chunks)
+        return -1;
+    int64_t nh = 0, nc = 0;
+    for (int64_t i = 0; i < n_rows; ++i) {
+        int64_t d = (int64_t)row_ptr[i + 1] - row_ptr[i];
+        if (d <= heavy_threshold)
+            continue;
+        int64_t c = (d + chunk - 1) / chunk;
+        if (heavy_rows)
+            heavy_rows[nh] = (int32_t)i;
+        if (chunk_start)
+            chunk_start[nh] = (int32_t)nc;
+        if (chunk_row)
+            for (int64_t j = 0; j < c; ++j)
+                chunk_row[nc + j] = (int32_t)nh;
+        nc += c;
+        nh += 1;
+    }
+    if (chunk_start)
+        chunk_start[nh] = (int32_t)nc;
+    *n_heavy = nh;
+    *n_chunks = nc;
+    return 0;
+}

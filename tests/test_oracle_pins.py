@@ -1,0 +1,411 @@
+"""Pins for the fp64 oracle: closed forms, invariants, brute force on tiny
+inputs and independent library computations (NumPy / PyTorch CPU float64).
+
+Each test is chosen so that a plausible mistake in the oracle (a dropped term,
+a wrong sign or index, a transposed operand, a missing max-subtraction, heads
+mixed up) fails at least one of them. CPU only.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from tests.golden import fixtures
+
+
+# ----------------------------------------------------------------------------
+# helpers: independent dense formulations (library softmax / matmul)
+# ----------------------------------------------------------------------------
+def np_softmax(x, axis=-1):
+    """Library-style softmax via scipy (independent of the oracle's loops)."""
+    from scipy.special import softmax
+    return softmax(x, axis=axis)
+
+
+def tiny_graph(rng, n, n_src, max_deg, allow_dup=False, sort=True):
+    deg = rng.integers(0, max_deg + 1, size=n)
+    rows, cols = [], []
+    for i, d in enumerate(deg):
+        if allow_dup:
+            c = rng.integers(0, n_src, size=d)
+        else:
+            d = min(d, n_src)
+            c = rng.choice(n_src, size=d, replace=False)
+        if sort:
+            c = np.sort(c)
+        rows.append(np.full(len(c), i))
+        cols.append(c)
+    deg = np.array([len(c) for c in cols])
+    rp = W.row_ptr_from_degrees(deg)
+    ci = np.concatenate(cols).astype(np.int32) if cols else np.zeros(0, np.int32)
+    return rp, ci
+
+
+def row_of_edge(rp):
+    deg = np.diff(rp.astype(np.int64))
+    return np.repeat(np.arange(deg.size), deg)
+
+
+# ----------------------------------------------------------------------------
+# O1 segmented edge softmax
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("case", fixtures.load("softmax_closed_form.txt"))
+def test_softmax_closed_forms(case):
+    rp = np.array(case["row_ptr"], dtype=np.int32)
+    H = int(case["H"][0])
+    s = np.array(case["scores"], dtype=np.float64)
+    # the fixture's ln values are exact in fp64 but the oracle receives fp32
+    # inputs, as the GPU does; compare at fp32-input resolution
+    out = oracle.edge_softmax(rp, s.astype(np.float32), H).ravel()
+    np.testing.assert_allclose(out, case["expected"], rtol=1e-6, atol=0)
+
+
+def test_softmax_matches_dense_masked_library_softmax():
+    rng = np.random.default_rng(10)
+    for H in (1, 3, 4):
+        rp, ci = tiny_graph(rng, 9, 7, 6)
+        E = int(rp[-1])
+        s = (3 * rng.standard_normal((E, H))).astype(np.float32)
+        got = oracle.edge_softmax(rp, s, H)
+        r = row_of_edge(rp)
+        for h in range(H):
+            dense = np.full((9, 7), -np.inf)
+            dense[r, ci] = s[:, h]
+            P = np.zeros_like(dense)
+            nz = np.isfinite(dense).any(axis=1)
+            P[nz] = np_softmax(dense[nz], axis=1)
+            np.testing.assert_allclose(got[:, h], P[r, ci], rtol=1e-13, atol=1e-15)
+
+
+def test_softmax_invariants():
+    rng = np.random.default_rng(11)
+    d = W.make_edge_softmax(seed=5)
+    rp, s, H = d["row_ptr"], d["scores"], d["H"]
+    out = oracle.edge_softmax(rp, s, H)
+    r = row_of_edge(rp)
+    sums = np.zeros((rp.size - 1, H))
+    np.add.at(sums, r, out)
+    nonempty = np.diff(rp) > 0
+    np.testing.assert_allclose(sums[nonempty], 1.0, rtol=0, atol=1e-13)
+    assert (out > 0).all()
+    # shift invariance per (row, head); shifts are exact in fp32 (multiples of 1/2)
+    shift = (rng.integers(-8, 8, size=(rp.size - 1, H)) / 2.0).astype(np.float32)
+    out2 = oracle.edge_softmax(rp, s + shift[r], H)
+    np.testing.assert_allclose(out2, out, rtol=1e-6)  # fp32 rounding of s+shift
+    # permutation equivariance inside each row
+    perm = np.arange(r.size)
+    for i in range(rp.size - 1):
+        seg = perm[rp[i]:rp[i + 1]]
+        perm[rp[i]:rp[i + 1]] = rng.permutation(seg)
+    out3 = oracle.edge_softmax(rp, s[perm], H)
+    np.testing.assert_allclose(out3, out[perm], rtol=1e-14)  # sum order differs
+
+
+def test_softmax_large_scores_need_max_subtraction():
+    rp = np.array([0, 3], dtype=np.int32)
+    s = np.array([[800.0], [799.0], [-800.0]], dtype=np.float32)
+    out = oracle.edge_softmax(rp, s, 1).ravel()
+    e = math.exp(-1.0)
+    np.testing.assert_allclose(out[:2], [1 / (1 + e), e / (1 + e)], rtol=1e-14)
+    assert out[2] == 0.0
+
+
+def test_softmax_all_minus_inf_row_is_nan_like_library():
+    import torch
+    rp = np.array([0, 2], dtype=np.int32)
+    s = np.full((2, 1), -np.inf, dtype=np.float32)
+    out = oracle.edge_softmax(rp, s, 1)
+    ref = torch.softmax(torch.tensor(s[:, 0], dtype=torch.float64), 0).numpy()
+    assert np.isnan(out).all() and np.isnan(ref).all()
+
+
+def test_softmax_page_generator_rows():
+    # edge-softmax page generator: degrees clamp(18 + (i mod 5) - 2, 1) -> 16..20
+    deg = W.page_mod_degrees(384, 18, 5)
+    assert deg.min() == 16 and deg.max() == 20
+    d = W.make_edge_softmax(seed=6, deg=deg, H=8)
+    out = oracle.edge_softmax(d["row_ptr"], d["scores"], 8)
+    sums = np.zeros((384, 8))
+    np.add.at(sums, row_of_edge(d["row_ptr"]), out)
+    np.testing.assert_allclose(sums, 1.0, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------
+# O3 SDDMM
+# ----------------------------------------------------------------------------
+def test_sddmm_closed_form():
+    (c,) = fixtures.load("sddmm_closed_form.txt")
+    a = np.array(c["src_feat"], np.float32).reshape(3, 4)
+    b = np.array(c["dst_feat"], np.float32).reshape(2, 4)
+    out = oracle.sddmm(np.array(c["src_idx"], np.int32), a, b, 1, 4,
+                       dst_idx=np.array(c["dst_idx"], np.int32))
+    np.testing.assert_array_equal(out.ravel(), c["expected"])
+
+
+def test_sddmm_equals_library_matmul_sampled_at_edges_full_size():
+    d = W.make_sddmm()
+    out, cond = oracle.sddmm(d["src_idx"], d["src_feat"], d["dst_feat"], 1, 128,
+                             dst_idx=d["dst_idx"], want_cond=True)
+    G = d["src_feat"].astype(np.float64) @ d["dst_feat"].astype(np.float64).T
+    ref = G[d["src_idx"], d["dst_idx"]]
+    np.testing.assert_allclose(out[:, 0], ref, rtol=1e-12, atol=1e-12)
+    assert (cond[:, 0] >= np.abs(out[:, 0]) - 1e-12).all()
+
+
+def test_sddmm_multihead_scale_and_csr_form():
+    rng = np.random.default_rng(12)
+    H, Dh, n = 3, 5, 6
+    rp, ci = tiny_graph(rng, n, n, 5, allow_dup=True)
+    q = rng.standard_normal((n, H, Dh)).astype(np.float32)
+    k = rng.standard_normal((n, H, Dh)).astype(np.float32)
+    scale = 0.37
+    csr = oracle.sddmm(ci, k, q, H, Dh, scale=scale, row_ptr=rp)
+    r = row_of_edge(rp)
+    coo = oracle.sddmm(ci, k, q, H, Dh, scale=scale, dst_idx=r.astype(np.int32))
+    np.testing.assert_array_equal(csr, coo)
+    ref = np.stack([(k[:, h].astype(np.float64) @ q[:, h].astype(np.float64).T)[ci, r]
+                    for h in range(H)], axis=1) * scale
+    np.testing.assert_allclose(csr, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_sddmm_bf16_inputs_widen_exactly():
+    rng = np.random.default_rng(13)
+    a = W.bf16_bits_from_f32(rng.standard_normal((7, 16)).astype(np.float32))
+    b = W.bf16_bits_from_f32(rng.standard_normal((5, 16)).astype(np.float32))
+    si = rng.integers(0, 7, 20).astype(np.int32)
+    di = rng.integers(0, 5, 20).astype(np.int32)
+    got = oracle.sddmm(si, a, b, 2, 8, dst_idx=di)
+    af = W.f32_from_bf16_bits(a).astype(np.float64).reshape(7, 2, 8)
+    bf = W.f32_from_bf16_bits(b).astype(np.float64).reshape(5, 2, 8)
+    ref = np.einsum("ehd,ehd->eh", af[si], bf[di])
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------
+# weighted SpMM and O2 (softmax + aggregation)
+# ----------------------------------------------------------------------------
+def test_spmm_equals_dense_matmul_with_duplicates_summed():
+    rng = np.random.default_rng(14)
+    H, Dh, n, n_src = 2, 3, 8, 5
+    rp, ci = tiny_graph(rng, n, n_src, 7, allow_dup=True, sort=False)
+    E = int(rp[-1])
+    w = rng.standard_normal((E, H))
+    feat = rng.standard_normal((n_src, H, Dh)).astype(np.float32)
+    out, cond = oracle.spmm_weighted(rp, ci, w, feat, H, Dh, want_cond=True)
+    r = row_of_edge(rp)
+    for h in range(H):
+        Wd = np.zeros((n, n_src))
+        np.add.at(Wd, (r, ci), w[:, h])
+        np.testing.assert_allclose(out[:, h], Wd @ feat[:, h].astype(np.float64),
+                                   rtol=1e-12, atol=1e-13)
+    assert (cond >= np.abs(out) - 1e-13).all()
+    empty = np.diff(rp) == 0
+    assert (out[empty] == 0).all()
+
+
+def test_aggregate_page_semantics_and_zero_rows():
+    d = W.make_aggregate(seed=15, n=40)
+    w = oracle.edge_softmax(d["row_ptr"], d["scores"], 1)
+    out = oracle.spmm_weighted(d["row_ptr"], d["col_idx"], w, d["values"], 1, d["F"])
+    # independent: per row, library softmax over the row's scores then a dot
+    rp = d["row_ptr"]
+    for i in range(40):
+        e0, e1 = rp[i], rp[i + 1]
+        if e0 == e1:
+            assert (out[i] == 0).all()
+            continue
+        p = np_softmax(d["scores"][e0:e1].astype(np.float64))
+        ref = p @ d["values"][d["col_idx"][e0:e1]].astype(np.float64)
+        np.testing.assert_allclose(out[i, 0], ref, rtol=1e-12, atol=1e-14)
+
+
+# ----------------------------------------------------------------------------
+# O4 fused layer
+# ----------------------------------------------------------------------------
+def test_fused_closed_form():
+    (c,) = fixtures.load("fused_closed_form.txt")
+    rp = np.array(c["row_ptr"], np.int32)
+    ci = np.array(c["col_idx"], np.int32)
+    q, k, v = (np.array(c[x], np.float64).reshape(3, 1, 2) for x in ("q", "k", "v"))
+    # ln 3 is not exact in fp32: feed fp64-exact values through fp32 and
+    # compare at fp32-input resolution
+    out = oracle.fused_layer(rp, ci, q.astype(np.float32), k.astype(np.float32),
+                             v.astype(np.float32), 1, 2, 1.0)
+    np.testing.assert_allclose(out.ravel(), c["expected"], rtol=1e-6, atol=1e-6)
+
+
+def dense_masked_attention(rp, ci, q, k, v, scale):
+    """Independent formulation: per head, dense logits Q K^T * scale plus
+    log(edge multiplicity) (-inf where no edge), library softmax, times V."""
+    n, H, Dh = q.shape
+    n_src = k.shape[0]
+    r = row_of_edge(rp)
+    cnt = np.zeros((n, n_src))
+    np.add.at(cnt, (r, ci), 1.0)
+    with np.errstate(divide="ignore"):
+        logm = np.log(cnt)
+    out = np.zeros((n, H, Dh))
+    nz = cnt.sum(1) > 0
+    for h in range(H):
+        S = q[:, h].astype(np.float64) @ k[:, h].astype(np.float64).T * scale + logm
+        A = np.zeros_like(S)
+        A[nz] = np_softmax(S[nz], axis=1)
+        out[:, h] = A @ v[:, h].astype(np.float64)
+    return out
+
+
+@pytest.mark.parametrize("dup", [False, True])
+def test_fused_equals_dense_masked_attention(dup):
+    rng = np.random.default_rng(16 + dup)
+    n, H, Dh = 11, 3, 4
+    rp, ci = tiny_graph(rng, n, n, 7, allow_dup=dup, sort=not dup)
+    q, k, v = (rng.standard_normal((n, H, Dh)).astype(np.float32) for _ in range(3))
+    got = oracle.fused_layer(rp, ci, q, k, v, H, Dh, 0.5)
+    ref = dense_masked_attention(rp, ci, q, k, v, 0.5)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_fused_special_cases():
+    rng = np.random.default_rng(18)
+    n, H, Dh = 5, 2, 3
+    k = rng.standard_normal((n, H, Dh)).astype(np.float32)
+    v = rng.standard_normal((n, H, Dh)).astype(np.float32)
+    q = rng.standard_normal((n, H, Dh)).astype(np.float32)
+    # row 0: single edge -> exactly v[src]; row 1: three edges to the same source
+    # -> exactly v[src]; row 2: empty -> 0; row 3: q = 0 -> plain average
+    rp = np.array([0, 1, 4, 4, 7, 7], np.int32)
+    ci = np.array([3, 2, 2, 2, 0, 1, 4], np.int32)
+    q[3] = 0
+    out = oracle.fused_layer(rp, ci, q, k, v, H, Dh, 0.125)
+    np.testing.assert_array_equal(out[0], v[3].astype(np.float64))
+    np.testing.assert_allclose(out[1], v[2].astype(np.float64), rtol=1e-15, atol=1e-15)
+    assert (out[2] == 0).all() and (out[4] == 0).all()
+    np.testing.assert_allclose(out[3], v[[0, 1, 4]].astype(np.float64).mean(0), rtol=1e-14)
+
+
+def test_fused_composes_from_stages_and_row_selection():
+    d = W.make_fused(seed=19, n=300, dmax=64)
+    args = (d["row_ptr"], d["col_idx"], d["q"], d["k"], d["v"], d["H"], d["Dh"], d["scale"])
+    full = oracle.fused_layer(*args)
+    s = oracle.sddmm(d["col_idx"], d["k"], d["q"], d["H"], d["Dh"], scale=d["scale"],
+                     row_ptr=d["row_ptr"])
+    w = oracle.edge_softmax(d["row_ptr"], s.astype(np.float32), d["H"])
+    agg = oracle.spmm_weighted(d["row_ptr"], d["col_idx"], w, d["v"], d["H"], d["Dh"])
+    np.testing.assert_allclose(full, agg, rtol=1e-5, atol=1e-6)  # fp32 rounding of s
+    rows = np.array([299, 0, 17, 17, 150])
+    sel = oracle.fused_layer(*args, rows=rows)
+    np.testing.assert_array_equal(sel, full[rows])
+    # bf16 bits are widened exactly: same as feeding the widened fp32 values
+    f32 = [W.f32_from_bf16_bits(d[x]) for x in ("q", "k", "v")]
+    full32 = oracle.fused_layer(d["row_ptr"], d["col_idx"], *f32, d["H"], d["Dh"], d["scale"])
+    np.testing.assert_array_equal(full32, full)
+
+
+def test_fused_matches_dense_on_bf16_zipf_graph():
+    d = W.make_fused(seed=20, n=64, dmax=32, mean=6.0)
+    f32 = [W.f32_from_bf16_bits(d[x]).reshape(64, 8, 64) for x in ("q", "k", "v")]
+    got = oracle.fused_layer(d["row_ptr"], d["col_idx"], d["q"], d["k"], d["v"], 8, 64, 0.125)
+    ref = dense_masked_attention(d["row_ptr"], d["col_idx"], *f32, 0.125)
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------
+# O5 dense-masked block: PyTorch CPU float64 modules
+# ----------------------------------------------------------------------------
+def torch_block(w, graphs):
+    import torch
+    from torch import nn
+    t = lambda a: torch.tensor(np.asarray(a), dtype=torch.float64)  # noqa: E731
+    D, H, P = w["D"], w["H"], w["P"]
+    ln = nn.LayerNorm(D, eps=w["ln_eps"]).double()
+    q_p, k_p, v_p, o_p = (nn.Linear(D, D, bias=False).double() for _ in range(4))
+    mlp = nn.Sequential(nn.Linear(P, P), nn.SiLU(), nn.Linear(P, H)).double()
+    with torch.no_grad():
+        ln.weight.copy_(t(w["ln_w"]))
+        ln.bias.copy_(t(w["ln_b"]))
+        q_p.weight.copy_(t(w["Wq"]))
+        k_p.weight.copy_(t(w["Wk"]))
+        v_p.weight.copy_(t(w["Wv"]))
+        o_p.weight.copy_(t(w["Wout"]))
+        mlp[0].weight.copy_(t(w["W1"]))
+        mlp[0].bias.copy_(t(w["b1"]))
+        mlp[2].weight.copy_(t(w["W2"]))
+        mlp[2].bias.copy_(t(w["b2"]))
+        x = t(w["nodes"][graphs])
+        pf = t(w["pair_feats"][graphs])
+        m = t(w["edge_mask"][graphs])
+        B, N, _ = x.shape
+        dh = D // H
+        h = ln(x)
+        q = q_p(h).view(B, N, H, dh).transpose(1, 2)
+        k = k_p(h).view(B, N, H, dh).transpose(1, 2)
+        v = v_p(h).view(B, N, H, dh).transpose(1, 2)
+        logits = q @ k.transpose(-2, -1) / math.sqrt(dh)
+        logits = logits + mlp(pf).permute(0, 3, 1, 2)
+        logits = logits.masked_fill(m.unsqueeze(1) < 0.5, float("-inf"))
+        a = torch.softmax(logits, dim=-1)
+        ctx = (a @ v).transpose(1, 2).reshape(B, N, D)
+        return (x + o_p(ctx)).numpy()
+
+
+@pytest.mark.parametrize("affine", [False, True])
+def test_dense_block_equals_torch_modules(affine):
+    w = W.make_dense(seed=21, B=6, affine_ln=affine, wstd=0.3)
+    g = np.array([0, 3, 5])
+    got = oracle.dense_block(w, graphs=g)
+    ref = torch_block(w, g)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_dense_block_other_shapes_and_fully_masked_row():
+    w = W.make_dense(seed=22, B=3, N=7, D=12, H=3, P=5, wstd=0.5, affine_ln=True)
+    w["edge_mask"][1, 4, :] = 0.0  # node 4 of graph 1 attends to nothing
+    got = oracle.dense_block(w)
+    ref = torch_block(w, np.arange(3))
+    assert np.isnan(got[1, 4]).all() and np.isnan(ref[1, 4]).all()
+    ok = ~np.isnan(ref)
+    np.testing.assert_allclose(got[ok], ref[ok], rtol=1e-12, atol=1e-12)
+    assert not np.isnan(got[0]).any()
+
+
+def test_dense_block_zero_out_proj_is_identity():
+    w = W.make_dense(seed=23, B=2)
+    w["Wout"][:] = 0
+    got = oracle.dense_block(w)
+    np.testing.assert_array_equal(got, w["nodes"].astype(np.float64))
+
+
+# ----------------------------------------------------------------------------
+# degree-bucket plan (integers): brute-force re-derivation
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("T,C", [(0, 1), (4, 3), (32, 32), (64, 16)])
+def test_plan_brute_force(T, C):
+    rng = np.random.default_rng(24)
+    deg = np.concatenate([rng.integers(0, 80, 200), [T, T + 1, C, C + 1, 2 * C, 0]])
+    rp = W.row_ptr_from_degrees(deg)
+    hr, cs, cr = oracle.plan(rp, T, C)
+    exp_hr, exp_cs, exp_cr = [], [0], []
+    for i, dgr in enumerate(deg):
+        if dgr > T:
+            nch = -(-int(dgr) // C)
+            exp_cr += [len(exp_hr)] * nch
+            exp_hr.append(i)
+            exp_cs.append(exp_cs[-1] + nch)
+    np.testing.assert_array_equal(hr, exp_hr)
+    np.testing.assert_array_equal(cs, exp_cs)
+    np.testing.assert_array_equal(cr, exp_cr)
+    # the chunks tile every heavy row's edge range exactly, each at most C long
+    covered = np.zeros(int(rp[-1]), dtype=np.int64)
+    for c, r in enumerate(cr):
+        row = hr[r]
+        j = c - cs[r]
+        e0 = rp[row] + j * C
+        e1 = min(e0 + C, rp[row + 1])
+        assert 0 < e1 - e0 <= C
+        covered[e0:e1] += 1
+    heavy_edges = np.zeros_like(covered)
+    for row in hr:
+        heavy_edges[rp[row]:rp[row + 1]] = 1
+    np.testing.assert_array_equal(covered, heavy_edges)
