@@ -1,0 +1,474 @@
+"""Benchmark: fused multi-head graph-attention layer on the 1e6-node power-law
+graph (Zipf(2.1) in-degrees clipped to [1,4096], mean 16; H=8, Dh=64, bf16).
+
+One step = one gat_fused_layer call (SDDMM -> segmented softmax -> weighted
+SpMM, fused; one kernel launch) over the whole graph, with the graph's
+degree-bucket plan built beforehand (a plan is per graph and shared by every
+layer and call on it; its build time is reported as plan_ms).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload fused|edge_softmax|aggregate|sddmm|dense]
+
+Prints one JSON line (rank 0). value = edge-heads/s over all ranks (each rank
+runs its own full, independent problem: weak scaling, no collective on the
+data path). e2e = the same metric with inputs copied from pinned host memory
+and the output copied back inside the timed region. --impl reference times the
+fp64 CPU oracle on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "edge-heads/s and achieved HBM GB/s (% of peak), fused CSR attention"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------------------
+# distributed helpers (host logic; exercised by a gloo test on CPU)
+# ----------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def dist_barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def dist_max(dist, x: float, device=None) -> float:
+    """Maximum of a float over all ranks (timing reduction only)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# peaks, clocks, profile summaries
+# ----------------------------------------------------------------------------
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_ordinal: int):
+        # nvidia-smi numbers GPUs physically; map the CUDA ordinal through
+        # CUDA_VISIBLE_DEVICES (an index or a UUID) when it is set
+        vis = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+        self.gpu = vis[local_ordinal] if local_ordinal < len(vis) else str(local_ordinal)
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.reader.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources of the fused kernel (to date ncu counters)."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_graph_attention_head_gb300", "csrc")
+    for f in ("row_engine.cuh", "fused_layer.cu", "common.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch recorded by an ncu capture of the current kernel
+    source (profiles/ncu_traffic.json), scaled to the full workload; None when
+    no capture matches the current source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        e = j[kernel]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch_full"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------
+# fused workload
+# ----------------------------------------------------------------------------
+def fused_bytes(n_rows, n_edges, H, Dh, esize=2):
+    """Algorithmic bytes of one layer under the gather model: per row, its
+    row_ptr entry, q row and out row; per edge, its col_idx entry and the k
+    and v rows of its source."""
+    row = H * Dh * esize
+    return (4 + 2 * row) * n_rows + (4 + 2 * row) * n_edges
+
+
+def fused_unique_bytes(n_rows, n_src, n_edges, H, Dh, esize=2):
+    row = H * Dh * esize
+    return 4 * (n_rows + 1) + 4 * n_edges + 2 * row * n_rows + 2 * row * n_src
+
+
+def to_dev(torch, a, dev):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if a.dtype == np.uint16:
+        t = t.view(torch.int16)
+    t = t.to(dev)
+    return t.view(torch.bfloat16) if a.dtype == np.uint16 else t
+
+
+def cpu_baseline_fused(d, budget_s=10.0, block=20000, start_row=0):
+    """The oracle timed on consecutive row blocks until budget_s elapses."""
+    import oracle
+    oracle.build()
+    rp = d["row_ptr"]
+    n = rp.size - 1
+    t0 = time.perf_counter()
+    edges = rows = 0
+    r = start_row
+    while time.perf_counter() - t0 < budget_s and rows < n:
+        sel = np.arange(r, min(n, r + block))
+        oracle.fused_layer(rp, d["col_idx"], d["q"], d["k"], d["v"], d["H"], d["Dh"],
+                           d["scale"], rows=sel)
+        edges += int(rp[sel[-1] + 1] - rp[sel[0]])
+        rows += sel.size
+        r = (r + block) % n
+    dt = time.perf_counter() - t0
+    return {"value": edges * d["H"] / dt, "unit": "edge-heads/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} consecutive rows ({edges} edges, {edges * d['H']} edge-heads) "
+                      f"of the same graph, fp64 C loops, single thread, {dt:.1f} s"}
+
+
+def bench_fused(args, rank, world, local, dist):
+    import torch
+    import sparse_graph_attention_head_gb300 as gat
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    t_gen = time.perf_counter()
+    d = W.make_fused(seed=3)
+    t_gen = time.perf_counter() - t_gen
+    n, E, H, Dh = d["n_rows"], d["n_edges"], d["H"], d["Dh"]
+    rp_h, ci_h = d["row_ptr"], d["col_idx"]
+    rp, ci = to_dev(torch, rp_h, dev), to_dev(torch, ci_h, dev)
+    q, k, v = (to_dev(torch, d[x], dev) for x in ("q", "k", "v"))
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+
+    # plan (per graph; timed separately)
+    gat.Plan(rp)  # warm the plan kernels once
+    torch.cuda.synchronize()
+    tp = time.perf_counter()
+    plan = gat.Plan(rp)
+    plan_ms = (time.perf_counter() - tp) * 1e3
+    info = plan.info()
+    ws = torch.empty(max(1, gat.gat_fused_layer_workspace_size(plan, H, Dh)), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], out=out, plan=plan, workspace=ws,
+                            stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    dist_barrier(dist)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for a, b in ev:
+            a.record(stream)
+            step()
+            b.record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    dist_barrier(dist)
+    torch.cuda.synchronize()
+    total_ms = t0.elapsed_time(t1)
+    per_launch = [a.elapsed_time(b) for a, b in ev]
+    ms_step = dist_max(dist, total_ms / args.steps, None)
+    kern_ms = statistics.mean(per_launch)
+
+    # end to end: pinned host inputs -> device, layer, output -> pinned host
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(  # noqa: E731
+        np.int16 if a.dtype == np.uint16 else a.dtype)).pin_memory()
+    h_in = [pin(rp_h), pin(ci_h), pin(d["q"]), pin(d["k"]), pin(d["v"])]
+    h_out = torch.empty(out.shape, dtype=torch.int16).pin_memory()
+    d_in = [rp, ci, q.view(torch.int16), k.view(torch.int16), v.view(torch.int16)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for hsrc, ddst in zip(h_in, d_in):
+            ddst.copy_(hsrc, non_blocking=True)
+        step()
+        h_out.copy_(out.view(torch.int16), non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    torch.cuda.synchronize()
+    dist_barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(2, args.steps // 4)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dist_barrier(dist)
+    e2e_ms = dist_max(dist, e0.elapsed_time(e1) / e2e_steps, None)
+
+    hbm_peak, _, peak_kind = measured_peaks()
+    alg = fused_bytes(n, E, H, Dh)
+    achieved = alg / (kern_ms * 1e-3) / 1e9
+    traffic = profiled_traffic("fused_engine_kernel")
+    res = {
+        "metric": METRIC,
+        "value": world * E * H / (ms_step * 1e-3),
+        "unit": "edge-heads/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "fused GAT layer: 1e6 rows, Zipf(2.1) in-degrees clipped to "
+                               "[1,4096] rescaled to mean 16, col_idx uniform sorted in-row, "
+                               "H=8, Dh=64, q/k/v bf16 N(0,1), seed 3",
+                   "n_rows": n, "n_edges": E, "H": H, "Dh": Dh,
+                   "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (q/k/v 3.07 GB vs 126 MB L2), no flush",
+                   "plan": info, "plan_ms": round(plan_ms, 3),
+                   "generate_s": round(t_gen, 1)},
+        "hbm_gbs": achieved,
+        "hbm_frac_of_peak": achieved / hbm_peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic,
+                     "kernel": "fused_engine_kernel<bf16,2,32,4>",
+                     "algorithmic_bytes_per_launch": alg,
+                     "kernel_ms": kern_ms, "peak_kind": f"{peak_kind} (burst copy)",
+                     "unique_byte_frac": fused_unique_bytes(n, n, E, H, Dh) /
+                                         (kern_ms * 1e-3) / 1e9 / hbm_peak},
+        "e2e": {"value": world * E * H / (e2e_ms * 1e-3), "unit": "edge-heads/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    return res, d
+
+
+def bench_reference(args, rank, world):
+    """--impl reference: the fp64 oracle, timed per step on a bounded sample."""
+    d = W.make_fused(seed=3)
+    import oracle
+    oracle.build()
+    rp = d["row_ptr"]
+    block = args.ref_rows
+    n = rp.size - 1
+
+    def step(i):
+        r0 = (i * block) % n
+        sel = np.arange(r0, min(n, r0 + block))
+        oracle.fused_layer(rp, d["col_idx"], d["q"], d["k"], d["v"], d["H"], d["Dh"],
+                           d["scale"], rows=sel)
+        return int(rp[sel[-1] + 1] - rp[sel[0]])
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    edges = sum(step(args.warmup + i) for i in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = edges * d["H"] / dt
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "edge-heads/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "fused GAT layer: 1e6 rows, Zipf(2.1) in-degrees clipped to "
+                               "[1,4096] rescaled to mean 16, col_idx uniform sorted in-row, "
+                               "H=8, Dh=64, q/k/v bf16 N(0,1), seed 3",
+                   "sample_rows_per_step": block},
+        "cpu_baseline": {"value": value, "unit": "edge-heads/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} steps of {block} consecutive rows each "
+                                   f"({edges} edges), fp64 C loops, single thread"},
+        "e2e": {"value": value, "unit": "edge-heads/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------
+# the smaller workloads (parity-test cases; timed here for the record)
+# ----------------------------------------------------------------------------
+def bench_small(name, args):
+    import torch
+    import sparse_graph_attention_head_gb300 as gat
+    dev = torch.device("cuda", 0)
+    g = W.WORKLOADS[name][0]()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    if name == "edge_softmax":
+        rp, s = t(g["row_ptr"]), t(g["scores"])
+        out = torch.empty_like(s)
+        fn = lambda: gat.gat_edge_softmax(rp, s, g["H"], out=out)  # noqa: E731
+        units, launches = g["n_edges"] * g["H"], 1
+    elif name == "aggregate":
+        rp, ci, s = t(g["row_ptr"]), t(g["col_idx"]), t(g["scores"]).reshape(-1, 1)
+        vals = t(g["values"]).reshape(g["n_src"], 1, g["F"])
+        w = torch.empty_like(s)
+        out = torch.empty((g["n_rows"], 1, g["F"]), device=dev)
+
+        def fn():
+            gat.gat_edge_softmax(rp, s, 1, out=w)
+            gat.gat_spmm_weighted(rp, ci, w, vals, 1, g["F"], out=out)
+        units, launches = g["n_edges"], 2
+    elif name == "sddmm":
+        si, di, a, b = t(g["src_idx"]), t(g["dst_idx"]), t(g["src_feat"]), t(g["dst_feat"])
+        out = torch.empty((g["n_edges"], 1), device=dev)
+        fn = lambda: gat.gat_sddmm(si, a, b, 1, g["F"], dst_idx=di, out=out)  # noqa: E731
+        units, launches = g["n_edges"], 1
+    elif name == "dense":
+        keys = ("nodes", "pair_feats", "edge_mask", "ln_w", "ln_b", "Wq", "Wk", "Wv", "W1",
+                "b1", "W2", "b2", "Wout")
+        tt = {k: t(g[k]) for k in keys}
+        out = torch.empty_like(tt["nodes"])
+        wk = [tt[k] for k in keys[5:]]
+        fn = lambda: gat.gat_dense_masked_attention(  # noqa: E731
+            tt["nodes"], tt["pair_feats"], tt["edge_mask"], tt["ln_w"], tt["ln_b"],
+            g["ln_eps"], *wk, H=g["H"], out=out)
+        units, launches = g["B"] * g["H"] * g["N"] * g["N"], 1
+    else:
+        raise ValueError(name)
+    for _ in range(max(3, args.warmup)):
+        fn()
+    torch.cuda.synchronize()
+    reps = 50
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    return {"ms_per_step": ms, "units_per_s": units / (ms * 1e-3), "launches_per_step": launches,
+            "warm": True}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gat", choices=["gat", "reference"])
+    ap.add_argument("--workload", default="fused",
+                    choices=["fused", "edge_softmax", "aggregate", "sddmm", "dense"])
+    ap.add_argument("--ref-rows", type=int, default=16000)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-extras", action="store_true", help="skip the smaller workloads")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(bench_reference(args, rank, world)), flush=True)
+        return
+
+    dist = dist_init(world, "nccl")
+    if args.workload != "fused":
+        if rank == 0:
+            print(json.dumps({"workload": args.workload, **bench_small(args.workload, args)}))
+        return
+    res, d = bench_fused(args, rank, world, local, dist)
+    if rank == 0:
+        if not args.no_extras:
+            res["other_workloads"] = {nm: bench_small(nm, args)
+                                      for nm in ("edge_softmax", "aggregate", "sddmm", "dense")}
+        res["cpu_baseline"] = cpu_baseline_fused(d, budget_s=args.cpu_budget)
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

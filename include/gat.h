@@ -1,0 +1,242 @@
+/*
+ * gat.h - C ABI of libgat, multi-head graph attention over CSR graphs on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the problem statements of five POPCORNBENCH
+ * transcripts, each about replacing a small PyTorch reference model:
+ *   [softmax page]   FW-GLM-5-1 l1_p6  - multi-head row-wise softmax over CSR edge scores
+ *   [aggregate page] Kimi-K2.6 l2_p37  - CSR softmax + neighbourhood aggregation
+ *   [spmm page]      FW-GLM-5-1 l1_p18 - multi-head weighted sparse aggregation
+ *   [block page]     Kimi-K2.6 l2_p4   - scene-graph relation attention block
+ *   [sddmm page]     FW-GLM-5-1 l1_p10 - edge-only SDDMM (gathered dot product)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Graphs: row_ptr is int32 [n_rows + 1], non-decreasing, row_ptr[0] = 0,
+ *   row_ptr[n_rows] = n_edges; row i owns edges [row_ptr[i], row_ptr[i+1]).
+ *   col_idx is int32 [n_edges] with 0 <= col_idx[e] < n_src. Row i is the
+ *   destination, col_idx[e] the source of edge e. Duplicate edges are allowed
+ *   and count separately; col_idx need not be sorted.
+ * - Per-edge tensors are [n_edges, H] row-major (heads contiguous per edge).
+ *   Node tensors are [n, H, Dh] row-major. Offsets are computed in 64 bits.
+ * - Every data pointer is DEVICE memory owned by the caller, aligned to at
+ *   least its element size. 16-byte aligned pointers with 16-byte rows per
+ *   head (Dh * element size a multiple of 16) take the vectorised kernels;
+ *   other layouts take a scalar kernel with the same semantics.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream). Every call only enqueues work on it and returns; results are
+ *   ready when the stream reaches that point. Calls never synchronise the
+ *   device, except gat_plan_create, which does (see there).
+ * - No entry point allocates device memory except gat_plan_create.
+ * - Errors: arguments the host can check (NULL pointers, negative sizes,
+ *   unsupported shapes, a plan built for another graph shape, a too-small
+ *   workspace) return an error code before anything is launched. A failed
+ *   launch returns GAT_ERR_CUDA; gat_last_error() then describes it. Device
+ *   contents of row_ptr/col_idx are NOT checked by the compute calls: an index
+ *   out of range is undefined behaviour there; call gat_validate_graph first
+ *   when the graph is untrusted.
+ * - Results are deterministic: no floating-point atomics; every reduction
+ *   runs in a fixed order, so repeated calls give bitwise-identical outputs.
+ * - Thread safety: calls on different streams may run concurrently, except
+ *   that one plan must not be used by two gat_fused_layer calls whose work
+ *   overlaps on the GPU (it holds per-row arrival counters).
+ */
+#ifndef GAT_H
+#define GAT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GAT_OK = 0,
+    GAT_ERR_INVALID_ARG = 1,        /* NULL pointer, negative size, inconsistent sizes */
+    GAT_ERR_UNSUPPORTED = 2,        /* shape or dtype this build does not implement */
+    GAT_ERR_CUDA = 3,               /* a CUDA runtime call or kernel launch failed */
+    GAT_ERR_WORKSPACE = 4,          /* workspace missing or too small */
+    GAT_ERR_INDEX_OUT_OF_RANGE = 5, /* gat_validate_graph found a bad row_ptr/col_idx */
+    GAT_ERR_PLAN_MISMATCH = 6       /* plan built for a different n_rows / n_edges */
+} gat_status_t;
+
+typedef enum {
+    GAT_F32 = 0, /* IEEE binary32 */
+    GAT_BF16 = 1 /* bfloat16; arithmetic is fp32, results rounded to nearest even */
+} gat_dtype_t;
+
+/* Opaque degree-bucket plan; owns a few device arrays (see gat_plan_create). */
+typedef struct gat_plan_s *gat_plan_t;
+
+/* Human-readable name of a status code (static storage). */
+const char *gat_status_string(gat_status_t status);
+
+/* Detail of the last error returned on the calling host thread (thread-local
+ * storage, valid until the next call on that thread). */
+const char *gat_last_error(void);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int32_t gat_version(void);
+
+/* ------------------------------------------------------------------------
+ * Degree-bucket plan
+ *
+ * The pages assign one thread, warp or block to a destination row; that
+ * choice is a load-balance question on a power-law graph. The plan sorts rows
+ * into two classes once per graph and is reused by every call on that graph:
+ *   light rows  deg <= heavy_threshold: one warp per row
+ *   heavy rows  deg >  heavy_threshold: cut into chunks of chunk_edges edges;
+ *               gat_fused_layer runs one warp per chunk and merges the chunks'
+ *               softmax states; gat_edge_softmax and gat_spmm_weighted run one
+ *               thread block per heavy row.
+ * Plan arrays (device, int32):
+ *   heavy_rows  [n_heavy]     ascending row ids with deg > heavy_threshold
+ *   chunk_start [n_heavy + 1] exclusive prefix sum of ceil(deg / chunk_edges)
+ *   chunk_row   [n_chunks]    index into heavy_rows of each chunk's row
+ * Chunk c of heavy_rows[r] covers edges [row_ptr[row] + j*chunk_edges,
+ * min(row_ptr[row] + (j+1)*chunk_edges, row_ptr[row+1])), j = c - chunk_start[r].
+ * ---------------------------------------------------------------------- */
+
+/* Build a plan for the graph `row_ptr` (device, [n_rows+1]).
+ * heavy_threshold <= 0 and chunk_edges <= 0 select the defaults (64, 64).
+ * Allocates the plan's device arrays (cudaMalloc), runs three small kernels on
+ * `stream` and synchronises `stream` once to read the class sizes back.
+ * Errors: GAT_ERR_INVALID_ARG (NULL row_ptr/plan, n_rows < 0, n_edges < 0),
+ * GAT_ERR_CUDA (allocation or launch failure; *plan is then NULL). */
+gat_status_t gat_plan_create(const int32_t *row_ptr, int64_t n_rows, int64_t n_edges,
+                             int32_t heavy_threshold, int32_t chunk_edges, void *stream,
+                             gat_plan_t *plan);
+
+/* Free a plan and its device arrays (NULL is accepted). The caller must make
+ * sure no enqueued work still uses it. */
+gat_status_t gat_plan_destroy(gat_plan_t plan);
+
+/* Sizes and parameters of a plan; any output pointer may be NULL. */
+gat_status_t gat_plan_info(gat_plan_t plan, int64_t *n_rows, int64_t *n_edges,
+                           int32_t *heavy_threshold, int32_t *chunk_edges,
+                           int64_t *n_heavy, int64_t *n_chunks);
+
+/* Copy the plan arrays into caller device buffers of sizes n_heavy,
+ * n_heavy + 1 and n_chunks (any pointer may be NULL to skip that array).
+ * Enqueued on `stream`. */
+gat_status_t gat_plan_export(gat_plan_t plan, int32_t *heavy_rows, int32_t *chunk_start,
+                             int32_t *chunk_row, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Graph validation (optional, for untrusted graphs)
+ *
+ * Checks on the device that row_ptr[0] == 0, row_ptr is non-decreasing,
+ * row_ptr[n_rows] == n_edges and 0 <= col_idx[e] < n_src (col_idx may be NULL
+ * to skip that check). Synchronises `stream`. Returns GAT_OK or
+ * GAT_ERR_INDEX_OUT_OF_RANGE; never traps. `flag` is caller device scratch of
+ * one int32 (its content is overwritten).
+ * ---------------------------------------------------------------------- */
+gat_status_t gat_validate_graph(const int32_t *row_ptr, const int32_t *col_idx,
+                                int64_t n_rows, int64_t n_src, int64_t n_edges,
+                                int32_t *flag, void *stream);
+
+/* ------------------------------------------------------------------------
+ * SDDMM [sddmm page, reference model: gather both endpoint feature rows of
+ * every edge, multiply elementwise, sum over the feature dimension],
+ * generalised to heads and a scale:
+ *     out[e,h] = scale * sum_{d<Dh} src_feat[src(e),h,d] * dst_feat[dst(e),h,d]
+ * COO form (row_ptr == NULL): src(e) = src_idx[e], dst(e) = dst_idx[e],
+ *   n_rows is ignored.
+ * CSR form (row_ptr != NULL): dst(e) = the row that owns e, src(e) = src_idx[e]
+ *   (the column index); dst_idx is ignored and n_dst must be >= n_rows.
+ * src_feat [n_src,H,Dh] and dst_feat [n_dst,H,Dh] share `dtype`; out is fp32
+ * [n_edges,H]. n_edges == 0 is a no-op.
+ * Errors: GAT_ERR_INVALID_ARG for NULL pointers (with n_edges > 0), negative
+ * sizes, H < 1 or Dh < 1; GAT_ERR_UNSUPPORTED for an unknown dtype.
+ * ---------------------------------------------------------------------- */
+gat_status_t gat_sddmm(const int32_t *row_ptr, const int32_t *src_idx, const int32_t *dst_idx,
+                       int64_t n_rows, int64_t n_edges, const void *src_feat, int64_t n_src,
+                       const void *dst_feat, int64_t n_dst, int32_t H, int32_t Dh, float scale,
+                       gat_dtype_t dtype, float *out, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Segmented edge softmax [softmax page, reference model: for every node,
+ * softmax over that node's CSR edge range, independently per head]:
+ *     out[e,h] = exp(s[e,h] - m) / sum_{e' in row} exp(s[e',h] - m),
+ *     m = max_{e' in row} s[e',h]
+ * scores/out are fp32 [n_edges,H]; out may alias scores (in place). Rows of
+ * degree 0 own no entries and write nothing. A row whose scores are all -inf
+ * yields NaN, as the reference softmax does. `plan` may be NULL (every row is
+ * handled by one warp) or a plan of this graph (heavy rows get a thread block).
+ * Errors: GAT_ERR_INVALID_ARG, GAT_ERR_PLAN_MISMATCH.
+ * ---------------------------------------------------------------------- */
+gat_status_t gat_edge_softmax(const int32_t *row_ptr, int64_t n_rows, int64_t n_edges, int32_t H,
+                              const float *scores, float *out, gat_plan_t plan, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Weighted SpMM [spmm page, reference model: each destination sums the
+ * per-edge, per-head weight times the source node's feature row;
+ * aggregate page: a zero-degree destination stays zero]:
+ *     out[i,h,d] = sum_{e in row i} w[e,h] * feat[col_idx[e],h,d]
+ * w is fp32 [n_edges,H]; feat [n_src,H,Dh] and out [n_rows,H,Dh] share
+ * `dtype` (fp32 accumulation). Zero-degree rows are written as zeros.
+ * The aggregate page's operation (softmax of per-edge scores, then this sum)
+ * is gat_edge_softmax followed by gat_spmm_weighted with H = 1.
+ * `plan` may be NULL or a plan of this graph.
+ * Errors: GAT_ERR_INVALID_ARG, GAT_ERR_UNSUPPORTED, GAT_ERR_PLAN_MISMATCH.
+ * ---------------------------------------------------------------------- */
+gat_status_t gat_spmm_weighted(const int32_t *row_ptr, const int32_t *col_idx, int64_t n_rows,
+                               int64_t n_src, int64_t n_edges, int32_t H, int32_t Dh,
+                               const float *w, const void *feat, gat_dtype_t dtype, void *out,
+                               gat_plan_t plan, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Fused multi-head graph-attention layer: SDDMM -> segmented softmax ->
+ * weighted SpMM in one pass (the composition of the sddmm, softmax and spmm
+ * pages' operations), with the softmax kept online so no score or weight
+ * ever reaches memory:
+ *     s[e,h]     = scale * sum_d q[i,h,d] * k[col_idx[e],h,d]
+ *     out[i,h,:] = sum_e softmax_e(s[.,h])[e] * v[col_idx[e],h,:]
+ *     out[i,:,:] = 0 for a zero-degree row i
+ * q/out are [n_rows,H,Dh], k/v are [n_src,H,Dh], all in `dtype` (fp32
+ * arithmetic, bf16 results rounded to nearest even).
+ * plan: NULL (every row by one warp; workspace unused) or a plan of this
+ * graph (heavy rows split into chunks whose partial softmax states go to
+ * `workspace` and are merged by the last chunk to finish).
+ * workspace: caller device memory, 16-byte aligned, at least the size
+ * reported by gat_fused_layer_workspace_size (may be NULL when that is 0).
+ * Errors: GAT_ERR_INVALID_ARG, GAT_ERR_UNSUPPORTED, GAT_ERR_PLAN_MISMATCH,
+ * GAT_ERR_WORKSPACE.
+ * ---------------------------------------------------------------------- */
+gat_status_t gat_fused_layer_workspace_size(gat_plan_t plan, int32_t H, int32_t Dh,
+                                            size_t *bytes);
+
+gat_status_t gat_fused_layer(const int32_t *row_ptr, const int32_t *col_idx, int64_t n_rows,
+                             int64_t n_src, int64_t n_edges, int32_t H, int32_t Dh, float scale,
+                             const void *q, const void *k, const void *v, gat_dtype_t dtype,
+                             void *out, gat_plan_t plan, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/* ------------------------------------------------------------------------
+ * Dense-masked small-graph attention block [block page, reference model],
+ * all fp32, per graph b of B:
+ *     xn    = LayerNorm(x; ln_w, ln_b, ln_eps)      biased variance, per node
+ *     Q,K,V = xn Wq^T, xn Wk^T, xn Wv^T             Wq/Wk/Wv [D,D] (out x in), no bias
+ *     r     = W2 SiLU(W1 pair[i,j] + b1) + b2       W1 [P,P], b1 [P], W2 [H,P], b2 [H]
+ *     logit = Q_i^h . K_j^h / sqrt(D/H) + r[h];  -inf where edge_mask[i,j] < 0.5
+ *     ctx   = softmax_j(logit) V^h                  (an all -inf row gives NaN)
+ *     out   = x + ctx Wout^T                        Wout [D,D], no bias
+ * nodes/out [B,N,D], pair_feats [B,N,N,P], edge_mask [B,N,N] (float 0/1).
+ * Head h owns feature dims [h*D/H, (h+1)*D/H). out must not alias nodes.
+ * Supported: 1 <= N <= 32, D % H == 0, D/H <= 32, D <= 128, D % 4 == 0,
+ * 1 <= P <= 32, 16-byte aligned pointers; else GAT_ERR_UNSUPPORTED.
+ * ---------------------------------------------------------------------- */
+gat_status_t gat_dense_masked_attention(int32_t B, int32_t N, int32_t D, int32_t H, int32_t P,
+                                        const float *nodes, const float *pair_feats,
+                                        const float *edge_mask, const float *ln_w,
+                                        const float *ln_b, float ln_eps, const float *Wq,
+                                        const float *Wk, const float *Wv, const float *W1,
+                                        const float *b1, const float *W2, const float *b2,
+                                        const float *Wout, float *out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GAT_H */

@@ -1,0 +1,145 @@
+// common.cuh - internal helpers shared by the libgat translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gat.h"
+
+namespace gat {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---------------------------------------------------------------------------
+// host-side error reporting (thread-local detail string, see gat_last_error)
+// ---------------------------------------------------------------------------
+gat_status_t fail(gat_status_t st, const char *fmt, ...);
+gat_status_t cuda_fail(cudaError_t err, const char *what);
+gat_status_t check_launch(const char *what);
+
+// ---------------------------------------------------------------------------
+// plan (host object)
+// ---------------------------------------------------------------------------
+}  // namespace gat
+
+struct gat_plan_s {
+    int64_t n_rows = 0, n_edges = 0;
+    int32_t heavy_threshold = 0, chunk_edges = 0;
+    int64_t n_heavy = 0, n_chunks = 0;
+    int64_t heavy_edges = 0;         // edges owned by heavy rows
+    int32_t *heavy_rows = nullptr;   // [n_heavy]
+    int32_t *chunk_start = nullptr;  // [n_heavy + 1]
+    int32_t *chunk_row = nullptr;    // [n_chunks]
+    int32_t *counters = nullptr;     // [n_heavy], arrival counters, zero between calls
+    int device = 0;
+};
+
+namespace gat {
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, o));
+    return x;
+}
+
+// 16-byte global load that bypasses L1 allocation (read-once gathers).
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// 16-byte global load through L2 only (data written earlier in the same
+// kernel by another SM: must not be served from a stale L1 line).
+__device__ __forceinline__ float4 ld_cg_f4(const float *p) {
+    return __ldcg(reinterpret_cast<const float4 *>(p));
+}
+
+// 16-byte streaming store (evict-first; the output is not re-read).
+__device__ __forceinline__ void st_stream16(void *p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Elements of a 16-byte vector as fp32.
+template <typename T>
+struct Vec;
+
+template <>
+struct Vec<float> {
+    static constexpr int N = 4;
+    __device__ __forceinline__ static void unpack(const uint4 &u, float *f) {
+        f[0] = __uint_as_float(u.x);
+        f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z);
+        f[3] = __uint_as_float(u.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float *f) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+    }
+};
+
+// bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 bits.
+template <>
+struct Vec<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ __forceinline__ static void unpack(const uint4 &u, float *f) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    __device__ __forceinline__ static uint4 pack(const float *f) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
+// Scalar element access for the non-vector kernels.
+__device__ __forceinline__ float load_elem(const float *p, int64_t i) { return __ldg(p + i); }
+__device__ __forceinline__ float load_elem(const __nv_bfloat16 *p, int64_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void store_elem(float *p, int64_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void store_elem(__nv_bfloat16 *p, int64_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Multiprocessor count of the current device (cached per device ordinal).
+inline int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 1;
+    }
+    return cache[dev];
+}
+
+}  // namespace gat

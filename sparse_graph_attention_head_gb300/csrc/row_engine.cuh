@@ -1,0 +1,481 @@
+// row_engine.cuh - the gather/aggregate engine behind gat_fused_layer and
+// gat_spmm_weighted.
+//
+// Layout of the work: one warp owns one destination row (or one fixed-size
+// edge chunk of a heavy row). The row's H*Dh features are spread over the
+// warp's lanes in 16-byte vectors, so every gathered feature row of a source
+// node is read as full, coalesced 16-byte accesses (the float4 idea of the
+// spmm page's vectorised draft, taken to bf16 and to all heads at once).
+//
+//   LE == 32: a row has V*32 vectors; lane l owns vectors l, l+32, ...,
+//             l+32(V-1) ("slots"); the warp walks the row's edges one by one.
+//   LE <  32: a row has LE vectors (V == 1); the warp is split into 32/LE
+//             edge subgroups, each walking every (32/LE)-th edge, and the
+//             subgroups' states are merged at the end of the row.
+// A head's Dh elements are G = Dh/VE consecutive vectors, i.e. G adjacent
+// lanes of one slot, so a per-head dot product is a G-lane xor-shuffle sum.
+//
+// Fused mode (SDDMM -> softmax -> SpMM, single pass): the score of each edge
+// is formed in registers and folded into an online softmax state (m, l, acc)
+// per head: m' = max(m, s), c = 2^(m-m'), l = l c + 2^(s-m'),
+// acc = acc c + 2^(s-m') v. Scores are pre-scaled by log2(e) so the
+// exponentials are exp2. Nothing per edge ever reaches memory.
+// SpMM mode: acc += w[e,h] * feat[src].
+//
+// Heavy rows (fused mode, with a plan) arrive as chunks; each chunk warp
+// writes its (m, l, acc) to a workspace slot, and the warp that finishes a
+// row's last chunk (arrival counter) merges all of that row's chunk states in
+// chunk order - deterministic, and without any spin-wait.
+#pragma once
+
+#include <climits>
+
+#include "common.cuh"
+
+namespace gat {
+
+constexpr int kEngineThreads = 256;  // 8 warps per block
+
+struct EngineParams {
+    const int32_t *row_ptr;
+    const int32_t *col_idx;
+    const void *q;    // fused: [n_rows, H, Dh]
+    const void *k;    // fused: [n_src, H, Dh]
+    const void *v;    // [n_src, H, Dh] (fused: values; spmm: features)
+    const float *w;   // spmm: [n_edges, H]
+    void *out;        // [n_rows, H, Dh]
+    int64_t n_rows;
+    int32_t H, Dh;
+    float qscale;     // fused: scale * log2(e)
+    // light/heavy split (no plan: heavy_threshold = INT_MAX, n_chunks = 0)
+    int32_t heavy_threshold;
+    int32_t chunk_edges;
+    int64_t n_chunks;
+    const int32_t *heavy_rows;
+    const int32_t *chunk_start;
+    const int32_t *chunk_row;
+    int32_t *counters;
+    float *partials;       // [n_chunks][slot_floats]
+    int64_t slot_floats;   // >= H*Dh + 2H, multiple of 4
+    // spmm heavy-row kernel: list of rows handled one block per row
+    int64_t n_block_rows;
+};
+
+// Vector-engine shape selection (shared by the fused layer and the SpMM):
+// V vectors per lane and LE lanes per edge for H heads of Dh elements of
+// elem_bytes each; false when the shape needs the scalar fallback.
+bool engine_shape(int H, int Dh, int elem_bytes, int &V, int &LE);
+
+// Bytes-per-chunk-slot helper: floats in one chunk state (acc, m, l), padded
+// to a multiple of four.
+int64_t slot_floats(int H, int Dh);
+
+// Grid size for a persistent kernel: at most `want` blocks, at most as many
+// as can be resident on the device at once.
+template <typename K>
+inline int64_t persistent_blocks(K kernel, int64_t want) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kEngineThreads, 0) !=
+            cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    if (want > cap) want = cap;
+    return want < 1 ? 1 : want;
+}
+
+template <typename T, int V, int LE>
+struct Lanes {
+    static constexpr int VE = Vec<T>::N;
+    static constexpr int ES = 32 / LE;  // edge subgroups per warp
+    int lane, sub, vi[V], head[V], G;
+    __device__ __forceinline__ Lanes(int Dh) {
+        lane = threadIdx.x & 31;
+        sub = lane / LE;
+        G = Dh / VE;
+#pragma unroll
+        for (int s = 0; s < V; ++s) {
+            vi[s] = (LE == 32) ? s * 32 + lane : (lane % LE);
+            head[s] = vi[s] / G;
+        }
+    }
+};
+
+// Edge range of one work item; returns false when the item is skipped.
+__device__ __forceinline__ bool item_range(const EngineParams &p, int64_t item, int64_t &row,
+                                           int &e0, int &e1, int &hr, int64_t &chunk) {
+    if (item < p.n_chunks) {
+        chunk = item;
+        hr = __ldg(p.chunk_row + chunk);
+        row = __ldg(p.heavy_rows + hr);
+        const int j = (int)(chunk - __ldg(p.chunk_start + hr));
+        const int rs = __ldg(p.row_ptr + row), re = __ldg(p.row_ptr + row + 1);
+        e0 = rs + j * p.chunk_edges;
+        e1 = min(e0 + p.chunk_edges, re);
+        return true;
+    }
+    chunk = -1;
+    hr = -1;
+    row = item - p.n_chunks;
+    e0 = __ldg(p.row_ptr + row);
+    e1 = __ldg(p.row_ptr + row + 1);
+    return (e1 - e0) <= p.heavy_threshold;
+}
+
+// ---------------------------------------------------------------------------
+// fused mode
+// ---------------------------------------------------------------------------
+template <typename T, int V, int LE, int U>
+struct FusedRow {
+    using L = Lanes<T, V, LE>;
+    static constexpr int VE = L::VE;
+    static constexpr int ES = L::ES;
+    float qf[V][VE];
+    float acc[V][VE];
+    float m[V], l[V];
+
+    __device__ __forceinline__ void load_q(const EngineParams &p, const L &ln, int64_t row) {
+        const char *qrow = static_cast<const char *>(p.q) + row * (int64_t)p.H * p.Dh * sizeof(T);
+#pragma unroll
+        for (int s = 0; s < V; ++s) {
+            uint4 u = ld_stream16(qrow + ln.vi[s] * 16);
+            Vec<T>::unpack(u, qf[s]);
+#pragma unroll
+            for (int t = 0; t < VE; ++t) qf[s][t] *= p.qscale;
+        }
+    }
+
+    __device__ __forceinline__ void run(const EngineParams &p, const L &ln, int e0, int e1) {
+#pragma unroll
+        for (int s = 0; s < V; ++s) {
+            m[s] = -INFINITY;
+            l[s] = 0.f;
+#pragma unroll
+            for (int t = 0; t < VE; ++t) acc[s][t] = 0.f;
+        }
+        const int64_t row_bytes = (int64_t)p.H * p.Dh * sizeof(T);
+        const char *kb = static_cast<const char *>(p.k);
+        const char *vb = static_cast<const char *>(p.v);
+        for (int base = e0; base < e1; base += 32) {
+            const int n = min(32, e1 - base);
+            const int my_ci = ln.lane < n ? __ldg(p.col_idx + base + ln.lane) : 0;
+            for (int j0 = 0; j0 < n; j0 += U * ES) {
+                uint4 kr[U][V], vr[U][V];
+                bool valid[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int j = j0 + u * ES + ln.sub;
+                    valid[u] = j < n;
+                    const int64_t src = __shfl_sync(kFull, my_ci, j & 31);
+                    if (valid[u]) {
+#pragma unroll
+                        for (int s = 0; s < V; ++s) {
+                            kr[u][s] = ld_stream16(kb + src * row_bytes + ln.vi[s] * 16);
+                            vr[u][s] = ld_stream16(vb + src * row_bytes + ln.vi[s] * 16);
+                        }
+                    } else {
+#pragma unroll
+                        for (int s = 0; s < V; ++s) {
+                            kr[u][s] = make_uint4(0, 0, 0, 0);
+                            vr[u][s] = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                }
+                float sc[U][V];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int s = 0; s < V; ++s) {
+                        float kf[VE];
+                        Vec<T>::unpack(kr[u][s], kf);
+                        float d = 0.f;
+#pragma unroll
+                        for (int t = 0; t < VE; ++t) d = fmaf(qf[s][t], kf[t], d);
+                        sc[u][s] = d;
+                    }
+                // per-head sums over the head's G lanes (uniform across the warp)
+                for (int o = 1; o < ln.G; o <<= 1) {
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+#pragma unroll
+                        for (int s = 0; s < V; ++s) sc[u][s] += __shfl_xor_sync(kFull, sc[u][s], o);
+                }
+#pragma unroll
+                for (int s = 0; s < V; ++s) {
+                    float mx = m[s];
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (valid[u]) mx = fmaxf(mx, sc[u][s]);
+                    if (mx == -INFINITY) continue;  // no edge for this subgroup yet
+                    const float c = exp2f(m[s] - mx);
+                    l[s] *= c;
+#pragma unroll
+                    for (int t = 0; t < VE; ++t) acc[s][t] *= c;
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const float pe = valid[u] ? exp2f(sc[u][s] - mx) : 0.f;
+                        l[s] += pe;
+                        float vf[VE];
+                        Vec<T>::unpack(vr[u][s], vf);
+#pragma unroll
+                        for (int t = 0; t < VE; ++t) acc[s][t] = fmaf(pe, vf[t], acc[s][t]);
+                    }
+                    m[s] = mx;
+                }
+            }
+        }
+        // merge the edge subgroups' states (LE < 32)
+#pragma unroll
+        for (int o = LE; o < 32; o <<= 1) {
+#pragma unroll
+            for (int s = 0; s < V; ++s) {
+                const float m2 = __shfl_xor_sync(kFull, m[s], o);
+                const float l2 = __shfl_xor_sync(kFull, l[s], o);
+                float a2[VE];
+#pragma unroll
+                for (int t = 0; t < VE; ++t) a2[t] = __shfl_xor_sync(kFull, acc[s][t], o);
+                const float mx = fmaxf(m[s], m2);
+                if (mx == -INFINITY) continue;
+                const float c1 = exp2f(m[s] - mx), c2 = exp2f(m2 - mx);
+                l[s] = l[s] * c1 + l2 * c2;
+#pragma unroll
+                for (int t = 0; t < VE; ++t) acc[s][t] = acc[s][t] * c1 + a2[t] * c2;
+                m[s] = mx;
+            }
+        }
+    }
+
+    __device__ __forceinline__ void store_out(const EngineParams &p, const L &ln, int64_t row) {
+        if (ln.sub != 0) return;
+        char *orow = static_cast<char *>(p.out) + row * (int64_t)p.H * p.Dh * sizeof(T);
+#pragma unroll
+        for (int s = 0; s < V; ++s) {
+            const float inv = l[s] > 0.f ? 1.f / l[s] : 0.f;
+            float o[VE];
+#pragma unroll
+            for (int t = 0; t < VE; ++t) o[t] = acc[s][t] * inv;
+            st_stream16(orow + ln.vi[s] * 16, Vec<T>::pack(o));
+        }
+    }
+
+    // chunk of a heavy row: publish the state; the last chunk merges the row
+    __device__ __forceinline__ void chunk_epilogue(const EngineParams &p, const L &ln, int64_t row,
+                                                   int hr, int64_t chunk) {
+        const int HD = p.H * p.Dh;
+        if (ln.sub == 0) {
+            float *slot = p.partials + chunk * p.slot_floats;
+#pragma unroll
+            for (int s = 0; s < V; ++s) {
+                float *a = slot + ln.vi[s] * VE;
+#pragma unroll
+                for (int t = 0; t < VE; t += 4)
+                    __stcg(reinterpret_cast<float4 *>(a + t),
+                           make_float4(acc[s][t], acc[s][t + 1], acc[s][t + 2], acc[s][t + 3]));
+                if (ln.vi[s] % ln.G == 0) {
+                    __stcg(slot + HD + ln.head[s], m[s]);
+                    __stcg(slot + HD + p.H + ln.head[s], l[s]);
+                }
+            }
+        }
+        __threadfence();
+        __syncwarp();
+        int old = 0;
+        if (ln.lane == 0) old = atomicAdd(p.counters + hr, 1);
+        old = __shfl_sync(kFull, old, 0);
+        const int c0 = __ldg(p.chunk_start + hr), c1 = __ldg(p.chunk_start + hr + 1);
+        if (old != c1 - c0 - 1) return;  // not the last chunk of this row
+        __threadfence();
+        // merge all chunk states of the row in chunk order
+#pragma unroll
+        for (int s = 0; s < V; ++s) {
+            m[s] = -INFINITY;
+            l[s] = 0.f;
+#pragma unroll
+            for (int t = 0; t < VE; ++t) acc[s][t] = 0.f;
+        }
+        for (int c = c0; c < c1; ++c) {
+            const float *slot = p.partials + (int64_t)c * p.slot_floats;
+#pragma unroll
+            for (int s = 0; s < V; ++s) {
+                const float mc = __ldcg(slot + HD + ln.head[s]);
+                const float lc = __ldcg(slot + HD + p.H + ln.head[s]);
+                float ac[VE];
+#pragma unroll
+                for (int t = 0; t < VE; t += 4) {
+                    float4 f = ld_cg_f4(slot + ln.vi[s] * VE + t);
+                    ac[t] = f.x;
+                    ac[t + 1] = f.y;
+                    ac[t + 2] = f.z;
+                    ac[t + 3] = f.w;
+                }
+                const float mx = fmaxf(m[s], mc);
+                if (mx == -INFINITY) continue;
+                const float a1 = exp2f(m[s] - mx), a2 = exp2f(mc - mx);
+                l[s] = l[s] * a1 + lc * a2;
+#pragma unroll
+                for (int t = 0; t < VE; ++t) acc[s][t] = acc[s][t] * a1 + ac[t] * a2;
+                m[s] = mx;
+            }
+        }
+        store_out(p, ln, row);
+        if (ln.lane == 0) p.counters[hr] = 0;  // ready for the next call
+    }
+};
+
+template <typename T, int V, int LE, int U>
+__global__ void __launch_bounds__(kEngineThreads)
+fused_engine_kernel(const EngineParams p) {
+    using L = Lanes<T, V, LE>;
+    const L ln(p.Dh);
+    FusedRow<T, V, LE, U> st;
+    const int64_t wpb = blockDim.x >> 5;
+    const int64_t n_warps = (int64_t)gridDim.x * wpb;
+    const int64_t n_items = p.n_chunks + p.n_rows;
+    for (int64_t item = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5); item < n_items;
+         item += n_warps) {
+        int64_t row, chunk;
+        int e0, e1, hr;
+        if (!item_range(p, item, row, e0, e1, hr, chunk)) continue;
+        st.load_q(p, ln, row);
+        st.run(p, ln, e0, e1);
+        if (chunk < 0)
+            st.store_out(p, ln, row);
+        else
+            st.chunk_epilogue(p, ln, row, hr, chunk);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// spmm mode
+// ---------------------------------------------------------------------------
+template <typename T, int V, int LE, int U>
+struct SpmmRow {
+    using L = Lanes<T, V, LE>;
+    static constexpr int VE = L::VE;
+    static constexpr int ES = L::ES;
+    float acc[V][VE];
+
+    // accumulate edges e0 + first, e0 + first + step, ... below e1 (step is
+    // a multiple of 32; the warp handles 32-edge tiles)
+    __device__ __forceinline__ void run(const EngineParams &p, const L &ln, int e0, int e1,
+                                        int tile0, int tile_step) {
+        const int64_t row_bytes = (int64_t)p.H * p.Dh * sizeof(T);
+        const char *fb = static_cast<const char *>(p.v);
+        for (int base = e0 + tile0 * 32; base < e1; base += tile_step * 32) {
+            const int n = min(32, e1 - base);
+            const int my_ci = ln.lane < n ? __ldg(p.col_idx + base + ln.lane) : 0;
+            for (int j0 = 0; j0 < n; j0 += U * ES) {
+                uint4 vr[U][V];
+                float wv[U][V];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int j = j0 + u * ES + ln.sub;
+                    const bool valid = j < n;
+                    const int64_t src = __shfl_sync(kFull, my_ci, j & 31);
+#pragma unroll
+                    for (int s = 0; s < V; ++s) {
+                        if (valid) {
+                            vr[u][s] = ld_stream16(fb + src * row_bytes + ln.vi[s] * 16);
+                            wv[u][s] = __ldg(p.w + (int64_t)(base + j) * p.H + ln.head[s]);
+                        } else {
+                            vr[u][s] = make_uint4(0, 0, 0, 0);
+                            wv[u][s] = 0.f;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int s = 0; s < V; ++s) {
+                        float vf[VE];
+                        Vec<T>::unpack(vr[u][s], vf);
+#pragma unroll
+                        for (int t = 0; t < VE; ++t) acc[s][t] = fmaf(wv[u][s], vf[t], acc[s][t]);
+                    }
+            }
+        }
+    }
+
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int s = 0; s < V; ++s)
+#pragma unroll
+            for (int t = 0; t < VE; ++t) acc[s][t] = 0.f;
+    }
+
+    __device__ __forceinline__ void merge_subgroups() {
+#pragma unroll
+        for (int o = LE; o < 32; o <<= 1)
+#pragma unroll
+            for (int s = 0; s < V; ++s)
+#pragma unroll
+                for (int t = 0; t < VE; ++t) acc[s][t] += __shfl_xor_sync(kFull, acc[s][t], o);
+    }
+
+    __device__ __forceinline__ void store_out(const EngineParams &p, const L &ln, int64_t row) {
+        if (ln.sub != 0) return;
+        char *orow = static_cast<char *>(p.out) + row * (int64_t)p.H * p.Dh * sizeof(T);
+#pragma unroll
+        for (int s = 0; s < V; ++s) st_stream16(orow + ln.vi[s] * 16, Vec<T>::pack(acc[s]));
+    }
+};
+
+// light rows (or every row without a plan): one warp per row
+template <typename T, int V, int LE, int U>
+__global__ void __launch_bounds__(kEngineThreads)
+spmm_engine_kernel(const EngineParams p) {
+    using L = Lanes<T, V, LE>;
+    const L ln(p.Dh);
+    SpmmRow<T, V, LE, U> st;
+    const int64_t wpb = blockDim.x >> 5;
+    const int64_t n_warps = (int64_t)gridDim.x * wpb;
+    for (int64_t row = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5); row < p.n_rows;
+         row += n_warps) {
+        const int e0 = __ldg(p.row_ptr + row), e1 = __ldg(p.row_ptr + row + 1);
+        if (e1 - e0 > p.heavy_threshold) continue;
+        st.zero();
+        st.run(p, ln, e0, e1, 0, 1);
+        st.merge_subgroups();
+        st.store_out(p, ln, row);
+    }
+}
+
+// heavy rows: one block per row; warp w takes 32-edge tiles w, w+8, ...;
+// the warps' sums are added in warp order through shared memory
+template <typename T, int V, int LE, int U>
+__global__ void __launch_bounds__(kEngineThreads)
+spmm_heavy_kernel(const EngineParams p) {
+    using L = Lanes<T, V, LE>;
+    constexpr int VE = L::VE;
+    constexpr int NW = kEngineThreads / 32;
+    __shared__ float red[NW][V * VE][32];
+    const L ln(p.Dh);
+    const int warp = threadIdx.x >> 5;
+    SpmmRow<T, V, LE, U> st;
+    for (int64_t b = blockIdx.x; b < p.n_block_rows; b += gridDim.x) {
+        const int64_t row = __ldg(p.heavy_rows + b);
+        const int e0 = __ldg(p.row_ptr + row), e1 = __ldg(p.row_ptr + row + 1);
+        st.zero();
+        st.run(p, ln, e0, e1, warp, NW);
+        st.merge_subgroups();
+#pragma unroll
+        for (int s = 0; s < V; ++s)
+#pragma unroll
+            for (int t = 0; t < VE; ++t) red[warp][s * VE + t][ln.lane] = st.acc[s][t];
+        __syncthreads();
+        if (warp == 0) {
+#pragma unroll
+            for (int s = 0; s < V; ++s)
+#pragma unroll
+                for (int t = 0; t < VE; ++t) {
+                    float a = red[0][s * VE + t][ln.lane];
+                    for (int w2 = 1; w2 < NW; ++w2) a += red[w2][s * VE + t][ln.lane];
+                    st.acc[s][t] = a;
+                }
+            st.store_out(p, ln, row);
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace gat

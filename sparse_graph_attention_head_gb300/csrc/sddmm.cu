@@ -1,0 +1,124 @@
+// sddmm.cu - gathered per-edge dot products (FW-GLM-5-1 l1_p10, reference
+// model: gather the two endpoint feature rows of every edge, multiply
+// elementwise, sum over the feature dimension), with heads and a scale.
+//
+// Work unit: one (edge, head) pair, handled by a group of G lanes; each lane
+// loads 16-byte vectors of both rows (coalesced across the group, the
+// warp-per-edge idea of the page's drafts narrowed to the head width) and the
+// group finishes with a xor-shuffle sum. Consecutive pairs of a warp are
+// consecutive heads of the same edge, so a warp reads whole feature rows.
+// CSR form: the destination row of an edge is found by binary search on
+// row_ptr.
+#include "common.cuh"
+
+namespace gat {
+
+constexpr int kSddmmThreads = 256;
+
+__device__ __forceinline__ int64_t row_of_edge(const int32_t *__restrict__ row_ptr, int64_t n_rows,
+                                               int64_t e) {
+    // largest r with row_ptr[r] <= e (rows of degree 0 are skipped over)
+    int64_t lo = 0, hi = n_rows;  // invariant: row_ptr[lo] <= e < row_ptr[hi]
+    while (hi - lo > 1) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (__ldg(row_ptr + mid) <= e)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+// VEC elements per load (16 bytes, or 1 for the scalar path); G lanes per pair
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kSddmmThreads)
+sddmm_kernel(const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ src_idx,
+             const int32_t *__restrict__ dst_idx, int64_t n_rows, int64_t n_edges,
+             const T *__restrict__ a, const T *__restrict__ b, int32_t H, int32_t Dh, float scale,
+             float *__restrict__ out, int G) {
+    const int lane = threadIdx.x & 31;
+    const int per_warp = 32 / G;
+    const int grp = lane / G, gl = lane % G;
+    const int64_t n_pairs = n_edges * H;
+    const int64_t wpb = blockDim.x >> 5;
+    const int64_t warp0 = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
+    const int64_t n_warps = (int64_t)gridDim.x * wpb;
+    const int nv = Dh / VEC;  // vectors per head row
+    for (int64_t pb = warp0 * per_warp; pb < n_pairs; pb += n_warps * per_warp) {
+        const int64_t pr = pb + grp;
+        const bool valid = pr < n_pairs;
+        float acc = 0.f;
+        if (valid) {
+            const int64_t e = pr / H;
+            const int h = (int)(pr - e * H);
+            const int64_t s = __ldg(src_idx + e);
+            const int64_t d = row_ptr ? row_of_edge(row_ptr, n_rows, e) : (int64_t)__ldg(dst_idx + e);
+            const T *ra = a + (s * H + h) * (int64_t)Dh;
+            const T *rb = b + (d * H + h) * (int64_t)Dh;
+            for (int t = gl; t < nv; t += G) {
+                if constexpr (VEC > 1) {
+                    float fa[VEC], fb[VEC];
+                    Vec<T>::unpack(ld_stream16(ra + t * VEC), fa);
+                    Vec<T>::unpack(ld_stream16(rb + t * VEC), fb);
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) acc = fmaf(fa[i], fb[i], acc);
+                } else {
+                    acc = fmaf(load_elem(ra, t), load_elem(rb, t), acc);
+                }
+            }
+        }
+        for (int o = 1; o < G; o <<= 1) acc += __shfl_xor_sync(kFull, acc, o);
+        if (valid && gl == 0) out[pr] = scale * acc;
+    }
+}
+
+template <typename T>
+static gat_status_t launch_sddmm(const int32_t *row_ptr, const int32_t *si, const int32_t *di,
+                                 int64_t n_rows, int64_t E, const void *a, const void *b,
+                                 int32_t H, int32_t Dh, float scale, float *out, cudaStream_t s) {
+    constexpr int VE = Vec<T>::N;
+    const bool vec = (Dh % VE == 0) && aligned16(a) && aligned16(b);
+    const int nv = vec ? Dh / VE : Dh;
+    int G = 1;
+    while (G < 32 && G * 2 <= nv) G *= 2;
+    const int64_t pairs = E * H;
+    const int64_t per_block = (int64_t)(kSddmmThreads / 32) * (32 / G);
+    int64_t blocks = (pairs + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    if (vec)
+        sddmm_kernel<T, VE><<<(unsigned)blocks, kSddmmThreads, 0, s>>>(
+            row_ptr, si, di, n_rows, E, static_cast<const T *>(a), static_cast<const T *>(b), H,
+            Dh, scale, out, G);
+    else
+        sddmm_kernel<T, 1><<<(unsigned)blocks, kSddmmThreads, 0, s>>>(
+            row_ptr, si, di, n_rows, E, static_cast<const T *>(a), static_cast<const T *>(b), H,
+            Dh, scale, out, G);
+    return check_launch("gat_sddmm");
+}
+
+}  // namespace gat
+
+using namespace gat;
+
+extern "C" gat_status_t gat_sddmm(const int32_t *row_ptr, const int32_t *src_idx,
+                                  const int32_t *dst_idx, int64_t n_rows, int64_t n_edges,
+                                  const void *src_feat, int64_t n_src, const void *dst_feat,
+                                  int64_t n_dst, int32_t H, int32_t Dh, float scale,
+                                  gat_dtype_t dtype, float *out, void *stream) {
+    if (n_edges < 0 || n_src < 0 || n_dst < 0 || H < 1 || Dh < 1 || (row_ptr && n_rows < 0))
+        return fail(GAT_ERR_INVALID_ARG, "gat_sddmm: bad sizes");
+    if (dtype != GAT_F32 && dtype != GAT_BF16)
+        return fail(GAT_ERR_UNSUPPORTED, "gat_sddmm: unknown dtype %d", (int)dtype);
+    if (n_edges == 0) return GAT_OK;
+    if (!src_idx || !src_feat || !dst_feat || !out || (!row_ptr && !dst_idx))
+        return fail(GAT_ERR_INVALID_ARG, "gat_sddmm: NULL pointer");
+    if (row_ptr && (n_rows < 1 || n_dst < n_rows))
+        return fail(GAT_ERR_INVALID_ARG, "gat_sddmm: CSR form needs 1 <= n_rows <= n_dst");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == GAT_F32)
+        return launch_sddmm<float>(row_ptr, src_idx, dst_idx, n_rows, n_edges, src_feat, dst_feat,
+                                   H, Dh, scale, out, s);
+    return launch_sddmm<__nv_bfloat16>(row_ptr, src_idx, dst_idx, n_rows, n_edges, src_feat,
+                                       dst_feat, H, Dh, scale, out, s);
+}

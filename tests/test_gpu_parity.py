@@ -1,0 +1,333 @@
+"""GPU parity: every entry point of libgat against the fp64 oracle on the same
+seeded inputs, through the C ABI (Python binding = argument marshalling).
+
+Small cases span several tiles and ragged tails and are compared element by
+element; the full-size workloads are compared on sampled outputs the oracle
+computes one by one, in the launch configuration the benchmark times.
+Integer outputs (the plan) are compared bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests.parity import assert_bf16, assert_fp32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gat():
+    from sparse_graph_attention_head_gb300 import build
+    build.build()
+    import sparse_graph_attention_head_gb300 as g
+    return g
+
+
+DEV = "cuda"
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def dev_bf16(bits):
+    return dev(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def host(t):
+    torch.cuda.synchronize()
+    if t.dtype == torch.bfloat16:
+        return t.float().cpu().numpy().astype(np.float64)
+    return t.cpu().numpy().astype(np.float64)
+
+
+# ----------------------------------------------------------------------------
+# edge softmax (multi-head CSR softmax workload)
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("use_plan", [False, True])
+def test_edge_softmax_workload(gat, use_plan):
+    d = W.make_edge_softmax()  # 384 rows, degrees 0..36, H=4, scores N(0, 2^2)
+    rp = dev(d["row_ptr"])
+    s = dev(d["scores"])
+    plan = gat.Plan(rp, heavy_threshold=20) if use_plan else None
+    out = gat.gat_edge_softmax(rp, s, 4, plan=plan)
+    o = oracle.edge_softmax(d["row_ptr"], d["scores"], 4)
+    assert_fp32(host(out), o, name="edge_softmax")
+
+
+@pytest.mark.parametrize("H", [1, 3, 8, 32])
+def test_edge_softmax_heads_in_place_and_long_rows(gat, H):
+    deg = np.array([0, 1, 2, 31, 32, 33, 300, 0, 5000, 7])
+    d = W.make_edge_softmax(seed=40 + H, deg=deg, H=H)
+    rp = dev(d["row_ptr"])
+    s = dev(d["scores"])
+    o = oracle.edge_softmax(d["row_ptr"], d["scores"], H)
+    for plan in (None, gat.Plan(rp, heavy_threshold=40)):
+        buf = s.clone()
+        gat.gat_edge_softmax(rp, buf, H, out=buf, plan=plan)  # in place
+        assert_fp32(host(buf), o, name=f"edge_softmax H={H}")
+
+
+def test_edge_softmax_extreme_scores_and_neg_inf_row(gat):
+    rp_h = np.array([0, 3, 5, 8], np.int32)
+    s_h = np.array([[80.0], [-80.0], [79.0], [-np.inf], [-np.inf], [3.0], [3.0], [3.0]],
+                   np.float32)
+    out = gat.gat_edge_softmax(dev(rp_h), dev(s_h), 1)
+    o = oracle.edge_softmax(rp_h, s_h, 1)
+    g = host(out)
+    assert np.isnan(g[3:5]).all() and np.isnan(o[3:5]).all()  # all -inf row -> NaN
+    assert_fp32(g[[0, 1, 2, 5, 6, 7]], o[[0, 1, 2, 5, 6, 7]])
+    np.testing.assert_allclose(g[5:8, 0], 1 / 3, rtol=1e-6)
+
+
+# ----------------------------------------------------------------------------
+# softmax + aggregation workload (edge softmax H=1 then weighted SpMM)
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("use_plan", [False, True])
+def test_aggregate_workload(gat, use_plan):
+    d = W.make_aggregate()  # 384 rows, degrees 0..36, col_idx unsorted, values [384,64]
+    rp, ci = dev(d["row_ptr"]), dev(d["col_idx"])
+    plan = gat.Plan(rp, heavy_threshold=24) if use_plan else None
+    w = gat.gat_edge_softmax(rp, dev(d["scores"]).reshape(-1, 1), 1, plan=plan)
+    out = gat.gat_spmm_weighted(rp, ci, w, dev(d["values"]).reshape(384, 1, 64), 1, 64,
+                                plan=plan)
+    w_o = oracle.edge_softmax(d["row_ptr"], d["scores"], 1)
+    o, c = oracle.spmm_weighted(d["row_ptr"], d["col_idx"], w_o, d["values"], 1, 64,
+                                want_cond=True)
+    n = np.diff(d["row_ptr"]).astype(np.float64)[:, None, None]
+    g = host(out)
+    assert (g[np.diff(d["row_ptr"]) == 0] == 0).all()  # zero-degree rows are exact zeros
+    rate = assert_fp32(g, o, c, n, name="aggregate")
+    assert rate > 0.99
+
+
+@pytest.mark.parametrize("H,Dh,dtype", [(1, 64, "f32"), (4, 32, "f32"), (8, 64, "f32"),
+                                         (8, 64, "bf16"), (2, 64, "bf16"), (1, 32, "bf16"),
+                                         (3, 24, "f32"), (5, 6, "bf16")])
+def test_spmm_shapes(gat, H, Dh, dtype):
+    rng = np.random.default_rng(50 + H * Dh)
+    deg = np.concatenate([rng.integers(0, 40, 300), [0, 65, 64, 200, 1500]])
+    n, n_src = deg.size, 257
+    rp, ci = W.make_csr(rng, deg, n_src, sort_within_rows=False)
+    E = int(rp[-1])
+    w = rng.standard_normal((E, H)).astype(np.float32)
+    f32 = rng.standard_normal((n_src, H, Dh)).astype(np.float32)
+    if dtype == "bf16":
+        bits = W.bf16_bits_from_f32(f32)
+        feat_d, feat_o = dev_bf16(bits), bits
+    else:
+        feat_d, feat_o = dev(f32), f32
+    o, c = oracle.spmm_weighted(rp, ci, w.astype(np.float64), feat_o, H, Dh, want_cond=True)
+    rpd = dev(rp)
+    for plan in (None, gat.Plan(rpd, heavy_threshold=64)):
+        out = gat.gat_spmm_weighted(rpd, dev(ci), dev(w), feat_d, H, Dh, plan=plan)
+        g = host(out)
+        if dtype == "bf16":
+            assert_bf16(g, o, c, name=f"spmm {H}x{Dh} bf16")
+        else:
+            assert_fp32(g, o, c, deg.astype(np.float64)[:, None, None], name=f"spmm {H}x{Dh}")
+
+
+# ----------------------------------------------------------------------------
+# SDDMM workload (COO) and CSR / multi-head / bf16 forms
+# ----------------------------------------------------------------------------
+def test_sddmm_workload(gat):
+    d = W.make_sddmm()  # src [1024,128], dst [768,128], 16384 edges
+    out = gat.gat_sddmm(dev(d["src_idx"]), dev(d["src_feat"]), dev(d["dst_feat"]), 1, 128,
+                        dst_idx=dev(d["dst_idx"]))
+    o, c = oracle.sddmm(d["src_idx"], d["src_feat"], d["dst_feat"], 1, 128,
+                        dst_idx=d["dst_idx"], want_cond=True)
+    rate = assert_fp32(host(out), o, c, 128, name="sddmm")
+    assert rate > 0.98
+
+
+@pytest.mark.parametrize("H,Dh,dtype", [(8, 64, "bf16"), (4, 32, "f32"), (3, 5, "f32"),
+                                         (2, 24, "bf16")])
+def test_sddmm_csr_multihead(gat, H, Dh, dtype):
+    rng = np.random.default_rng(60 + Dh)
+    deg = np.concatenate([rng.integers(0, 30, 200), [0, 0, 300]])
+    rp, ci = W.make_csr(rng, deg, 150, sort_within_rows=True)
+    n = deg.size
+    k32 = rng.standard_normal((150, H, Dh)).astype(np.float32)
+    q32 = rng.standard_normal((n, H, Dh)).astype(np.float32)
+    if dtype == "bf16":
+        kb, qb = W.bf16_bits_from_f32(k32), W.bf16_bits_from_f32(q32)
+        kd, qd, ko, qo = dev_bf16(kb), dev_bf16(qb), kb, qb
+    else:
+        kd, qd, ko, qo = dev(k32), dev(q32), k32, q32
+    out = gat.gat_sddmm(dev(ci), kd, qd, H, Dh, scale=0.3, row_ptr=dev(rp))
+    o, c = oracle.sddmm(ci, ko, qo, H, Dh, scale=0.3, row_ptr=rp, want_cond=True)
+    assert_fp32(host(out), o, c, Dh, name="sddmm csr")
+
+
+# ----------------------------------------------------------------------------
+# degree-bucket plan: bit-exact against the oracle's definition
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("T,C", [(64, 64), (16, 32), (1, 1), (4095, 4096)])
+def test_plan_bit_exact(gat, T, C):
+    rng = np.random.default_rng(70)
+    deg = np.concatenate([W.zipf_degrees(rng, 30000), [0, T, T + 1, C, C + 1, 2 * C, 9000],
+                          np.zeros(5000, np.int64)])
+    rp = W.row_ptr_from_degrees(deg)
+    plan = gat.Plan(dev(rp), heavy_threshold=T, chunk_edges=C)
+    hr, cs, cr = (host(t).astype(np.int64) for t in plan.export())
+    ohr, ocs, ocr = oracle.plan(rp, T, C)
+    np.testing.assert_array_equal(hr, ohr)
+    np.testing.assert_array_equal(cs, ocs)
+    np.testing.assert_array_equal(cr, ocr)
+
+
+def test_plan_empty_and_all_light(gat):
+    rp = np.zeros(11, np.int32)
+    plan = gat.Plan(dev(rp), n_edges=0)
+    assert plan.info()["n_heavy"] == 0 and plan.info()["n_chunks"] == 0
+    rp = W.row_ptr_from_degrees(np.full(100, 3))
+    plan = gat.Plan(dev(rp))
+    assert plan.info()["n_heavy"] == 0
+
+
+# ----------------------------------------------------------------------------
+# fused layer
+# ----------------------------------------------------------------------------
+def fused_case(n, seed, H=8, Dh=64, dtype="bf16", deg=None, dmax=4096, mean=16.0):
+    d = W.make_fused(seed=seed, n=n, H=H, Dh=Dh, deg=deg, dmax=dmax, mean=mean, dtype=dtype)
+    if dtype == "bf16":
+        qd, kd, vd = (dev_bf16(d[x]) for x in ("q", "k", "v"))
+    else:
+        qd, kd, vd = (dev(d[x]) for x in ("q", "k", "v"))
+    return d, dev(d["row_ptr"]), dev(d["col_idx"]), qd, kd, vd
+
+
+def check_fused(d, g, rows=None):
+    o, c = oracle.fused_layer(d["row_ptr"], d["col_idx"], d["q"], d["k"], d["v"], d["H"],
+                              d["Dh"], d["scale"], rows=rows, want_cond=True)
+    if rows is not None:
+        g = g[rows]
+    if d["dtype"] == "bf16":
+        return assert_bf16(g, o, c, name="fused bf16")
+    deg = np.diff(d["row_ptr"]).astype(np.float64)
+    n = deg if rows is None else deg[rows]
+    return assert_fp32(g, o, c, n[:, None, None], name="fused fp32")
+
+
+@pytest.mark.parametrize("use_plan", [False, True])
+def test_fused_small_power_law(gat, use_plan):
+    deg = W.zipf_degrees(np.random.default_rng(80), 6000, dmax=2000)
+    deg[[5, 17]] = [0, 3000]
+    d, rp, ci, q, k, v = fused_case(6000, 81, deg=deg)
+    plan = gat.Plan(rp) if use_plan else None
+    out = gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], plan=plan)
+    g = host(out)
+    assert (g[5] == 0).all()
+    check_fused(d, g)
+
+
+@pytest.mark.parametrize("H,Dh,dtype", [(8, 64, "f32"), (4, 64, "bf16"), (2, 64, "bf16"),
+                                         (1, 64, "bf16"), (1, 32, "bf16"), (4, 32, "f32"),
+                                         (1, 64, "f32"), (3, 24, "f32"), (2, 40, "bf16")])
+def test_fused_shapes(gat, H, Dh, dtype):
+    deg = W.zipf_degrees(np.random.default_rng(90 + Dh), 1500, dmax=700)
+    d, rp, ci, q, k, v = fused_case(1500, 91 + H, H=H, Dh=Dh, dtype=dtype, deg=deg)
+    for plan in (None, gat.Plan(rp, heavy_threshold=48, chunk_edges=40)):
+        out = gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], plan=plan)
+        check_fused(d, host(out))
+
+
+def test_fused_edge_cases(gat):
+    # E = 0: every row is zero-degree -> exact zeros
+    d, rp, ci, q, k, v = fused_case(50, 100, deg=np.zeros(50, np.int64))
+    out = gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], plan=gat.Plan(rp, n_edges=0))
+    assert (host(out) == 0).all()
+    # a single row
+    d, rp, ci, q, k, v = fused_case(1, 101, deg=np.array([37]))
+    check_fused(d, host(gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], plan=gat.Plan(rp))))
+    # one row of degree 100000 (split into ~1563 chunks) among light rows, and
+    # degrees at the thresholds +-1
+    deg = np.array([3, 100000, 63, 64, 65, 127, 128, 129, 1, 0])
+    d, rp, ci, q, k, v = fused_case(10, 102, deg=deg)
+    plan = gat.Plan(rp)
+    assert plan.info()["n_chunks"] == 1563 + 2 + 2 + 2 + 3
+    check_fused(d, host(gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], plan=plan)))
+
+
+def test_fused_duplicates_unsorted_equal_scores(gat):
+    rng = np.random.default_rng(103)
+    deg = rng.integers(1, 90, 400)
+    d, rp, ci, q, k, v = fused_case(400, 104, deg=deg)
+    ci_h = rng.integers(0, 5, d["n_edges"]).astype(np.int32)  # many duplicates, unsorted
+    d["col_idx"] = ci_h
+    # rows whose queries are zero see equal scores everywhere -> plain averages
+    d["q"][:50] = 0
+    q = dev_bf16(d["q"])
+    out = gat.gat_fused_layer(rp, dev(ci_h), q, k, v, d["scale"], plan=gat.Plan(rp))
+    check_fused(d, host(out))
+
+
+def test_fused_deterministic(gat):
+    d, rp, ci, q, k, v = fused_case(20000, 105)
+    plan = gat.Plan(rp)
+    a = gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], plan=plan)
+    b = gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], plan=plan)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_fused_errors(gat):
+    d, rp, ci, q, k, v = fused_case(300, 106, deg=np.full(300, 100))
+    plan = gat.Plan(rp)
+    small = torch.empty(16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(gat.GatError, match="GAT_ERR_WORKSPACE"):
+        gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], plan=plan, workspace=small)
+    other = gat.Plan(dev(W.row_ptr_from_degrees(np.full(10, 3))))
+    with pytest.raises(gat.GatError, match="GAT_ERR_PLAN_MISMATCH"):
+        gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], plan=other)
+
+
+def test_validate_graph(gat):
+    rp = W.row_ptr_from_degrees(np.array([2, 0, 3]))
+    ci = np.array([0, 1, 2, 2, 0], np.int32)
+    gat.gat_validate_graph(dev(rp), dev(ci), 3)
+    bad = ci.copy()
+    bad[3] = 7
+    with pytest.raises(gat.GatError, match="GAT_ERR_INDEX_OUT_OF_RANGE"):
+        gat.gat_validate_graph(dev(rp), dev(bad), 3)
+    bad_rp = rp.copy()
+    bad_rp[2] = 1
+    with pytest.raises(gat.GatError, match="GAT_ERR_INDEX_OUT_OF_RANGE"):
+        gat.gat_validate_graph(dev(bad_rp), dev(ci), 3)
+
+
+# ----------------------------------------------------------------------------
+# full-size fused workload: 1e6 rows, Zipf(2.1) mean 16, H=8, Dh=64, bf16
+# ----------------------------------------------------------------------------
+@pytest.fixture(scope="module")
+def full_fused(gat):
+    d, rp, ci, q, k, v = fused_case(1_000_000, 3)
+    plan = gat.Plan(rp)
+    return d, rp, ci, q, k, v, plan
+
+
+def test_full_size_plan_bit_exact(gat, full_fused):
+    d, rp, ci, q, k, v, plan = full_fused
+    inf = plan.info()
+    hr, cs, cr = (host(t).astype(np.int64) for t in plan.export())
+    ohr, ocs, ocr = oracle.plan(d["row_ptr"], inf["heavy_threshold"], inf["chunk_edges"])
+    np.testing.assert_array_equal(hr, ohr)
+    np.testing.assert_array_equal(cs, ocs)
+    np.testing.assert_array_equal(cr, ocr)
+
+
+def test_full_size_fused_sampled_rows(gat, full_fused):
+    d, rp, ci, q, k, v, plan = full_fused
+    out = gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], plan=plan)
+    g = host(out)
+    deg = np.diff(d["row_ptr"])
+    rng = np.random.default_rng(7)
+    heaviest = np.argsort(deg)[-12:]
+    at_thr = np.flatnonzero((deg >= 63) & (deg <= 66))[:8]
+    rows = np.unique(np.concatenate([heaviest, at_thr, rng.integers(0, deg.size, 300),
+                                     [0, deg.size - 1]]))
+    check_fused(d, g, rows=rows)
+    assert np.isfinite(g).all()
