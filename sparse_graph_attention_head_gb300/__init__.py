@@ -45,7 +45,7 @@ def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"libgat.so is not built ({LIB_PATH} missing); build it with "
-            "sparse_graph_attention_head_gb300.build.build()")
+            "python sparse_graph_attention_head_gb300/build.py")
     lib = ctypes.CDLL(LIB_PATH)
     P, I64, I32, F, SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
                           ctypes.c_size_t)

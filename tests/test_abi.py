@@ -12,8 +12,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def lib():
-    from sparse_graph_attention_head_gb300 import build
-    path = build.build()
+    import __graft_entry__
+    path = __graft_entry__._build_module().build()
     return ctypes.CDLL(path)
 
 
@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
     assert not missing, missing
 
 
-def test_python_binding_covers_every_export():
+def test_python_binding_covers_every_export(lib):
     import sparse_graph_attention_head_gb300 as gat
     assert sorted(gat.EXPORTS) == declared_functions()
 

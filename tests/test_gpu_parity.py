@@ -19,8 +19,8 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(scope="module")
 def gat():
-    from sparse_graph_attention_head_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import sparse_graph_attention_head_gb300 as g
     return g
 
