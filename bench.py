@@ -422,13 +422,13 @@ def bench_small(name, args):
         fn()
     torch.cuda.synchronize()
     reps = 50
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
     for _ in range(reps):
         fn()
-    b.record()
+    ev1.record()
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / reps
+    ms = ev0.elapsed_time(ev1) / reps
     return {"ms_per_step": ms, "units_per_s": units / (ms * 1e-3), "launches_per_step": launches,
             "warm": True}
 
@@ -462,8 +462,12 @@ def main():
     res, d = bench_fused(args, rank, world, local, dist)
     if rank == 0:
         if not args.no_extras:
-            res["other_workloads"] = {nm: bench_small(nm, args)
-                                      for nm in ("edge_softmax", "aggregate", "sddmm", "dense")}
+            res["other_workloads"] = {}
+            for nm in ("edge_softmax", "aggregate", "sddmm", "dense"):
+                try:
+                    res["other_workloads"][nm] = bench_small(nm, args)
+                except Exception as exc:  # keep the headline line if a side workload fails
+                    res["other_workloads"][nm] = {"error": repr(exc)}
         res["cpu_baseline"] = cpu_baseline_fused(d, budget_s=args.cpu_budget)
         print(json.dumps(res), flush=True)
     if dist is not None:

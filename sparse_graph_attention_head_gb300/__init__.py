@@ -66,7 +66,7 @@ def _load() -> ctypes.CDLL:
         "gat_fused_layer_workspace_size": ([P, I32, I32, P], ctypes.c_int),
         "gat_fused_layer": ([P, P, I64, I64, I64, I32, I32, F, P, P, P, ctypes.c_int, P, P, P, SZ,
                              P], ctypes.c_int),
-        "gat_dense_masked_attention": ([I32] * 5 + [P] * 5 + [F] + [P] * 9 + [P, P],
+        "gat_dense_masked_attention": ([I32] * 5 + [P] * 5 + [F] + [P] * 8 + [P, P],
                                        ctypes.c_int),
     }
     for name, (args, res) in sigs.items():
