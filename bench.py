@@ -225,7 +225,7 @@ def bench_fused(args, rank, world, local, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     t_gen = time.perf_counter()
-    d = W.make_fused(seed=3)
+    d = W.make_fused(seed=3, n=args.n_rows)
     t_gen = time.perf_counter() - t_gen
     n, E, H, Dh = d["n_rows"], d["n_edges"], d["H"], d["Dh"]
     rp_h, ci_h = d["row_ptr"], d["col_idx"]
@@ -442,7 +442,10 @@ def main():
     ap.add_argument("--workload", default="fused",
                     choices=["fused", "edge_softmax", "aggregate", "sddmm", "dense"])
     ap.add_argument("--ref-rows", type=int, default=16000)
-    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle time for cpu_baseline (0: skip)")
+    ap.add_argument("--n-rows", type=int, default=1_000_000,
+                    help="rows of the fused workload (smaller only for profiling captures)")
     ap.add_argument("--no-extras", action="store_true", help="skip the smaller workloads")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -468,7 +471,8 @@ def main():
                     res["other_workloads"][nm] = bench_small(nm, args)
                 except Exception as exc:  # keep the headline line if a side workload fails
                     res["other_workloads"][nm] = {"error": repr(exc)}
-        res["cpu_baseline"] = cpu_baseline_fused(d, budget_s=args.cpu_budget)
+        if args.cpu_budget > 0:
+            res["cpu_baseline"] = cpu_baseline_fused(d, budget_s=args.cpu_budget)
         print(json.dumps(res), flush=True)
     if dist is not None:
         dist.destroy_process_group()
