@@ -54,7 +54,7 @@ def _load():
         lib.oracle_fused_layer.argtypes = [P, P, I64, I32, I32, D, P, P, P, ctypes.c_int,
                                            P, I64, P, P]
         lib.oracle_dense_block.argtypes = [I32, I32, I32, I32, I32, P, P, P, P, P, D,
-                                           P, P, P, P, P, P, P, P, P, I64, P]
+                                           P, P, P, P, P, P, P, P, P, I64, P, P]
         lib.oracle_plan.argtypes = [P, I64, I32, I32, P, P, P, P, P]
         for f in ("oracle_edge_softmax", "oracle_spmm_weighted", "oracle_sddmm",
                   "oracle_fused_layer", "oracle_dense_block", "oracle_plan"):
@@ -144,9 +144,9 @@ def fused_layer(row_ptr, col_idx, q, k, v, H, Dh, scale, rows=None, want_cond=Fa
     return (out, cond) if want_cond else out
 
 
-def dense_block(w: dict, graphs=None):
+def dense_block(w: dict, graphs=None, want_cond=False):
     """Dense-masked attention block on the arrays of ``workloads.make_dense``.
-    Returns fp64 [n_sel,N,D]."""
+    Returns fp64 [n_sel,N,D] (and the conditioning scale when want_cond)."""
     B, N, D, H, P = (int(w[x]) for x in ("B", "N", "D", "H", "P"))
     f = lambda name: _c(w[name], np.float32)  # noqa: E731
     arrs = [f(x) for x in ("nodes", "pair_feats", "edge_mask", "ln_w", "ln_b")]
@@ -154,10 +154,11 @@ def dense_block(w: dict, graphs=None):
     sel = None if graphs is None else _c(graphs, np.int64)
     n_sel = B if sel is None else sel.size
     out = np.empty((n_sel, N, D), dtype=np.float64)
+    cond = np.empty_like(out) if want_cond else None
     _check(_load().oracle_dense_block(B, N, D, H, P, *[_p(a) for a in arrs],
                                       float(w["ln_eps"]), *[_p(a) for a in wts],
-                                      _p(sel), n_sel, _p(out)), "oracle_dense_block")
-    return out
+                                      _p(sel), n_sel, _p(out), _p(cond)), "oracle_dense_block")
+    return (out, cond) if want_cond else out
 
 
 def plan(row_ptr, heavy_threshold, chunk):

@@ -260,6 +260,8 @@ int oracle_fused_layer(const int32_t *row_ptr, const int32_t *col_idx,
  *   ctx_i^h = sum_j a[i,j] V_j^h
  *   out_i   = x_i + Wout ctx_i                   (Linear(D,D), no bias; residual)
  * graphs (optional) selects n_sel graphs; out is then [n_sel,N,D].
+ * cond (optional, same shape) receives |x| + sum_c |Wout[r][c] ctx[c]|, the
+ * scale of the terms summed into each output (for the tolerance).
  */
 int oracle_dense_block(int32_t B, int32_t N, int32_t D, int32_t H, int32_t P,
                        const float *nodes, const float *pair, const float *mask,
@@ -267,7 +269,8 @@ int oracle_dense_block(int32_t B, int32_t N, int32_t D, int32_t H, int32_t P,
                        const float *Wq, const float *Wk, const float *Wv,
                        const float *W1, const float *b1, const float *W2,
                        const float *b2, const float *Wout,
-                       const int64_t *graphs, int64_t n_sel, double *out)
+                       const int64_t *graphs, int64_t n_sel, double *out,
+                       double *cond)
 {
     if (B < 0 || N < 1 || D < 1 || H < 1 || P < 1 || D % H != 0 || !out)
         return -1;
@@ -369,10 +372,14 @@ int oracle_dense_block(int32_t B, int32_t N, int32_t D, int32_t H, int32_t P,
         double *o = out + t * (int64_t)nd;
         for (int32_t n = 0; n < N; ++n)
             for (int32_t r = 0; r < D; ++r) {
-                double a = 0.0;
-                for (int32_t c = 0; c < D; ++c)
+                double a = 0.0, ca = fabs((double)x[n * D + r]);
+                for (int32_t c = 0; c < D; ++c) {
                     a += (double)Wout[r * D + c] * ctx[n * D + c];
+                    ca += fabs((double)Wout[r * D + c] * ctx[n * D + c]);
+                }
                 o[n * D + r] = (double)x[n * D + r] + a;
+                if (cond)
+                    cond[t * (int64_t)nd + n * D + r] = ca;
             }
     }
 done:

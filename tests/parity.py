@@ -36,8 +36,8 @@ def assert_fp32(g, o, cond=None, n_terms=None, name="fp32"):
     if cond is not None:
         n = np.maximum(np.asarray(n_terms if n_terms is not None else 1, dtype=np.float64), 1.0)
         scale = np.maximum(scale, np.asarray(cond) / np.sqrt(n))
-    tol = 1e-6 + 1e-5 * scale
     nan_o = np.isnan(o)
+    tol = np.where(nan_o, np.inf, 1e-6 + 1e-5 * scale)
     assert (np.isnan(g) == nan_o).all(), f"{name}: NaN pattern differs"
     _report(name, np.where(nan_o, 0, g), np.where(nan_o, 0, o), tol)
     strict = np.abs(g - o) <= 1e-6 + 1e-5 * np.abs(o)
