@@ -214,6 +214,33 @@ gat_status_t gat_fused_layer(const int32_t *row_ptr, const int32_t *col_idx, int
                              void *stream);
 
 /* ------------------------------------------------------------------------
+ * Fused layer without any device allocation. The source pages have no
+ * counterpart: this is a deployment variant of gat_fused_layer for callers
+ * that cannot call cudaMalloc (a framework that owns all device memory
+ * through its own pool, an allocator or memory-pressure callback, a process
+ * whose allocation budget is spent, an embedding that only hands over the
+ * input and output buffers). Same operation, arguments and results as
+ * gat_fused_layer with a default plan (heavy rows: degree > 64, chunks of 64
+ * edges); q, k, v, out must be 16-byte aligned and (H, Dh) a shape of the
+ * vector engine (else GAT_ERR_UNSUPPORTED).
+ * Scratch: the plan, the arrival counters and the chunk softmax states live
+ * in one static 32 MiB device array inside the library, which every GPU that
+ * loads the library holds until the process exits. A graph whose plan and
+ * chunk states do not fit returns GAT_ERR_WORKSPACE before any layer work is
+ * enqueued (use gat_fused_layer with a plan and a workspace instead).
+ * The array is shared by all calls and keeps the previous call's contents
+ * (each call clears what must start at zero); calls whose work overlaps on
+ * the GPU race on it and must be serialised by the caller.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. Every call synchronises `stream` once to read the plan's size.
+ * ---------------------------------------------------------------------- */
+gat_status_t gat_fused_layer_no_alloc(const int32_t *row_ptr, const int32_t *col_idx,
+                                      int64_t n_rows, int64_t n_src, int64_t n_edges, int32_t H,
+                                      int32_t Dh, float scale, const void *q, const void *k,
+                                      const void *v, gat_dtype_t dtype, void *out, void *stream);
+
+/* ------------------------------------------------------------------------
  * Dense-masked small-graph attention block [block page, reference model],
  * all fp32, per graph b of B:
  *     xn    = LayerNorm(x; ln_w, ln_b, ln_eps)      biased variance, per node

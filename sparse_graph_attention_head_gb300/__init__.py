@@ -30,6 +30,7 @@ EXPORTS = (
     "gat_plan_create", "gat_plan_destroy", "gat_plan_info", "gat_plan_export",
     "gat_validate_graph", "gat_sddmm", "gat_edge_softmax", "gat_spmm_weighted",
     "gat_fused_layer_workspace_size", "gat_fused_layer", "gat_dense_masked_attention",
+    "gat_fused_layer_no_alloc",
 )
 
 
@@ -68,6 +69,8 @@ def _load() -> ctypes.CDLL:
                              P], ctypes.c_int),
         "gat_dense_masked_attention": ([I32] * 5 + [P] * 5 + [F] + [P] * 8 + [P, P],
                                        ctypes.c_int),
+        "gat_fused_layer_no_alloc": ([P, P, I64, I64, I64, I32, I32, F, P, P, P, ctypes.c_int, P,
+                                      P], ctypes.c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -271,6 +274,21 @@ def gat_fused_layer(row_ptr, col_idx, q, k, v, scale, out=None, plan=None, works
         _ptr(row_ptr), _ptr(col_idx) if E else None, n_rows, k.shape[0], E, H, Dh, float(scale),
         _ptr(q), _ptr(k), _ptr(v), _dtype(q), _ptr(out), _plan_handle(plan),
         _ptr(workspace), ws_bytes, _stream(stream)))
+    return out
+
+
+def gat_fused_layer_no_alloc(row_ptr, col_idx, q, k, v, scale, out, stream=None):
+    """gat_fused_layer for callers that cannot allocate device memory: the
+    plan and chunk states live in the library's static device scratch, so the
+    caller provides only the inputs and the preallocated ``out``. Calls that
+    overlap on the GPU race on that scratch; see include/gat.h."""
+    _idx(row_ptr, "row_ptr")
+    _idx(col_idx, "col_idx")
+    n_rows, H, Dh = q.shape
+    E = col_idx.numel()
+    _check("gat_fused_layer_no_alloc", _lib.gat_fused_layer_no_alloc(
+        _ptr(row_ptr), _ptr(col_idx) if E else None, n_rows, k.shape[0], E, H, Dh, float(scale),
+        _ptr(q), _ptr(k), _ptr(v), _dtype(q), _ptr(out), _stream(stream)))
     return out
 
 
