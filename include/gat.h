@@ -99,8 +99,8 @@ int32_t gat_version(void);
  * ---------------------------------------------------------------------- */
 
 /* Build a plan for the graph `row_ptr` (device, [n_rows+1]).
- * heavy_threshold <= 0 and chunk_edges <= 0 select the defaults (64, 64).
- * Allocates the plan's device arrays (cudaMalloc), runs three small kernels on
+ * heavy_threshold <= 0 and chunk_edges <= 0 select the defaults (128, 256).
+ * Allocates the plan's device arrays (cudaMalloc), runs four small kernels on
  * `stream` and synchronises `stream` once to read the class sizes back.
  * Errors: GAT_ERR_INVALID_ARG (NULL row_ptr/plan, n_rows < 0, n_edges < 0),
  * GAT_ERR_CUDA (allocation or launch failure; *plan is then NULL). */

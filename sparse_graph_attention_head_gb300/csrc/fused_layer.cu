@@ -67,16 +67,7 @@ fused_generic_kernel(const EngineParams p) {
 
 template <typename T, int V, int LE>
 static gat_status_t launch_fused_fast(const EngineParams &p, cudaStream_t s) {
-    constexpr int U = 8 / V;
-    auto kern = fused_engine_kernel<T, V, LE, U>;
-    static int64_t cap = 0;
-    if (cap == 0) cap = persistent_blocks(kern, INT64_MAX);
-    const int64_t items = p.n_chunks + p.n_rows;
-    const int64_t wpb = kEngineThreads / 32;
-    int64_t blocks = (items + wpb - 1) / wpb;
-    if (blocks > cap) blocks = cap;
-    kern<<<(unsigned)blocks, kEngineThreads, 0, s>>>(p);
-    return check_launch("gat_fused_layer");
+    return launch_fused_engine<T, V, LE>(p, s);
 }
 
 bool engine_shape(int H, int Dh, int elem_bytes, int &V, int &LE) {
@@ -182,6 +173,7 @@ extern "C" gat_status_t gat_fused_layer(const int32_t *row_ptr, const int32_t *c
         p.heavy_rows = plan->heavy_rows;
         p.chunk_start = plan->chunk_start;
         p.chunk_row = plan->chunk_row;
+        p.chunk_desc = plan->chunk_desc;
         p.counters = plan->counters;
         if (p.n_chunks > 0) {
             const size_t need = (size_t)p.n_chunks * (size_t)p.slot_floats * sizeof(float);

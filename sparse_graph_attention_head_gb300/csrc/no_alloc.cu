@@ -37,6 +37,9 @@ __global__ void plan_scan_kernel(const Counts *block_counts, int64_t nb, Counts 
 __global__ void plan_fill_kernel(const int32_t *row_ptr, int64_t n_rows, int32_t T, int32_t C,
                                  const Counts *offsets, const Counts *totals,
                                  int32_t *heavy_rows, int32_t *chunk_start, int32_t *chunk_row);
+__global__ void plan_desc_kernel(const int32_t *row_ptr, const int32_t *heavy_rows,
+                                 const int32_t *chunk_start, int64_t n_heavy, int32_t C,
+                                 int4 *desc);
 
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 constexpr int32_t kNoAllocThreshold = 64;  // heavy rows: degree > 64
@@ -72,14 +75,7 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 template <typename T, int V, int LE>
 static gat_status_t launch_no_alloc(const EngineParams &p, cudaStream_t s) {
-    constexpr int U = 8 / V;
-    auto kern = fused_engine_kernel<T, V, LE, U>;
-    const int64_t cap = persistent_blocks(kern, INT64_MAX);
-    const int64_t wpb = kEngineThreads / 32;
-    int64_t blocks = (p.n_chunks + p.n_rows + wpb - 1) / wpb;
-    if (blocks > cap) blocks = cap;
-    kern<<<(unsigned)blocks, kEngineThreads, 0, s>>>(p);
-    return check_launch("gat_fused_layer_no_alloc");
+    return launch_fused_engine<T, V, LE>(p, s);
 }
 
 template <typename T>
@@ -154,6 +150,8 @@ extern "C" gat_status_t gat_fused_layer_no_alloc(const int32_t *row_ptr, const i
     off += align256((size_t)tot.chunks * 4);
     const size_t o_cnt = off;
     off += align256((size_t)tot.heavy * 4);
+    const size_t o_desc = off;
+    off += align256((size_t)tot.chunks * sizeof(int4));
     const size_t o_part = off;
     off += align256((size_t)tot.chunks * (size_t)sf * sizeof(float));
     if (off > kNoAllocScratchBytes)
@@ -180,6 +178,7 @@ extern "C" gat_status_t gat_fused_layer_no_alloc(const int32_t *row_ptr, const i
     p.chunk_start = reinterpret_cast<int32_t *>(sc + o_start);
     p.chunk_row = reinterpret_cast<int32_t *>(sc + o_crow);
     p.counters = reinterpret_cast<int32_t *>(sc + o_cnt);
+    p.chunk_desc = reinterpret_cast<int4 *>(sc + o_desc);
     p.partials = reinterpret_cast<float *>(sc + o_part);
     p.slot_floats = sf;
     if (tot.heavy > 0) {  // arrival counters start at zero in every call
@@ -192,6 +191,14 @@ extern "C" gat_status_t gat_fused_layer_no_alloc(const int32_t *row_ptr, const i
                                                  const_cast<int32_t *>(p.chunk_start),
                                                  const_cast<int32_t *>(p.chunk_row));
     if ((st = check_launch("gat_fused_layer_no_alloc: plan fill")) != GAT_OK) return st;
+    if (tot.heavy > 0) {
+        int64_t db = (tot.heavy + 255) / 256;
+        if (db > 4096) db = 4096;
+        plan_desc_kernel<<<(unsigned)db, 256, 0, s>>>(row_ptr, p.heavy_rows, p.chunk_start,
+                                                     tot.heavy, kNoAllocChunk,
+                                                     const_cast<int4 *>(p.chunk_desc));
+        if ((st = check_launch("gat_fused_layer_no_alloc: chunk descriptors")) != GAT_OK) return st;
+    }
     if (dtype == GAT_F32) return dispatch_no_alloc<float>(p, V, LE, s);
     return dispatch_no_alloc<__nv_bfloat16>(p, V, LE, s);
 }

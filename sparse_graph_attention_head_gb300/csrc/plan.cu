@@ -224,6 +224,25 @@ plan_fill_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t T,
     if (blockIdx.x == 0 && threadIdx.x == 0) chunk_start[totals->heavy] = (int32_t)totals->chunks;
 }
 
+// One 16-byte descriptor per chunk {row, first edge, end edge, heavy index},
+// so a warp learns its chunk's edge range with one load instead of a chain
+// chunk_row -> heavy_rows / chunk_start -> row_ptr.
+__global__ void __launch_bounds__(kPlanThreads)
+plan_desc_kernel(const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ heavy_rows,
+                 const int32_t *__restrict__ chunk_start, int64_t n_heavy, int32_t C,
+                 int4 *__restrict__ desc) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t hr = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; hr < n_heavy; hr += stride) {
+        const int32_t row = heavy_rows[hr];
+        const int32_t rs = row_ptr[row], re = row_ptr[row + 1];
+        const int32_t c0 = chunk_start[hr], c1 = chunk_start[hr + 1];
+        for (int32_t c = c0; c < c1; ++c) {
+            const int32_t e0 = rs + (c - c0) * C;
+            desc[c] = make_int4(row, e0, min(e0 + C, re), (int32_t)hr);
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // graph validation
 // ---------------------------------------------------------------------------
@@ -277,6 +296,7 @@ extern "C" gat_status_t gat_plan_destroy(gat_plan_t p) {
     cudaFree(p->chunk_start);
     cudaFree(p->chunk_row);
     cudaFree(p->counters);
+    cudaFree(p->chunk_desc);
     delete p;
     return GAT_OK;
 }
@@ -294,8 +314,8 @@ extern "C" gat_status_t gat_plan_create(const int32_t *row_ptr, int64_t n_rows, 
     gat_plan_s *p = new gat_plan_s();
     p->n_rows = n_rows;
     p->n_edges = n_edges;
-    p->heavy_threshold = heavy_threshold > 0 ? heavy_threshold : 64;
-    p->chunk_edges = chunk_edges > 0 ? chunk_edges : 64;
+    p->heavy_threshold = heavy_threshold > 0 ? heavy_threshold : 128;
+    p->chunk_edges = chunk_edges > 0 ? chunk_edges : 256;
     cudaGetDevice(&p->device);
     if (n_rows == 0) {
         cudaError_t e = cudaMalloc(&p->chunk_start, sizeof(int32_t));
@@ -338,6 +358,7 @@ extern "C" gat_status_t gat_plan_create(const int32_t *row_ptr, int64_t n_rows, 
     if (e == cudaSuccess && p->n_heavy) e = cudaMalloc(&p->heavy_rows, p->n_heavy * sizeof(int32_t));
     if (e == cudaSuccess && p->n_heavy) e = cudaMalloc(&p->counters, p->n_heavy * sizeof(int32_t));
     if (e == cudaSuccess && p->n_chunks) e = cudaMalloc(&p->chunk_row, p->n_chunks * sizeof(int32_t));
+    if (e == cudaSuccess && p->n_chunks) e = cudaMalloc(&p->chunk_desc, p->n_chunks * sizeof(int4));
     if (e == cudaSuccess && p->n_heavy)
         e = cudaMemsetAsync(p->counters, 0, p->n_heavy * sizeof(int32_t), s);
     if (e != cudaSuccess) {
@@ -348,6 +369,14 @@ extern "C" gat_status_t gat_plan_create(const int32_t *row_ptr, int64_t n_rows, 
         row_ptr, n_rows, p->heavy_threshold, p->chunk_edges, scratch + nb, scratch + 2 * nb,
         p->heavy_rows, p->chunk_start, p->chunk_row);
     if ((st = check_launch("gat_plan_create: fill")) != GAT_OK) goto out_fail;
+    if (p->n_heavy > 0) {
+        int64_t db = (p->n_heavy + kPlanThreads - 1) / kPlanThreads;
+        if (db > 4096) db = 4096;
+        plan_desc_kernel<<<(unsigned)db, kPlanThreads, 0, s>>>(row_ptr, p->heavy_rows, p->chunk_start,
+                                                              p->n_heavy, p->chunk_edges,
+                                                              p->chunk_desc);
+        if ((st = check_launch("gat_plan_create: descriptors")) != GAT_OK) goto out_fail;
+    }
     e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) {
         st = cuda_fail(e, "gat_plan_create: fill");

@@ -54,6 +54,7 @@ struct EngineParams {
     const int32_t *heavy_rows;
     const int32_t *chunk_start;
     const int32_t *chunk_row;
+    const int4 *chunk_desc;  // [n_chunks] {row, e0, e1, heavy index}
     int32_t *counters;
     float *partials;       // [n_chunks][slot_floats]
     int64_t slot_floats;   // >= H*Dh + 2H, multiple of 4
@@ -101,6 +102,24 @@ struct Lanes {
     }
 };
 
+// 2^x with the hardware's approximate exp2 (relative error about 2^-22;
+// subnormal results flush to zero, far below any softmax weight that matters;
+// 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Work item metadata {row, e0, e1, heavy index or -1}, issued as loads whose
+// results are only needed when the item starts (so they overlap the previous
+// item): one 16-byte descriptor for a chunk, two row_ptr entries for a row.
+__device__ __forceinline__ int4 item_meta(const EngineParams &p, int64_t item) {
+    if (item < p.n_chunks) return __ldg(p.chunk_desc + item);
+    const int64_t row = item - p.n_chunks;
+    return make_int4((int)row, __ldg(p.row_ptr + row), __ldg(p.row_ptr + row + 1), -1);
+}
+
 // Edge range of one work item; returns false when the item is skipped.
 __device__ __forceinline__ bool item_range(const EngineParams &p, int64_t item, int64_t &row,
                                            int &e0, int &e1, int &hr, int64_t &chunk) {
@@ -145,7 +164,14 @@ struct FusedRow {
         }
     }
 
-    __device__ __forceinline__ void run(const EngineParams &p, const L &ln, int e0, int e1) {
+    // Walk edges [e0, e1). first_ci is this lane's col_idx[e0 + lane] (already
+    // loaded). Right after the first batch's gathers are issued, the col_idx
+    // tile of the warp's next item [ne0, ne1) is fetched into next_ci
+    // (next_ready), so the next item can start gathering at once; a next
+    // item that is a light-row slot beyond the threshold is not fetched.
+    __device__ __forceinline__ void run(const EngineParams &p, const L &ln, int e0, int e1,
+                                        int first_ci, int ne0, int ne1, bool next_is_row,
+                                        int &next_ci, bool &next_ready) {
 #pragma unroll
         for (int s = 0; s < V; ++s) {
             m[s] = -INFINITY;
@@ -158,7 +184,8 @@ struct FusedRow {
         const char *vb = static_cast<const char *>(p.v);
         for (int base = e0; base < e1; base += 32) {
             const int n = min(32, e1 - base);
-            const int my_ci = ln.lane < n ? __ldg(p.col_idx + base + ln.lane) : 0;
+            const int my_ci =
+                base == e0 ? first_ci : (ln.lane < n ? __ldg(p.col_idx + base + ln.lane) : 0);
             for (int j0 = 0; j0 < n; j0 += U * ES) {
                 uint4 kr[U][V], vr[U][V];
                 bool valid[U];
@@ -179,6 +206,13 @@ struct FusedRow {
                             kr[u][s] = make_uint4(0, 0, 0, 0);
                             vr[u][s] = make_uint4(0, 0, 0, 0);
                         }
+                    }
+                }
+                if (base == e0 && j0 == 0 && !next_ready) {
+                    const int nn = ne1 - ne0;
+                    if (nn > 0 && !(next_is_row && nn > p.heavy_threshold)) {
+                        next_ci = ln.lane < nn ? __ldg(p.col_idx + ne0 + ln.lane) : 0;
+                        next_ready = true;
                     }
                 }
                 float sc[U][V];
@@ -207,13 +241,13 @@ struct FusedRow {
                     for (int u = 0; u < U; ++u)
                         if (valid[u]) mx = fmaxf(mx, sc[u][s]);
                     if (mx == -INFINITY) continue;  // no edge for this subgroup yet
-                    const float c = exp2f(m[s] - mx);
+                    const float c = fast_exp2(m[s] - mx);
                     l[s] *= c;
 #pragma unroll
                     for (int t = 0; t < VE; ++t) acc[s][t] *= c;
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
-                        const float pe = valid[u] ? exp2f(sc[u][s] - mx) : 0.f;
+                        const float pe = valid[u] ? fast_exp2(sc[u][s] - mx) : 0.f;
                         l[s] += pe;
                         float vf[VE];
                         Vec<T>::unpack(vr[u][s], vf);
@@ -236,7 +270,7 @@ struct FusedRow {
                 for (int t = 0; t < VE; ++t) a2[t] = __shfl_xor_sync(kFull, acc[s][t], o);
                 const float mx = fmaxf(m[s], m2);
                 if (mx == -INFINITY) continue;
-                const float c1 = exp2f(m[s] - mx), c2 = exp2f(m2 - mx);
+                const float c1 = fast_exp2(m[s] - mx), c2 = fast_exp2(m2 - mx);
                 l[s] = l[s] * c1 + l2 * c2;
 #pragma unroll
                 for (int t = 0; t < VE; ++t) acc[s][t] = acc[s][t] * c1 + a2[t] * c2;
@@ -310,7 +344,7 @@ struct FusedRow {
                 }
                 const float mx = fmaxf(m[s], mc);
                 if (mx == -INFINITY) continue;
-                const float a1 = exp2f(m[s] - mx), a2 = exp2f(mc - mx);
+                const float a1 = fast_exp2(m[s] - mx), a2 = fast_exp2(mc - mx);
                 l[s] = l[s] * a1 + lc * a2;
 #pragma unroll
                 for (int t = 0; t < VE; ++t) acc[s][t] = acc[s][t] * a1 + ac[t] * a2;
@@ -322,8 +356,14 @@ struct FusedRow {
     }
 };
 
-template <typename T, int V, int LE, int U>
-__global__ void __launch_bounds__(kEngineThreads)
+// Persistent: warp w takes items w, w + W, w + 2W, ... (chunks of heavy rows
+// first, then rows). While an item is processed, the next item's metadata
+// (and, once that arrives, its first col_idx tile) is already being fetched.
+// Blocks of 4 warps, MINB resident per SM (5 -> 96 registers, 20 warps/SM).
+constexpr int kFusedThreads = 128;
+
+template <typename T, int V, int LE, int U, int MINB>
+__global__ void __launch_bounds__(kFusedThreads, MINB)
 fused_engine_kernel(const EngineParams p) {
     using L = Lanes<T, V, LE>;
     const L ln(p.Dh);
@@ -331,18 +371,56 @@ fused_engine_kernel(const EngineParams p) {
     const int64_t wpb = blockDim.x >> 5;
     const int64_t n_warps = (int64_t)gridDim.x * wpb;
     const int64_t n_items = p.n_chunks + p.n_rows;
-    for (int64_t item = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5); item < n_items;
-         item += n_warps) {
-        int64_t row, chunk;
-        int e0, e1, hr;
-        if (!item_range(p, item, row, e0, e1, hr, chunk)) continue;
-        st.load_q(p, ln, row);
-        st.run(p, ln, e0, e1);
-        if (chunk < 0)
-            st.store_out(p, ln, row);
+    int64_t item = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
+    if (item >= n_items) return;
+    int4 meta = item_meta(p, item);
+    int ci_tile = 0;
+    bool ci_ready = false;
+    for (; item < n_items; item += n_warps) {
+        const int4 cur = meta;  // {row, e0, e1, heavy index or -1}
+        const int64_t nxt = item + n_warps;
+        const bool has_next = nxt < n_items;
+        meta = has_next ? item_meta(p, nxt) : make_int4(0, 0, 0, -1);
+        const bool is_chunk = item < p.n_chunks;
+        if (!is_chunk && cur.z - cur.y > p.heavy_threshold) {  // a heavy row: done as chunks
+            ci_ready = false;
+            continue;
+        }
+        const int first_ci =
+            ci_ready ? ci_tile : (ln.lane < cur.z - cur.y ? __ldg(p.col_idx + cur.y + ln.lane) : 0);
+        bool next_ready = false;
+        st.load_q(p, ln, cur.x);
+        st.run(p, ln, cur.y, cur.z, first_ci, has_next ? meta.y : 0, has_next ? meta.z : 0,
+               nxt >= p.n_chunks, ci_tile, next_ready);
+        ci_ready = next_ready;
+        if (!is_chunk)
+            st.store_out(p, ln, cur.x);
         else
-            st.chunk_epilogue(p, ln, row, hr, chunk);
+            st.chunk_epilogue(p, ln, cur.x, cur.w, item);
     }
+}
+
+// Host-side launch of the fused engine for one (T, V, LE): U edges in flight
+// per warp (V=1: 4, V=2: 3, V=4: 1), five resident 4-warp blocks per SM.
+template <typename T, int V, int LE>
+inline gat_status_t launch_fused_engine(const EngineParams &p, cudaStream_t s) {
+    constexpr int U = V == 1 ? 4 : (V == 2 ? 3 : 1);
+    auto kern = fused_engine_kernel<T, V, LE, U, 5>;
+    static int64_t cap = 0;
+    if (cap == 0) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFusedThreads, 0) !=
+                cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        cap = (int64_t)sm_count() * per_sm;
+    }
+    const int64_t items = p.n_chunks + p.n_rows;
+    const int64_t wpb = kFusedThreads / 32;
+    int64_t blocks = (items + wpb - 1) / wpb;
+    if (blocks > cap) blocks = cap;
+    kern<<<(unsigned)blocks, kFusedThreads, 0, s>>>(p);
+    return check_launch("fused_engine_kernel");
 }
 
 // ---------------------------------------------------------------------------

@@ -245,10 +245,13 @@ def test_fused_edge_cases(gat):
     check_fused(d, host(gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], plan=gat.Plan(rp))))
     # one row of degree 100000 (split into ~1563 chunks) among light rows, and
     # degrees at the thresholds +-1
-    deg = np.array([3, 100000, 63, 64, 65, 127, 128, 129, 1, 0])
-    d, rp, ci, q, k, v = fused_case(10, 102, deg=deg)
+    deg = np.array([3, 100000, 63, 64, 65, 127, 128, 129, 255, 256, 257, 1, 0])
+    d, rp, ci, q, k, v = fused_case(deg.size, 102, deg=deg)
     plan = gat.Plan(rp)
-    assert plan.info()["n_chunks"] == 1563 + 2 + 2 + 2 + 3
+    inf = plan.info()
+    T, C = inf["heavy_threshold"], inf["chunk_edges"]
+    assert inf["n_chunks"] == sum(-(-int(x) // C) for x in deg if x > T)
+    assert inf["n_chunks"] > 100  # the 100000-edge row is split
     check_fused(d, host(gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], plan=plan)))
 
 
@@ -275,8 +278,9 @@ def test_fused_deterministic(gat):
 
 
 def test_fused_errors(gat):
-    d, rp, ci, q, k, v = fused_case(300, 106, deg=np.full(300, 100))
+    d, rp, ci, q, k, v = fused_case(300, 106, deg=np.full(300, 700))
     plan = gat.Plan(rp)
+    assert plan.info()["n_chunks"] > 0
     small = torch.empty(16, dtype=torch.uint8, device=DEV)
     with pytest.raises(gat.GatError, match="GAT_ERR_WORKSPACE"):
         gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], plan=plan, workspace=small)
