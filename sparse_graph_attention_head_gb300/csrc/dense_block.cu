@@ -146,6 +146,14 @@ dense_block_kernel(const DenseParams p) {
     }
 }
 
+// tensor-core path (dense_block_tc.cu); GAT_ERR_UNSUPPORTED outside its shapes
+gat_status_t dense_block_tc(int32_t B, int32_t N, int32_t D, int32_t H, int32_t P,
+                            const float *nodes, const float *pair, const float *mask,
+                            const float *ln_w, const float *ln_b, float ln_eps, const float *Wq,
+                            const float *Wk, const float *Wv, const float *W1, const float *b1,
+                            const float *W2, const float *b2, const float *Wout, float *out,
+                            cudaStream_t s);
+
 }  // namespace gat
 
 using namespace gat;
@@ -169,6 +177,14 @@ extern "C" gat_status_t gat_dense_masked_attention(
     if (!aligned16(nodes) || !aligned16(Wq) || !aligned16(Wk) || !aligned16(Wv) ||
         !aligned16(Wout) || !aligned16(out))
         return fail(GAT_ERR_UNSUPPORTED, "gat_dense_masked_attention: pointers must be 16-byte aligned");
+    // the module shape of the block page runs its projections on the tensor
+    // cores (dense_block_tc.cu); every other shape runs the SIMT kernel below
+    if (aligned16(pair_feats) && aligned16(ln_w) && aligned16(ln_b)) {
+        const gat_status_t st =
+            dense_block_tc(B, N, D, H, P, nodes, pair_feats, edge_mask, ln_w, ln_b, ln_eps, Wq,
+                           Wk, Wv, W1, b1, W2, b2, Wout, out, static_cast<cudaStream_t>(stream));
+        if (st != GAT_ERR_UNSUPPORTED) return st;
+    }
     DenseParams p{B, N, D, H, P, nodes, pair_feats, edge_mask, ln_w, ln_b, ln_eps,
                   Wq, Wk, Wv, W1, b1, W2, b2, Wout, out};
     const int DS = D + 1;

@@ -1,0 +1,516 @@
+// dense_block_tc.cu - the dense-masked attention block with its projections on
+// the 5th-generation tensor cores (tcgen05, kind::tf32, accumulators in TMEM).
+//
+// The block page's module (Kimi-K2.6 l2_p4, reference model) spends three
+// quarters of its arithmetic in four D x D projections (Q, K, V, out). Here they
+// run as 128-row tcgen05 MMAs: a tile is 4 graphs, each padded to 32 rows, so
+// graph g of the tile owns TMEM lanes 32g..32g+31 and is handled by warps g and
+// g+4 (the two warps allowed to read that lane quarter). fp32 accuracy comes
+// from the 3xTF32 split: every operand x = hi + lo with hi = tf32(x) (round to
+// nearest) and lo = x - hi, and A*B ~ hi_A hi_B + hi_A lo_B + lo_A hi_B (the
+// dropped lo_A lo_B term and lo's own tf32 truncation are ~2^-20 relative).
+//
+// Roles inside one CTA (8 warps, persistent over tiles, one CTA per SM):
+//   warps 0-3  LayerNorm (thread per node row) -> hi/lo A operand in shared
+//              memory; then the relation-MLP bias of most node pairs.
+//   warps 4-7  split the weights into 32-column hi/lo B chunks (2-slot ring)
+//              and, through their first thread, issue the MMAs of each chunk
+//              (commit -> one mbarrier per ring slot); then the remaining MLP
+//              pairs.
+//   all        attention per (graph, head pair): Q, K, V rows from TMEM, K and
+//              V staged in shared memory, scores + bias + mask, softmax,
+//              context -> hi/lo A operand; out-projection chunks into the TMEM
+//              columns that held Q; residual add; store.
+// Operands use the no-swizzle K-major layout of 8-row x 16-byte core
+// matrices (leading byte offset 128 between K neighbours, stride byte offset
+// (D/4)*128 between 8-row groups). Every mbarrier wait is bounded; giving up
+// sets a device flag that the host turns into GAT_ERR_CUDA.
+#include "common.cuh"
+
+namespace gat {
+
+namespace tc {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kGraphs = 4;      // graphs per tile (one 32-row TMEM lane quarter each)
+constexpr int kRows = 128;      // MMA M
+constexpr int kNB = 32;         // output columns per weight chunk (MMA N)
+constexpr int kTmemCols = 512;  // Q|K|V need 3D columns
+constexpr uint32_t kWaitTries = 1u << 24;
+
+__device__ int g_tc_error;  // set when a bounded wait gives up
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// byte offset of element (r, k) of a K-major tile whose rows have K elements
+__device__ __forceinline__ uint32_t kmaj(int r, int k, int K) {
+    return (uint32_t)((r >> 3) * (K >> 2) * 128 + (k >> 2) * 128 + (r & 7) * 16 + (k & 3) * 4);
+}
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
+}
+
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+__device__ __forceinline__ void split4(const float4 &v, float4 &hi, float4 &lo) {
+    hi = make_float4(tf32_rna(v.x), tf32_rna(v.y), tf32_rna(v.z), tf32_rna(v.w));
+    lo = make_float4(v.x - hi.x, v.y - hi.y, v.z - hi.z, v.w - hi.w);
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         int accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// bounded wait for the completion of the phase with parity `parity`
+__device__ __forceinline__ void mbar_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done = 0;
+    for (uint32_t it = 0; it < kWaitTries && !done; ++it) {
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+    }
+    if (!done) atomicExch(&g_tc_error, 1);
+}
+
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// 8 consecutive TMEM columns of this warp's 32 lanes
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct Params {
+    int32_t B, N;
+    const float *nodes, *pair, *mask, *ln_w, *ln_b;
+    float ln_eps;
+    const float *Wq, *Wk, *Wv, *W1, *b1, *W2, *b2, *Wout;
+    float *out;
+};
+
+// Shared memory carve-up in bytes; tensor-core operands 1024-aligned.
+template <int P, int H, int DH>
+struct Smem {
+    static constexpr int D = H * DH;
+    static constexpr uint32_t kA = kRows * D * 4, kB = kNB * D * 4;
+    static constexpr uint32_t al(uint32_t x) { return (x + 1023u) & ~1023u; }
+    static constexpr uint32_t a_hi = 0, a_lo = al(a_hi + kA), b_hi0 = al(a_lo + kA),
+                              b_lo0 = al(b_hi0 + kB), b_hi1 = al(b_lo0 + kB),
+                              b_lo1 = al(b_hi1 + kB), mlp = al(b_lo1 + kB),
+                              bias = mlp + (uint32_t)((P * P + P + H * P + H) * 4);
+    // bias [4][H][N][N] and the per-warp K/V staging [8][2][N][DH] follow;
+    // their size depends on N (<= 32)
+    __host__ __device__ static uint32_t stage(int N) { return bias + kGraphs * H * N * N * 4; }
+    __host__ __device__ static uint32_t total(int N) { return stage(N) + kWarps * 2 * N * DH * 4; }
+    __device__ static uint32_t b_hi(int s) { return s ? b_hi1 : b_hi0; }
+    __device__ static uint32_t b_lo(int s) { return s ? b_lo1 : b_lo0; }
+};
+
+// Weight chunk `chunk` of [Wq; Wk; Wv] (chunk < 3D/32) or of Wout (after),
+// split into the hi/lo B operand of ring slot s by the 128 threads of warps
+// 4-7 (t = 0..127); the output column runs fastest across threads so the
+// 16-byte shared stores of a warp land in distinct banks.
+template <int P, int H, int DH>
+__device__ __forceinline__ void load_b_chunk(const Params &p, int chunk, unsigned char *sm, int s,
+                                             int t) {
+    using L = Smem<P, H, DH>;
+    constexpr int D = L::D, n_qkv = 3 * D / kNB;
+    const float *W;
+    int row0;
+    if (chunk < n_qkv) {
+        const int r = chunk * kNB;
+        W = r < D ? p.Wq : (r < 2 * D ? p.Wk : p.Wv);
+        row0 = r % D;
+    } else {
+        W = p.Wout;
+        row0 = (chunk - n_qkv) * kNB;
+    }
+    constexpr int kg_n = D / 4;
+#pragma unroll 2
+    for (int idx = t; idx < kNB * kg_n; idx += 128) {
+        const int o = idx % kNB, kg = idx / kNB;
+        const float4 w = __ldg(reinterpret_cast<const float4 *>(W + (int64_t)(row0 + o) * D) + kg);
+        float4 hi, lo;
+        split4(w, hi, lo);
+        const uint32_t off = kmaj(o, 4 * kg, D);
+        *reinterpret_cast<float4 *>(sm + L::b_hi(s) + off) = hi;
+        *reinterpret_cast<float4 *>(sm + L::b_lo(s) + off) = lo;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// The 3xTF32 MMAs of one 32-column chunk: D[:, col0:col0+32] = A B^T.
+template <int D>
+__device__ __forceinline__ void issue_chunk(uint32_t tmem, int col0, uint32_t a_hi, uint32_t a_lo,
+                                            uint32_t b_hi, uint32_t b_lo) {
+    constexpr uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) |
+                               ((uint32_t)(kNB >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+    constexpr uint32_t lbo = 128, sbo = (uint32_t)(D / 4) * 128;
+    const uint32_t d = tmem + (uint32_t)col0;
+#pragma unroll
+    for (int k0 = 0; k0 < D; k0 += 8) {
+        const uint32_t ko = (uint32_t)(k0 / 4) * 128;
+        const uint64_t ah = smem_desc(a_hi + ko, lbo, sbo), al = smem_desc(a_lo + ko, lbo, sbo);
+        const uint64_t bh = smem_desc(b_hi + ko, lbo, sbo), bl = smem_desc(b_lo + ko, lbo, sbo);
+        mma_tf32(d, ah, bh, idesc, k0 > 0);
+        mma_tf32(d, ah, bl, idesc, 1);
+        mma_tf32(d, al, bh, idesc, 1);
+    }
+}
+
+// Relation-MLP bias of pairs (n, j), j in [j0, j1), for all heads.
+template <int P, int H>
+__device__ __forceinline__ void mlp_bias(const float *prow, int j0, int j1, const float *w1,
+                                         const float *bb1, const float *w2, const float *bb2,
+                                         float *bias_g, int N, int n) {
+    for (int j = j0; j < j1; ++j) {
+        float pf[P];
+#pragma unroll
+        for (int c4 = 0; c4 < P; c4 += 4) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(prow + j * P + c4));
+            pf[c4] = v.x;
+            pf[c4 + 1] = v.y;
+            pf[c4 + 2] = v.z;
+            pf[c4 + 3] = v.w;
+        }
+        float r[H];
+#pragma unroll
+        for (int h = 0; h < H; ++h) r[h] = bb2[h];
+#pragma unroll
+        for (int u = 0; u < P; ++u) {
+            float a = bb1[u];
+#pragma unroll
+            for (int c = 0; c < P; ++c) a = fmaf(w1[u * P + c], pf[c], a);
+            const float hid = a / (1.0f + expf(-a));
+#pragma unroll
+            for (int h = 0; h < H; ++h) r[h] = fmaf(w2[h * P + u], hid, r[h]);
+        }
+#pragma unroll
+        for (int h = 0; h < H; ++h) bias_g[(h * N + n) * N + j] = r[h];
+    }
+}
+
+template <int P, int H, int DH>
+__global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
+    using L = Smem<P, H, DH>;
+    constexpr int D = L::D, n_qkv = 3 * D / kNB, n_out = D / kNB;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    __shared__ uint64_t bar[2];
+    __shared__ uint32_t tmem_slot;
+    const int N = p.N;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = warp & 3;      // graph of the tile / TMEM lane quarter
+    const int half = warp >> 2;  // 0: warps 0-3, 1: warps 4-7
+    float *w1 = reinterpret_cast<float *>(sm + L::mlp), *bb1 = w1 + P * P, *w2 = bb1 + P,
+          *bb2 = w2 + H * P;
+    float *bias = reinterpret_cast<float *>(sm + L::bias);
+    float *stage = reinterpret_cast<float *>(sm + L::stage(N)) + warp * 2 * N * DH;
+    const uint32_t a_hi = smem_u32(sm + L::a_hi), a_lo = smem_u32(sm + L::a_lo);
+    const float inv_sqrt_dh = 1.0f / sqrtf((float)DH);
+    const int jsplit = (N * 5 + 7) / 8;  // MLP pairs [0, jsplit) on warps 0-3, rest on 4-7
+
+    for (int i = tid; i < P * P; i += kThreads) w1[i] = p.W1[i];
+    for (int i = tid; i < P; i += kThreads) bb1[i] = p.b1[i];
+    for (int i = tid; i < H * P; i += kThreads) w2[i] = p.W2[i];
+    for (int i = tid; i < H; i += kThreads) bb2[i] = p.b2[i];
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[0])));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[1])));
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = tmem_slot;
+    const uint32_t lane_q = (uint32_t)(32 * g) << 16;  // this warp's TMEM lane quarter
+    uint32_t ncommit[2] = {0, 0};                       // commits issued per mbarrier
+
+    const int n_tiles = (p.B + kGraphs - 1) / kGraphs;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        const int64_t b = (int64_t)tile * kGraphs + g;  // this warp's graph
+        const int n = lane;                             // node row of this lane
+        const bool rvalid = b < p.B && n < N;
+        const int row = 32 * g + lane;                  // MMA row / TMEM lane
+        const float *x = p.nodes + (b * N + n) * (int64_t)D;
+        const float *prow = p.pair + ((b * N + n) * (int64_t)N) * P;
+        float *bias_g = bias + g * H * N * N;
+
+        // ---- LayerNorm -> A (warps 0-3) | weight chunk 0 -> slot 0 (warps 4-7)
+        if (half == 0) {
+            float mean = 0.f, rstd = 0.f;
+            if (rvalid) {
+                float s = 0.f;
+#pragma unroll 4
+                for (int k = 0; k < D; k += 4) {
+                    const float4 v = __ldg(reinterpret_cast<const float4 *>(x + k));
+                    s += (v.x + v.y) + (v.z + v.w);
+                }
+                mean = s / (float)D;
+                float v2 = 0.f;
+#pragma unroll 4
+                for (int k = 0; k < D; k += 4) {
+                    const float4 v = __ldg(reinterpret_cast<const float4 *>(x + k));
+                    const float a0 = v.x - mean, a1 = v.y - mean, a2 = v.z - mean, a3 = v.w - mean;
+                    v2 = fmaf(a0, a0, v2);
+                    v2 = fmaf(a1, a1, v2);
+                    v2 = fmaf(a2, a2, v2);
+                    v2 = fmaf(a3, a3, v2);
+                }
+                rstd = 1.0f / sqrtf(v2 / (float)D + p.ln_eps);
+            }
+#pragma unroll 4
+            for (int k = 0; k < D; k += 4) {
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (rvalid) {
+                    const float4 v = __ldg(reinterpret_cast<const float4 *>(x + k));
+                    const float4 gw = __ldg(reinterpret_cast<const float4 *>(p.ln_w + k));
+                    const float4 gb = __ldg(reinterpret_cast<const float4 *>(p.ln_b + k));
+                    a = make_float4((v.x - mean) * rstd * gw.x + gb.x,
+                                    (v.y - mean) * rstd * gw.y + gb.y,
+                                    (v.z - mean) * rstd * gw.z + gb.z,
+                                    (v.w - mean) * rstd * gw.w + gb.w);
+                }
+                float4 hi, lo;
+                split4(a, hi, lo);
+                const uint32_t off = kmaj(row, k, D);
+                *reinterpret_cast<float4 *>(sm + L::a_hi + off) = hi;
+                *reinterpret_cast<float4 *>(sm + L::a_lo + off) = lo;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        } else {
+            // every MMA of the previous tile completed before its epilogue
+            load_b_chunk<P, H, DH>(p, 0, sm, 0, tid - 128);
+        }
+        __syncthreads();
+
+        // ---- Q|K|V: warps 4-7 stream chunks and issue; warps 0-3 start the MLP
+        if (half == 1) {
+            for (int c = 0; c < n_qkv; ++c) {
+                const int s = c & 1;
+                if (c > 0) {
+                    if (c >= 2) mbar_wait(&bar[s], (ncommit[s] - 1) & 1);  // chunk c-2 done
+                    load_b_chunk<P, H, DH>(p, c, sm, s, tid - 128);
+                }
+                named_sync(1, 128);
+                if (tid == 128) {
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    issue_chunk<D>(tmem, c * kNB, a_hi, a_lo, smem_u32(sm + L::b_hi(s)),
+                                   smem_u32(sm + L::b_lo(s)));
+                    mma_commit(&bar[s]);
+                }
+                ++ncommit[s];
+            }
+            if (rvalid) mlp_bias<P, H>(prow, jsplit, N, w1, bb1, w2, bb2, bias_g, N, n);
+        } else {
+            ncommit[0] += (n_qkv + 1) / 2;
+            ncommit[1] += n_qkv / 2;
+            if (rvalid) mlp_bias<P, H>(prow, 0, jsplit, w1, bb1, w2, bb2, bias_g, N, n);
+        }
+        __syncthreads();
+        {
+            const int s = (n_qkv - 1) & 1;  // the last commit covers every earlier MMA
+            mbar_wait(&bar[s], (ncommit[s] - 1) & 1);
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+
+        // ---- attention: warp w -> graph g, heads [half*H/2, (half+1)*H/2)
+        {
+            const float *mk = p.mask + (b * N + n) * (int64_t)N;
+            float *sk = stage, *sv = stage + N * DH;
+#pragma unroll 1
+            for (int hh = 0; hh < H / 2; ++hh) {
+                const int h = half * (H / 2) + hh;
+                float q[DH], kv[DH];
+#pragma unroll
+                for (int c0 = 0; c0 < DH; c0 += 8) {
+                    tmem_ld8(tmem + lane_q + (uint32_t)(h * DH + c0), q + c0);
+                    tmem_ld8(tmem + lane_q + (uint32_t)(D + h * DH + c0), kv + c0);
+                    if (rvalid) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) sk[n * DH + c0 + i] = kv[c0 + i];
+                    }
+                    tmem_ld8(tmem + lane_q + (uint32_t)(2 * D + h * DH + c0), kv + c0);
+                    if (rvalid) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) sv[n * DH + c0 + i] = kv[c0 + i];
+                    }
+                }
+                __syncwarp();
+                float sc[32];
+                float m = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    float s = -INFINITY;
+                    if (j < N && rvalid) {
+                        float a = 0.f;
+#pragma unroll
+                        for (int c = 0; c < DH; ++c) a = fmaf(q[c], sk[j * DH + c], a);
+                        s = a * inv_sqrt_dh + bias_g[(h * N + n) * N + j];
+                        if (__ldg(mk + j) < 0.5f) s = -INFINITY;
+                    }
+                    sc[j] = s;
+                    m = fmaxf(m, s);
+                }
+                float z = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float e = (j < N) ? expf(sc[j] - m) : 0.f;  // all -inf row: NaN
+                    sc[j] = e;
+                    z += e;
+                }
+                float ctx[DH];
+#pragma unroll
+                for (int c = 0; c < DH; ++c) ctx[c] = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (j < N) {
+                        const float a = sc[j] / z;
+#pragma unroll
+                        for (int c = 0; c < DH; ++c) ctx[c] = fmaf(a, sv[j * DH + c], ctx[c]);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < DH; c += 4) {
+                    const float4 v = rvalid ? make_float4(ctx[c], ctx[c + 1], ctx[c + 2], ctx[c + 3])
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                    float4 hi, lo;
+                    split4(v, hi, lo);
+                    const uint32_t off = kmaj(row, h * DH + c, D);
+                    *reinterpret_cast<float4 *>(sm + L::a_hi + off) = hi;
+                    *reinterpret_cast<float4 *>(sm + L::a_lo + off) = lo;
+                }
+                __syncwarp();
+            }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();
+
+        // ---- out = ctx Wout^T into TMEM columns [0, D) (Q is no longer read)
+        if (half == 1) {
+            for (int c = 0; c < n_out; ++c) {
+                const int s = c & 1;
+                if (c >= 2) mbar_wait(&bar[s], (ncommit[s] - 1) & 1);
+                load_b_chunk<P, H, DH>(p, n_qkv + c, sm, s, tid - 128);
+                named_sync(1, 128);
+                if (tid == 128) {
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    issue_chunk<D>(tmem, c * kNB, a_hi, a_lo, smem_u32(sm + L::b_hi(s)),
+                                   smem_u32(sm + L::b_lo(s)));
+                    mma_commit(&bar[s]);
+                }
+                ++ncommit[s];
+            }
+        } else {
+            ncommit[0] += (n_out + 1) / 2;
+            ncommit[1] += n_out / 2;
+        }
+        __syncthreads();
+        {
+            const int s = (n_out - 1) & 1;
+            mbar_wait(&bar[s], (ncommit[s] - 1) & 1);
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+
+        // ---- residual add and store: warp w stores columns [half*D/2, (half+1)*D/2);
+        // a tile whose MMA wait gave up is written as NaN, never as silent garbage
+        {
+            const float fail = *reinterpret_cast<volatile int *>(&g_tc_error) ? NAN : 0.f;
+            float *o = p.out + (b * N + n) * (int64_t)D;
+#pragma unroll
+            for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 8) {
+                float v[8];
+                tmem_ld8(tmem + lane_q + (uint32_t)c0, v);
+                if (rvalid) {
+                    const float4 x0 = __ldg(reinterpret_cast<const float4 *>(x + c0));
+                    const float4 x1 = __ldg(reinterpret_cast<const float4 *>(x + c0 + 4));
+                    reinterpret_cast<float4 *>(o + c0)[0] =
+                        make_float4(x0.x + v[0] + fail, x0.y + v[1] + fail, x0.z + v[2] + fail,
+                                    x0.w + v[3] + fail);
+                    reinterpret_cast<float4 *>(o + c0)[1] =
+                        make_float4(x1.x + v[4] + fail, x1.y + v[5] + fail, x1.z + v[6] + fail,
+                                    x1.w + v[7] + fail);
+                }
+            }
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();
+    }
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols));
+}
+
+}  // namespace tc
+
+// Host side: GAT_ERR_UNSUPPORTED when the shape is outside this path (the
+// caller then runs the SIMT kernel). This build instantiates P=16, H=4,
+// head_dim=24 (D=96), the block page's module shape, for N <= 32 nodes.
+gat_status_t dense_block_tc(int32_t B, int32_t N, int32_t D, int32_t H, int32_t P,
+                            const float *nodes, const float *pair, const float *mask,
+                            const float *ln_w, const float *ln_b, float ln_eps, const float *Wq,
+                            const float *Wk, const float *Wv, const float *W1, const float *b1,
+                            const float *W2, const float *b2, const float *Wout, float *out,
+                            cudaStream_t s) {
+    constexpr int kP = 16, kH = 4, kDH = 24;
+    using L = tc::Smem<kP, kH, kDH>;
+    if (P != kP || H != kH || D != kH * kDH || N < 1 || N > 32) return GAT_ERR_UNSUPPORTED;
+    const uint32_t smem = L::total(N);
+    if (smem > 227u * 1024u - 64u) return GAT_ERR_UNSUPPORTED;
+    auto kern = tc::dense_tc_kernel<kP, kH, kDH>;
+    static uint32_t configured = 0;
+    if (smem > configured) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return cuda_fail(e, "gat_dense_masked_attention: smem attribute");
+        configured = smem;
+    }
+    int zero = 0;
+    cudaError_t e = cudaMemcpyToSymbolAsync(tc::g_tc_error, &zero, sizeof(int), 0,
+                                            cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gat_dense_masked_attention: error flag");
+    tc::Params p{B, N, nodes, pair, mask, ln_w, ln_b, ln_eps, Wq, Wk, Wv, W1, b1, W2, b2, Wout, out};
+    const int64_t tiles = (B + tc::kGraphs - 1) / tc::kGraphs;
+    int64_t blocks = sm_count();
+    if (blocks > tiles) blocks = tiles;
+    kern<<<(unsigned)blocks, tc::kThreads, smem, s>>>(p);
+    return check_launch("gat_dense_masked_attention (tcgen05)");
+}
+
+}  // namespace gat
