@@ -140,29 +140,48 @@ struct Smem {
 // Weight chunk `chunk` of [Wq; Wk; Wv] (chunk < 3D/32) or of Wout (after),
 // split into the hi/lo B operand of ring slot s by the 128 threads of warps
 // 4-7 (t = 0..127); the output column runs fastest across threads so the
-// 16-byte shared stores of a warp land in distinct banks.
+// 16-byte shared stores of a warp land in distinct banks. Two steps, so the
+// global loads of the next chunk can be in
+// flight while the loader waits for its ring slot: fetch (global -> the
+// thread's registers) and store (split -> shared memory).
+template <int D>
+struct ChunkRegs {
+    static constexpr int kPer = kNB * (D / 4) / 128;  // float4 per loader thread
+    static_assert(kNB * (D / 4) % 128 == 0, "chunk must split evenly over 128 threads");
+    float4 w[kPer];
+};
+
 template <int P, int H, int DH>
-__device__ __forceinline__ void load_b_chunk(const Params &p, int chunk, unsigned char *sm, int s,
-                                             int t) {
-    using L = Smem<P, H, DH>;
-    constexpr int D = L::D, n_qkv = 3 * D / kNB;
+__device__ __forceinline__ void fetch_chunk(const Params &p, int chunk, ChunkRegs<H * DH> &r,
+                                            int t) {
+    constexpr int D = H * DH, n_qkv = 3 * D / kNB;
     const float *W;
     int row0;
     if (chunk < n_qkv) {
-        const int r = chunk * kNB;
-        W = r < D ? p.Wq : (r < 2 * D ? p.Wk : p.Wv);
-        row0 = r % D;
+        const int rr = chunk * kNB;
+        W = rr < D ? p.Wq : (rr < 2 * D ? p.Wk : p.Wv);
+        row0 = rr % D;
     } else {
         W = p.Wout;
         row0 = (chunk - n_qkv) * kNB;
     }
-    constexpr int kg_n = D / 4;
-#pragma unroll 2
-    for (int idx = t; idx < kNB * kg_n; idx += 128) {
-        const int o = idx % kNB, kg = idx / kNB;
-        const float4 w = __ldg(reinterpret_cast<const float4 *>(W + (int64_t)(row0 + o) * D) + kg);
+#pragma unroll
+    for (int i = 0; i < ChunkRegs<D>::kPer; ++i) {
+        const int idx = t + 128 * i, o = idx % kNB, kg = idx / kNB;
+        r.w[i] = __ldg(reinterpret_cast<const float4 *>(W + (int64_t)(row0 + o) * D) + kg);
+    }
+}
+
+template <int P, int H, int DH>
+__device__ __forceinline__ void store_chunk(const ChunkRegs<H * DH> &r, unsigned char *sm, int s,
+                                            int t) {
+    using L = Smem<P, H, DH>;
+    constexpr int D = L::D;
+#pragma unroll
+    for (int i = 0; i < ChunkRegs<D>::kPer; ++i) {
+        const int idx = t + 128 * i, o = idx % kNB, kg = idx / kNB;
         float4 hi, lo;
-        split4(w, hi, lo);
+        split4(r.w[i], hi, lo);
         const uint32_t off = kmaj(o, 4 * kg, D);
         *reinterpret_cast<float4 *>(sm + L::b_hi(s) + off) = hi;
         *reinterpret_cast<float4 *>(sm + L::b_lo(s) + off) = lo;
@@ -189,20 +208,32 @@ __device__ __forceinline__ void issue_chunk(uint32_t tmem, int col0, uint32_t a_
     }
 }
 
-// Relation-MLP bias of pairs (n, j), j in [j0, j1), for all heads.
+// Relation-MLP bias of pairs (n, j), j in [j0, j1), for all heads; stored as
+// bias_g[(h*N + j)*N + n] so a warp's lanes (n) write and read consecutive
+// words. The next pair's features are loaded while the current one computes.
 template <int P, int H>
 __device__ __forceinline__ void mlp_bias(const float *prow, int j0, int j1, const float *w1,
                                          const float *bb1, const float *w2, const float *bb2,
                                          float *bias_g, int N, int n) {
+    float4 nxt[P / 4];
+    if (j0 < j1) {
+#pragma unroll
+        for (int c4 = 0; c4 < P / 4; ++c4)
+            nxt[c4] = __ldg(reinterpret_cast<const float4 *>(prow + j0 * P) + c4);
+    }
     for (int j = j0; j < j1; ++j) {
         float pf[P];
 #pragma unroll
-        for (int c4 = 0; c4 < P; c4 += 4) {
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(prow + j * P + c4));
-            pf[c4] = v.x;
-            pf[c4 + 1] = v.y;
-            pf[c4 + 2] = v.z;
-            pf[c4 + 3] = v.w;
+        for (int c4 = 0; c4 < P / 4; ++c4) {
+            pf[4 * c4] = nxt[c4].x;
+            pf[4 * c4 + 1] = nxt[c4].y;
+            pf[4 * c4 + 2] = nxt[c4].z;
+            pf[4 * c4 + 3] = nxt[c4].w;
+        }
+        if (j + 1 < j1) {
+#pragma unroll
+            for (int c4 = 0; c4 < P / 4; ++c4)
+                nxt[c4] = __ldg(reinterpret_cast<const float4 *>(prow + (j + 1) * P) + c4);
         }
         float r[H];
 #pragma unroll
@@ -217,7 +248,7 @@ __device__ __forceinline__ void mlp_bias(const float *prow, int j0, int j1, cons
             for (int h = 0; h < H; ++h) r[h] = fmaf(w2[h * P + u], hid, r[h]);
         }
 #pragma unroll
-        for (int h = 0; h < H; ++h) bias_g[(h * N + n) * N + j] = r[h];
+        for (int h = 0; h < H; ++h) bias_g[(h * N + j) * N + n] = r[h];
     }
 }
 
@@ -272,21 +303,23 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         float *bias_g = bias + g * H * N * N;
 
         // ---- LayerNorm -> A (warps 0-3) | weight chunk 0 -> slot 0 (warps 4-7)
+        ChunkRegs<D> cr;  // next weight chunk, in flight in the loader threads' registers
         if (half == 0) {
+            // one read of the node row (registers), two-pass mean / biased variance
+            float4 xv[D / 4];
             float mean = 0.f, rstd = 0.f;
             if (rvalid) {
+#pragma unroll
+                for (int k4 = 0; k4 < D / 4; ++k4) xv[k4] = __ldg(reinterpret_cast<const float4 *>(x) + k4);
                 float s = 0.f;
-#pragma unroll 4
-                for (int k = 0; k < D; k += 4) {
-                    const float4 v = __ldg(reinterpret_cast<const float4 *>(x + k));
-                    s += (v.x + v.y) + (v.z + v.w);
-                }
+#pragma unroll
+                for (int k4 = 0; k4 < D / 4; ++k4) s += (xv[k4].x + xv[k4].y) + (xv[k4].z + xv[k4].w);
                 mean = s / (float)D;
                 float v2 = 0.f;
-#pragma unroll 4
-                for (int k = 0; k < D; k += 4) {
-                    const float4 v = __ldg(reinterpret_cast<const float4 *>(x + k));
-                    const float a0 = v.x - mean, a1 = v.y - mean, a2 = v.z - mean, a3 = v.w - mean;
+#pragma unroll
+                for (int k4 = 0; k4 < D / 4; ++k4) {
+                    const float a0 = xv[k4].x - mean, a1 = xv[k4].y - mean, a2 = xv[k4].z - mean,
+                                a3 = xv[k4].w - mean;
                     v2 = fmaf(a0, a0, v2);
                     v2 = fmaf(a1, a1, v2);
                     v2 = fmaf(a2, a2, v2);
@@ -294,13 +327,13 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 }
                 rstd = 1.0f / sqrtf(v2 / (float)D + p.ln_eps);
             }
-#pragma unroll 4
-            for (int k = 0; k < D; k += 4) {
+#pragma unroll
+            for (int k4 = 0; k4 < D / 4; ++k4) {
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (rvalid) {
-                    const float4 v = __ldg(reinterpret_cast<const float4 *>(x + k));
-                    const float4 gw = __ldg(reinterpret_cast<const float4 *>(p.ln_w + k));
-                    const float4 gb = __ldg(reinterpret_cast<const float4 *>(p.ln_b + k));
+                    const float4 v = xv[k4];
+                    const float4 gw = __ldg(reinterpret_cast<const float4 *>(p.ln_w) + k4);
+                    const float4 gb = __ldg(reinterpret_cast<const float4 *>(p.ln_b) + k4);
                     a = make_float4((v.x - mean) * rstd * gw.x + gb.x,
                                     (v.y - mean) * rstd * gw.y + gb.y,
                                     (v.z - mean) * rstd * gw.z + gb.z,
@@ -308,14 +341,16 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 }
                 float4 hi, lo;
                 split4(a, hi, lo);
-                const uint32_t off = kmaj(row, k, D);
+                const uint32_t off = kmaj(row, 4 * k4, D);
                 *reinterpret_cast<float4 *>(sm + L::a_hi + off) = hi;
                 *reinterpret_cast<float4 *>(sm + L::a_lo + off) = lo;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         } else {
             // every MMA of the previous tile completed before its epilogue
-            load_b_chunk<P, H, DH>(p, 0, sm, 0, tid - 128);
+            fetch_chunk<P, H, DH>(p, 0, cr, tid - 128);
+            store_chunk<P, H, DH>(cr, sm, 0, tid - 128);
+            fetch_chunk<P, H, DH>(p, 1, cr, tid - 128);
         }
         __syncthreads();
 
@@ -325,7 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 const int s = c & 1;
                 if (c > 0) {
                     if (c >= 2) mbar_wait(&bar[s], (ncommit[s] - 1) & 1);  // chunk c-2 done
-                    load_b_chunk<P, H, DH>(p, c, sm, s, tid - 128);
+                    store_chunk<P, H, DH>(cr, sm, s, tid - 128);
+                    if (c + 1 < n_qkv) fetch_chunk<P, H, DH>(p, c + 1, cr, tid - 128);
                 }
                 named_sync(1, 128);
                 if (tid == 128) {
@@ -359,16 +395,20 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 float q[DH], kv[DH];
 #pragma unroll
                 for (int c0 = 0; c0 < DH; c0 += 8) {
+                    // staged row-major ([node][c]) with 16-byte stores; the reads below
+                    // are 16-byte warp-wide broadcasts
                     tmem_ld8(tmem + lane_q + (uint32_t)(h * DH + c0), q + c0);
                     tmem_ld8(tmem + lane_q + (uint32_t)(D + h * DH + c0), kv + c0);
                     if (rvalid) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) sk[n * DH + c0 + i] = kv[c0 + i];
+                        float4 *d4 = reinterpret_cast<float4 *>(sk + n * DH + c0);
+                        d4[0] = make_float4(kv[c0], kv[c0 + 1], kv[c0 + 2], kv[c0 + 3]);
+                        d4[1] = make_float4(kv[c0 + 4], kv[c0 + 5], kv[c0 + 6], kv[c0 + 7]);
                     }
                     tmem_ld8(tmem + lane_q + (uint32_t)(2 * D + h * DH + c0), kv + c0);
                     if (rvalid) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) sv[n * DH + c0 + i] = kv[c0 + i];
+                        float4 *d4 = reinterpret_cast<float4 *>(sv + n * DH + c0);
+                        d4[0] = make_float4(kv[c0], kv[c0 + 1], kv[c0 + 2], kv[c0 + 3]);
+                        d4[1] = make_float4(kv[c0 + 4], kv[c0 + 5], kv[c0 + 6], kv[c0 + 7]);
                     }
                 }
                 __syncwarp();
@@ -380,8 +420,14 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                     if (j < N && rvalid) {
                         float a = 0.f;
 #pragma unroll
-                        for (int c = 0; c < DH; ++c) a = fmaf(q[c], sk[j * DH + c], a);
-                        s = a * inv_sqrt_dh + bias_g[(h * N + n) * N + j];
+                        for (int c = 0; c < DH; c += 4) {
+                            const float4 k4 = *reinterpret_cast<const float4 *>(sk + j * DH + c);
+                            a = fmaf(q[c], k4.x, a);
+                            a = fmaf(q[c + 1], k4.y, a);
+                            a = fmaf(q[c + 2], k4.z, a);
+                            a = fmaf(q[c + 3], k4.w, a);
+                        }
+                        s = a * inv_sqrt_dh + bias_g[(h * N + j) * N + n];
                         if (__ldg(mk + j) < 0.5f) s = -INFINITY;
                     }
                     sc[j] = s;
@@ -402,7 +448,13 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                     if (j < N) {
                         const float a = sc[j] / z;
 #pragma unroll
-                        for (int c = 0; c < DH; ++c) ctx[c] = fmaf(a, sv[j * DH + c], ctx[c]);
+                        for (int c = 0; c < DH; c += 4) {
+                            const float4 v4 = *reinterpret_cast<const float4 *>(sv + j * DH + c);
+                            ctx[c] = fmaf(a, v4.x, ctx[c]);
+                            ctx[c + 1] = fmaf(a, v4.y, ctx[c + 1]);
+                            ctx[c + 2] = fmaf(a, v4.z, ctx[c + 2]);
+                            ctx[c + 3] = fmaf(a, v4.w, ctx[c + 3]);
+                        }
                     }
                 }
 #pragma unroll
@@ -418,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 __syncwarp();
             }
         }
+        if (half == 1) fetch_chunk<P, H, DH>(p, n_qkv, cr, tid - 128);  // out-projection chunk 0
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncthreads();
@@ -427,7 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             for (int c = 0; c < n_out; ++c) {
                 const int s = c & 1;
                 if (c >= 2) mbar_wait(&bar[s], (ncommit[s] - 1) & 1);
-                load_b_chunk<P, H, DH>(p, n_qkv + c, sm, s, tid - 128);
+                store_chunk<P, H, DH>(cr, sm, s, tid - 128);
+                if (c + 1 < n_out) fetch_chunk<P, H, DH>(p, n_qkv + c + 1, cr, tid - 128);
                 named_sync(1, 128);
                 if (tid == 128) {
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
