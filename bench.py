@@ -411,11 +411,13 @@ def bench_small(name, args):
     dev = torch.device("cuda", 0)
     g = W.WORKLOADS[name][0]()
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    flops, tensor_flops = 0.0, 0.0
     if name == "edge_softmax":
         rp, s = t(g["row_ptr"]), t(g["scores"])
         out = torch.empty_like(s)
         fn = lambda: gat.gat_edge_softmax(rp, s, g["H"], out=out)  # noqa: E731
         units, launches = g["n_edges"] * g["H"], 1
+        alg_bytes = 4 * (g["n_rows"] + 1) + 8 * g["n_edges"] * g["H"]
     elif name == "aggregate":
         rp, ci, s = t(g["row_ptr"]), t(g["col_idx"]), t(g["scores"]).reshape(-1, 1)
         vals = t(g["values"]).reshape(g["n_src"], 1, g["F"])
@@ -426,11 +428,17 @@ def bench_small(name, args):
             gat.gat_edge_softmax(rp, s, 1, out=w)
             gat.gat_spmm_weighted(rp, ci, w, vals, 1, g["F"], out=out)
         units, launches = g["n_edges"], 2
+        # softmax: row_ptr + scores in + weights out; spmm: row_ptr, col_idx,
+        # weights, one gathered value row per edge, one output row per row
+        alg_bytes = (4 * (g["n_rows"] + 1) + 8 * g["n_edges"]) + \
+            (4 * (g["n_rows"] + 1) + g["n_edges"] * (4 + 4 + 4 * g["F"]) + 4 * g["F"] * g["n_rows"])
     elif name == "sddmm":
         si, di, a, b = t(g["src_idx"]), t(g["dst_idx"]), t(g["src_feat"]), t(g["dst_feat"])
         out = torch.empty((g["n_edges"], 1), device=dev)
         fn = lambda: gat.gat_sddmm(si, a, b, 1, g["F"], dst_idx=di, out=out)  # noqa: E731
         units, launches = g["n_edges"], 1
+        alg_bytes = g["n_edges"] * (4 + 4 + 2 * 4 * g["F"] + 4)
+        flops = 2.0 * g["n_edges"] * g["F"]
     elif name == "dense":
         keys = ("nodes", "pair_feats", "edge_mask", "ln_w", "ln_b", "Wq", "Wk", "Wv", "W1",
                 "b1", "W2", "b2", "Wout")
@@ -441,6 +449,14 @@ def bench_small(name, args):
             tt["nodes"], tt["pair_feats"], tt["edge_mask"], tt["ln_w"], tt["ln_b"],
             g["ln_eps"], *wk, H=g["H"], out=out)
         units, launches = g["B"] * g["H"] * g["N"] * g["N"], 1
+        B_, N_, D_, H_, P_ = g["B"], g["N"], g["D"], g["H"], g["P"]
+        # per graph: nodes + pair features + mask in, output out (fp32)
+        alg_bytes = B_ * 4 * (2 * N_ * D_ + N_ * N_ * P_ + N_ * N_) + 4 * (4 * D_ * D_)
+        proj = 2.0 * N_ * D_ * D_ * 4                        # Q, K, V, out projections
+        attn = 2.0 * 2 * H_ * N_ * N_ * (D_ // H_)           # Q K^T and A V
+        mlp = 2.0 * N_ * N_ * (P_ * P_ + H_ * P_)            # relation MLP
+        flops = B_ * (proj + attn + mlp)
+        tensor_flops = B_ * proj
     else:
         raise ValueError(name)
     for _ in range(max(3, args.warmup)):
@@ -454,8 +470,24 @@ def bench_small(name, args):
     ev1.record()
     torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1) / reps
-    return {"ms_per_step": ms, "units_per_s": units / (ms * 1e-3), "launches_per_step": launches,
-            "warm": True}
+    hbm_peak, bf16_peak, kind = measured_peaks()
+    res = {"ms_per_step": ms, "units_per_s": units / (ms * 1e-3), "launches_per_step": launches,
+           "warm": True, "algorithmic_bytes": alg_bytes,
+           "achieved_gbs": alg_bytes / (ms * 1e-3) / 1e9,
+           "hbm_frac": alg_bytes / (ms * 1e-3) / 1e9 / hbm_peak}
+    if flops:
+        res["achieved_tflops"] = flops / (ms * 1e-3) / 1e12
+    if tensor_flops:
+        # tf32 tensor peak = measured bf16 peak x nominal tf32/bf16 ratio (1.1/2.25);
+        # 3xTF32 issues three tensor products per useful one
+        tf32_peak = bf16_peak * (1.1 / 2.25)
+        res["projection_tflops_useful"] = tensor_flops / (ms * 1e-3) / 1e12
+        res["tensor_issue_frac_of_tf32_peak"] = 3 * tensor_flops / (ms * 1e-3) / 1e12 / tf32_peak
+        res["tf32_peak_tflops"] = tf32_peak
+        res["peak_kind"] = kind
+    if name in ("edge_softmax", "aggregate", "sddmm"):
+        res["note"] = "L2-resident and launch-latency bound at this size; fractions are not a roofline claim"
+    return res
 
 
 def main():

@@ -4,38 +4,42 @@
 // The block page's module (Kimi-K2.6 l2_p4, reference model) spends three
 // quarters of its arithmetic in four D x D projections (Q, K, V, out). Here they
 // run as 128-row tcgen05 MMAs: a tile is 4 graphs, each padded to 32 rows, so
-// graph g of the tile owns TMEM lanes 32g..32g+31 and is handled by warps g and
-// g+4 (the two warps allowed to read that lane quarter). fp32 accuracy comes
-// from the 3xTF32 split: every operand x = hi + lo with hi = tf32(x) (round to
-// nearest) and lo = x - hi, and A*B ~ hi_A hi_B + hi_A lo_B + lo_A hi_B (the
-// dropped lo_A lo_B term and lo's own tf32 truncation are ~2^-20 relative).
+// graph g of the tile owns TMEM lanes 32g..32g+31 and is served by the four
+// warps g, g+4, g+8, g+12 (the warps allowed to read that lane quarter). fp32
+// accuracy comes from the 3xTF32 split: every operand x = hi + lo with
+// hi = tf32(x) (round to nearest) and lo = x - hi, and
+// A*B ~ hi_A hi_B + hi_A lo_B + lo_A hi_B (the dropped lo_A lo_B term and lo's
+// own tf32 truncation are ~2^-20 relative).
 //
-// Roles inside one CTA (8 warps, persistent over tiles, one CTA per SM):
-//   warps 0-3  LayerNorm (thread per node row) -> hi/lo A operand in shared
-//              memory; then the relation-MLP bias of most node pairs.
-//   warps 4-7  split the weights into 32-column hi/lo B chunks (2-slot ring)
-//              and, through their first thread, issue the MMAs of each chunk
-//              (commit -> one mbarrier per ring slot); then the remaining MLP
-//              pairs.
-//   all        attention per (graph, head pair): Q, K, V rows from TMEM, K and
-//              V staged in shared memory, scores + bias + mask, softmax,
-//              context -> hi/lo A operand; out-projection chunks into the TMEM
-//              columns that held Q; residual add; store.
-// Operands use the no-swizzle K-major layout of 8-row x 16-byte core
-// matrices (leading byte offset 128 between K neighbours, stride byte offset
-// (D/4)*128 between 8-row groups). Every mbarrier wait is bounded; giving up
-// sets a device flag that the host turns into GAT_ERR_CUDA.
+// One CTA of 16 warps per SM, persistent over tiles. Warp w has lane quarter
+// (graph) g = w % 4 and role group k = w / 4:
+//   k = 0  LayerNorm, thread per node row -> hi/lo A operand (shared memory,
+//          no-swizzle K-major 8-row x 16-byte core matrices)
+//   k = 1  splits the weights into 48-column hi/lo B chunks (2-slot ring, the
+//          next chunk's global loads in flight in registers) and, through its
+//          first thread, issues each chunk's MMAs (commit -> one mbarrier per
+//          ring slot)
+//   all    relation-MLP bias of the node pairs (split over the four groups,
+//          the groups that start early take more pairs)
+//   k      attention for head k: Q, K, V rows from TMEM, K and V staged in the
+//          A region (idle once Q|K|V are in TMEM), scores + bias + mask,
+//          softmax, context kept in registers until every warp has read its
+//          staging, then written as the hi/lo A operand of the out-projection
+//   k = 1  out-projection chunks into the TMEM columns that held Q
+//   k      residual add and store of output columns [kD/4, (k+1)D/4)
+// Every mbarrier wait is bounded; a wait that gives up raises a device flag
+// and the tile is written as NaN (never as silent garbage).
 #include "common.cuh"
 
 namespace gat {
 
 namespace tc {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kGraphs = 4;      // graphs per tile (one 32-row TMEM lane quarter each)
 constexpr int kRows = 128;      // MMA M
-constexpr int kNB = 32;         // output columns per weight chunk (MMA N)
+constexpr int kNB = 48;         // output columns per weight chunk (MMA N)
 constexpr int kTmemCols = 512;  // Q|K|V need 3D columns
 constexpr uint32_t kWaitTries = 1u << 24;
 
@@ -129,21 +133,22 @@ struct Smem {
                               b_lo0 = al(b_hi0 + kB), b_hi1 = al(b_lo0 + kB),
                               b_lo1 = al(b_hi1 + kB), mlp = al(b_lo1 + kB),
                               bias = mlp + (uint32_t)((P * P + P + H * P + H) * 4);
-    // bias [4][H][N][N] and the per-warp K/V staging [8][2][N][DH] follow;
-    // their size depends on N (<= 32)
-    __host__ __device__ static uint32_t stage(int N) { return bias + kGraphs * H * N * N * 4; }
-    __host__ __device__ static uint32_t total(int N) { return stage(N) + kWarps * 2 * N * DH * 4; }
+    // K/V staging of attention reuses [a_hi, a_lo + kA): 16 warps x 2 x N x DH floats
+    __host__ __device__ static uint32_t stage_bytes(int N) { return kWarps * 2 * N * DH * 4; }
+    __host__ __device__ static uint32_t total(int N) { return bias + kGraphs * H * N * N * 4; }
+    __host__ __device__ static bool fits(int N) {
+        return stage_bytes(N) <= a_lo + kA && total(N) <= 227u * 1024u - 64u;
+    }
     __device__ static uint32_t b_hi(int s) { return s ? b_hi1 : b_hi0; }
     __device__ static uint32_t b_lo(int s) { return s ? b_lo1 : b_lo0; }
 };
 
-// Weight chunk `chunk` of [Wq; Wk; Wv] (chunk < 3D/32) or of Wout (after),
-// split into the hi/lo B operand of ring slot s by the 128 threads of warps
-// 4-7 (t = 0..127); the output column runs fastest across threads so the
-// 16-byte shared stores of a warp land in distinct banks. Two steps, so the
-// global loads of the next chunk can be in
-// flight while the loader waits for its ring slot: fetch (global -> the
-// thread's registers) and store (split -> shared memory).
+// Weight chunk `chunk` of [Wq; Wk; Wv] (chunk < 3D/kNB) or of Wout (after),
+// split into the hi/lo B operand of ring slot s by the 128 threads of group 1
+// (t = 0..127). Output column fastest across threads, so a warp's 16-byte
+// shared stores land in distinct banks. Two steps, so the next chunk's global
+// loads are in flight while the loader waits for its ring slot: fetch (global
+// -> registers) and store (split -> shared memory).
 template <int D>
 struct ChunkRegs {
     static constexpr int kPer = kNB * (D / 4) / 128;  // float4 per loader thread
@@ -155,20 +160,20 @@ template <int P, int H, int DH>
 __device__ __forceinline__ void fetch_chunk(const Params &p, int chunk, ChunkRegs<H * DH> &r,
                                             int t) {
     constexpr int D = H * DH, n_qkv = 3 * D / kNB;
-    const float *W;
-    int row0;
-    if (chunk < n_qkv) {
-        const int rr = chunk * kNB;
-        W = rr < D ? p.Wq : (rr < 2 * D ? p.Wk : p.Wv);
-        row0 = rr % D;
-    } else {
-        W = p.Wout;
-        row0 = (chunk - n_qkv) * kNB;
-    }
 #pragma unroll
     for (int i = 0; i < ChunkRegs<D>::kPer; ++i) {
         const int idx = t + 128 * i, o = idx % kNB, kg = idx / kNB;
-        r.w[i] = __ldg(reinterpret_cast<const float4 *>(W + (int64_t)(row0 + o) * D) + kg);
+        int row;
+        const float *W;
+        if (chunk < n_qkv) {
+            const int rr = chunk * kNB + o;  // row of the stacked [Wq; Wk; Wv]
+            W = rr < D ? p.Wq : (rr < 2 * D ? p.Wk : p.Wv);
+            row = rr % D;
+        } else {
+            W = p.Wout;
+            row = (chunk - n_qkv) * kNB + o;
+        }
+        r.w[i] = __ldg(reinterpret_cast<const float4 *>(W + (int64_t)row * D) + kg);
     }
 }
 
@@ -189,7 +194,7 @@ __device__ __forceinline__ void store_chunk(const ChunkRegs<H * DH> &r, unsigned
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// The 3xTF32 MMAs of one 32-column chunk: D[:, col0:col0+32] = A B^T.
+// The 3xTF32 MMAs of one kNB-column chunk: D[:, col0:col0+kNB] = A B^T.
 template <int D>
 __device__ __forceinline__ void issue_chunk(uint32_t tmem, int col0, uint32_t a_hi, uint32_t a_lo,
                                             uint32_t b_hi, uint32_t b_lo) {
@@ -240,10 +245,14 @@ __device__ __forceinline__ void mlp_bias(const float *prow, int j0, int j1, cons
         for (int h = 0; h < H; ++h) r[h] = bb2[h];
 #pragma unroll
         for (int u = 0; u < P; ++u) {
-            float a = bb1[u];
+            float a0 = bb1[u], a1 = 0.f;
 #pragma unroll
-            for (int c = 0; c < P; ++c) a = fmaf(w1[u * P + c], pf[c], a);
-            const float hid = a / (1.0f + expf(-a));
+            for (int c = 0; c < P; c += 2) {
+                a0 = fmaf(w1[u * P + c], pf[c], a0);
+                a1 = fmaf(w1[u * P + c + 1], pf[c + 1], a1);
+            }
+            const float a = a0 + a1;
+            const float hid = __fdividef(a, 1.0f + expf(-a));  // SiLU
 #pragma unroll
             for (int h = 0; h < H; ++h) r[h] = fmaf(w2[h * P + u], hid, r[h]);
         }
@@ -256,20 +265,27 @@ template <int P, int H, int DH>
 __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
     using L = Smem<P, H, DH>;
     constexpr int D = L::D, n_qkv = 3 * D / kNB, n_out = D / kNB;
+    static_assert(H == 4, "one attention head per role group");
+    static_assert(3 * D % kNB == 0 && D % kNB == 0 && DH % 8 == 0, "chunking");
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ uint64_t bar[2];
     __shared__ uint32_t tmem_slot;
     const int N = p.N;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = warp & 3;      // graph of the tile / TMEM lane quarter
-    const int half = warp >> 2;  // 0: warps 0-3, 1: warps 4-7
+    const int g = warp & 3;   // graph of the tile / TMEM lane quarter
+    const int grp = warp >> 2;  // role group, also the attention head
+    const int tl = tid - 128;   // loader thread index (group 1)
     float *w1 = reinterpret_cast<float *>(sm + L::mlp), *bb1 = w1 + P * P, *w2 = bb1 + P,
           *bb2 = w2 + H * P;
     float *bias = reinterpret_cast<float *>(sm + L::bias);
-    float *stage = reinterpret_cast<float *>(sm + L::stage(N)) + warp * 2 * N * DH;
+    float *stage = reinterpret_cast<float *>(sm) + warp * 2 * N * DH;  // in the A region
     const uint32_t a_hi = smem_u32(sm + L::a_hi), a_lo = smem_u32(sm + L::a_lo);
     const float inv_sqrt_dh = 1.0f / sqrtf((float)DH);
-    const int jsplit = (N * 5 + 7) / 8;  // MLP pairs [0, jsplit) on warps 0-3, rest on 4-7
+    // relation-MLP pair ranges: groups 2 and 3 start at once, group 0 after
+    // LayerNorm, group 1 after issuing Q|K|V
+    const int jb2 = 0, jb3 = (3 * N) / 8, jb0 = (6 * N) / 8, jb1 = min(N, (6 * N) / 8 + (N + 5) / 6);
+    const int j_lo = grp == 2 ? jb2 : grp == 3 ? jb3 : grp == 0 ? jb0 : jb1;
+    const int j_hi = grp == 2 ? jb3 : grp == 3 ? jb0 : grp == 0 ? jb1 : N;
 
     for (int i = tid; i < P * P; i += kThreads) w1[i] = p.W1[i];
     for (int i = tid; i < P; i += kThreads) bb1[i] = p.b1[i];
@@ -302,24 +318,23 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         const float *prow = p.pair + ((b * N + n) * (int64_t)N) * P;
         float *bias_g = bias + g * H * N * N;
 
-        // ---- LayerNorm -> A (warps 0-3) | weight chunk 0 -> slot 0 (warps 4-7)
-        ChunkRegs<D> cr;  // next weight chunk, in flight in the loader threads' registers
-        if (half == 0) {
-            // one read of the node row (registers), two-pass mean / biased variance
-            float4 xv[D / 4];
+        // ---- LayerNorm -> A (group 0) | first weight chunk (group 1) | MLP (groups 2, 3)
+        ChunkRegs<D> cr;
+        if (grp == 0) {
             float mean = 0.f, rstd = 0.f;
             if (rvalid) {
-#pragma unroll
-                for (int k4 = 0; k4 < D / 4; ++k4) xv[k4] = __ldg(reinterpret_cast<const float4 *>(x) + k4);
                 float s = 0.f;
-#pragma unroll
-                for (int k4 = 0; k4 < D / 4; ++k4) s += (xv[k4].x + xv[k4].y) + (xv[k4].z + xv[k4].w);
+#pragma unroll 6
+                for (int k4 = 0; k4 < D / 4; ++k4) {
+                    const float4 v = __ldg(reinterpret_cast<const float4 *>(x) + k4);
+                    s += (v.x + v.y) + (v.z + v.w);
+                }
                 mean = s / (float)D;
                 float v2 = 0.f;
-#pragma unroll
+#pragma unroll 6
                 for (int k4 = 0; k4 < D / 4; ++k4) {
-                    const float a0 = xv[k4].x - mean, a1 = xv[k4].y - mean, a2 = xv[k4].z - mean,
-                                a3 = xv[k4].w - mean;
+                    const float4 v = __ldg(reinterpret_cast<const float4 *>(x) + k4);
+                    const float a0 = v.x - mean, a1 = v.y - mean, a2 = v.z - mean, a3 = v.w - mean;
                     v2 = fmaf(a0, a0, v2);
                     v2 = fmaf(a1, a1, v2);
                     v2 = fmaf(a2, a2, v2);
@@ -327,11 +342,11 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 }
                 rstd = 1.0f / sqrtf(v2 / (float)D + p.ln_eps);
             }
-#pragma unroll
+#pragma unroll 6
             for (int k4 = 0; k4 < D / 4; ++k4) {
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (rvalid) {
-                    const float4 v = xv[k4];
+                    const float4 v = __ldg(reinterpret_cast<const float4 *>(x) + k4);
                     const float4 gw = __ldg(reinterpret_cast<const float4 *>(p.ln_w) + k4);
                     const float4 gb = __ldg(reinterpret_cast<const float4 *>(p.ln_b) + k4);
                     a = make_float4((v.x - mean) * rstd * gw.x + gb.x,
@@ -346,22 +361,22 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 *reinterpret_cast<float4 *>(sm + L::a_lo + off) = lo;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        } else {
+        } else if (grp == 1) {
             // every MMA of the previous tile completed before its epilogue
-            fetch_chunk<P, H, DH>(p, 0, cr, tid - 128);
-            store_chunk<P, H, DH>(cr, sm, 0, tid - 128);
-            fetch_chunk<P, H, DH>(p, 1, cr, tid - 128);
+            fetch_chunk<P, H, DH>(p, 0, cr, tl);
+            store_chunk<P, H, DH>(cr, sm, 0, tl);
+            fetch_chunk<P, H, DH>(p, 1, cr, tl);
         }
-        __syncthreads();
+        __syncthreads();  // A operand and chunk 0 in shared memory
 
-        // ---- Q|K|V: warps 4-7 stream chunks and issue; warps 0-3 start the MLP
-        if (half == 1) {
+        // ---- Q|K|V (group 1 streams chunks and issues) and the relation MLP
+        if (grp == 1) {
             for (int c = 0; c < n_qkv; ++c) {
                 const int s = c & 1;
                 if (c > 0) {
                     if (c >= 2) mbar_wait(&bar[s], (ncommit[s] - 1) & 1);  // chunk c-2 done
-                    store_chunk<P, H, DH>(cr, sm, s, tid - 128);
-                    if (c + 1 < n_qkv) fetch_chunk<P, H, DH>(p, c + 1, cr, tid - 128);
+                    store_chunk<P, H, DH>(cr, sm, s, tl);
+                    if (c + 1 < n_qkv) fetch_chunk<P, H, DH>(p, c + 1, cr, tl);
                 }
                 named_sync(1, 128);
                 if (tid == 128) {
@@ -372,116 +387,111 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 }
                 ++ncommit[s];
             }
-            if (rvalid) mlp_bias<P, H>(prow, jsplit, N, w1, bb1, w2, bb2, bias_g, N, n);
         } else {
             ncommit[0] += (n_qkv + 1) / 2;
             ncommit[1] += n_qkv / 2;
-            if (rvalid) mlp_bias<P, H>(prow, 0, jsplit, w1, bb1, w2, bb2, bias_g, N, n);
         }
-        __syncthreads();
+        if (rvalid) mlp_bias<P, H>(prow, j_lo, j_hi, w1, bb1, w2, bb2, bias_g, N, n);
+        __syncthreads();  // bias complete
         {
             const int s = (n_qkv - 1) & 1;  // the last commit covers every earlier MMA
             mbar_wait(&bar[s], (ncommit[s] - 1) & 1);
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
-        // ---- attention: warp w -> graph g, heads [half*H/2, (half+1)*H/2)
+        // ---- attention, head h = grp: K, V staged in the (now idle) A region
+        const int h = grp;
+        float ctx[DH];
         {
             const float *mk = p.mask + (b * N + n) * (int64_t)N;
             float *sk = stage, *sv = stage + N * DH;
-#pragma unroll 1
-            for (int hh = 0; hh < H / 2; ++hh) {
-                const int h = half * (H / 2) + hh;
-                float q[DH], kv[DH];
+            float q[DH], kv[8];
 #pragma unroll
-                for (int c0 = 0; c0 < DH; c0 += 8) {
-                    // staged row-major ([node][c]) with 16-byte stores; the reads below
-                    // are 16-byte warp-wide broadcasts
-                    tmem_ld8(tmem + lane_q + (uint32_t)(h * DH + c0), q + c0);
-                    tmem_ld8(tmem + lane_q + (uint32_t)(D + h * DH + c0), kv + c0);
-                    if (rvalid) {
-                        float4 *d4 = reinterpret_cast<float4 *>(sk + n * DH + c0);
-                        d4[0] = make_float4(kv[c0], kv[c0 + 1], kv[c0 + 2], kv[c0 + 3]);
-                        d4[1] = make_float4(kv[c0 + 4], kv[c0 + 5], kv[c0 + 6], kv[c0 + 7]);
-                    }
-                    tmem_ld8(tmem + lane_q + (uint32_t)(2 * D + h * DH + c0), kv + c0);
-                    if (rvalid) {
-                        float4 *d4 = reinterpret_cast<float4 *>(sv + n * DH + c0);
-                        d4[0] = make_float4(kv[c0], kv[c0 + 1], kv[c0 + 2], kv[c0 + 3]);
-                        d4[1] = make_float4(kv[c0 + 4], kv[c0 + 5], kv[c0 + 6], kv[c0 + 7]);
-                    }
+            for (int c0 = 0; c0 < DH; c0 += 8) {
+                tmem_ld8(tmem + lane_q + (uint32_t)(h * DH + c0), q + c0);
+                tmem_ld8(tmem + lane_q + (uint32_t)(D + h * DH + c0), kv);
+                if (rvalid) {
+                    float4 *d4 = reinterpret_cast<float4 *>(sk + n * DH + c0);
+                    d4[0] = make_float4(kv[0], kv[1], kv[2], kv[3]);
+                    d4[1] = make_float4(kv[4], kv[5], kv[6], kv[7]);
                 }
-                __syncwarp();
-                float sc[32];
-                float m = -INFINITY;
+                tmem_ld8(tmem + lane_q + (uint32_t)(2 * D + h * DH + c0), kv);
+                if (rvalid) {
+                    float4 *d4 = reinterpret_cast<float4 *>(sv + n * DH + c0);
+                    d4[0] = make_float4(kv[0], kv[1], kv[2], kv[3]);
+                    d4[1] = make_float4(kv[4], kv[5], kv[6], kv[7]);
+                }
+            }
+            __syncwarp();
+            float sc[32];
+            float m = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    float s = -INFINITY;
-                    if (j < N && rvalid) {
-                        float a = 0.f;
+            for (int j = 0; j < 32; ++j) {
+                float s = -INFINITY;
+                if (j < N && rvalid) {
+                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-                        for (int c = 0; c < DH; c += 4) {
-                            const float4 k4 = *reinterpret_cast<const float4 *>(sk + j * DH + c);
-                            a = fmaf(q[c], k4.x, a);
-                            a = fmaf(q[c + 1], k4.y, a);
-                            a = fmaf(q[c + 2], k4.z, a);
-                            a = fmaf(q[c + 3], k4.w, a);
-                        }
-                        s = a * inv_sqrt_dh + bias_g[(h * N + j) * N + n];
-                        if (__ldg(mk + j) < 0.5f) s = -INFINITY;
+                    for (int c = 0; c < DH; c += 4) {
+                        const float4 k4 = *reinterpret_cast<const float4 *>(sk + j * DH + c);
+                        a0 = fmaf(q[c], k4.x, a0);
+                        a1 = fmaf(q[c + 1], k4.y, a1);
+                        a2 = fmaf(q[c + 2], k4.z, a2);
+                        a3 = fmaf(q[c + 3], k4.w, a3);
                     }
-                    sc[j] = s;
-                    m = fmaxf(m, s);
+                    s = ((a0 + a1) + (a2 + a3)) * inv_sqrt_dh + bias_g[(h * N + j) * N + n];
+                    if (__ldg(mk + j) < 0.5f) s = -INFINITY;
                 }
-                float z = 0.f;
+                sc[j] = s;
+                m = fmaxf(m, s);
+            }
+            float z = 0.f;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float e = (j < N) ? expf(sc[j] - m) : 0.f;  // all -inf row: NaN
-                    sc[j] = e;
-                    z += e;
-                }
-                float ctx[DH];
+            for (int j = 0; j < 32; ++j) {
+                const float e = (j < N) ? expf(sc[j] - m) : 0.f;  // all -inf row: NaN
+                sc[j] = e;
+                z += e;
+            }
+            const float inv_z = 1.0f / z;
 #pragma unroll
-                for (int c = 0; c < DH; ++c) ctx[c] = 0.f;
+            for (int c = 0; c < DH; ++c) ctx[c] = 0.f;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (j < N) {
-                        const float a = sc[j] / z;
+            for (int j = 0; j < 32; ++j) {
+                if (j < N) {
+                    const float a = sc[j] * inv_z;
 #pragma unroll
-                        for (int c = 0; c < DH; c += 4) {
-                            const float4 v4 = *reinterpret_cast<const float4 *>(sv + j * DH + c);
-                            ctx[c] = fmaf(a, v4.x, ctx[c]);
-                            ctx[c + 1] = fmaf(a, v4.y, ctx[c + 1]);
-                            ctx[c + 2] = fmaf(a, v4.z, ctx[c + 2]);
-                            ctx[c + 3] = fmaf(a, v4.w, ctx[c + 3]);
-                        }
+                    for (int c = 0; c < DH; c += 4) {
+                        const float4 v4 = *reinterpret_cast<const float4 *>(sv + j * DH + c);
+                        ctx[c] = fmaf(a, v4.x, ctx[c]);
+                        ctx[c + 1] = fmaf(a, v4.y, ctx[c + 1]);
+                        ctx[c + 2] = fmaf(a, v4.z, ctx[c + 2]);
+                        ctx[c + 3] = fmaf(a, v4.w, ctx[c + 3]);
                     }
                 }
-#pragma unroll
-                for (int c = 0; c < DH; c += 4) {
-                    const float4 v = rvalid ? make_float4(ctx[c], ctx[c + 1], ctx[c + 2], ctx[c + 3])
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-                    float4 hi, lo;
-                    split4(v, hi, lo);
-                    const uint32_t off = kmaj(row, h * DH + c, D);
-                    *reinterpret_cast<float4 *>(sm + L::a_hi + off) = hi;
-                    *reinterpret_cast<float4 *>(sm + L::a_lo + off) = lo;
-                }
-                __syncwarp();
             }
         }
-        if (half == 1) fetch_chunk<P, H, DH>(p, n_qkv, cr, tid - 128);  // out-projection chunk 0
+        if (grp == 1) fetch_chunk<P, H, DH>(p, n_qkv, cr, tl);  // out-projection chunk 0
+        __syncthreads();  // every warp is done with its staging: A region free again
+#pragma unroll
+        for (int c = 0; c < DH; c += 4) {
+            const float4 v = rvalid ? make_float4(ctx[c], ctx[c + 1], ctx[c + 2], ctx[c + 3])
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 hi, lo;
+            split4(v, hi, lo);
+            const uint32_t off = kmaj(row, h * DH + c, D);
+            *reinterpret_cast<float4 *>(sm + L::a_hi + off) = hi;
+            *reinterpret_cast<float4 *>(sm + L::a_lo + off) = lo;
+        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncthreads();
 
         // ---- out = ctx Wout^T into TMEM columns [0, D) (Q is no longer read)
-        if (half == 1) {
+        if (grp == 1) {
             for (int c = 0; c < n_out; ++c) {
                 const int s = c & 1;
                 if (c >= 2) mbar_wait(&bar[s], (ncommit[s] - 1) & 1);
-                store_chunk<P, H, DH>(cr, sm, s, tid - 128);
-                if (c + 1 < n_out) fetch_chunk<P, H, DH>(p, n_qkv + c + 1, cr, tid - 128);
+                store_chunk<P, H, DH>(cr, sm, s, tl);
+                if (c + 1 < n_out) fetch_chunk<P, H, DH>(p, n_qkv + c + 1, cr, tl);
                 named_sync(1, 128);
                 if (tid == 128) {
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -502,13 +512,13 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
-        // ---- residual add and store: warp w stores columns [half*D/2, (half+1)*D/2);
-        // a tile whose MMA wait gave up is written as NaN, never as silent garbage
+        // ---- residual add and store of columns [grp*D/4, (grp+1)*D/4); a tile whose
+        // MMA wait gave up is written as NaN, never as silent garbage
         {
             const float fail = *reinterpret_cast<volatile int *>(&g_tc_error) ? NAN : 0.f;
             float *o = p.out + (b * N + n) * (int64_t)D;
 #pragma unroll
-            for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 8) {
+            for (int c0 = grp * (D / 4); c0 < (grp + 1) * (D / 4); c0 += 8) {
                 float v[8];
                 tmem_ld8(tmem + lane_q + (uint32_t)c0, v);
                 if (rvalid) {
@@ -535,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
 
 // Host side: GAT_ERR_UNSUPPORTED when the shape is outside this path (the
 // caller then runs the SIMT kernel). This build instantiates P=16, H=4,
-// head_dim=24 (D=96), the block page's module shape, for N <= 32 nodes.
+// head_dim=24 (D=96), the block page's module shape, for up to 28 nodes.
 gat_status_t dense_block_tc(int32_t B, int32_t N, int32_t D, int32_t H, int32_t P,
                             const float *nodes, const float *pair, const float *mask,
                             const float *ln_w, const float *ln_b, float ln_eps, const float *Wq,
@@ -544,9 +554,9 @@ gat_status_t dense_block_tc(int32_t B, int32_t N, int32_t D, int32_t H, int32_t 
                             cudaStream_t s) {
     constexpr int kP = 16, kH = 4, kDH = 24;
     using L = tc::Smem<kP, kH, kDH>;
-    if (P != kP || H != kH || D != kH * kDH || N < 1 || N > 32) return GAT_ERR_UNSUPPORTED;
+    if (P != kP || H != kH || D != kH * kDH || N < 1 || N > 32 || !L::fits(N))
+        return GAT_ERR_UNSUPPORTED;
     const uint32_t smem = L::total(N);
-    if (smem > 227u * 1024u - 64u) return GAT_ERR_UNSUPPORTED;
     auto kern = tc::dense_tc_kernel<kP, kH, kDH>;
     static uint32_t configured = 0;
     if (smem > configured) {
