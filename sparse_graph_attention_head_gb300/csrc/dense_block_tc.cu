@@ -13,18 +13,19 @@
 //
 // One CTA of 16 warps per SM, persistent over tiles. Warp w has lane quarter
 // (graph) g = w % 4 and role group k = w / 4:
-//   k = 0  LayerNorm, thread per node row -> hi/lo A operand (shared memory,
-//          no-swizzle K-major 8-row x 16-byte core matrices)
+//   all    LayerNorm, warp w on the tile's 8-row group w -> hi/lo A operand
+//          (shared memory, no-swizzle K-major 8-row x 16-byte core matrices)
 //   k = 1  splits the weights into 48-column hi/lo B chunks (2-slot ring, the
 //          next chunk's global loads in flight in registers) and, through its
 //          first thread, issues each chunk's MMAs (commit -> one mbarrier per
 //          ring slot)
-//   all    relation-MLP bias of the node pairs (split over the four groups,
-//          the groups that start early take more pairs)
+//   all    relation-MLP bias of the node pairs with the edge mask folded in
+//          (-inf where masked), split over the four groups (the groups that
+//          start early take more pairs)
 //   k      attention for head k: Q, K, V rows from TMEM, K and V staged in the
-//          A region (idle once Q|K|V are in TMEM), scores + bias + mask,
-//          softmax, context kept in registers until every warp has read its
-//          staging, then written as the hi/lo A operand of the out-projection
+//          A region (idle once Q|K|V are in TMEM), scores + bias, softmax,
+//          context kept in registers until every warp has read its staging,
+//          then written as the hi/lo A operand of the out-projection
 //   k = 1  out-projection chunks into the TMEM columns that held Q
 //   k      residual add and store of output columns [kD/4, (k+1)D/4)
 // Every mbarrier wait is bounded; a wait that gives up raises a device flag
@@ -213,13 +214,14 @@ __device__ __forceinline__ void issue_chunk(uint32_t tmem, int col0, uint32_t a_
     }
 }
 
-// Relation-MLP bias of pairs (n, j), j in [j0, j1), for all heads; stored as
+// Relation-MLP bias of pairs (n, j), j in [j0, j1), for all heads, with the
+// edge mask folded in (-inf where mask < 0.5); stored as
 // bias_g[(h*N + j)*N + n] so a warp's lanes (n) write and read consecutive
 // words. The next pair's features are loaded while the current one computes.
 template <int P, int H>
-__device__ __forceinline__ void mlp_bias(const float *prow, int j0, int j1, const float *w1,
-                                         const float *bb1, const float *w2, const float *bb2,
-                                         float *bias_g, int N, int n) {
+__device__ __forceinline__ void mlp_bias(const float *prow, const float *mrow, int j0, int j1,
+                                         const float *w1, const float *bb1, const float *w2,
+                                         const float *bb2, float *bias_g, int N, int n) {
     float4 nxt[P / 4];
     if (j0 < j1) {
 #pragma unroll
@@ -252,12 +254,13 @@ __device__ __forceinline__ void mlp_bias(const float *prow, int j0, int j1, cons
                 a1 = fmaf(w1[u * P + c + 1], pf[c + 1], a1);
             }
             const float a = a0 + a1;
-            const float hid = __fdividef(a, 1.0f + expf(-a));  // SiLU
+            const float hid = __fdividef(a, 1.0f + __expf(-a));  // SiLU
 #pragma unroll
             for (int h = 0; h < H; ++h) r[h] = fmaf(w2[h * P + u], hid, r[h]);
         }
+        const bool masked = __ldg(mrow + j) < 0.5f;
 #pragma unroll
-        for (int h = 0; h < H; ++h) bias_g[(h * N + j) * N + n] = r[h];
+        for (int h = 0; h < H; ++h) bias_g[(h * N + j) * N + n] = masked ? -INFINITY : r[h];
     }
 }
 
@@ -318,52 +321,65 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         const float *prow = p.pair + ((b * N + n) * (int64_t)N) * P;
         float *bias_g = bias + g * H * N * N;
 
-        // ---- LayerNorm -> A (group 0) | first weight chunk (group 1) | MLP (groups 2, 3)
+        // ---- LayerNorm -> A, all warps: warp w normalises the 8-row group w of the
+        // tile (graph w/4, nodes 8(w%4)..+7); lane = (row r8 = lane%8, column
+        // group cg = lane/8), column groups cg, cg+4, ... of 4 floats, so the
+        // row loads are contiguous and the 16-byte A stores hit distinct banks.
+        // Group 1 has weight chunk 0's loads in flight meanwhile.
         ChunkRegs<D> cr;
-        if (grp == 0) {
-            float mean = 0.f, rstd = 0.f;
-            if (rvalid) {
-                float s = 0.f;
-#pragma unroll 6
-                for (int k4 = 0; k4 < D / 4; ++k4) {
-                    const float4 v = __ldg(reinterpret_cast<const float4 *>(x) + k4);
-                    s += (v.x + v.y) + (v.z + v.w);
-                }
-                mean = s / (float)D;
-                float v2 = 0.f;
-#pragma unroll 6
-                for (int k4 = 0; k4 < D / 4; ++k4) {
-                    const float4 v = __ldg(reinterpret_cast<const float4 *>(x) + k4);
-                    const float a0 = v.x - mean, a1 = v.y - mean, a2 = v.z - mean, a3 = v.w - mean;
-                    v2 = fmaf(a0, a0, v2);
-                    v2 = fmaf(a1, a1, v2);
-                    v2 = fmaf(a2, a2, v2);
-                    v2 = fmaf(a3, a3, v2);
-                }
-                rstd = 1.0f / sqrtf(v2 / (float)D + p.ln_eps);
+        if (grp == 1) fetch_chunk<P, H, DH>(p, 0, cr, tl);  // previous tile's MMAs are done
+        {
+            constexpr int NCG = D / 16;  // column groups per lane
+            const int r8 = lane & 7, cg = lane >> 3;
+            const int lg = warp >> 2, ln_node = 8 * (warp & 3) + r8;  // graph, node
+            const int64_t lb = (int64_t)tile * kGraphs + lg;
+            const bool lvalid = lb < p.B && ln_node < N;
+            const int lrow = 32 * lg + ln_node;
+            const float4 *xr = reinterpret_cast<const float4 *>(p.nodes + (lb * N + ln_node) * (int64_t)D);
+            float4 xv[NCG];
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < NCG; ++i) {
+                xv[i] = lvalid ? __ldg(xr + cg + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                s += (xv[i].x + xv[i].y) + (xv[i].z + xv[i].w);
             }
-#pragma unroll 6
-            for (int k4 = 0; k4 < D / 4; ++k4) {
+            s += __shfl_xor_sync(kFull, s, 8);
+            s += __shfl_xor_sync(kFull, s, 16);
+            const float mean = s / (float)D;
+            float v2 = 0.f;
+#pragma unroll
+            for (int i = 0; i < NCG; ++i) {
+                const float a0 = xv[i].x - mean, a1 = xv[i].y - mean, a2 = xv[i].z - mean,
+                            a3 = xv[i].w - mean;
+                v2 = fmaf(a0, a0, v2);
+                v2 = fmaf(a1, a1, v2);
+                v2 = fmaf(a2, a2, v2);
+                v2 = fmaf(a3, a3, v2);
+            }
+            v2 += __shfl_xor_sync(kFull, v2, 8);
+            v2 += __shfl_xor_sync(kFull, v2, 16);
+            const float rstd = 1.0f / sqrtf(v2 / (float)D + p.ln_eps);
+#pragma unroll
+            for (int i = 0; i < NCG; ++i) {
+                const int k4 = cg + 4 * i;
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (rvalid) {
-                    const float4 v = __ldg(reinterpret_cast<const float4 *>(x) + k4);
+                if (lvalid) {
                     const float4 gw = __ldg(reinterpret_cast<const float4 *>(p.ln_w) + k4);
                     const float4 gb = __ldg(reinterpret_cast<const float4 *>(p.ln_b) + k4);
-                    a = make_float4((v.x - mean) * rstd * gw.x + gb.x,
-                                    (v.y - mean) * rstd * gw.y + gb.y,
-                                    (v.z - mean) * rstd * gw.z + gb.z,
-                                    (v.w - mean) * rstd * gw.w + gb.w);
+                    a = make_float4((xv[i].x - mean) * rstd * gw.x + gb.x,
+                                    (xv[i].y - mean) * rstd * gw.y + gb.y,
+                                    (xv[i].z - mean) * rstd * gw.z + gb.z,
+                                    (xv[i].w - mean) * rstd * gw.w + gb.w);
                 }
                 float4 hi, lo;
                 split4(a, hi, lo);
-                const uint32_t off = kmaj(row, 4 * k4, D);
+                const uint32_t off = kmaj(lrow, 4 * k4, D);
                 *reinterpret_cast<float4 *>(sm + L::a_hi + off) = hi;
                 *reinterpret_cast<float4 *>(sm + L::a_lo + off) = lo;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        } else if (grp == 1) {
-            // every MMA of the previous tile completed before its epilogue
-            fetch_chunk<P, H, DH>(p, 0, cr, tl);
+        }
+        if (grp == 1) {
             store_chunk<P, H, DH>(cr, sm, 0, tl);
             fetch_chunk<P, H, DH>(p, 1, cr, tl);
         }
@@ -391,7 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             ncommit[0] += (n_qkv + 1) / 2;
             ncommit[1] += n_qkv / 2;
         }
-        if (rvalid) mlp_bias<P, H>(prow, j_lo, j_hi, w1, bb1, w2, bb2, bias_g, N, n);
+        if (rvalid)
+            mlp_bias<P, H>(prow, p.mask + (b * N + n) * (int64_t)N, j_lo, j_hi, w1, bb1, w2, bb2,
+                           bias_g, N, n);
         __syncthreads();  // bias complete
         {
             const int s = (n_qkv - 1) & 1;  // the last commit covers every earlier MMA
@@ -403,7 +421,6 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         const int h = grp;
         float ctx[DH];
         {
-            const float *mk = p.mask + (b * N + n) * (int64_t)N;
             float *sk = stage, *sv = stage + N * DH;
             float q[DH], kv[8];
 #pragma unroll
@@ -439,7 +456,6 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                         a3 = fmaf(q[c + 3], k4.w, a3);
                     }
                     s = ((a0 + a1) + (a2 + a3)) * inv_sqrt_dh + bias_g[(h * N + j) * N + n];
-                    if (__ldg(mk + j) < 0.5f) s = -INFINITY;
                 }
                 sc[j] = s;
                 m = fmaxf(m, s);
