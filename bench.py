@@ -493,12 +493,14 @@ def bench_small(name, args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200,
+                    help="timed layer calls (200 x ~5 ms: about a second, several clock samples)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gat", choices=["gat", "reference"])
     ap.add_argument("--workload", default="fused",
                     choices=["fused", "edge_softmax", "aggregate", "sddmm", "dense"])
-    ap.add_argument("--ref-rows", type=int, default=16000)
+    ap.add_argument("--ref-rows", type=int, default=5000,
+                    help="--impl reference: consecutive rows per step (~0.2 s of oracle work)")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for cpu_baseline (0: skip)")
     ap.add_argument("--n-rows", type=int, default=1_000_000,
