@@ -45,8 +45,15 @@ def build(force: bool = False) -> str:
 def _load():
     global _lib
     if _lib is None:
-        build()
-        lib = ctypes.CDLL(_LIB)
+        # GAT_ORACLE_LIB names another compiled oracle (the mutation tests
+        # plant mistakes in a copy of oracle.c and check the pins catch them)
+        override = os.environ.get("GAT_ORACLE_LIB")
+        if override:
+            path = override
+        else:
+            build()
+            path = _LIB
+        lib = ctypes.CDLL(path)
         P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_double
         lib.oracle_edge_softmax.argtypes = [P, I64, I32, P, P]
         lib.oracle_spmm_weighted.argtypes = [P, P, I64, I32, I32, P, P, ctypes.c_int, P, P]

@@ -112,6 +112,20 @@ def test_softmax_large_scores_need_max_subtraction():
     assert out[2] == 0.0
 
 
+def test_softmax_heads_with_far_apart_scales():
+    """Each head subtracts its own maximum: heads whose scores sit near +700
+    and -700 would underflow (or overflow) with another head's maximum."""
+    rng = np.random.default_rng(25)
+    rp = np.array([0, 5, 9], dtype=np.int32)
+    s = np.stack([700 + rng.standard_normal(9), -700 + rng.standard_normal(9)], 1).astype(np.float32)
+    out = oracle.edge_softmax(rp, s, 2)
+    for h in range(2):
+        for i in range(2):
+            seg = slice(rp[i], rp[i + 1])
+            np.testing.assert_allclose(out[seg, h], np_softmax(s[seg, h].astype(np.float64)),
+                                       rtol=1e-12)
+
+
 def test_softmax_all_minus_inf_row_is_nan_like_library():
     import torch
     rp = np.array([0, 2], dtype=np.int32)
