@@ -7,7 +7,8 @@ degree-bucket plan built beforehand (a plan is per graph and shared by every
 layer and call on it; its build time is reported as plan_ms).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload fused|edge_softmax|aggregate|sddmm|dense]
+                    [--workload fused|edge_softmax|aggregate|sddmm|dense|spmm_heads|
+                               edge_softmax_h8]
 
 Prints one JSON line (rank 0). value = edge-heads/s over all ranks (each rank
 runs its own full, independent problem: weak scaling, no collective on the
@@ -409,10 +410,34 @@ def bench_small(name, args):
     import torch
     import sparse_graph_attention_head_gb300 as gat
     dev = torch.device("cuda", 0)
-    g = W.WORKLOADS[name][0]()
+    g = W.WORKLOADS[name][0]() if name in ("edge_softmax", "aggregate", "sddmm", "dense") else None
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
     flops, tensor_flops = 0.0, 0.0
-    if name == "edge_softmax":
+    if name == "spmm_heads":
+        # head_dim 32, 8 heads, fp32 weights and features, 1e6-row power-law graph
+        g = W.make_spmm_heads()
+        rp, ci, w, feat = t(g["row_ptr"]), t(g["col_idx"]), t(g["w"]), t(g["feat"])
+        out = torch.empty_like(feat)
+        plan = gat.Plan(rp)
+        fn = lambda: gat.gat_spmm_weighted(rp, ci, w, feat, g["H"], g["Dh"], out=out,  # noqa: E731
+                                           plan=plan)
+        units, launches = g["n_edges"] * g["H"], 2
+        row = 4 * g["H"] * g["Dh"]
+        # per row: row_ptr entry and output row; per edge: col_idx entry, H
+        # weights and the gathered feature row
+        alg_bytes = (4 + row) * g["n_rows"] + (4 + 4 * g["H"] + row) * g["n_edges"]
+        flops = 2.0 * g["n_edges"] * g["H"] * g["Dh"]
+    elif name == "edge_softmax_h8":
+        # 8 heads on the 1e6-row power-law graph
+        deg = W.zipf_degrees(np.random.default_rng(3), 1_000_000)
+        g = W.make_edge_softmax(seed=6, deg=deg, H=8)
+        rp, s = t(g["row_ptr"]), t(g["scores"])
+        out = torch.empty_like(s)
+        plan = gat.Plan(rp)
+        fn = lambda: gat.gat_edge_softmax(rp, s, g["H"], out=out, plan=plan)  # noqa: E731
+        units, launches = g["n_edges"] * g["H"], 2
+        alg_bytes = 4 * (g["n_rows"] + 1) + 8 * g["n_edges"] * g["H"]
+    elif name == "edge_softmax":
         rp, s = t(g["row_ptr"]), t(g["scores"])
         out = torch.empty_like(s)
         fn = lambda: gat.gat_edge_softmax(rp, s, g["H"], out=out)  # noqa: E731
@@ -498,7 +523,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gat", choices=["gat", "reference"])
     ap.add_argument("--workload", default="fused",
-                    choices=["fused", "edge_softmax", "aggregate", "sddmm", "dense"])
+                    choices=["fused", "edge_softmax", "aggregate", "sddmm", "dense", "spmm_heads",
+                             "edge_softmax_h8"])
     ap.add_argument("--ref-rows", type=int, default=5000,
                     help="--impl reference: consecutive rows per step (~0.2 s of oracle work)")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
@@ -525,7 +551,8 @@ def main():
     if rank == 0:
         if not args.no_extras:
             res["other_workloads"] = {}
-            for nm in ("edge_softmax", "aggregate", "sddmm", "dense"):
+            for nm in ("edge_softmax", "aggregate", "sddmm", "dense", "spmm_heads",
+                       "edge_softmax_h8"):
                 try:
                     res["other_workloads"][nm] = bench_small(nm, args)
                 except Exception as exc:  # keep the headline line if a side workload fails

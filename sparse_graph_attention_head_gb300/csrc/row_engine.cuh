@@ -20,7 +20,7 @@
 // per head: m' = max(m, s), c = 2^(m-m'), l = l c + 2^(s-m'),
 // acc = acc c + 2^(s-m') v. Scores are pre-scaled by log2(e) so the
 // exponentials are exp2. Nothing per edge ever reaches memory.
-// SpMM mode: acc += w[e,h] * feat[src].
+// SpMM mode (spmm.cu): acc += w[e,h] * feat[src].
 //
 // Heavy rows (fused mode, with a plan) arrive as chunks; each chunk warp
 // writes its (m, l, acc) to a workspace slot, and the warp that finishes a
@@ -421,139 +421,6 @@ inline gat_status_t launch_fused_engine(const EngineParams &p, cudaStream_t s) {
     if (blocks > cap) blocks = cap;
     kern<<<(unsigned)blocks, kFusedThreads, 0, s>>>(p);
     return check_launch("fused_engine_kernel");
-}
-
-// ---------------------------------------------------------------------------
-// spmm mode
-// ---------------------------------------------------------------------------
-template <typename T, int V, int LE, int U>
-struct SpmmRow {
-    using L = Lanes<T, V, LE>;
-    static constexpr int VE = L::VE;
-    static constexpr int ES = L::ES;
-    float acc[V][VE];
-
-    // accumulate edges e0 + first, e0 + first + step, ... below e1 (step is
-    // a multiple of 32; the warp handles 32-edge tiles)
-    __device__ __forceinline__ void run(const EngineParams &p, const L &ln, int e0, int e1,
-                                        int tile0, int tile_step) {
-        const int64_t row_bytes = (int64_t)p.H * p.Dh * sizeof(T);
-        const char *fb = static_cast<const char *>(p.v);
-        for (int base = e0 + tile0 * 32; base < e1; base += tile_step * 32) {
-            const int n = min(32, e1 - base);
-            const int my_ci = ln.lane < n ? __ldg(p.col_idx + base + ln.lane) : 0;
-            for (int j0 = 0; j0 < n; j0 += U * ES) {
-                uint4 vr[U][V];
-                float wv[U][V];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int j = j0 + u * ES + ln.sub;
-                    const bool valid = j < n;
-                    const int64_t src = __shfl_sync(kFull, my_ci, j & 31);
-#pragma unroll
-                    for (int s = 0; s < V; ++s) {
-                        if (valid) {
-                            vr[u][s] = ld_stream16(fb + src * row_bytes + ln.vi[s] * 16);
-                            wv[u][s] = __ldg(p.w + (int64_t)(base + j) * p.H + ln.head[s]);
-                        } else {
-                            vr[u][s] = make_uint4(0, 0, 0, 0);
-                            wv[u][s] = 0.f;
-                        }
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-#pragma unroll
-                    for (int s = 0; s < V; ++s) {
-                        float vf[VE];
-                        Vec<T>::unpack(vr[u][s], vf);
-#pragma unroll
-                        for (int t = 0; t < VE; ++t) acc[s][t] = fmaf(wv[u][s], vf[t], acc[s][t]);
-                    }
-            }
-        }
-    }
-
-    __device__ __forceinline__ void zero() {
-#pragma unroll
-        for (int s = 0; s < V; ++s)
-#pragma unroll
-            for (int t = 0; t < VE; ++t) acc[s][t] = 0.f;
-    }
-
-    __device__ __forceinline__ void merge_subgroups() {
-#pragma unroll
-        for (int o = LE; o < 32; o <<= 1)
-#pragma unroll
-            for (int s = 0; s < V; ++s)
-#pragma unroll
-                for (int t = 0; t < VE; ++t) acc[s][t] += __shfl_xor_sync(kFull, acc[s][t], o);
-    }
-
-    __device__ __forceinline__ void store_out(const EngineParams &p, const L &ln, int64_t row) {
-        if (ln.sub != 0) return;
-        char *orow = static_cast<char *>(p.out) + row * (int64_t)p.H * p.Dh * sizeof(T);
-#pragma unroll
-        for (int s = 0; s < V; ++s) st_stream16(orow + ln.vi[s] * 16, Vec<T>::pack(acc[s]));
-    }
-};
-
-// light rows (or every row without a plan): one warp per row
-template <typename T, int V, int LE, int U>
-__global__ void __launch_bounds__(kEngineThreads)
-spmm_engine_kernel(const EngineParams p) {
-    using L = Lanes<T, V, LE>;
-    const L ln(p.Dh);
-    SpmmRow<T, V, LE, U> st;
-    const int64_t wpb = blockDim.x >> 5;
-    const int64_t n_warps = (int64_t)gridDim.x * wpb;
-    for (int64_t row = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5); row < p.n_rows;
-         row += n_warps) {
-        const int e0 = __ldg(p.row_ptr + row), e1 = __ldg(p.row_ptr + row + 1);
-        if (e1 - e0 > p.heavy_threshold) continue;
-        st.zero();
-        st.run(p, ln, e0, e1, 0, 1);
-        st.merge_subgroups();
-        st.store_out(p, ln, row);
-    }
-}
-
-// heavy rows: one block per row; warp w takes 32-edge tiles w, w+8, ...;
-// the warps' sums are added in warp order through shared memory
-template <typename T, int V, int LE, int U>
-__global__ void __launch_bounds__(kEngineThreads)
-spmm_heavy_kernel(const EngineParams p) {
-    using L = Lanes<T, V, LE>;
-    constexpr int VE = L::VE;
-    constexpr int NW = kEngineThreads / 32;
-    __shared__ float red[NW][V * VE][32];
-    const L ln(p.Dh);
-    const int warp = threadIdx.x >> 5;
-    SpmmRow<T, V, LE, U> st;
-    for (int64_t b = blockIdx.x; b < p.n_block_rows; b += gridDim.x) {
-        const int64_t row = __ldg(p.heavy_rows + b);
-        const int e0 = __ldg(p.row_ptr + row), e1 = __ldg(p.row_ptr + row + 1);
-        st.zero();
-        st.run(p, ln, e0, e1, warp, NW);
-        st.merge_subgroups();
-#pragma unroll
-        for (int s = 0; s < V; ++s)
-#pragma unroll
-            for (int t = 0; t < VE; ++t) red[warp][s * VE + t][ln.lane] = st.acc[s][t];
-        __syncthreads();
-        if (warp == 0) {
-#pragma unroll
-            for (int s = 0; s < V; ++s)
-#pragma unroll
-                for (int t = 0; t < VE; ++t) {
-                    float a = red[0][s * VE + t][ln.lane];
-                    for (int w2 = 1; w2 < NW; ++w2) a += red[w2][s * VE + t][ln.lane];
-                    st.acc[s][t] = a;
-                }
-            st.store_out(p, ln, row);
-        }
-        __syncthreads();
-    }
 }
 
 }  // namespace gat

@@ -1,7 +1,8 @@
 // spmm.cu - gat_spmm_weighted: out[i,h,:] = sum_e w[e,h] * feat[col_idx[e],h,:]
 // (FW-GLM-5-1 l1_p18, reference model; Kimi-K2.6 l2_p37: a destination with
-// no edges stays zero). Light rows: one warp per row (row_engine.cuh);
-// heavy rows (with a plan): one block per row, warps summed in warp order.
+// no edges stays zero). Light rows: one warp per row, persistent, with the
+// next row's metadata prefetched; heavy rows (with a plan): one 8-warp block
+// per row, warps summed in warp order. Lane layout: row_engine.cuh.
 #include <climits>
 
 #include "row_engine.cuh"
@@ -46,23 +47,208 @@ spmm_generic_kernel(const EngineParams p) {
     }
 }
 
+// Accumulator of one warp: acc += w[e,h] * feat[col_idx[e],h,:] over 32-edge
+// tiles, U edges (per edge subgroup) in flight at a time.
+template <typename T, int V, int LE, int U>
+struct SpmmAcc {
+    using L = Lanes<T, V, LE>;
+    static constexpr int VE = L::VE;
+    static constexpr int ES = L::ES;
+    float acc[V][VE];
+
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int s = 0; s < V; ++s)
+#pragma unroll
+            for (int t = 0; t < VE; ++t) acc[s][t] = 0.f;
+    }
+
+    // Tiles e0 + 32*tile0, e0 + 32*(tile0 + tile_step), ... below e1. first_ci
+    // is this lane's col_idx entry of the first tile when have_first. Right
+    // after the first gathers are issued, the col_idx tile of [ne0, ne1) is
+    // fetched into next_ci when want_next (so the warp's next row can start
+    // gathering at once).
+    __device__ __forceinline__ void run(const EngineParams &p, const L &ln, int e0, int e1,
+                                        int tile0, int tile_step, int first_ci, bool have_first,
+                                        int ne0, int ne1, bool want_next, int &next_ci,
+                                        bool &next_ready) {
+        const int64_t row_bytes = (int64_t)p.H * p.Dh * sizeof(T);
+        const char *fb = static_cast<const char *>(p.v);
+        const int first = e0 + tile0 * 32;
+        for (int base = first; base < e1; base += tile_step * 32) {
+            const int n = min(32, e1 - base);
+            const int my_ci = (have_first && base == first)
+                                  ? first_ci
+                                  : (ln.lane < n ? __ldg(p.col_idx + base + ln.lane) : 0);
+            for (int j0 = 0; j0 < n; j0 += U * ES) {
+                uint4 vr[U][V];
+                float wv[U][V];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int j = j0 + u * ES + ln.sub;
+                    const bool valid = j < n;
+                    const int64_t src = __shfl_sync(kFull, my_ci, j & 31);
+#pragma unroll
+                    for (int s = 0; s < V; ++s) {
+                        if (valid) {
+                            vr[u][s] = ld_stream16(fb + src * row_bytes + ln.vi[s] * 16);
+                            wv[u][s] = __ldg(p.w + (int64_t)(base + j) * p.H + ln.head[s]);
+                        } else {
+                            vr[u][s] = make_uint4(0, 0, 0, 0);
+                            wv[u][s] = 0.f;
+                        }
+                    }
+                }
+                if (want_next && !next_ready) {
+                    const int nn = ne1 - ne0;
+                    next_ci = ln.lane < nn ? __ldg(p.col_idx + ne0 + ln.lane) : 0;
+                    next_ready = true;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int s = 0; s < V; ++s) {
+                        float vf[VE];
+                        Vec<T>::unpack(vr[u][s], vf);
+#pragma unroll
+                        for (int t = 0; t < VE; ++t) acc[s][t] = fmaf(wv[u][s], vf[t], acc[s][t]);
+                    }
+            }
+        }
+    }
+
+    // sum the edge subgroups (LE < 32) in a fixed butterfly order
+    __device__ __forceinline__ void merge_subgroups() {
+#pragma unroll
+        for (int o = LE; o < 32; o <<= 1)
+#pragma unroll
+            for (int s = 0; s < V; ++s)
+#pragma unroll
+                for (int t = 0; t < VE; ++t) acc[s][t] += __shfl_xor_sync(kFull, acc[s][t], o);
+    }
+
+    __device__ __forceinline__ void store_out(const EngineParams &p, const L &ln, int64_t row) {
+        if (ln.sub != 0) return;
+        char *orow = static_cast<char *>(p.out) + row * (int64_t)p.H * p.Dh * sizeof(T);
+#pragma unroll
+        for (int s = 0; s < V; ++s) st_stream16(orow + ln.vi[s] * 16, Vec<T>::pack(acc[s]));
+    }
+};
+
+// Light rows (every row without a plan): persistent warps, warp w takes rows
+// w, w + W, ... While a row is processed, the next row's row_ptr entries
+// and then its first col_idx tile are already being fetched.
+constexpr int kSpmmThreads = 128;
+
+template <typename T, int V, int LE, int U>
+__global__ void __launch_bounds__(kSpmmThreads, 4)
+spmm_rows_kernel(const EngineParams p) {
+    using L = Lanes<T, V, LE>;
+    const L ln(p.Dh);
+    SpmmAcc<T, V, LE, U> st;
+    const int64_t wpb = blockDim.x >> 5;
+    const int64_t n_warps = (int64_t)gridDim.x * wpb;
+    int64_t row = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
+    if (row >= p.n_rows) return;
+    int ne0 = __ldg(p.row_ptr + row), ne1 = __ldg(p.row_ptr + row + 1);
+    int ci_tile = 0;
+    bool ci_ready = false;
+    for (; row < p.n_rows; row += n_warps) {
+        const int e0 = ne0, e1 = ne1;
+        const int64_t nxt = row + n_warps;
+        const bool has_next = nxt < p.n_rows;
+        ne0 = has_next ? __ldg(p.row_ptr + nxt) : 0;
+        ne1 = has_next ? __ldg(p.row_ptr + nxt + 1) : 0;
+        if (e1 - e0 > p.heavy_threshold) {  // a heavy row: the heavy-row kernel's
+            ci_ready = false;
+            continue;
+        }
+        const int first_ci =
+            ci_ready ? ci_tile : (ln.lane < e1 - e0 ? __ldg(p.col_idx + e0 + ln.lane) : 0);
+        bool next_ready = false;
+        const bool want_next = has_next && ne1 > ne0 && ne1 - ne0 <= p.heavy_threshold;
+        st.zero();
+        st.run(p, ln, e0, e1, 0, 1, first_ci, true, ne0, ne1, want_next, ci_tile, next_ready);
+        ci_ready = next_ready;
+        st.merge_subgroups();
+        st.store_out(p, ln, row);
+    }
+}
+
+// Heavy rows: one block of kSpmmHeavyThreads per row (8 warps); warp w takes
+// 32-edge tiles w, w + 8, ... The warps' sums meet in shared memory and each
+// output element is summed over the warps in warp order (deterministic).
+constexpr int kSpmmHeavyThreads = 256;
+
+template <typename T, int V, int LE, int U>
+__global__ void __launch_bounds__(kSpmmHeavyThreads)
+spmm_heavy_kernel(const EngineParams p) {
+    using L = Lanes<T, V, LE>;
+    constexpr int VE = L::VE;
+    constexpr int NW = kSpmmHeavyThreads / 32;
+    constexpr int PER_WARP = V * VE * 32;  // floats of one warp's row sum
+    extern __shared__ float red[];          // [NW][PER_WARP]
+    const L ln(p.Dh);
+    const int warp = threadIdx.x >> 5;
+    SpmmAcc<T, V, LE, U> st;
+    int dummy_ci = 0;
+    bool dummy_ready = false;
+    for (int64_t b = blockIdx.x; b < p.n_block_rows; b += gridDim.x) {
+        const int64_t row = __ldg(p.heavy_rows + b);
+        const int e0 = __ldg(p.row_ptr + row), e1 = __ldg(p.row_ptr + row + 1);
+        st.zero();
+        st.run(p, ln, e0, e1, warp, NW, 0, false, 0, 0, false, dummy_ci, dummy_ready);
+        st.merge_subgroups();
+#pragma unroll
+        for (int s = 0; s < V; ++s)
+#pragma unroll
+            for (int t = 0; t < VE; ++t) red[warp * PER_WARP + (s * VE + t) * 32 + ln.lane] = st.acc[s][t];
+        __syncthreads();
+        for (int i = threadIdx.x; i < PER_WARP; i += kSpmmHeavyThreads) {
+            float a = red[i];
+            for (int w2 = 1; w2 < NW; ++w2) a += red[w2 * PER_WARP + i];
+            red[i] = a;
+        }
+        __syncthreads();
+        if (warp == 0) {
+#pragma unroll
+            for (int s = 0; s < V; ++s)
+#pragma unroll
+                for (int t = 0; t < VE; ++t) st.acc[s][t] = red[(s * VE + t) * 32 + ln.lane];
+            st.store_out(p, ln, row);
+        }
+        __syncthreads();
+    }
+}
+
 template <typename T, int V, int LE>
 static gat_status_t launch_spmm_fast(const EngineParams &p, cudaStream_t s) {
-    constexpr int U = 8 / V;
-    auto kern = spmm_engine_kernel<T, V, LE, U>;
-    static int64_t cap = 0;
-    if (cap == 0) cap = persistent_blocks(kern, INT64_MAX);
-    const int64_t wpb = kEngineThreads / 32;
+    constexpr int U = V == 4 ? 2 : 8;  // edges in flight per warp (8 KB at V = 2)
+    auto kern = spmm_rows_kernel<T, V, LE, U>;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSpmmThreads, 0) !=
+            cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int64_t wpb = kSpmmThreads / 32;
     int64_t blocks = (p.n_rows + wpb - 1) / wpb;
+    const int64_t cap = (int64_t)sm_count() * per_sm;
     if (blocks > cap) blocks = cap;
-    kern<<<(unsigned)blocks, kEngineThreads, 0, s>>>(p);
+    kern<<<(unsigned)blocks, kSpmmThreads, 0, s>>>(p);
     gat_status_t st = check_launch("gat_spmm_weighted");
     if (st != GAT_OK || p.n_block_rows == 0) return st;
     auto hk = spmm_heavy_kernel<T, V, LE, U>;
-    static int64_t hcap = 0;
-    if (hcap == 0) hcap = persistent_blocks(hk, INT64_MAX);
-    int64_t hb = p.n_block_rows < hcap ? p.n_block_rows : hcap;
-    hk<<<(unsigned)hb, kEngineThreads, 0, s>>>(p);
+    const int smem = kSpmmHeavyThreads / 32 * V * Vec<T>::N * 32 * (int)sizeof(float);
+    cudaError_t err = cudaFuncSetAttribute(hk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return cuda_fail(err, "gat_spmm_weighted: shared memory attribute");
+    int hper_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&hper_sm, hk, kSpmmHeavyThreads, smem) !=
+            cudaSuccess ||
+        hper_sm < 1)
+        hper_sm = 1;
+    const int64_t hcap = (int64_t)sm_count() * hper_sm;
+    const int64_t hb = p.n_block_rows < hcap ? p.n_block_rows : hcap;
+    hk<<<(unsigned)hb, kSpmmHeavyThreads, smem, s>>>(p);
     return check_launch("gat_spmm_weighted: heavy rows");
 }
 

@@ -57,7 +57,7 @@ def test_edge_softmax_workload(gat, use_plan):
     assert_fp32(host(out), o, name="edge_softmax")
 
 
-@pytest.mark.parametrize("H", [1, 3, 8, 32])
+@pytest.mark.parametrize("H", [1, 3, 4, 5, 8, 12, 32, 40])
 def test_edge_softmax_heads_in_place_and_long_rows(gat, H):
     deg = np.array([0, 1, 2, 31, 32, 33, 300, 0, 5000, 7])
     d = W.make_edge_softmax(seed=40 + H, deg=deg, H=H)
@@ -335,3 +335,61 @@ def test_full_size_fused_sampled_rows(gat, full_fused):
                                      [0, deg.size - 1]]))
     check_fused(d, g, rows=rows)
     assert np.isfinite(g).all()
+
+
+# ----------------------------------------------------------------------------
+# multi-head weighted aggregation at head_dim 32 (8 heads, fp32) and the
+# 8-head softmax, on power-law graphs with the default plan (the launch
+# configuration the benchmark times)
+# ----------------------------------------------------------------------------
+def _sub_csr(row_ptr, col_idx, w, rows):
+    """The CSR of the selected rows alone (slicing only, no arithmetic)."""
+    deg = (row_ptr[rows + 1] - row_ptr[rows]).astype(np.int64)
+    rp = np.zeros(rows.size + 1, dtype=np.int64)
+    rp[1:] = np.cumsum(deg)
+    take = np.concatenate([np.arange(row_ptr[r], row_ptr[r + 1]) for r in rows]) \
+        if rp[-1] else np.zeros(0, dtype=np.int64)
+    return rp.astype(np.int32), col_idx[take], w[take], deg
+
+
+def test_spmm_heads_100k_elementwise(gat):
+    d = W.make_spmm_heads(n=100_000)
+    H, Dh = d["H"], d["Dh"]
+    rp = dev(d["row_ptr"])
+    plan = gat.Plan(rp)
+    assert plan.info()["n_heavy"] > 0
+    out = gat.gat_spmm_weighted(rp, dev(d["col_idx"]), dev(d["w"]), dev(d["feat"]), H, Dh,
+                                plan=plan)
+    o, c = oracle.spmm_weighted(d["row_ptr"], d["col_idx"], d["w"].astype(np.float64),
+                                d["feat"], H, Dh, want_cond=True)
+    deg = np.diff(d["row_ptr"]).astype(np.float64)
+    rate = assert_fp32(host(out), o, c, deg[:, None, None], name="spmm 8x32 100k")
+    assert rate > 0.99
+
+
+def test_spmm_heads_full_size_sampled_rows(gat):
+    d = W.make_spmm_heads()
+    H, Dh = d["H"], d["Dh"]
+    rp = dev(d["row_ptr"])
+    out = gat.gat_spmm_weighted(rp, dev(d["col_idx"]), dev(d["w"]), dev(d["feat"]), H, Dh,
+                                plan=gat.Plan(rp))
+    g = host(out)
+    deg = np.diff(d["row_ptr"])
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([np.argsort(deg)[-12:], rng.integers(0, deg.size, 400),
+                                     [0, deg.size - 1]]))
+    srp, sci, sw, sdeg = _sub_csr(d["row_ptr"], d["col_idx"], d["w"], rows)
+    o, c = oracle.spmm_weighted(srp, sci, sw.astype(np.float64), d["feat"], H, Dh,
+                                want_cond=True)
+    assert_fp32(g[rows], o, c, np.maximum(sdeg, 1).astype(np.float64)[:, None, None],
+                name="spmm 8x32 1e6 sampled")
+    assert np.isfinite(g).all()
+
+
+def test_edge_softmax_8_heads_power_law_full_size(gat):
+    deg = W.zipf_degrees(np.random.default_rng(3), 1_000_000)
+    d = W.make_edge_softmax(seed=6, deg=deg, H=8)
+    rp = dev(d["row_ptr"])
+    out = gat.gat_edge_softmax(rp, dev(d["scores"]), 8, plan=gat.Plan(rp))
+    o = oracle.edge_softmax(d["row_ptr"], d["scores"], 8)
+    assert_fp32(host(out), o, name="edge_softmax 8 heads 1e6")

@@ -21,6 +21,8 @@ Workloads (shapes follow the problem statements on the source pages):
 * ``dense``         - dense-masked small-graph attention block, B graphs of 24
   nodes, D=96, H=4, P=16, mask Bernoulli(0.3) with a unit diagonal, all Linear
   weights and biases ~ N(0, 0.02^2)    (POPCORNBENCH Kimi-K2.6 l2_p4)
+* ``spmm_heads``    - multi-head weighted aggregation at head_dim 32, 8 heads,
+  fp32, on a power-law graph like ``fused``'s (POPCORNBENCH FW-GLM-5-1 l1_p18)
 
 Draw order inside each generator is fixed and documented, so a seed fully
 determines every array.
@@ -33,7 +35,7 @@ __all__ = [
     "bf16_bits_from_f32", "f32_from_bf16_bits", "row_ptr_from_degrees",
     "uniform_degrees", "zipf_degrees", "page_mod_degrees",
     "make_edge_softmax", "make_aggregate", "make_sddmm", "make_fused",
-    "make_dense", "make_csr", "WORKLOADS",
+    "make_dense", "make_csr", "make_spmm_heads", "WORKLOADS",
 ]
 
 
@@ -201,6 +203,24 @@ def make_fused(seed: int = 3, n: int = 1_000_000, H: int = 8, Dh: int = 64,
                 n_edges=int(rp[-1]), H=H, Dh=Dh, scale=1.0 / np.sqrt(Dh), dtype=dtype)
 
 
+def make_spmm_heads(seed: int = 5, n: int = 1_000_000, H: int = 8, Dh: int = 32,
+                    deg: np.ndarray | None = None, dmax: int = 4096, mean: float = 16.0) -> dict:
+    """Multi-head weighted aggregation at head_dim 32 on a power-law graph.
+
+    Draws from default_rng(seed): Zipf degrees (unless ``deg``), col_idx
+    (sorted within rows), edge weights U[0,1) fp32 [E,H]; then features fp32
+    [n,H,Dh] ~ N(0,1) from block stream [seed, 1].
+    """
+    rng = np.random.default_rng(seed)
+    if deg is None:
+        deg = zipf_degrees(rng, n, 2.1, dmax, mean)
+    rp, ci = make_csr(rng, deg, n, sort_within_rows=True)
+    E = int(rp[-1])
+    w = rng.random((E, H), dtype=np.float32)
+    feat = _block_normals([seed, 1], n * H * Dh, False).reshape(n, H, Dh)
+    return dict(row_ptr=rp, col_idx=ci, w=w, feat=feat, n_rows=n, n_src=n, n_edges=E, H=H, Dh=Dh)
+
+
 def make_dense(seed: int = 4, B: int = 8192, N: int = 24, D: int = 96, H: int = 4,
                P: int = 16, wstd: float = 0.02, p_edge: float = 0.3,
                affine_ln: bool = False) -> dict:
@@ -234,4 +254,6 @@ WORKLOADS = {
     "sddmm": (make_sddmm, 2, "COO SDDMM, 1024x768 nodes, 16384 edges, feat 128"),
     "fused": (make_fused, 3, "fused GAT layer, 1e6 rows, Zipf(2.1) mean 16, H=8, Dh=64, bf16"),
     "dense": (make_dense, 4, "dense-masked small-graph block, B=8192, N=24, D=96, H=4, P=16"),
+    "spmm_heads": (make_spmm_heads, 5, "weighted aggregation, 1e6 rows, Zipf(2.1) mean 16, H=8, "
+                   "Dh=32, fp32"),
 }
