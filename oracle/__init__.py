@@ -63,8 +63,11 @@ def _load():
         lib.oracle_dense_block.argtypes = [I32, I32, I32, I32, I32, P, P, P, P, P, D,
                                            P, P, P, P, P, P, P, P, P, I64, P, P]
         lib.oracle_plan.argtypes = [P, I64, I32, I32, P, P, P, P, P]
+        lib.oracle_fused_backward.argtypes = [P, P, I64, I64, I32, I32, D, P, P, P, P,
+                                              ctypes.c_int, P, P, P, P, P, P]
         for f in ("oracle_edge_softmax", "oracle_spmm_weighted", "oracle_sddmm",
-                  "oracle_fused_layer", "oracle_dense_block", "oracle_plan"):
+                  "oracle_fused_layer", "oracle_dense_block", "oracle_plan",
+                  "oracle_fused_backward"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -149,6 +152,28 @@ def fused_layer(row_ptr, col_idx, q, k, v, H, Dh, scale, rows=None, want_cond=Fa
                                       _p(ka), _p(va), dt, _p(sel), n_sel, _p(out),
                                       _p(cond)), "oracle_fused_layer")
     return (out, cond) if want_cond else out
+
+
+def fused_backward(row_ptr, col_idx, q, k, v, dout, H, Dh, scale, n_src=None,
+                   want_cond=False):
+    """Gradients of the fused layer for an upstream gradient ``dout``.
+    Returns fp64 (dq [n_rows,H,Dh], dk [n_src,H,Dh], dv [n_src,H,Dh]) and,
+    with ``want_cond``, their conditioning scales in the same shapes."""
+    rp, ci = _c(row_ptr, np.int32), _c(col_idx, np.int32)
+    qa, dt = _feat(q)
+    ka, _ = _feat(k)
+    va, _ = _feat(v)
+    ga, _ = _feat(dout)
+    n = rp.size - 1
+    ns = (va.size // (H * Dh)) if n_src is None else int(n_src)
+    dq = np.empty((n, H, Dh))
+    dk = np.empty((ns, H, Dh))
+    dv = np.empty((ns, H, Dh))
+    conds = [np.empty_like(dq), np.empty_like(dk), np.empty_like(dv)] if want_cond else [None] * 3
+    _check(_load().oracle_fused_backward(_p(rp), _p(ci), n, ns, H, Dh, float(scale), _p(qa),
+                                         _p(ka), _p(va), _p(ga), dt, _p(dq), _p(dk), _p(dv),
+                                         *[_p(c) for c in conds]), "oracle_fused_backward")
+    return (dq, dk, dv, *conds) if want_cond else (dq, dk, dv)
 
 
 def dense_block(w: dict, graphs=None, want_cond=False):

@@ -248,6 +248,118 @@ int oracle_fused_layer(const int32_t *row_ptr, const int32_t *col_idx,
 }
 
 /*
+ * Backward of the fused layer: the chain rule through the forward above
+ * (score -> two-pass softmax -> aggregation). [P5] notes that in the
+ * backward pass the gradients of an edge land on the feature rows of its
+ * endpoints, so rows shared by several edges collect several contributions;
+ * here they are plain sums over the edges. Given dout [n_rows,H,Dh], for each
+ * row i, head h and edge e in the row with source j = col_idx[e]:
+ *     s[e]      = scale * <q[i,h], k[j,h]>
+ *     a[e]      = exp(s[e] - max s) / sum exp(s - max s)   (two-pass)
+ *     da[e]     = <dout[i,h], v[j,h]>
+ *     Delta     = sum_e a[e] da[e]
+ *     ds[e]     = a[e] (da[e] - Delta)
+ *     dq[i,h]  += scale * ds[e] * k[j,h]
+ *     dk[j,h]  += scale * ds[e] * q[i,h]
+ *     dv[j,h]  += a[e] * dout[i,h]
+ * dq is [n_rows,H,Dh]; dk, dv are [n_src,H,Dh]; all start at zero, so a
+ * zero-degree row and a source no edge reads get zeros. cdq/cdk/cdv
+ * (optional) receive the sum of |terms| of each output element, with each
+ * ds[e] counted as a[e] (|da[e]| + |Delta|).
+ */
+int oracle_fused_backward(const int32_t *row_ptr, const int32_t *col_idx,
+                          int64_t n_rows, int64_t n_src, int32_t H, int32_t Dh,
+                          double scale, const void *q, const void *k, const void *v,
+                          const void *dout, int dtype, double *dq, double *dk,
+                          double *dv, double *cdq, double *cdk, double *cdv)
+{
+    if (!row_ptr || n_rows < 0 || n_src < 0 || H < 1 || Dh < 1 || !dq || !dk || !dv)
+        return -1;
+    const int64_t HD = (int64_t)H * Dh;
+    memset(dq, 0, (size_t)(n_rows * HD) * sizeof(double));
+    memset(dk, 0, (size_t)(n_src * HD) * sizeof(double));
+    memset(dv, 0, (size_t)(n_src * HD) * sizeof(double));
+    if (cdq)
+        memset(cdq, 0, (size_t)(n_rows * HD) * sizeof(double));
+    if (cdk)
+        memset(cdk, 0, (size_t)(n_src * HD) * sizeof(double));
+    if (cdv)
+        memset(cdv, 0, (size_t)(n_src * HD) * sizeof(double));
+    int64_t dm = max_degree(row_ptr, n_rows);
+    size_t cap = (size_t)(dm > 0 ? dm : 1);
+    double *s = (double *)malloc(cap * sizeof(double));
+    double *a = (double *)malloc(cap * sizeof(double));
+    double *da = (double *)malloc(cap * sizeof(double));
+    if (!s || !a || !da) {
+        free(s);
+        free(a);
+        free(da);
+        return -2;
+    }
+    for (int64_t i = 0; i < n_rows; ++i) {
+        int64_t e0 = row_ptr[i], e1 = row_ptr[i + 1];
+        if (e1 == e0)
+            continue;
+        for (int32_t h = 0; h < H; ++h) {
+            const int64_t qi = i * HD + (int64_t)h * Dh;
+            for (int64_t e = e0; e < e1; ++e) {
+                int64_t j = col_idx[e];
+                if (j < 0 || j >= n_src) {
+                    free(s);
+                    free(a);
+                    free(da);
+                    return -1;
+                }
+                const int64_t kj = j * HD + (int64_t)h * Dh;
+                double sc = 0.0, dd = 0.0;
+                for (int32_t d = 0; d < Dh; ++d) {
+                    sc += elem(q, dtype, qi + d) * elem(k, dtype, kj + d);
+                    dd += elem(dout, dtype, qi + d) * elem(v, dtype, kj + d);
+                }
+                s[e - e0] = scale * sc;
+                da[e - e0] = dd;
+            }
+            double m = -INFINITY;
+            for (int64_t e = e0; e < e1; ++e)
+                if (s[e - e0] > m)
+                    m = s[e - e0];
+            double Z = 0.0;
+            for (int64_t e = e0; e < e1; ++e)
+                Z += exp(s[e - e0] - m);
+            double Delta = 0.0;
+            for (int64_t e = e0; e < e1; ++e) {
+                a[e - e0] = exp(s[e - e0] - m) / Z;
+                Delta += a[e - e0] * da[e - e0];
+            }
+            for (int64_t e = e0; e < e1; ++e) {
+                const int64_t kj = (int64_t)col_idx[e] * HD + (int64_t)h * Dh;
+                const double ae = a[e - e0];
+                const double ds = ae * (da[e - e0] - Delta);
+                const double ds_abs = ae * (fabs(da[e - e0]) + fabs(Delta));
+                for (int32_t d = 0; d < Dh; ++d) {
+                    const double kv = elem(k, dtype, kj + d);
+                    const double qv = elem(q, dtype, qi + d);
+                    const double gv = elem(dout, dtype, qi + d);
+                    dq[qi + d] += scale * ds * kv;
+                    dk[kj + d] += scale * ds * qv;
+                    dv[kj + d] += ae * gv;
+                    if (cdq)
+                        cdq[qi + d] += fabs(scale) * ds_abs * fabs(kv);
+                    if (cdk)
+                        cdk[kj + d] += fabs(scale) * ds_abs * fabs(qv);
+                    if (cdv)
+                        cdv[kj + d] += ae * fabs(gv);
+                }
+            }
+        }
+    }
+    free(s);
+    free(a);
+    free(da);
+    return 0;
+}
+
+/*
  * Dense-masked small-graph attention block [P4, reference model]. Per graph b
  * (nodes x[N,D], pair feats [N,N,P], mask [N,N]), with head h owning feature
  * dims [h*dh, (h+1)*dh), dh = D/H:

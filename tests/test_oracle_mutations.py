@@ -44,6 +44,14 @@ MUTATIONS = [
     ("plan chunks rounded down", "int64_t c = (d + chunk - 1) / chunk;", "int64_t c = d / chunk;"),
     ("bf16 widened with the wrong shift", "uint32_t u = (uint32_t)bits << 16;",
      "uint32_t u = (uint32_t)bits << 15;"),
+    ("backward Delta dropped", "const double ds = ae * (da[e - e0] - Delta);",
+     "const double ds = ae * da[e - e0];"),
+    ("backward dv weighted by the wrong factor", "dv[kj + d] += ae * gv;",
+     "dv[kj + d] += da[e - e0] * gv;"),
+    ("backward dk from k", "dk[kj + d] += scale * ds * qv;", "dk[kj + d] += scale * ds * kv;"),
+    ("backward dq scale dropped", "dq[qi + d] += scale * ds * kv;", "dq[qi + d] += ds * kv;"),
+    ("backward da against k", "dd += elem(dout, dtype, qi + d) * elem(v, dtype, kj + d);",
+     "dd += elem(dout, dtype, qi + d) * elem(k, dtype, kj + d);"),
 ]
 
 

@@ -326,6 +326,105 @@ def test_fused_matches_dense_on_bf16_zipf_graph():
 
 
 # ----------------------------------------------------------------------------
+# O6 backward of the fused layer: central differences of the (pinned) forward
+# oracle, PyTorch float64 autograd of dense masked attention, special cases
+# ----------------------------------------------------------------------------
+def _grid_values(rng, shape):
+    """fp32 values on a coarse binary grid (multiples of 1/64 in [-2, 2)), so
+    that x +/- 2^-14 is exact in fp32 and finite differences see exact inputs."""
+    return (rng.integers(-128, 128, size=shape) / 64.0).astype(np.float32)
+
+
+@pytest.mark.parametrize("dup", [False, True])
+def test_backward_equals_central_differences_of_forward(dup):
+    rng = np.random.default_rng(60 + dup)
+    n, n_src, H, Dh, scale = 6, 5, 2, 3, 0.7
+    rp, ci = tiny_graph(rng, n, n_src, 4, allow_dup=dup, sort=not dup)
+    x = {"q": _grid_values(rng, (n, H, Dh)), "k": _grid_values(rng, (n_src, H, Dh)),
+         "v": _grid_values(rng, (n_src, H, Dh))}
+    g = _grid_values(rng, (n, H, Dh))
+    grads = dict(zip("qkv", oracle.fused_backward(rp, ci, x["q"], x["k"], x["v"], g, H, Dh,
+                                                  scale)))
+
+    def loss(**over):
+        a = {**x, **over}
+        out = oracle.fused_layer(rp, ci, a["q"], a["k"], a["v"], H, Dh, scale)
+        return float((out * g.astype(np.float64)).sum())
+
+    step = 2.0 ** -14
+    for name in "qkv":
+        fd = np.zeros(x[name].shape)
+        for idx in np.ndindex(x[name].shape):
+            xp, xm = x[name].copy(), x[name].copy()
+            xp[idx] += step
+            xm[idx] -= step
+            fd[idx] = (loss(**{name: xp}) - loss(**{name: xm})) / (2 * step)
+        np.testing.assert_allclose(grads[name], fd, rtol=1e-6, atol=1e-8, err_msg=name)
+
+
+def test_backward_equals_torch_autograd_of_dense_masked_attention():
+    import torch
+    rng = np.random.default_rng(62)
+    n, n_src, H, Dh, scale = 9, 7, 3, 4, 0.5
+    rp, ci = tiny_graph(rng, n, n_src, 6)
+    q, g = (rng.standard_normal((n, H, Dh)).astype(np.float32) for _ in range(2))
+    k, v = (rng.standard_normal((n_src, H, Dh)).astype(np.float32) for _ in range(2))
+    Q, K, V = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+    mask = torch.zeros((n, n_src), dtype=torch.bool)
+    mask[torch.as_tensor(row_of_edge(rp)), torch.as_tensor(ci.astype(np.int64))] = True
+    nz = mask.any(1)
+    S = torch.einsum("ihd,jhd->hij", Q, K) * scale
+    S = S[:, nz].masked_fill(~mask[nz][None], float("-inf"))
+    A = torch.softmax(S, dim=-1)
+    out = torch.zeros((n, H, Dh), dtype=torch.float64)
+    out[nz] = torch.einsum("hij,jhd->ihd", A, V)
+    (out * torch.tensor(g, dtype=torch.float64)).sum().backward()
+    dq, dk, dv = oracle.fused_backward(rp, ci, q, k, v, g, H, Dh, scale)
+    assert (~nz).any()  # the graph has an empty row
+    for got, ref in ((dq, Q.grad), (dk, K.grad), (dv, V.grad)):
+        np.testing.assert_allclose(got, ref.numpy(), rtol=1e-11, atol=1e-13)
+
+
+def test_backward_special_cases():
+    rng = np.random.default_rng(63)
+    n, n_src, H, Dh = 5, 4, 2, 3
+    q, g = (rng.standard_normal((n, H, Dh)).astype(np.float32) for _ in range(2))
+    k, v = (rng.standard_normal((n_src, H, Dh)).astype(np.float32) for _ in range(2))
+    # one edge per row: the softmax weight is 1 whatever the score, so dq = dk = 0
+    # exactly and dv[j] is the sum of dout over the rows reading j
+    rp = np.arange(n + 1, dtype=np.int32)
+    ci = np.array([2, 0, 2, 3, 2], np.int32)
+    dq, dk, dv = oracle.fused_backward(rp, ci, q, k, v, g, H, Dh, 0.3)
+    assert (dq == 0).all() and (dk == 0).all()
+    ref = np.zeros((n_src, H, Dh))
+    np.add.at(ref, ci, g.astype(np.float64))
+    np.testing.assert_allclose(dv, ref, rtol=1e-15, atol=1e-15)
+    assert (dv[1] == 0).all()  # a source no edge reads
+    # empty rows contribute nothing; dq of an empty row is zero
+    rp2 = np.array([0, 0, 2, 2, 3, 3], np.int32)
+    ci2 = np.array([1, 3, 0], np.int32)
+    dq2, dk2, dv2, cq, ck, cv = oracle.fused_backward(rp2, ci2, q, k, v, g, H, Dh, 0.3,
+                                                      want_cond=True)
+    assert (dq2[[0, 2, 3, 4]] == 0).all() and (dk2[2] == 0).all() and (dv2[2] == 0).all()
+    assert (cq >= np.abs(dq2)).all() and (ck >= np.abs(dk2)).all() and (cv >= np.abs(dv2)).all()
+    # row 3's single edge: no dq/dk, dv[0] = dout[3]
+    np.testing.assert_array_equal(dv2[0], g[3].astype(np.float64))
+
+
+def test_backward_bf16_inputs_widen_exactly():
+    rng = np.random.default_rng(64)
+    n, H, Dh = 7, 2, 8
+    rp, ci = tiny_graph(rng, n, n, 5, allow_dup=True, sort=False)
+    f = [rng.standard_normal((n, H, Dh)).astype(np.float32) for _ in range(4)]
+    bits = [W.bf16_bits_from_f32(a) for a in f]
+    wid = [W.f32_from_bf16_bits(b) for b in bits]
+    a = oracle.fused_backward(rp, ci, *bits, H, Dh, 0.25)
+    b = oracle.fused_backward(rp, ci, *wid, H, Dh, 0.25)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+# ----------------------------------------------------------------------------
 # O5 dense-masked block: PyTorch CPU float64 modules
 # ----------------------------------------------------------------------------
 def torch_block(w, graphs):
