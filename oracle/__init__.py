@@ -65,9 +65,10 @@ def _load():
         lib.oracle_plan.argtypes = [P, I64, I32, I32, P, P, P, P, P]
         lib.oracle_fused_backward.argtypes = [P, P, I64, I64, I32, I32, D, P, P, P, P,
                                               ctypes.c_int, P, P, P, P, P, P]
+        lib.oracle_transpose.argtypes = [P, P, I64, I64, P, P, P]
         for f in ("oracle_edge_softmax", "oracle_spmm_weighted", "oracle_sddmm",
                   "oracle_fused_layer", "oracle_dense_block", "oracle_plan",
-                  "oracle_fused_backward"):
+                  "oracle_fused_backward", "oracle_transpose"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -191,6 +192,20 @@ def dense_block(w: dict, graphs=None, want_cond=False):
                                       float(w["ln_eps"]), *[_p(a) for a in wts],
                                       _p(sel), n_sel, _p(out), _p(cond)), "oracle_dense_block")
     return (out, cond) if want_cond else out
+
+
+def transpose(row_ptr, col_idx, n_src):
+    """Edges grouped by source, each group in edge order: (src_ptr [n_src+1],
+    perm [E], dst [E]) int32 arrays."""
+    rp, ci = _c(row_ptr, np.int32), _c(col_idx, np.int32)
+    n = rp.size - 1
+    E = int(rp[-1]) if rp.size else 0
+    sp = np.empty(int(n_src) + 1, dtype=np.int32)
+    perm = np.empty(E, dtype=np.int32)
+    dst = np.empty(E, dtype=np.int32)
+    _check(_load().oracle_transpose(_p(rp), _p(ci), n, int(n_src), _p(sp), _p(perm), _p(dst)),
+           "oracle_transpose")
+    return sp, perm, dst
 
 
 def plan(row_ptr, heavy_threshold, chunk):

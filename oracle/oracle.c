@@ -360,6 +360,45 @@ int oracle_fused_backward(const int32_t *row_ptr, const int32_t *col_idx,
 }
 
 /*
+ * Transposed view of a CSR graph for the backward pass (the gradients of
+ * [P5]'s backward discussion land on source rows): the edges grouped by
+ * source node, each group in increasing edge order (a stable counting sort
+ * by col_idx). src_ptr [n_src+1]: group offsets; perm [E]: edge ids;
+ * dst [E]: destination row of perm[k].
+ */
+int oracle_transpose(const int32_t *row_ptr, const int32_t *col_idx, int64_t n_rows,
+                     int64_t n_src, int32_t *src_ptr, int32_t *perm, int32_t *dst)
+{
+    if (!row_ptr || n_rows < 0 || n_src < 0 || !src_ptr)
+        return -1;
+    int64_t E = row_ptr[n_rows];
+    int64_t *next = (int64_t *)malloc((size_t)(n_src > 0 ? n_src : 1) * sizeof(int64_t));
+    if (!next)
+        return -2;
+    for (int64_t j = 0; j <= n_src; ++j)
+        src_ptr[j] = 0;
+    for (int64_t e = 0; e < E; ++e) {
+        if (col_idx[e] < 0 || col_idx[e] >= n_src) {
+            free(next);
+            return -1;
+        }
+        src_ptr[col_idx[e] + 1] += 1;
+    }
+    for (int64_t j = 0; j < n_src; ++j)
+        src_ptr[j + 1] += src_ptr[j];
+    for (int64_t j = 0; j < n_src; ++j)
+        next[j] = src_ptr[j];
+    for (int64_t i = 0; i < n_rows; ++i)
+        for (int64_t e = row_ptr[i]; e < row_ptr[i + 1]; ++e) {
+            int64_t k = next[col_idx[e]]++;
+            perm[k] = (int32_t)e;
+            dst[k] = (int32_t)i;
+        }
+    free(next);
+    return 0;
+}
+
+/*
  * Dense-masked small-graph attention block [P4, reference model]. Per graph b
  * (nodes x[N,D], pair feats [N,N,P], mask [N,N]), with head h owning feature
  * dims [h*dh, (h+1)*dh), dh = D/H:

@@ -50,6 +50,8 @@ MUTATIONS = [
      "dv[kj + d] += da[e - e0] * gv;"),
     ("backward dk from k", "dk[kj + d] += scale * ds * qv;", "dk[kj + d] += scale * ds * kv;"),
     ("backward dq scale dropped", "dq[qi + d] += scale * ds * kv;", "dq[qi + d] += ds * kv;"),
+    ("transpose counts shifted", "src_ptr[col_idx[e] + 1] += 1;", "src_ptr[col_idx[e]] += 1;"),
+    ("transpose records the source as the row", "dst[k] = (int32_t)i;", "dst[k] = col_idx[e];"),
     ("backward da against k", "dd += elem(dout, dtype, qi + d) * elem(v, dtype, kj + d);",
      "dd += elem(dout, dtype, qi + d) * elem(k, dtype, kj + d);"),
 ]

@@ -424,6 +424,17 @@ def test_backward_bf16_inputs_widen_exactly():
         np.testing.assert_array_equal(x, y)
 
 
+@pytest.mark.parametrize("n,n_src,max_deg", [(50, 30, 9), (200, 7, 40), (1, 1, 0), (30, 1000, 3)])
+def test_transpose_equals_stable_library_argsort(n, n_src, max_deg):
+    rng = np.random.default_rng(65 + n)
+    rp, ci = tiny_graph(rng, n, n_src, max_deg, allow_dup=True, sort=False)
+    sp, perm, dst = oracle.transpose(rp, ci, n_src)
+    order = np.argsort(ci, kind="stable")
+    np.testing.assert_array_equal(perm, order)
+    np.testing.assert_array_equal(dst, row_of_edge(rp)[order])
+    np.testing.assert_array_equal(sp, np.concatenate([[0], np.cumsum(np.bincount(ci, minlength=n_src))]))
+
+
 # ----------------------------------------------------------------------------
 # O5 dense-masked block: PyTorch CPU float64 modules
 # ----------------------------------------------------------------------------
