@@ -8,7 +8,7 @@ layer and call on it; its build time is reported as plan_ms).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                     [--workload fused|edge_softmax|aggregate|sddmm|dense|spmm_heads|
-                               edge_softmax_h8]
+                               edge_softmax_h8|fused_backward]
 
 Prints one JSON line (rank 0). value = edge-heads/s over all ranks (each rank
 runs its own full, independent problem: weak scaling, no collective on the
@@ -413,6 +413,7 @@ def bench_small(name, args):
     g = W.WORKLOADS[name][0]() if name in ("edge_softmax", "aggregate", "sddmm", "dense") else None
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
     flops, tensor_flops = 0.0, 0.0
+    extra = {}
     if name == "spmm_heads":
         # head_dim 32, 8 heads, fp32 weights and features, 1e6-row power-law graph
         g = W.make_spmm_heads()
@@ -427,6 +428,33 @@ def bench_small(name, args):
         # weights and the gathered feature row
         alg_bytes = (4 + row) * g["n_rows"] + (4 + 4 * g["H"] + row) * g["n_edges"]
         flops = 2.0 * g["n_edges"] * g["H"] * g["Dh"]
+    elif name == "fused_backward":
+        # gradients of the fused layer on the 1e6-row power-law graph (bf16, H=8, Dh=64)
+        g = W.make_fused_backward()
+        bt = lambda a: t(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+        rp, ci = t(g["row_ptr"]), t(g["col_idx"])
+        q, k, v, go = (bt(g[x]) for x in ("q", "k", "v", "dout"))
+        plan = gat.Plan(rp)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        tr = gat.Transpose(rp, ci, g["n_src"])
+        torch.cuda.synchronize()
+        transpose_ms = (time.perf_counter() - t0) * 1e3
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(gat.gat_fused_layer_backward_workspace_size(
+            plan, g["n_rows"], g["n_edges"], g["H"], g["Dh"]), dtype=torch.uint8, device=dev)
+        fn = lambda: gat.gat_fused_layer_backward(rp, ci, q, k, v, go, g["scale"], tr,  # noqa: E731
+                                                  plan=plan, dq=dq, dk=dk, dv=dv, workspace=ws)
+        units, launches = g["n_edges"] * g["H"], 4
+        rb = 2 * g["H"] * g["Dh"]
+        # per edge: col_idx, k and v rows (pass A), score and da written then
+        # read (8H each way), perm and dst, q and dout rows (pass B); per row:
+        # row_ptr, q, dout in, dq out, lse and Delta written (8H; their reads
+        # in pass B are gathers of this table); per source: src_ptr, dk, dv out
+        alg_bytes = (g["n_edges"] * (4 + 2 * rb + 16 * g["H"] + 8 + 2 * rb)
+                     + g["n_rows"] * (4 + 3 * rb + 8 * g["H"]) + g["n_src"] * (4 + 2 * rb))
+        flops = 2.0 * g["n_edges"] * g["H"] * g["Dh"] * 6
+        extra = {"transpose_build_ms": transpose_ms, "transpose": tr.info()}
     elif name == "edge_softmax_h8":
         # 8 heads on the 1e6-row power-law graph
         deg = W.zipf_degrees(np.random.default_rng(3), 1_000_000)
@@ -510,6 +538,7 @@ def bench_small(name, args):
         res["tensor_issue_frac_of_tf32_peak"] = 3 * tensor_flops / (ms * 1e-3) / 1e12 / tf32_peak
         res["tf32_peak_tflops"] = tf32_peak
         res["peak_kind"] = kind
+    res.update(extra)
     if name in ("edge_softmax", "aggregate", "sddmm"):
         res["note"] = "L2-resident and launch-latency bound at this size; fractions are not a roofline claim"
     return res
@@ -524,7 +553,7 @@ def main():
     ap.add_argument("--impl", default="gat", choices=["gat", "reference"])
     ap.add_argument("--workload", default="fused",
                     choices=["fused", "edge_softmax", "aggregate", "sddmm", "dense", "spmm_heads",
-                             "edge_softmax_h8"])
+                             "edge_softmax_h8", "fused_backward"])
     ap.add_argument("--ref-rows", type=int, default=5000,
                     help="--impl reference: consecutive rows per step (~0.2 s of oracle work)")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
@@ -552,7 +581,7 @@ def main():
         if not args.no_extras:
             res["other_workloads"] = {}
             for nm in ("edge_softmax", "aggregate", "sddmm", "dense", "spmm_heads",
-                       "edge_softmax_h8"):
+                       "edge_softmax_h8", "fused_backward"):
                 try:
                     res["other_workloads"][nm] = bench_small(nm, args)
                 except Exception as exc:  # keep the headline line if a side workload fails

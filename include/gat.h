@@ -214,6 +214,91 @@ gat_status_t gat_fused_layer(const int32_t *row_ptr, const int32_t *col_idx, int
                              void *stream);
 
 /* ------------------------------------------------------------------------
+ * Transposed (source-major) view of a graph, for the backward pass
+ * [sddmm page, discussion of the backward pass: an edge's gradients land on
+ * the feature rows of its endpoints, and a row shared by several edges
+ * collects several contributions; the page adds them with atomics].
+ * gat_transpose_create lists, for every source node j, the edges that read j
+ * (col_idx[e] == j) in increasing edge order, so per-source sums run in a
+ * fixed order without floating-point atomics:
+ *   src_ptr [n_src + 1]  group offsets (exclusive prefix sum of the number
+ *                        of edges reading each source)
+ *   perm    [n_edges]    edge ids, group after group
+ *   dst     [n_edges]    the row that owns edge perm[k]
+ * plus a degree plan over src_ptr (sources read by more than 128 edges are
+ * summed by one thread block each).
+ * Allocates its device arrays and temporary scratch (cudaMalloc), runs a few
+ * kernels on `stream` and synchronises it (three times). row_ptr must be a
+ * valid row pointer array (see gat_validate_graph).
+ * Errors: GAT_ERR_INVALID_ARG (NULL output / pointers, negative or too large
+ * sizes), GAT_ERR_INDEX_OUT_OF_RANGE (a col_idx entry outside [0, n_src);
+ * nothing is built), GAT_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+typedef struct gat_transpose_s *gat_transpose_t;
+
+gat_status_t gat_transpose_create(const int32_t *row_ptr, const int32_t *col_idx,
+                                  int64_t n_rows, int64_t n_src, int64_t n_edges, void *stream,
+                                  gat_transpose_t *transpose);
+
+/* Free a transpose (NULL is accepted); no enqueued work may still use it. */
+gat_status_t gat_transpose_destroy(gat_transpose_t transpose);
+
+/* Sizes of a transpose; any output pointer may be NULL. max_src_degree is
+ * the largest number of edges reading one source; n_heavy_src the number of
+ * sources its degree plan treats as heavy. */
+gat_status_t gat_transpose_info(gat_transpose_t transpose, int64_t *n_rows, int64_t *n_src,
+                                int64_t *n_edges, int32_t *max_src_degree, int64_t *n_heavy_src);
+
+/* Copy src_ptr [n_src+1], perm [n_edges] and dst [n_edges] into caller device
+ * buffers (any pointer may be NULL to skip that array); enqueued on `stream`. */
+gat_status_t gat_transpose_export(gat_transpose_t transpose, int32_t *src_ptr, int32_t *perm,
+                                  int32_t *dst, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Backward of gat_fused_layer: the chain rule through its score, softmax and
+ * aggregation. With a[e] the softmax weights of the forward and dout
+ * [n_rows,H,Dh] the gradient of the loss with respect to out, for every row
+ * i, head h and edge e of the row (source j = col_idx[e]):
+ *     da[e]   = <dout[i,h,:], v[j,h,:]>
+ *     Delta   = sum_e a[e] da[e]                (over the row's edges)
+ *     ds[e]   = a[e] (da[e] - Delta)
+ *     dq[i,h] = scale * sum_e ds[e] k[j,h,:]                    [n_rows,H,Dh]
+ *     dk[j,h] = scale * sum over edges e reading j of ds[e] q[i(e),h,:]
+ *     dv[j,h] = sum over edges e reading j of a[e] dout[i(e),h,:]  [n_src,H,Dh]
+ * A zero-degree row gets dq = 0; a source no edge reads gets dk = dv = 0.
+ * q, k, v, dout, dq, dk, dv share `dtype` (fp32 arithmetic, bf16 results
+ * rounded to nearest even); the forward's output is not needed (the scores
+ * and weights are recomputed).
+ * Two passes: over the rows (CSR; recomputes each edge's score and da, writes
+ * them and each row's log-sum-exp and Delta into the workspace, and dq) and
+ * over the sources of `transpose` (sums dk, dv per source in edge order).
+ * Results are bitwise repeatable.
+ * plan: NULL or the forward plan of this graph (its heavy rows are cut into
+ * chunks whose partial states go to the workspace and are merged by the last
+ * chunk to finish; the plan's arrival counters are used, so one plan must not
+ * serve two calls whose work overlaps on the GPU). transpose: required, from
+ * gat_transpose_create on the same graph.
+ * workspace: caller device memory, 16-byte aligned, at least the size that
+ * gat_fused_layer_backward_workspace_size reports for the same plan and
+ * shape (8 * n_edges * H + 8 * n_rows * H bytes plus the chunk states, each
+ * part rounded up to 256 bytes); contents on entry are ignored.
+ * Errors: GAT_ERR_INVALID_ARG (NULL pointers, bad sizes, no transpose),
+ * GAT_ERR_UNSUPPORTED (dtype), GAT_ERR_PLAN_MISMATCH (plan or transpose of
+ * another graph shape), GAT_ERR_WORKSPACE.
+ * ---------------------------------------------------------------------- */
+gat_status_t gat_fused_layer_backward_workspace_size(gat_plan_t plan, int64_t n_rows,
+                                                     int64_t n_edges, int32_t H, int32_t Dh,
+                                                     size_t *bytes);
+
+gat_status_t gat_fused_layer_backward(const int32_t *row_ptr, const int32_t *col_idx,
+                                      int64_t n_rows, int64_t n_src, int64_t n_edges, int32_t H,
+                                      int32_t Dh, float scale, const void *q, const void *k,
+                                      const void *v, const void *dout, gat_dtype_t dtype,
+                                      void *dq, void *dk, void *dv, gat_plan_t plan,
+                                      gat_transpose_t transpose, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * Fused layer without any device allocation. The source pages have no
  * counterpart: this is a deployment variant of gat_fused_layer for callers
  * that cannot call cudaMalloc (a framework that owns all device memory

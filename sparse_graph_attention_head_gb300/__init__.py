@@ -31,6 +31,8 @@ EXPORTS = (
     "gat_validate_graph", "gat_sddmm", "gat_edge_softmax", "gat_spmm_weighted",
     "gat_fused_layer_workspace_size", "gat_fused_layer", "gat_dense_masked_attention",
     "gat_fused_layer_no_alloc",
+    "gat_transpose_create", "gat_transpose_destroy", "gat_transpose_info", "gat_transpose_export",
+    "gat_fused_layer_backward_workspace_size", "gat_fused_layer_backward",
 )
 
 
@@ -71,6 +73,13 @@ def _load() -> ctypes.CDLL:
                                        ctypes.c_int),
         "gat_fused_layer_no_alloc": ([P, P, I64, I64, I64, I32, I32, F, P, P, P, ctypes.c_int, P,
                                       P], ctypes.c_int),
+        "gat_transpose_create": ([P, P, I64, I64, I64, P, P], ctypes.c_int),
+        "gat_transpose_destroy": ([P], ctypes.c_int),
+        "gat_transpose_info": ([P, P, P, P, P, P], ctypes.c_int),
+        "gat_transpose_export": ([P, P, P, P, P], ctypes.c_int),
+        "gat_fused_layer_backward_workspace_size": ([P, I64, I64, I32, I32, P], ctypes.c_int),
+        "gat_fused_layer_backward": ([P, P, I64, I64, I64, I32, I32, F, P, P, P, P, ctypes.c_int,
+                                      P, P, P, P, P, P, SZ, P], ctypes.c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -290,6 +299,87 @@ def gat_fused_layer_no_alloc(row_ptr, col_idx, q, k, v, scale, out, stream=None)
         _ptr(row_ptr), _ptr(col_idx) if E else None, n_rows, k.shape[0], E, H, Dh, float(scale),
         _ptr(q), _ptr(k), _ptr(v), _dtype(q), _ptr(out), _stream(stream)))
     return out
+
+
+class Transpose:
+    """Source-major view of one graph (``gat_transpose_create``): for every
+    source, the edges that read it, in edge order. Owns device arrays."""
+
+    def __init__(self, row_ptr: torch.Tensor, col_idx: torch.Tensor, n_src: int, stream=None):
+        _idx(row_ptr, "row_ptr")
+        _idx(col_idx, "col_idx")
+        n_rows, E = row_ptr.numel() - 1, col_idx.numel()
+        h = ctypes.c_void_p()
+        _check("gat_transpose_create", _lib.gat_transpose_create(
+            _ptr(row_ptr), _ptr(col_idx) if E else None, n_rows, n_src, E, _stream(stream),
+            ctypes.byref(h)))
+        self.handle = h.value
+        self.device = row_ptr.device
+
+    def info(self) -> dict:
+        vals = [ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32(),
+                ctypes.c_int64()]
+        _check("gat_transpose_info",
+               _lib.gat_transpose_info(self.handle, *[ctypes.byref(v) for v in vals]))
+        keys = ("n_rows", "n_src", "n_edges", "max_src_degree", "n_heavy_src")
+        return {k: v.value for k, v in zip(keys, vals)}
+
+    def export(self, stream=None):
+        """(src_ptr, perm, dst) as int32 device tensors."""
+        inf = self.info()
+        sp = torch.empty(inf["n_src"] + 1, dtype=torch.int32, device=self.device)
+        perm = torch.empty(inf["n_edges"], dtype=torch.int32, device=self.device)
+        dst = torch.empty(inf["n_edges"], dtype=torch.int32, device=self.device)
+        e = inf["n_edges"] > 0
+        _check("gat_transpose_export", _lib.gat_transpose_export(
+            self.handle, _ptr(sp), _ptr(perm) if e else None, _ptr(dst) if e else None,
+            _stream(stream)))
+        return sp, perm, dst
+
+    def destroy(self):
+        if getattr(self, "handle", None):
+            _lib.gat_transpose_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def gat_transpose_create(row_ptr, col_idx, n_src, stream=None) -> Transpose:
+    return Transpose(row_ptr, col_idx, n_src, stream)
+
+
+def gat_fused_layer_backward_workspace_size(plan, n_rows, n_edges, H, Dh) -> int:
+    n = ctypes.c_size_t()
+    _check("gat_fused_layer_backward_workspace_size",
+           _lib.gat_fused_layer_backward_workspace_size(_plan_handle(plan), n_rows, n_edges, H, Dh,
+                                                        ctypes.byref(n)))
+    return n.value
+
+
+def gat_fused_layer_backward(row_ptr, col_idx, q, k, v, dout, scale, transpose, plan=None,
+                             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of gat_fused_layer for the upstream gradient
+    ``dout`` [n_rows,H,Dh]; ``transpose`` from gat_transpose_create."""
+    _idx(row_ptr, "row_ptr")
+    _idx(col_idx, "col_idx")
+    n_rows, H, Dh = q.shape
+    n_src, E = k.shape[0], col_idx.numel()
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        need = gat_fused_layer_backward_workspace_size(plan, n_rows, E, H, Dh)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("gat_fused_layer_backward", _lib.gat_fused_layer_backward(
+        _ptr(row_ptr), _ptr(col_idx) if E else None, n_rows, n_src, E, H, Dh, float(scale),
+        _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _dtype(q), _ptr(dq), _ptr(dk), _ptr(dv),
+        _plan_handle(plan), transpose.handle, _ptr(workspace), ws_bytes, _stream(stream)))
+    return dq, dk, dv
 
 
 def gat_dense_masked_attention(nodes, pair_feats, edge_mask, ln_w, ln_b, ln_eps, Wq, Wk, Wv,

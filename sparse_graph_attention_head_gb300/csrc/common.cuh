@@ -36,6 +36,17 @@ struct gat_plan_s {
     int device = 0;
 };
 
+// Transposed (source-major) view of a CSR graph, built by gat_transpose_create.
+struct gat_transpose_s {
+    int64_t n_rows = 0, n_src = 0, n_edges = 0;
+    int32_t max_src_degree = 0;
+    int32_t *src_ptr = nullptr;  // [n_src + 1] offsets of each source's edge group
+    int32_t *perm = nullptr;     // [n_edges] edge ids, grouped by source, edge order within
+    int32_t *dst = nullptr;      // [n_edges] destination row of perm[k]
+    gat_plan_t src_plan = nullptr;  // degree plan over src_ptr (heavy sources)
+    int device = 0;
+};
+
 namespace gat {
 
 // ---------------------------------------------------------------------------

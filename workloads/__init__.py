@@ -21,6 +21,8 @@ Workloads (shapes follow the problem statements on the source pages):
 * ``dense``         - dense-masked small-graph attention block, B graphs of 24
   nodes, D=96, H=4, P=16, mask Bernoulli(0.3) with a unit diagonal, all Linear
   weights and biases ~ N(0, 0.02^2)    (POPCORNBENCH Kimi-K2.6 l2_p4)
+* ``fused_backward`` - the fused workload plus an upstream gradient
+  dout [N,8,64] ~ N(0,1) (bf16), for the backward of the fused layer
 * ``spmm_heads``    - multi-head weighted aggregation at head_dim 32, 8 heads,
   fp32, on a power-law graph like ``fused``'s (POPCORNBENCH FW-GLM-5-1 l1_p18)
 
@@ -35,7 +37,7 @@ __all__ = [
     "bf16_bits_from_f32", "f32_from_bf16_bits", "row_ptr_from_degrees",
     "uniform_degrees", "zipf_degrees", "page_mod_degrees",
     "make_edge_softmax", "make_aggregate", "make_sddmm", "make_fused",
-    "make_dense", "make_csr", "make_spmm_heads", "WORKLOADS",
+    "make_dense", "make_csr", "make_spmm_heads", "make_fused_backward", "WORKLOADS",
 ]
 
 
@@ -201,6 +203,16 @@ def make_fused(seed: int = 3, n: int = 1_000_000, H: int = 8, Dh: int = 64,
                for t in range(3))
     return dict(row_ptr=rp, col_idx=ci, q=q, k=k, v=v, n_rows=n, n_src=n,
                 n_edges=int(rp[-1]), H=H, Dh=Dh, scale=1.0 / np.sqrt(Dh), dtype=dtype)
+
+
+def make_fused_backward(seed: int = 7, n: int = 1_000_000, H: int = 8, Dh: int = 64,
+                        deg: np.ndarray | None = None, dmax: int = 4096, mean: float = 16.0,
+                        dtype: str = "bf16") -> dict:
+    """The fused workload's arrays (``make_fused`` with this seed) plus an
+    upstream gradient dout [n,H,Dh] ~ N(0,1) from block stream [seed, 4]."""
+    d = make_fused(seed, n, H, Dh, deg, dmax, mean, dtype)
+    d["dout"] = _block_normals([seed, 4], n * H * Dh, dtype == "bf16").reshape(n, H, Dh)
+    return d
 
 
 def make_spmm_heads(seed: int = 5, n: int = 1_000_000, H: int = 8, Dh: int = 32,
