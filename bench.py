@@ -430,7 +430,7 @@ def bench_small(name, args):
         flops = 2.0 * g["n_edges"] * g["H"] * g["Dh"]
     elif name == "fused_backward":
         # gradients of the fused layer on the 1e6-row power-law graph (bf16, H=8, Dh=64)
-        g = W.make_fused_backward()
+        g = W.make_fused_backward(n=args.n_rows)
         bt = lambda a: t(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
         rp, ci = t(g["row_ptr"]), t(g["col_idx"])
         q, k, v, go = (bt(g[x]) for x in ("q", "k", "v", "dout"))

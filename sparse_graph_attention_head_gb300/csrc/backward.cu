@@ -45,6 +45,7 @@ struct BwdParams {
     void *dq, *dk, *dv;
     int64_t n_rows, n_src;
     int32_t H, Dh;
+    int32_t hgroups;  // pass A: head groups per row (32 vectors each)
     float scale;   // the layer's score scale
     float qscale;  // scale * log2(e)
     float2 *ws;     // [E, H] (score in log2 units, da)
@@ -55,8 +56,8 @@ struct BwdParams {
     const int4 *chunk_desc;      // {row, e0, e1, heavy index}
     const int32_t *chunk_start;  // [n_heavy + 1]
     int32_t *counters;           // [n_heavy], zero between calls
-    float *partials;             // [n_chunks][slot_floats]
-    int64_t slot_floats;         // >= 2*H*Dh + 3*H, multiple of 4
+    float *partials;             // [n_chunks][hgroups][slot_floats]
+    int64_t slot_floats;         // one head group's state, multiple of 4
     // transposed view (sources)
     const int32_t *src_ptr, *perm, *dst;
     int32_t src_threshold;
@@ -74,168 +75,163 @@ __device__ __forceinline__ float bexp2(float x) {
 // ---------------------------------------------------------------------------
 // pass A: rows
 // ---------------------------------------------------------------------------
-template <typename T, int V, int U>
-struct BwdRow {
-    using L = Lanes<T, V, 32>;
-    static constexpr int VE = L::VE;
-    uint4 qraw[V], graw[V];  // q and dout of the row, as stored
-    float A[V][VE], B[V][VE];
-    float m[V], l[V], S[V];
+// Pass A works on head groups: a row's H*Dh elements are cut into HG groups
+// of 32 16-byte vectors (HG = the forward's V), and one warp takes one
+// (item, group) pair, lane l owning vector l of the group. A group holds
+// HL = H / HG whole heads, G lanes each.
+constexpr float kRescale = 8.f;  // the running max is moved only by more than this (log2 units)
 
-    __device__ __forceinline__ void begin(const BwdParams &p, const L &ln, int64_t row) {
+template <typename T, int U>
+struct BwdRow {
+    using L = Lanes<T, 1, 32>;
+    static constexpr int VE = L::VE;
+    float qf[VE], gf[VE];  // q * qscale and dout of the row's group
+    float A[VE], B[VE];
+    float m, l, S;
+
+    // this lane's q and dout vectors of (row, group g)
+    __device__ __forceinline__ static void load_qg(const BwdParams &p, const L &ln, int64_t row,
+                                                   int g, uint4 &qr, uint4 &gr) {
         const int64_t rb = (int64_t)p.H * p.Dh * sizeof(T);
-        const char *qrow = static_cast<const char *>(p.q) + row * rb;
-        const char *grow = static_cast<const char *>(p.dout) + row * rb;
-#pragma unroll
-        for (int s = 0; s < V; ++s) {
-            qraw[s] = ld_stream16(qrow + ln.vi[s] * 16);
-            graw[s] = ld_stream16(grow + ln.vi[s] * 16);
-#pragma unroll
-            for (int t = 0; t < VE; ++t) A[s][t] = B[s][t] = 0.f;
-            m[s] = -INFINITY;
-            l[s] = 0.f;
-            S[s] = 0.f;
-        }
+        const int64_t off = row * rb + (int64_t)(g * 32 + ln.lane) * 16;
+        qr = ld_stream16(static_cast<const char *>(p.q) + off);
+        gr = ld_stream16(static_cast<const char *>(p.dout) + off);
     }
 
-    // edges [e0, e1), one 32-edge tile after another
-    __device__ __forceinline__ void run(const BwdParams &p, const L &ln, int e0, int e1) {
+    __device__ __forceinline__ void begin(const BwdParams &p, const uint4 &qr, const uint4 &gr) {
+        Vec<T>::unpack(qr, qf);
+        Vec<T>::unpack(gr, gf);
+#pragma unroll
+        for (int t = 0; t < VE; ++t) {
+            qf[t] *= p.qscale;
+            A[t] = B[t] = 0.f;
+        }
+        m = -INFINITY;
+        l = 0.f;
+        S = 0.f;
+    }
+
+    // edges [e0, e1) of the row, one 32-edge tile after another
+    __device__ __forceinline__ void run(const BwdParams &p, const L &ln, int e0, int e1, int g) {
         const int64_t rb = (int64_t)p.H * p.Dh * sizeof(T);
-        const char *kb = static_cast<const char *>(p.k);
-        const char *vb = static_cast<const char *>(p.v);
+        const int64_t goff = (int64_t)(g * 32 + ln.lane) * 16;
+        const char *kb = static_cast<const char *>(p.k) + goff;
+        const char *vb = static_cast<const char *>(p.v) + goff;
+        const int HL = p.H / p.hgroups;
+        const int head = g * HL + ln.head[0];
+        const bool leader = ln.lane % ln.G == 0;
         for (int base = e0; base < e1; base += 32) {
             const int n = min(32, e1 - base);
             const int my_ci = ln.lane < n ? __ldg(p.col_idx + base + ln.lane) : 0;
             for (int j0 = 0; j0 < n; j0 += U) {
-                uint4 kr[U][V], vr[U][V];
+                uint4 kr[U], vr[U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int64_t src = __shfl_sync(kFull, my_ci, (j0 + u) & 31);
-#pragma unroll
-                    for (int s = 0; s < V; ++s) {
-                        if (j0 + u < n) {
-                            kr[u][s] = ld_stream16(kb + src * rb + ln.vi[s] * 16);
-                            vr[u][s] = ld_stream16(vb + src * rb + ln.vi[s] * 16);
-                        } else {
-                            kr[u][s] = make_uint4(0, 0, 0, 0);
-                            vr[u][s] = make_uint4(0, 0, 0, 0);
-                        }
+                    if (j0 + u < n) {
+                        kr[u] = ld_stream16(kb + src * rb);
+                        vr[u] = ld_stream16(vb + src * rb);
+                    } else {
+                        kr[u] = vr[u] = make_uint4(0, 0, 0, 0);
                     }
                 }
-                float sc[U][V], da[U][V];
+                float sc[U], da[U];
 #pragma unroll
-                for (int s = 0; s < V; ++s) {
-                    float qf[VE], gf[VE];
-                    Vec<T>::unpack(qraw[s], qf);
-                    Vec<T>::unpack(graw[s], gf);
+                for (int u = 0; u < U; ++u) {
+                    float kf[VE], vf[VE];
+                    Vec<T>::unpack(kr[u], kf);
+                    Vec<T>::unpack(vr[u], vf);
+                    float a = 0.f, b = 0.f;
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        float kf[VE], vf[VE];
-                        Vec<T>::unpack(kr[u][s], kf);
-                        Vec<T>::unpack(vr[u][s], vf);
-                        float a = 0.f, b = 0.f;
-#pragma unroll
-                        for (int t = 0; t < VE; ++t) {
-                            a = fmaf(qf[t], kf[t], a);
-                            b = fmaf(gf[t], vf[t], b);
-                        }
-                        sc[u][s] = a;
-                        da[u][s] = b;
+                    for (int t = 0; t < VE; ++t) {
+                        a = fmaf(qf[t], kf[t], a);
+                        b = fmaf(gf[t], vf[t], b);
                     }
+                    sc[u] = a;
+                    da[u] = b;
                 }
                 for (int o = 1; o < ln.G; o <<= 1) {
 #pragma unroll
-                    for (int u = 0; u < U; ++u)
-#pragma unroll
-                        for (int s = 0; s < V; ++s) {
-                            sc[u][s] += __shfl_xor_sync(kFull, sc[u][s], o);
-                            da[u][s] += __shfl_xor_sync(kFull, da[u][s], o);
-                        }
+                    for (int u = 0; u < U; ++u) {
+                        sc[u] += __shfl_xor_sync(kFull, sc[u], o);
+                        da[u] += __shfl_xor_sync(kFull, da[u], o);
+                    }
                 }
+                // the head's first lane records the edge's score and da
+                if (leader)
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (j0 + u < n)
+                            p.ws[(int64_t)(base + j0 + u) * p.H + head] = make_float2(sc[u], da[u]);
+                float mx = -INFINITY;
 #pragma unroll
                 for (int u = 0; u < U; ++u)
-#pragma unroll
-                    for (int s = 0; s < V; ++s) sc[u][s] *= p.qscale;
-                // the head's first lane records the edge's score and da
-#pragma unroll
-                for (int s = 0; s < V; ++s)
-                    if (ln.vi[s] % ln.G == 0)
-#pragma unroll
-                        for (int u = 0; u < U; ++u)
-                            if (j0 + u < n) {
-                                const int64_t x = (int64_t)(base + j0 + u) * p.H + ln.head[s];
-                                p.ws[x] = make_float2(sc[u][s], da[u][s]);
-                            }
-#pragma unroll
-                for (int s = 0; s < V; ++s) {
-                    float mx = m[s];
-#pragma unroll
-                    for (int u = 0; u < U; ++u)
-                        if (j0 + u < n) mx = fmaxf(mx, sc[u][s]);
-                    const float c = bexp2(m[s] - mx);  // m = -inf at the start: c = 0
-                    l[s] *= c;
-                    S[s] *= c;
+                    if (j0 + u < n) mx = fmaxf(mx, sc[u]);
+                // terms are 2^(s - m) <= 2^kRescale, so the state is rescaled
+                // only when a score passes the running max by more than that
+                if (mx > m + kRescale) {
+                    const float c = bexp2(m - mx);  // m = -inf at the start: c = 0
+                    l *= c;
+                    S *= c;
 #pragma unroll
                     for (int t = 0; t < VE; ++t) {
-                        A[s][t] *= c;
-                        B[s][t] *= c;
+                        A[t] *= c;
+                        B[t] *= c;
                     }
+                    m = mx;
+                }
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        if (j0 + u >= n) continue;
-                        const float pe = bexp2(sc[u][s] - mx), pd = pe * da[u][s];
-                        l[s] += pe;
-                        S[s] += pd;
-                        float kf[VE];
-                        Vec<T>::unpack(kr[u][s], kf);
+                for (int u = 0; u < U; ++u) {
+                    if (j0 + u >= n) continue;
+                    const float pe = bexp2(sc[u] - m), pd = pe * da[u];
+                    l += pe;
+                    S += pd;
+                    float kf[VE];
+                    Vec<T>::unpack(kr[u], kf);
 #pragma unroll
-                        for (int t = 0; t < VE; ++t) {
-                            A[s][t] = fmaf(pd, kf[t], A[s][t]);
-                            B[s][t] = fmaf(pe, kf[t], B[s][t]);
-                        }
+                    for (int t = 0; t < VE; ++t) {
+                        A[t] = fmaf(pd, kf[t], A[t]);
+                        B[t] = fmaf(pe, kf[t], B[t]);
                     }
-                    m[s] = mx;
                 }
             }
         }
     }
 
-    // dq of the row and its (lse, Delta) per head
-    __device__ __forceinline__ void finish(const BwdParams &p, const L &ln, int64_t row) {
-        char *orow = static_cast<char *>(p.dq) + row * (int64_t)p.H * p.Dh * sizeof(T);
-        float2 *st = p.stats + row * p.H;
+    // dq of the row's group and its heads' (lse, Delta)
+    __device__ __forceinline__ void finish(const BwdParams &p, const L &ln, int64_t row, int g) {
+        const int64_t rb = (int64_t)p.H * p.Dh * sizeof(T);
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float delta = S * inv;
+        float o[VE];
 #pragma unroll
-        for (int s = 0; s < V; ++s) {
-            const float inv = l[s] > 0.f ? 1.f / l[s] : 0.f;
-            const float delta = S[s] * inv;
-            float o[VE];
-#pragma unroll
-            for (int t = 0; t < VE; ++t) o[t] = p.scale * (A[s][t] - delta * B[s][t]) * inv;
-            st_stream16(orow + ln.vi[s] * 16, Vec<T>::pack(o));
-            if (ln.vi[s] % ln.G == 0) st[ln.head[s]] = make_float2(m[s] + log2f(l[s]), delta);
-        }
+        for (int t = 0; t < VE; ++t) o[t] = p.scale * (A[t] - delta * B[t]) * inv;
+        st_stream16(static_cast<char *>(p.dq) + row * rb + (int64_t)(g * 32 + ln.lane) * 16,
+                    Vec<T>::pack(o));
+        if (ln.lane % ln.G == 0)
+            p.stats[row * p.H + g * (p.H / p.hgroups) + ln.head[0]] =
+                make_float2(m + log2f(l), delta);
     }
 
-    // a chunk of a heavy row: publish the state; the last chunk to arrive
-    // merges the row's chunk states in chunk order and finishes the row
+    // A chunk of a heavy row: publish the group's state; the warp that
+    // completes the row's last (chunk, group) pair merges every group of the
+    // row over its chunks in chunk order and finishes the row.
     __device__ __forceinline__ void chunk_epilogue(const BwdParams &p, const L &ln, int64_t row,
-                                                   int hr, int64_t chunk) {
-        const int HD = p.H * p.Dh;
-        float *slot = p.partials + chunk * p.slot_floats;
+                                                   int hr, int64_t chunk, int g) {
+        constexpr int HDL = 32 * VE;  // elements of a group
+        const int HL = p.H / p.hgroups;
+        float *slot = p.partials + (chunk * p.hgroups + g) * p.slot_floats;
 #pragma unroll
-        for (int s = 0; s < V; ++s) {
-#pragma unroll
-            for (int t = 0; t < VE; t += 4) {
-                __stcg(reinterpret_cast<float4 *>(slot + ln.vi[s] * VE + t),
-                       make_float4(A[s][t], A[s][t + 1], A[s][t + 2], A[s][t + 3]));
-                __stcg(reinterpret_cast<float4 *>(slot + HD + ln.vi[s] * VE + t),
-                       make_float4(B[s][t], B[s][t + 1], B[s][t + 2], B[s][t + 3]));
-            }
-            if (ln.vi[s] % ln.G == 0) {
-                __stcg(slot + 2 * HD + ln.head[s], m[s]);
-                __stcg(slot + 2 * HD + p.H + ln.head[s], l[s]);
-                __stcg(slot + 2 * HD + 2 * p.H + ln.head[s], S[s]);
-            }
+        for (int t = 0; t < VE; t += 4) {
+            __stcg(reinterpret_cast<float4 *>(slot + ln.lane * VE + t),
+                   make_float4(A[t], A[t + 1], A[t + 2], A[t + 3]));
+            __stcg(reinterpret_cast<float4 *>(slot + HDL + ln.lane * VE + t),
+                   make_float4(B[t], B[t + 1], B[t + 2], B[t + 3]));
+        }
+        if (ln.lane % ln.G == 0) {
+            __stcg(slot + 2 * HDL + ln.head[0], m);
+            __stcg(slot + 2 * HDL + HL + ln.head[0], l);
+            __stcg(slot + 2 * HDL + 2 * HL + ln.head[0], S);
         }
         __threadfence();
         __syncwarp();
@@ -243,72 +239,84 @@ struct BwdRow {
         if (ln.lane == 0) old = atomicAdd(p.counters + hr, 1);
         old = __shfl_sync(kFull, old, 0);
         const int c0 = __ldg(p.chunk_start + hr), c1 = __ldg(p.chunk_start + hr + 1);
-        if (old != c1 - c0 - 1) return;  // not the row's last chunk
+        if (old != (c1 - c0) * p.hgroups - 1) return;  // not the row's last piece
         __threadfence();
-#pragma unroll
-        for (int s = 0; s < V; ++s) {
+        for (int g2 = 0; g2 < p.hgroups; ++g2) {
             float mx = -INFINITY;
             for (int c = c0; c < c1; ++c)
-                mx = fmaxf(mx, __ldcg(p.partials + (int64_t)c * p.slot_floats + 2 * HD + ln.head[s]));
+                mx = fmaxf(mx, __ldcg(p.partials + ((int64_t)c * p.hgroups + g2) * p.slot_floats +
+                                      2 * HDL + ln.head[0]));
             float ls = 0.f, ss = 0.f;
 #pragma unroll
-            for (int t = 0; t < VE; ++t) A[s][t] = B[s][t] = 0.f;
+            for (int t = 0; t < VE; ++t) A[t] = B[t] = 0.f;
             for (int c = c0; c < c1; ++c) {
-                const float *sl = p.partials + (int64_t)c * p.slot_floats;
-                const float mc = __ldcg(sl + 2 * HD + ln.head[s]);
+                const float *sl = p.partials + ((int64_t)c * p.hgroups + g2) * p.slot_floats;
+                const float mc = __ldcg(sl + 2 * HDL + ln.head[0]);
                 if (mc == -INFINITY) continue;
                 const float w = bexp2(mc - mx);
-                ls += w * __ldcg(sl + 2 * HD + p.H + ln.head[s]);
-                ss += w * __ldcg(sl + 2 * HD + 2 * p.H + ln.head[s]);
+                ls += w * __ldcg(sl + 2 * HDL + HL + ln.head[0]);
+                ss += w * __ldcg(sl + 2 * HDL + 2 * HL + ln.head[0]);
 #pragma unroll
                 for (int t = 0; t < VE; t += 4) {
-                    const float4 fa = ld_cg_f4(sl + ln.vi[s] * VE + t);
-                    const float4 fb = ld_cg_f4(sl + HD + ln.vi[s] * VE + t);
-                    A[s][t] += w * fa.x;
-                    A[s][t + 1] += w * fa.y;
-                    A[s][t + 2] += w * fa.z;
-                    A[s][t + 3] += w * fa.w;
-                    B[s][t] += w * fb.x;
-                    B[s][t + 1] += w * fb.y;
-                    B[s][t + 2] += w * fb.z;
-                    B[s][t + 3] += w * fb.w;
+                    const float4 fa = ld_cg_f4(sl + ln.lane * VE + t);
+                    const float4 fb = ld_cg_f4(sl + HDL + ln.lane * VE + t);
+                    A[t] += w * fa.x;
+                    A[t + 1] += w * fa.y;
+                    A[t + 2] += w * fa.z;
+                    A[t + 3] += w * fa.w;
+                    B[t] += w * fb.x;
+                    B[t + 1] += w * fb.y;
+                    B[t + 2] += w * fb.z;
+                    B[t + 3] += w * fb.w;
                 }
             }
-            m[s] = mx;
-            l[s] = ls;
-            S[s] = ss;
+            m = mx;
+            l = ls;
+            S = ss;
+            finish(p, ln, row, g2);
         }
-        finish(p, ln, row);
         if (ln.lane == 0) p.counters[hr] = 0;  // ready for the next call
     }
 };
 
-// Persistent: warp w takes items w, w + W, ...: the chunks of heavy rows
-// (plan order), then every row (heavy ones skipped: their chunks did them).
-template <typename T, int V, int U>
-__global__ void __launch_bounds__(kBwdThreads, V == 4 ? 2 : 4)
+// Persistent: warp w takes items w, w + W, ...: (chunk, group) pairs of the
+// heavy rows (plan order), then (row, group) pairs of every row (heavy rows
+// skipped: their chunks did them). The groups of one row go to adjacent warps.
+template <typename T, int U>
+__global__ void __launch_bounds__(kBwdThreads, 8)
 bwd_rows_kernel(const BwdParams p) {
-    using L = Lanes<T, V, 32>;
+    using L = Lanes<T, 1, 32>;
     const L ln(p.Dh);
-    BwdRow<T, V, U> st;
+    BwdRow<T, U> st;
     const int64_t wpb = blockDim.x >> 5;
     const int64_t n_warps = (int64_t)gridDim.x * wpb;
-    const int64_t n_items = p.n_chunks + p.n_rows;
+    const int64_t n_items = (p.n_chunks + p.n_rows) * p.hgroups;
     for (int64_t item = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5); item < n_items;
          item += n_warps) {
-        if (item < p.n_chunks) {
-            const int4 d = __ldg(p.chunk_desc + item);
-            st.begin(p, ln, d.x);
-            st.run(p, ln, d.y, d.z);
-            st.chunk_epilogue(p, ln, d.x, d.w, item);
+        const int64_t it = item / p.hgroups;
+        const int g = (int)(item - it * p.hgroups);
+        int64_t row;
+        int e0, e1, hr = -1;
+        if (it < p.n_chunks) {
+            const int4 d = __ldg(p.chunk_desc + it);
+            row = d.x;
+            e0 = d.y;
+            e1 = d.z;
+            hr = d.w;
         } else {
-            const int64_t row = item - p.n_chunks;
-            const int e0 = __ldg(p.row_ptr + row), e1 = __ldg(p.row_ptr + row + 1);
+            row = it - p.n_chunks;
+            e0 = __ldg(p.row_ptr + row);
+            e1 = __ldg(p.row_ptr + row + 1);
             if (e1 - e0 > p.row_threshold) continue;
-            st.begin(p, ln, row);
-            st.run(p, ln, e0, e1);
-            st.finish(p, ln, row);
         }
+        uint4 qr, gr;
+        BwdRow<T, U>::load_qg(p, ln, row, g, qr, gr);
+        st.begin(p, qr, gr);
+        st.run(p, ln, e0, e1, g);
+        if (hr >= 0)
+            st.chunk_epilogue(p, ln, row, hr, it, g);
+        else
+            st.finish(p, ln, row, g);
     }
 }
 
@@ -580,11 +588,12 @@ static gat_status_t launch_grid(K kern, int64_t items, int threads, int smem, co
 
 template <typename T, int V>
 static gat_status_t launch_bwd_fast(const BwdParams &p, cudaStream_t s) {
-    constexpr int UA = V == 4 ? 1 : (V == 2 ? 2 : 4);  // edges in flight, pass A
+    constexpr int UA = 2;                              // edges in flight, pass A
     constexpr int UB = V == 4 ? 1 : (V == 2 ? 3 : 4);  // pass B
     constexpr int VE = 16 / (int)sizeof(T);
     const int wpb = kBwdThreads / 32;
-    gat_status_t st = launch_grid(bwd_rows_kernel<T, V, UA>, (p.n_chunks + p.n_rows + wpb - 1) / wpb,
+    gat_status_t st = launch_grid(bwd_rows_kernel<T, UA>,
+                                  ((p.n_chunks + p.n_rows) * p.hgroups + wpb - 1) / wpb,
                                   kBwdThreads, 0, p, s, "backward rows");
     if (st != GAT_OK) return st;
     st = launch_grid(bwd_src_kernel<T, V, UB>, (p.n_src + wpb - 1) / wpb, kBwdThreads, 0, p, s,
@@ -617,7 +626,6 @@ static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 // plan of heavy rows on the vector path) one chunk state per chunk.
 struct BwdLayout {
     size_t ws_off, st_off, part_off, total;
-    int64_t slot_floats;
 };
 
 static BwdLayout bwd_layout(int64_t n_rows, int64_t n_edges, int32_t H, int32_t Dh,
@@ -626,8 +634,11 @@ static BwdLayout bwd_layout(int64_t n_rows, int64_t n_edges, int32_t H, int32_t 
     L.ws_off = 0;
     L.st_off = round256((size_t)n_edges * (size_t)H * sizeof(float2));
     L.part_off = L.st_off + round256((size_t)n_rows * 2 * (size_t)H * sizeof(float));
-    L.slot_floats = ((2 * (int64_t)H * Dh + 3 * (int64_t)H) + 3) & ~(int64_t)3;
-    L.total = L.part_off + round256((size_t)n_chunks * (size_t)L.slot_floats * sizeof(float));
+    // head groups of 32 vectors: at most H*Dh/128 of them (fp32), each state
+    // 2*(elements) + 3*(heads) floats rounded up to a multiple of 4
+    const int64_t hg_max = ((int64_t)H * Dh + 127) / 128;
+    const int64_t per_chunk = 2 * (int64_t)H * Dh + 3 * (int64_t)H + 3 * hg_max;
+    L.total = L.part_off + round256((size_t)n_chunks * (size_t)per_chunk * sizeof(float));
     return L;
 }
 
@@ -691,6 +702,7 @@ extern "C" gat_status_t gat_fused_layer_backward(
     p.n_src = n_src;
     p.H = H;
     p.Dh = Dh;
+    p.hgroups = 1;
     p.scale = scale;
     p.qscale = scale * kLog2eB;
     char *wsb = static_cast<char *>(workspace);
@@ -707,6 +719,7 @@ extern "C" gat_status_t gat_fused_layer_backward(
                         (n_src == 0 || (aligned16(dk) && aligned16(dv)));
     int V, LE;
     if (vec_ok && engine_shape(H, Dh, eb, V, LE) && LE == 32) {
+        p.hgroups = V;
         if (plan && plan->n_chunks > 0) {
             p.row_threshold = plan->heavy_threshold;
             p.n_chunks = plan->n_chunks;
@@ -714,7 +727,8 @@ extern "C" gat_status_t gat_fused_layer_backward(
             p.chunk_start = plan->chunk_start;
             p.counters = plan->counters;
             p.partials = reinterpret_cast<float *>(wsb + lay.part_off);
-            p.slot_floats = lay.slot_floats;
+            const int64_t hl = H / V, hdl = (int64_t)H * Dh / V;
+            p.slot_floats = (2 * hdl + 3 * hl + 3) & ~(int64_t)3;
         }
         if (transpose->src_plan && transpose->src_plan->n_heavy > 0) {
             p.src_threshold = transpose->src_plan->heavy_threshold;
