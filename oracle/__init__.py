@@ -66,7 +66,13 @@ def _load():
         lib.oracle_fused_backward.argtypes = [P, P, I64, I64, I32, I32, D, P, P, P, P,
                                               ctypes.c_int, P, P, P, P, P, P]
         lib.oracle_transpose.argtypes = [P, P, I64, I64, P, P, P]
-        for f in ("oracle_edge_softmax", "oracle_spmm_weighted", "oracle_sddmm",
+        lib.oracle_fp8_decode.argtypes = [P, I64, P]
+        lib.oracle_fp8_encode.argtypes = [P, I64, P]
+        lib.oracle_fp8_quantize.argtypes = [P, ctypes.c_int, I64, I32, I32, P, P]
+        lib.oracle_fused_layer_fp8.argtypes = [P, P, I64, I32, I32, D, P, ctypes.c_int, P, P, P,
+                                               P, P, I64, P, P]
+        for f in ("oracle_fp8_decode", "oracle_fp8_encode", "oracle_fp8_quantize",
+                  "oracle_fused_layer_fp8","oracle_edge_softmax", "oracle_spmm_weighted", "oracle_sddmm",
                   "oracle_fused_layer", "oracle_dense_block", "oracle_plan",
                   "oracle_fused_backward", "oracle_transpose"):
             getattr(lib, f).restype = ctypes.c_int
@@ -206,6 +212,52 @@ def transpose(row_ptr, col_idx, n_src):
     _check(_load().oracle_transpose(_p(rp), _p(ci), n, int(n_src), _p(sp), _p(perm), _p(dst)),
            "oracle_transpose")
     return sp, perm, dst
+
+
+def fp8_decode(codes):
+    """E4M3 codes (uint8) -> fp64 values."""
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _check(_load().oracle_fp8_decode(_p(c), c.size, _p(out)), "oracle_fp8_decode")
+    return out
+
+
+def fp8_encode(x):
+    """fp32 values -> nearest E4M3 codes (ties to even, saturating at 448)."""
+    a = _c(x, np.float32)
+    out = np.empty(a.shape, dtype=np.uint8)
+    _check(_load().oracle_fp8_encode(_p(a), a.size, _p(out)), "oracle_fp8_encode")
+    return out
+
+
+def fp8_quantize(x, H, Dh):
+    """Per (row, head) scaled E4M3 quantisation: (codes uint8 [n,H,Dh],
+    scales fp32 [n,H])."""
+    a, dt = _feat(x)
+    n = a.size // (H * Dh)
+    codes = np.empty((n, H, Dh), dtype=np.uint8)
+    scales = np.empty((n, H), dtype=np.float32)
+    _check(_load().oracle_fp8_quantize(_p(a), dt, n, H, Dh, _p(codes), _p(scales)),
+           "oracle_fp8_quantize")
+    return codes, scales
+
+
+def fused_layer_fp8(row_ptr, col_idx, q, k8, ks, v8, vs, H, Dh, scale, rows=None,
+                    want_cond=False):
+    """Fused layer with E4M3 k/v tables and per (node, head) scales. fp64."""
+    rp, ci = _c(row_ptr, np.int32), _c(col_idx, np.int32)
+    qa, dt = _feat(q)
+    k8c, v8c = _c(k8, np.uint8), _c(v8, np.uint8)
+    ksc, vsc = _c(ks, np.float32), _c(vs, np.float32)
+    sel = None if rows is None else _c(rows, np.int64)
+    n = rp.size - 1
+    n_sel = n if sel is None else sel.size
+    out = np.empty((n_sel, H, Dh), dtype=np.float64)
+    cond = np.empty_like(out) if want_cond else None
+    _check(_load().oracle_fused_layer_fp8(_p(rp), _p(ci), n, H, Dh, float(scale), _p(qa), dt,
+                                          _p(k8c), _p(ksc), _p(v8c), _p(vsc), _p(sel), n_sel,
+                                          _p(out), _p(cond)), "oracle_fused_layer_fp8")
+    return (out, cond) if want_cond else out
 
 
 def plan(row_ptr, heavy_threshold, chunk):

@@ -399,6 +399,185 @@ int oracle_transpose(const int32_t *row_ptr, const int32_t *col_idx, int64_t n_r
 }
 
 /*
+ * FP8 E4M3 feature tables (an extension of the fused layer's bf16 tables:
+ * the k and v gathers are most of its bytes). E4M3 as defined by the OCP
+ * 8-bit floating point format: 1 sign bit, 4 exponent bits (bias 7), 3
+ * mantissa bits; exponent field 0 encodes subnormals m/8 * 2^-6; field 15
+ * with mantissa 7 is NaN; there are no infinities; the largest finite
+ * magnitude is 1.75 * 2^8 = 448.
+ */
+static double e4m3_decode(uint8_t c)
+{
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* nearest E4M3 value, ties to the even mantissa; magnitudes that round past
+ * 448 saturate to 448; NaN stays NaN */
+static uint8_t e4m3_encode(double y)
+{
+    if (y != y)
+        return 0x7F;
+    uint8_t sign = signbit(y) ? 0x80 : 0;
+    double a = fabs(y);
+    /* units of the grid at this magnitude: 2^-9 below 2^-6 (subnormals) */
+    int e = 0;
+    if (a >= ldexp(1.0, -6)) {
+        frexp(a, &e);
+        e -= 1; /* a in [2^e, 2^(e+1)) */
+    } else {
+        e = -6;
+    }
+    double ulp = ldexp(1.0, e - 3);
+    double q = a / ulp; /* exact: a power-of-two scaling */
+    double fl = floor(q);
+    double r = q - fl;
+    double n = fl;
+    if (r > 0.5 || (r == 0.5 && fmod(fl, 2.0) != 0.0))
+        n = fl + 1.0;
+    double v = n * ulp;
+    if (v > 448.0)
+        v = 448.0;
+    /* re-express v: normal if v >= 2^-6 */
+    uint8_t code;
+    if (v < ldexp(1.0, -6)) {
+        code = (uint8_t)(v / ldexp(1.0, -9));
+    } else {
+        int ev;
+        double mant = frexp(v, &ev); /* v = mant * 2^ev, mant in [0.5, 1) */
+        int E = ev - 1 + 7;
+        int M = (int)((mant * 2.0 - 1.0) * 8.0);
+        code = (uint8_t)((E << 3) | M);
+    }
+    return sign | code;
+}
+
+int oracle_fp8_decode(const uint8_t *codes, int64_t n, double *out)
+{
+    if ((!codes || !out) && n > 0)
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e4m3_decode(codes[i]);
+    return 0;
+}
+
+int oracle_fp8_encode(const float *x, int64_t n, uint8_t *codes)
+{
+    if ((!x || !codes) && n > 0)
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        codes[i] = e4m3_encode((double)x[i]);
+    return 0;
+}
+
+/*
+ * Per (row, head) scaled E4M3 quantisation of x [n,H,Dh]: scale = amax / 448
+ * (fp32 division; 1 when the head's elements are all zero), code =
+ * E4M3(x / scale) with the division in fp32, as the decision is taken in
+ * the quantiser's own precision. scales is [n,H] fp32.
+ */
+int oracle_fp8_quantize(const void *x, int dtype, int64_t n, int32_t H, int32_t Dh,
+                        uint8_t *codes, float *scales)
+{
+    if (n < 0 || H < 1 || Dh < 1 || ((!x || !codes || !scales) && n > 0))
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        for (int32_t h = 0; h < H; ++h) {
+            const int64_t o = (i * H + h) * (int64_t)Dh;
+            float amax = 0.0f;
+            for (int32_t d = 0; d < Dh; ++d) {
+                float v = (float)fabs(elem(x, dtype, o + d));
+                if (v > amax)
+                    amax = v;
+            }
+            volatile float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+            scales[i * H + h] = sc;
+            for (int32_t d = 0; d < Dh; ++d) {
+                volatile float y = (float)elem(x, dtype, o + d) / sc;
+                codes[o + d] = e4m3_encode((double)y);
+            }
+        }
+    return 0;
+}
+
+/*
+ * The fused layer (oracle_fused_layer's definition, two-pass softmax) with
+ * k and v given as E4M3 codes and per (node, head) scales:
+ * k[j,h,d] = decode(k8[j,h,d]) * ks[j,h], likewise v. q in `dtype`.
+ */
+int oracle_fused_layer_fp8(const int32_t *row_ptr, const int32_t *col_idx, int64_t n_rows,
+                           int32_t H, int32_t Dh, double scale, const void *q, int dtype,
+                           const uint8_t *k8, const float *ks, const uint8_t *v8,
+                           const float *vs, const int64_t *rows, int64_t n_sel, double *out,
+                           double *cond)
+{
+    if (!row_ptr || n_rows < 0 || H < 1 || Dh < 1 || !out)
+        return -1;
+    if (!rows)
+        n_sel = n_rows;
+    const int64_t HD = (int64_t)H * Dh;
+    int64_t dm = max_degree(row_ptr, n_rows);
+    double *s = (double *)malloc((size_t)(dm > 0 ? dm : 1) * sizeof(double));
+    if (!s)
+        return -2;
+    for (int64_t t = 0; t < n_sel; ++t) {
+        int64_t i = rows ? rows[t] : t;
+        if (i < 0 || i >= n_rows) {
+            free(s);
+            return -1;
+        }
+        int64_t e0 = row_ptr[i], e1 = row_ptr[i + 1];
+        for (int32_t h = 0; h < H; ++h) {
+            double *o = out + t * HD + (int64_t)h * Dh;
+            double *c = cond ? cond + t * HD + (int64_t)h * Dh : NULL;
+            for (int32_t d = 0; d < Dh; ++d) {
+                o[d] = 0.0;
+                if (c)
+                    c[d] = 0.0;
+            }
+            if (e1 == e0)
+                continue;
+            for (int64_t e = e0; e < e1; ++e) {
+                int64_t src = col_idx[e];
+                double acc = 0.0;
+                for (int32_t d = 0; d < Dh; ++d)
+                    acc += elem(q, dtype, i * HD + (int64_t)h * Dh + d) *
+                           (e4m3_decode(k8[src * HD + (int64_t)h * Dh + d]) *
+                            (double)ks[src * H + h]);
+                s[e - e0] = scale * acc;
+            }
+            double m = -INFINITY;
+            for (int64_t e = e0; e < e1; ++e)
+                if (s[e - e0] > m)
+                    m = s[e - e0];
+            double Z = 0.0;
+            for (int64_t e = e0; e < e1; ++e)
+                Z += exp(s[e - e0] - m);
+            for (int64_t e = e0; e < e1; ++e) {
+                int64_t src = col_idx[e];
+                double w = exp(s[e - e0] - m) / Z;
+                for (int32_t d = 0; d < Dh; ++d) {
+                    double val = e4m3_decode(v8[src * HD + (int64_t)h * Dh + d]) *
+                                 (double)vs[src * H + h];
+                    o[d] += w * val;
+                    if (c)
+                        c[d] += w * fabs(val);
+                }
+            }
+        }
+    }
+    free(s);
+    return 0;
+}
+
+/*
  * Dense-masked small-graph attention block [P4, reference model]. Per graph b
  * (nodes x[N,D], pair feats [N,N,P], mask [N,N]), with head h owning feature
  * dims [h*dh, (h+1)*dh), dh = D/H:

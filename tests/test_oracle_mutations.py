@@ -52,6 +52,14 @@ MUTATIONS = [
     ("backward dq scale dropped", "dq[qi + d] += scale * ds * kv;", "dq[qi + d] += ds * kv;"),
     ("transpose counts shifted", "src_ptr[col_idx[e] + 1] += 1;", "src_ptr[col_idx[e]] += 1;"),
     ("transpose records the source as the row", "dst[k] = (int32_t)i;", "dst[k] = col_idx[e];"),
+    ("e4m3 exponent bias", "v = ldexp(1.0 + (double)m / 8.0, e - 7);",
+     "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    ("e4m3 subnormal scale", "v = ldexp((double)m / 8.0, -6);", "v = ldexp((double)m / 8.0, -7);"),
+    ("e4m3 ties away from zero", "if (r > 0.5 || (r == 0.5 && fmod(fl, 2.0) != 0.0))",
+     "if (r >= 0.5)"),
+    ("fp8 quantiser range", "volatile float sc = amax > 0.0f ? amax / 448.0f : 1.0f;",
+     "volatile float sc = amax > 0.0f ? amax / 240.0f : 1.0f;"),
+    ("fp8 fused layer v scaled by k's scale", "(double)vs[src * H + h];", "(double)ks[src * H + h];"),
     ("backward da against k", "dd += elem(dout, dtype, qi + d) * elem(v, dtype, kj + d);",
      "dd += elem(dout, dtype, qi + d) * elem(k, dtype, kj + d);"),
 ]

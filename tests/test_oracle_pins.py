@@ -436,6 +436,88 @@ def test_transpose_equals_stable_library_argsort(n, n_src, max_deg):
 
 
 # ----------------------------------------------------------------------------
+# O7 fp8 (E4M3) feature tables: codec against PyTorch's float8_e4m3fn,
+# quantiser invariants, the fp8 fused layer against the fused layer
+# ----------------------------------------------------------------------------
+def test_fp8_decode_all_codes_equal_library():
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.fp8_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert (np.isnan(got) == nan).all() and nan.sum() == 2  # 0x7F and 0xFF
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+
+
+def test_fp8_encode_equals_library_rounding_and_saturates():
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    vals = oracle.fp8_decode(codes)
+    fin = np.isfinite(vals)
+    grid = np.unique(vals[fin])
+    mids = (grid[1:] + grid[:-1]) / 2  # exact ties: nearest-even decides
+    rng = np.random.default_rng(66)
+    x = np.concatenate([grid, mids, np.nextafter(mids, np.inf), np.nextafter(mids, -np.inf),
+                        rng.standard_normal(20000) * 60, rng.standard_normal(2000) * 0.01])
+    x = x[np.abs(x) <= 448].astype(np.float32)
+    got = oracle.fp8_encode(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(got, ref)
+    # every finite code is its own value's encoding
+    np.testing.assert_array_equal(oracle.fp8_encode(vals[fin].astype(np.float32)), codes[fin])
+    # beyond the largest finite value: saturation
+    big = np.array([449, 464, 480, 1e4, 3e38, -500], np.float32)
+    np.testing.assert_array_equal(oracle.fp8_encode(big), [0x7E] * 5 + [0xFE])
+
+
+def test_fp8_quantize_invariants():
+    rng = np.random.default_rng(67)
+    n, H, Dh = 50, 4, 16
+    x = (rng.standard_normal((n, H, Dh)) * rng.uniform(0.01, 100, (n, H, 1))).astype(np.float32)
+    x[3, 1] = 0.0  # an all-zero head
+    codes, scales = oracle.fp8_quantize(x, H, Dh)
+    assert scales[3, 1] == 1.0 and (codes[3, 1] == 0).all()
+    amax = np.abs(x).max(-1)
+    nz = amax > 0
+    np.testing.assert_array_equal(scales[nz], (amax[nz] / np.float32(448)).astype(np.float32))
+    # the largest element of each head lands on +-448
+    arg = np.abs(x).argmax(-1)
+    top = np.take_along_axis(codes, arg[..., None], -1)[..., 0]
+    assert np.isin(top[nz], [0x7E, 0xFE]).all()
+    # dequantised values within half a grid step (1/16 relative for normals)
+    deq = oracle.fp8_decode(codes) * scales[..., None]
+    err = np.abs(deq - x)
+    tol = np.maximum(np.abs(x) / 16, scales[..., None] * 2.0 ** -10)
+    assert (err <= tol * (1 + 1e-6)).all()
+    # bf16 inputs widen exactly
+    bits = W.bf16_bits_from_f32(x)
+    c2, s2 = oracle.fp8_quantize(bits, H, Dh)
+    c3, s3 = oracle.fp8_quantize(W.f32_from_bf16_bits(bits), H, Dh)
+    np.testing.assert_array_equal(c2, c3)
+    np.testing.assert_array_equal(s2, s3)
+
+
+def test_fused_fp8_equals_fused_layer_on_dequantised_tables():
+    rng = np.random.default_rng(68)
+    n, H, Dh = 40, 2, 16
+    rp, ci = tiny_graph(rng, n, n, 9, allow_dup=True, sort=False)
+    q = rng.standard_normal((n, H, Dh)).astype(np.float32)
+    k8 = rng.integers(0, 256, (n, H, Dh), dtype=np.uint8)
+    v8 = rng.integers(0, 256, (n, H, Dh), dtype=np.uint8)
+    for c in (k8, v8):
+        c[(c & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    # power-of-two scales: decode * scale is exact in fp32
+    ks = (2.0 ** rng.integers(-8, -2, (n, H))).astype(np.float32)
+    vs = (2.0 ** rng.integers(-4, 0, (n, H))).astype(np.float32)
+    kf = (oracle.fp8_decode(k8) * ks[..., None]).astype(np.float32)
+    vf = (oracle.fp8_decode(v8) * vs[..., None]).astype(np.float32)
+    got = oracle.fused_layer_fp8(rp, ci, q, k8, ks, v8, vs, H, Dh, 0.25)
+    ref = oracle.fused_layer(rp, ci, q, kf, vf, H, Dh, 0.25)
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------
 # O5 dense-masked block: PyTorch CPU float64 modules
 # ----------------------------------------------------------------------------
 def torch_block(w, graphs):
