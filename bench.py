@@ -8,7 +8,7 @@ layer and call on it; its build time is reported as plan_ms).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                     [--workload fused|edge_softmax|aggregate|sddmm|dense|spmm_heads|
-                               edge_softmax_h8|fused_backward]
+                               edge_softmax_h8|fused_backward|fused_fp8]
 
 Prints one JSON line (rank 0). value = edge-heads/s over all ranks (each rank
 runs its own full, independent problem: weak scaling, no collective on the
@@ -455,6 +455,37 @@ def bench_small(name, args):
                      + g["n_rows"] * (4 + 3 * rb + 8 * g["H"]) + g["n_src"] * (4 + 2 * rb))
         flops = 2.0 * g["n_edges"] * g["H"] * g["Dh"] * 6
         extra = {"transpose_build_ms": transpose_ms, "transpose": tr.info()}
+    elif name == "fused_fp8":
+        # the fused workload (1e6 rows, Zipf, H=8, Dh=64) with k/v quantised to
+        # E4M3 + per (node, head) scales on the device; q/out bf16
+        g = W.make_fused(seed=3, n=args.n_rows)
+        bt = lambda a: t(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+        rp, ci = t(g["row_ptr"]), t(g["col_idx"])
+        q, k, v = (bt(g[x]) for x in ("q", "k", "v"))
+        plan = gat.Plan(rp)
+        k8, ks = torch.empty(k.shape, dtype=torch.uint8, device=dev), \
+            torch.empty(k.shape[:2], dtype=torch.float32, device=dev)
+        v8, vs = torch.empty_like(k8), torch.empty_like(ks)
+        qa, qb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(2):  # warm, then timed: both tables
+            qa.record()
+            gat.gat_quantize_fp8(k, k8, ks)
+            gat.gat_quantize_fp8(v, v8, vs)
+            qb.record()
+        torch.cuda.synchronize()
+        out = torch.empty_like(q)
+        ws = torch.empty(max(1, gat.gat_fused_layer_workspace_size(plan, g["H"], g["Dh"])),
+                         dtype=torch.uint8, device=dev)
+        fn = lambda: gat.gat_fused_layer_fp8(rp, ci, q, k8, ks, v8, vs, g["scale"],  # noqa: E731
+                                             out=out, plan=plan, workspace=ws)
+        units, launches = g["n_edges"] * g["H"], 1
+        hd = g["H"] * g["Dh"]
+        # per row: row_ptr, q and out rows (bf16); per edge: col_idx, the k8 and
+        # v8 rows (1 B per element) and their 2H scales
+        alg_bytes = g["n_rows"] * (4 + 4 * hd) + g["n_edges"] * (4 + 2 * hd + 8 * g["H"])
+        extra = {"quantize_ms_both_tables": qa.elapsed_time(qb),
+                 "bytes_vs_bf16_layer": alg_bytes / fused_bytes(g["n_rows"], g["n_edges"],
+                                                                 g["H"], g["Dh"])}
     elif name == "edge_softmax_h8":
         # 8 heads on the 1e6-row power-law graph
         deg = W.zipf_degrees(np.random.default_rng(3), 1_000_000)
@@ -553,7 +584,7 @@ def main():
     ap.add_argument("--impl", default="gat", choices=["gat", "reference"])
     ap.add_argument("--workload", default="fused",
                     choices=["fused", "edge_softmax", "aggregate", "sddmm", "dense", "spmm_heads",
-                             "edge_softmax_h8", "fused_backward"])
+                             "edge_softmax_h8", "fused_backward", "fused_fp8"])
     ap.add_argument("--ref-rows", type=int, default=5000,
                     help="--impl reference: consecutive rows per step (~0.2 s of oracle work)")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
@@ -581,7 +612,7 @@ def main():
         if not args.no_extras:
             res["other_workloads"] = {}
             for nm in ("edge_softmax", "aggregate", "sddmm", "dense", "spmm_heads",
-                       "edge_softmax_h8", "fused_backward"):
+                       "edge_softmax_h8", "fused_backward", "fused_fp8"):
                 try:
                     res["other_workloads"][nm] = bench_small(nm, args)
                 except Exception as exc:  # keep the headline line if a side workload fails

@@ -214,6 +214,38 @@ gat_status_t gat_fused_layer(const int32_t *row_ptr, const int32_t *col_idx, int
                              void *stream);
 
 /* ------------------------------------------------------------------------
+ * fp8 feature tables. In gat_fused_layer the gathers of the k and v rows are
+ * nearly all of the bytes [softmax, sddmm and spmm pages, reference models:
+ * every edge reads its source's rows]; stored as E4M3 with one fp32 scale per
+ * (node, head), a bf16 row of H*Dh elements shrinks from 2*H*Dh to
+ * H*Dh + 4*H bytes.
+ *
+ * gat_quantize_fp8: x [n,H,Dh] (dtype) -> codes [n,H,Dh] (uint8, E4M3: 1 sign,
+ * 4 exponent bits with bias 7, 3 mantissa bits, largest finite 448) and
+ * scales [n,H] (fp32): scale = max_d |x[i,h,d]| / 448 (1 for an all-zero
+ * head), code = E4M3(x / scale) rounded to nearest even and saturating at
+ * +-448 (both divisions in fp32). Errors: GAT_ERR_INVALID_ARG, _UNSUPPORTED.
+ *
+ * gat_fused_layer_fp8: gat_fused_layer with
+ *     k[j,h,:] = E4M3(k8[j,h,:]) * k_scale[j,h],  v likewise,
+ * q and out [n_rows,H,Dh] in `dtype`, fp32 arithmetic. Same plan and
+ * workspace rules as gat_fused_layer (size from
+ * gat_fused_layer_workspace_size). The vector kernel takes H*Dh of 512 or
+ * 1024 with Dh a power-of-two multiple of 16 and 16-byte aligned pointers;
+ * other shapes (Dh <= 256) take a scalar kernel (no chunks, workspace
+ * unused). Errors: as gat_fused_layer; GAT_ERR_UNSUPPORTED for Dh > 256.
+ * ---------------------------------------------------------------------- */
+gat_status_t gat_quantize_fp8(const void *x, gat_dtype_t dtype, int64_t n, int32_t H, int32_t Dh,
+                              uint8_t *codes, float *scales, void *stream);
+
+gat_status_t gat_fused_layer_fp8(const int32_t *row_ptr, const int32_t *col_idx, int64_t n_rows,
+                                 int64_t n_src, int64_t n_edges, int32_t H, int32_t Dh,
+                                 float scale, const void *q, gat_dtype_t dtype, const uint8_t *k8,
+                                 const float *k_scale, const uint8_t *v8, const float *v_scale,
+                                 void *out, gat_plan_t plan, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * Transposed (source-major) view of a graph, for the backward pass
  * [sddmm page, discussion of the backward pass: an edge's gradients land on
  * the feature rows of its endpoints, and a row shared by several edges

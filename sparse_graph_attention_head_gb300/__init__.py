@@ -33,6 +33,7 @@ EXPORTS = (
     "gat_fused_layer_no_alloc",
     "gat_transpose_create", "gat_transpose_destroy", "gat_transpose_info", "gat_transpose_export",
     "gat_fused_layer_backward_workspace_size", "gat_fused_layer_backward",
+    "gat_quantize_fp8", "gat_fused_layer_fp8",
 )
 
 
@@ -78,6 +79,9 @@ def _load() -> ctypes.CDLL:
         "gat_transpose_info": ([P, P, P, P, P, P], ctypes.c_int),
         "gat_transpose_export": ([P, P, P, P, P], ctypes.c_int),
         "gat_fused_layer_backward_workspace_size": ([P, I64, I64, I32, I32, P], ctypes.c_int),
+        "gat_quantize_fp8": ([P, ctypes.c_int, I64, I32, I32, P, P, P], ctypes.c_int),
+        "gat_fused_layer_fp8": ([P, P, I64, I64, I64, I32, I32, F, P, ctypes.c_int, P, P, P, P, P,
+                                 P, P, SZ, P], ctypes.c_int),
         "gat_fused_layer_backward": ([P, P, I64, I64, I64, I32, I32, F, P, P, P, P, ctypes.c_int,
                                       P, P, P, P, P, P, SZ, P], ctypes.c_int),
     }
@@ -298,6 +302,39 @@ def gat_fused_layer_no_alloc(row_ptr, col_idx, q, k, v, scale, out, stream=None)
     _check("gat_fused_layer_no_alloc", _lib.gat_fused_layer_no_alloc(
         _ptr(row_ptr), _ptr(col_idx) if E else None, n_rows, k.shape[0], E, H, Dh, float(scale),
         _ptr(q), _ptr(k), _ptr(v), _dtype(q), _ptr(out), _stream(stream)))
+    return out
+
+
+def gat_quantize_fp8(x, codes=None, scales=None, stream=None):
+    """Per (node, head) scaled E4M3 quantisation of x [n,H,Dh]: returns
+    (codes uint8 [n,H,Dh], scales fp32 [n,H])."""
+    n, H, Dh = x.shape
+    codes = torch.empty((n, H, Dh), dtype=torch.uint8, device=x.device) if codes is None else codes
+    scales = torch.empty((n, H), dtype=torch.float32, device=x.device) if scales is None else scales
+    _check("gat_quantize_fp8", _lib.gat_quantize_fp8(
+        _ptr(x), _dtype(x), n, H, Dh, _ptr(codes), _ptr(scales), _stream(stream)))
+    return codes, scales
+
+
+def gat_fused_layer_fp8(row_ptr, col_idx, q, k8, k_scale, v8, v_scale, scale, out=None,
+                        plan=None, workspace=None, stream=None):
+    """gat_fused_layer with E4M3 k/v tables and per (node, head) scales."""
+    _idx(row_ptr, "row_ptr")
+    _idx(col_idx, "col_idx")
+    n_rows, H, Dh = q.shape
+    E = col_idx.numel()
+    if out is None:
+        out = torch.empty_like(q)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if plan is not None and workspace is None:
+        need = gat_fused_layer_workspace_size(plan, H, Dh)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            ws_bytes = need
+    _check("gat_fused_layer_fp8", _lib.gat_fused_layer_fp8(
+        _ptr(row_ptr), _ptr(col_idx) if E else None, n_rows, k8.shape[0], E, H, Dh, float(scale),
+        _ptr(q), _dtype(q), _ptr(k8), _ptr(k_scale), _ptr(v8), _ptr(v_scale), _ptr(out),
+        _plan_handle(plan), _ptr(workspace), ws_bytes, _stream(stream)))
     return out
 
 

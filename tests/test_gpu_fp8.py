@@ -1,0 +1,135 @@
+"""GPU parity of the fp8 (E4M3) feature-table path: the quantiser's codes
+and scales bit for bit against the oracle's (both divide in fp32 and round to
+the nearest E4M3 value), and the fp8 fused layer against the fp64 oracle on
+the same codes, element by element on graphs with heavy rows and on sampled
+rows of the 1e6-row power-law graph."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests.parity import assert_bf16, assert_fp32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gat():
+    import __graft_entry__
+    __graft_entry__.build()
+    import sparse_graph_attention_head_gb300 as g
+    return g
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda")
+
+
+def dev_feat(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return dev(a.view(np.int16)).view(torch.bfloat16)
+    return dev(a)
+
+
+def host(t):
+    torch.cuda.synchronize()
+    if t.dtype == torch.bfloat16:
+        return t.float().cpu().numpy().astype(np.float64)
+    return t.cpu().numpy()
+
+
+@pytest.mark.parametrize("H,Dh,dtype", [(8, 64, "bf16"), (8, 64, "f32"), (3, 20, "f32"),
+                                         (1, 7, "bf16"), (16, 128, "bf16")])
+def test_quantize_bit_exact(gat, H, Dh, dtype):
+    rng = np.random.default_rng(90 + H + Dh)
+    n = 700
+    x = (rng.standard_normal((n, H, Dh)) * 10.0 ** rng.uniform(-6, 4, (n, H, 1))).astype(np.float32)
+    x[5] = 0.0
+    x[6, 0, :] = -0.0
+    x[7, 0, 0] = 1e30
+    xin = W.bf16_bits_from_f32(x) if dtype == "bf16" else x
+    codes, scales = gat.gat_quantize_fp8(dev_feat(xin))
+    oc, osc = oracle.fp8_quantize(xin, H, Dh)
+    np.testing.assert_array_equal(host(scales), osc)
+    np.testing.assert_array_equal(host(codes), oc)
+
+
+def fp8_case(seed, n, H, Dh, dtype, deg, n_src=None):
+    rng = np.random.default_rng(seed)
+    n_src = n if n_src is None else n_src
+    rp, ci = W.make_csr(rng, deg, n_src, sort_within_rows=False)
+    f = lambda m: rng.standard_normal((m, H, Dh)).astype(np.float32)  # noqa: E731
+    q, k, v = f(n), f(n_src), f(n_src)
+    if dtype == "bf16":
+        q = W.bf16_bits_from_f32(q)
+    k8, ks = oracle.fp8_quantize(k, H, Dh)
+    v8, vs = oracle.fp8_quantize(v, H, Dh)
+    return rp, ci, q, k8, ks, v8, vs
+
+
+def check(gat, rp, ci, q, k8, ks, v8, vs, H, Dh, scale, plan_kw, name, rows=None):
+    rpd = dev(rp)
+    plan = gat.Plan(rpd, **plan_kw) if plan_kw is not None else None
+    out = gat.gat_fused_layer_fp8(rpd, dev(ci), dev_feat(q), dev(k8), dev(ks), dev(v8), dev(vs),
+                                  scale, plan=plan)
+    g = host(out).astype(np.float64)
+    o, c = oracle.fused_layer_fp8(rp, ci, q, k8, ks, v8, vs, H, Dh, scale, rows=rows,
+                                  want_cond=True)
+    if rows is not None:
+        g = g[rows]
+    if q.dtype == np.uint16:
+        return assert_bf16(g, o, c, name=name)
+    deg = np.maximum(np.diff(rp.astype(np.int64)), 1).astype(np.float64)
+    n = deg if rows is None else deg[rows]
+    return assert_fp32(g, o, c, n[:, None, None], name=name)
+
+
+@pytest.mark.parametrize("H,Dh,dtype", [(8, 64, "bf16"), (8, 64, "f32"), (16, 64, "bf16"),
+                                         (4, 256, "f32"), (4, 32, "bf16"), (3, 24, "f32"),
+                                         (2, 200, "bf16")])
+def test_fused_fp8_shapes(gat, H, Dh, dtype):
+    rng = np.random.default_rng(95 + H * Dh)
+    deg = np.concatenate([rng.integers(0, 40, 300), [0, 129, 700, 2000]])
+    rp, ci, q, k8, ks, v8, vs = fp8_case(96 + H, deg.size, H, Dh, dtype, deg, n_src=251)
+    for plan_kw in (None, {"heavy_threshold": 100, "chunk_edges": 96}):
+        check(gat, rp, ci, q, k8, ks, v8, vs, H, Dh, 1 / np.sqrt(Dh), plan_kw,
+              f"fp8 {H}x{Dh} {dtype} plan={plan_kw is not None}")
+
+
+def test_fused_fp8_power_law_100k(gat):
+    d = W.make_fused(seed=3, n=100_000)
+    k8, ks = oracle.fp8_quantize(d["k"], 8, 64)
+    v8, vs = oracle.fp8_quantize(d["v"], 8, 64)
+    check(gat, d["row_ptr"], d["col_idx"], d["q"], k8, ks, v8, vs, 8, 64, d["scale"], {},
+          "fp8 zipf 1e5")
+
+
+def test_fused_fp8_full_size_quantised_on_device(gat):
+    """The benchmark's configuration: the 1e6-row graph's bf16 k/v quantised by
+    gat_quantize_fp8 on the device; the codes are checked against the oracle's
+    on sampled node rows and the layer on sampled output rows."""
+    d = W.make_fused(seed=3, n=1_000_000)
+    rpd, cid = dev(d["row_ptr"]), dev(d["col_idx"])
+    k8, ks = gat.gat_quantize_fp8(dev_feat(d["k"]))
+    v8, vs = gat.gat_quantize_fp8(dev_feat(d["v"]))
+    out = gat.gat_fused_layer_fp8(rpd, cid, dev_feat(d["q"]), k8, ks, v8, vs, d["scale"],
+                                  plan=gat.Plan(rpd))
+    g = host(out).astype(np.float64)
+    rng = np.random.default_rng(13)
+    nodes = rng.integers(0, 1_000_000, 300)
+    ok8, oks = oracle.fp8_quantize(d["k"][nodes], 8, 64)
+    np.testing.assert_array_equal(host(k8)[nodes], ok8)
+    np.testing.assert_array_equal(host(ks)[nodes], oks)
+    hk8, hks, hv8, hvs = host(k8), host(ks), host(v8), host(vs)
+    deg = np.diff(d["row_ptr"])
+    rows = np.unique(np.concatenate([np.argsort(deg)[-6:], rng.integers(0, deg.size, 200)]))
+    o, c = oracle.fused_layer_fp8(d["row_ptr"], d["col_idx"], d["q"], hk8, hks, hv8, hvs, 8, 64,
+                                  d["scale"], rows=rows, want_cond=True)
+    assert_bf16(g[rows], o, c, name="fp8 1e6 sampled rows")
+    # quantisation error against the bf16 layer: a few percent of the
+    # output's scale (reported by the bench; bounded here against gross errors)
+    ob, cb = oracle.fused_layer(d["row_ptr"], d["col_idx"], d["q"], d["k"], d["v"], 8, 64,
+                                d["scale"], rows=rows, want_cond=True)
+    assert np.abs(g[rows] - ob).max() <= 0.25 * cb.max()
