@@ -10,7 +10,9 @@
 //
 //   gat_quantize_fp8: scale[n,h] = max_d |x[n,h,d]| / 448 (1 for an all-zero
 //     head), code = E4M3(x / scale), nearest-even, saturating (448 is the
-//     largest finite E4M3 magnitude); one warp per (node, head).
+//     largest finite E4M3 magnitude); one warp per node row with 16-byte
+//     loads when a head is a power-of-two number of vectors, else one warp
+//     per (node, head).
 //   gat_fused_layer_fp8: gat_fused_layer's lane layout with 16-byte vectors
 //     of 16 fp8 elements: lane l of a warp holds vectors l, l+32 (V per lane)
 //     of the row's H*Dh codes; a head is Dh/16 adjacent lanes. Per edge:
@@ -360,6 +362,57 @@ quantize_fp8_kernel(const T *__restrict__ x, int64_t n, int32_t H, int32_t Dh,
     }
 }
 
+// quantiser, vector form: one warp per node row; lane l takes 16-byte vectors
+// l, l+32, ... of the row; a head is G = Dh/VE adjacent lanes (G a power of
+// two), so its maximum is a G-lane shuffle; each vector's VE codes leave as
+// one VE-byte store.
+template <typename T>
+__global__ void __launch_bounds__(256)
+quantize_fp8_vec_kernel(const T *__restrict__ x, int64_t n, int32_t H, int32_t Dh,
+                        uint8_t *__restrict__ codes, float *__restrict__ scales) {
+    constexpr int VE = Vec<T>::N;
+    const int lane = threadIdx.x & 31;
+    const int G = Dh / VE;
+    const int nvec = H * G;  // vectors per row, a multiple of G
+    const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < n;
+         row += n_warps) {
+        const char *xr = reinterpret_cast<const char *>(x + row * (int64_t)H * Dh);
+        for (int j0 = 0; j0 < nvec; j0 += 32) {  // warp-uniform
+            const int j = j0 + lane;
+            float f[VE];
+            if (j < nvec) {
+                Vec<T>::unpack(ld_stream16(xr + (int64_t)j * 16), f);
+            } else {
+#pragma unroll
+                for (int t = 0; t < VE; ++t) f[t] = 0.f;
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int t = 0; t < VE; ++t) amax = fmaxf(amax, fabsf(f[t]));
+            for (int o = 1; o < G; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+            if (j >= nvec) continue;
+            const float sc = amax > 0.f ? amax / 448.f : 1.f;  // IEEE division
+            if (j % G == 0) scales[row * H + j / G] = sc;
+            uint32_t w[VE / 4];
+#pragma unroll
+            for (int t = 0; t < VE; t += 4) {
+                uint32_t b = 0;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    b |= (uint32_t)__nv_cvt_float_to_fp8(f[t + u] / sc, __NV_SATFINITE, __NV_E4M3)
+                         << (8 * u);
+                w[t / 4] = b;
+            }
+            uint8_t *cr = codes + row * (int64_t)H * Dh + (int64_t)j * VE;
+            if (VE == 8)
+                *reinterpret_cast<uint2 *>(cr) = make_uint2(w[0], w[VE / 4 - 1]);
+            else
+                *reinterpret_cast<uint32_t *>(cr) = w[0];
+        }
+    }
+}
+
 template <typename T, int V>
 static gat_status_t launch_fp8_fast(const Fp8Params &p, cudaStream_t s) {
     constexpr int U = V == 1 ? 4 : 2;
@@ -408,8 +461,22 @@ extern "C" gat_status_t gat_quantize_fp8(const void *x, gat_dtype_t dtype, int64
     if (n == 0) return GAT_OK;
     if (!x || !codes || !scales) return fail(GAT_ERR_INVALID_ARG, "gat_quantize_fp8: NULL pointer");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int64_t blocks = (n * H + 7) / 8;
     const int64_t cap = (int64_t)sm_count() * 8;
+    const int VE = dtype == GAT_F32 ? 4 : 8;
+    const int G = Dh / VE;
+    if (Dh % VE == 0 && G <= 32 && (G & (G - 1)) == 0 && aligned16(x) &&
+        (reinterpret_cast<uintptr_t>(codes) % VE) == 0) {
+        int64_t blocks = (n + 7) / 8;
+        if (blocks > cap) blocks = cap;
+        if (dtype == GAT_F32)
+            quantize_fp8_vec_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(
+                static_cast<const float *>(x), n, H, Dh, codes, scales);
+        else
+            quantize_fp8_vec_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
+                static_cast<const __nv_bfloat16 *>(x), n, H, Dh, codes, scales);
+        return check_launch("gat_quantize_fp8");
+    }
+    int64_t blocks = (n * H + 7) / 8;
     if (blocks > cap) blocks = cap;
     if (dtype == GAT_F32)
         quantize_fp8_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const float *>(x), n,
