@@ -420,9 +420,11 @@ def bench_small(name, args):
         rp, ci, w, feat = t(g["row_ptr"]), t(g["col_idx"]), t(g["w"]), t(g["feat"])
         out = torch.empty_like(feat)
         plan = gat.Plan(rp)
+        ws = torch.empty(max(1, gat.gat_spmm_weighted_workspace_size(plan, g["H"], g["Dh"])),
+                         dtype=torch.uint8, device=dev)
         fn = lambda: gat.gat_spmm_weighted(rp, ci, w, feat, g["H"], g["Dh"], out=out,  # noqa: E731
-                                           plan=plan)
-        units, launches = g["n_edges"] * g["H"], 2
+                                           plan=plan, workspace=ws)
+        units, launches = g["n_edges"] * g["H"], 1
         row = 4 * g["H"] * g["Dh"]
         # per row: row_ptr entry and output row; per edge: col_idx entry, H
         # weights and the gathered feature row

@@ -88,8 +88,10 @@ int32_t gat_version(void);
  *   light rows  deg <= heavy_threshold: one warp per row
  *   heavy rows  deg >  heavy_threshold: cut into chunks of chunk_edges edges;
  *               gat_fused_layer runs one warp per chunk and merges the chunks'
- *               softmax states; gat_edge_softmax and gat_spmm_weighted run one
- *               thread block per heavy row.
+ *               softmax states; gat_spmm_weighted does the same with
+ *               partial sums when given a workspace (else one thread block
+ *               per heavy row); gat_edge_softmax runs one thread block per
+ *               heavy row.
  * Plan arrays (device, int32):
  *   heavy_rows  [n_heavy]     ascending row ids with deg > heavy_threshold
  *   chunk_start [n_heavy + 1] exclusive prefix sum of ceil(deg / chunk_edges)
@@ -178,13 +180,24 @@ gat_status_t gat_edge_softmax(const int32_t *row_ptr, int64_t n_rows, int64_t n_
  * `dtype` (fp32 accumulation). Zero-degree rows are written as zeros.
  * The aggregate page's operation (softmax of per-edge scores, then this sum)
  * is gat_edge_softmax followed by gat_spmm_weighted with H = 1.
- * `plan` may be NULL or a plan of this graph.
- * Errors: GAT_ERR_INVALID_ARG, GAT_ERR_UNSUPPORTED, GAT_ERR_PLAN_MISMATCH.
+ * plan: NULL (every row by one warp) or a plan of this graph. With a plan,
+ * heavy rows are cut into chunks whose partial sums go to `workspace` (at
+ * least gat_spmm_weighted_workspace_size bytes, 16-byte aligned) and are
+ * added in chunk order by the chunk that finishes last, all in one launch;
+ * with workspace NULL each heavy row takes one thread block in a second
+ * launch instead. The plan's arrival counters are used in the first form
+ * (one plan must not serve two such calls whose work overlaps on the GPU).
+ * Errors: GAT_ERR_INVALID_ARG, GAT_ERR_UNSUPPORTED, GAT_ERR_PLAN_MISMATCH,
+ * GAT_ERR_WORKSPACE (a workspace given but too small or misaligned).
  * ---------------------------------------------------------------------- */
+gat_status_t gat_spmm_weighted_workspace_size(gat_plan_t plan, int32_t H, int32_t Dh,
+                                              size_t *bytes);
+
 gat_status_t gat_spmm_weighted(const int32_t *row_ptr, const int32_t *col_idx, int64_t n_rows,
                                int64_t n_src, int64_t n_edges, int32_t H, int32_t Dh,
                                const float *w, const void *feat, gat_dtype_t dtype, void *out,
-                               gat_plan_t plan, void *stream);
+                               gat_plan_t plan, void *workspace, size_t workspace_bytes,
+                               void *stream);
 
 /* ------------------------------------------------------------------------
  * Fused multi-head graph-attention layer: SDDMM -> segmented softmax ->

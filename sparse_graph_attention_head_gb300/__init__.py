@@ -33,7 +33,7 @@ EXPORTS = (
     "gat_fused_layer_no_alloc",
     "gat_transpose_create", "gat_transpose_destroy", "gat_transpose_info", "gat_transpose_export",
     "gat_fused_layer_backward_workspace_size", "gat_fused_layer_backward",
-    "gat_quantize_fp8", "gat_fused_layer_fp8",
+    "gat_quantize_fp8", "gat_fused_layer_fp8", "gat_spmm_weighted_workspace_size",
 )
 
 
@@ -65,8 +65,9 @@ def _load() -> ctypes.CDLL:
         "gat_sddmm": ([P, P, P, I64, I64, P, I64, P, I64, I32, I32, F, ctypes.c_int, P, P],
                       ctypes.c_int),
         "gat_edge_softmax": ([P, I64, I64, I32, P, P, P, P], ctypes.c_int),
-        "gat_spmm_weighted": ([P, P, I64, I64, I64, I32, I32, P, P, ctypes.c_int, P, P, P],
-                              ctypes.c_int),
+        "gat_spmm_weighted": ([P, P, I64, I64, I64, I32, I32, P, P, ctypes.c_int, P, P, P, SZ,
+                               P], ctypes.c_int),
+        "gat_spmm_weighted_workspace_size": ([P, I32, I32, P], ctypes.c_int),
         "gat_fused_layer_workspace_size": ([P, I32, I32, P], ctypes.c_int),
         "gat_fused_layer": ([P, P, I64, I64, I64, I32, I32, F, P, P, P, ctypes.c_int, P, P, P, SZ,
                              P], ctypes.c_int),
@@ -245,19 +246,35 @@ def gat_edge_softmax(row_ptr, scores, H, out=None, plan=None, stream=None):
     return out
 
 
+def gat_spmm_weighted_workspace_size(plan, H, Dh) -> int:
+    n = ctypes.c_size_t()
+    _check("gat_spmm_weighted_workspace_size",
+           _lib.gat_spmm_weighted_workspace_size(_plan_handle(plan), H, Dh, ctypes.byref(n)))
+    return n.value
+
+
 def gat_spmm_weighted(row_ptr, col_idx, w, feat, H, Dh, n_rows=None, out=None, plan=None,
-                      stream=None):
-    """out[i,h,:] = sum_e w[e,h] feat[col_idx[e],h,:]; out has feat's dtype."""
+                      workspace=None, no_workspace=False, stream=None):
+    """out[i,h,:] = sum_e w[e,h] feat[col_idx[e],h,:]; out has feat's dtype.
+    With a plan, heavy rows run as chunks through ``workspace`` (allocated
+    here when None); ``no_workspace=True`` passes none (a block per heavy row)."""
     _idx(row_ptr, "row_ptr")
     _idx(col_idx, "col_idx")
     n_rows = row_ptr.numel() - 1 if n_rows is None else n_rows
     E = col_idx.numel()
     if out is None:
         out = torch.empty((n_rows, H, Dh), dtype=feat.dtype, device=feat.device)
+    if no_workspace:
+        workspace = None
+    elif plan is not None and workspace is None:
+        need = gat_spmm_weighted_workspace_size(plan, H, Dh)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=feat.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("gat_spmm_weighted", _lib.gat_spmm_weighted(
         _ptr(row_ptr), _ptr(col_idx) if E else None, n_rows, feat.numel() // (H * Dh), E, H, Dh,
         _ptr(w) if E else None, _ptr(feat), _dtype(feat), _ptr(out), _plan_handle(plan),
-        _stream(stream)))
+        _ptr(workspace), ws_bytes, _stream(stream)))
     return out
 
 

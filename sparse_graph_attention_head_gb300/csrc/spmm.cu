@@ -1,8 +1,10 @@
 // spmm.cu - gat_spmm_weighted: out[i,h,:] = sum_e w[e,h] * feat[col_idx[e],h,:]
 // (FW-GLM-5-1 l1_p18, reference model; Kimi-K2.6 l2_p37: a destination with
-// no edges stays zero). Light rows: one warp per row, persistent, with the
-// next row's metadata prefetched; heavy rows (with a plan): one 8-warp block
-// per row, warps summed in warp order. Lane layout: row_engine.cuh.
+// no edges stays zero). One warp per row, persistent, with the next item's
+// metadata prefetched. Heavy rows of a plan: with a workspace, cut into
+// chunks in the same launch and summed by the last chunk in chunk order;
+// without one, one 8-warp block per row in a second launch, warps summed in
+// warp order. Lane layout: row_engine.cuh.
 #include <climits>
 
 #include "row_engine.cuh"
@@ -133,45 +135,94 @@ struct SpmmAcc {
 #pragma unroll
         for (int s = 0; s < V; ++s) st_stream16(orow + ln.vi[s] * 16, Vec<T>::pack(acc[s]));
     }
+
+    // A chunk of a heavy row: publish the chunk's sum; the warp that finishes
+    // the row's last chunk (arrival counter) adds the row's chunk sums in
+    // chunk order and writes the row.
+    __device__ __forceinline__ void chunk_epilogue(const EngineParams &p, const L &ln, int64_t row,
+                                                   int hr, int64_t chunk) {
+        if (ln.sub == 0) {
+            float *slot = p.partials + chunk * p.slot_floats;
+#pragma unroll
+            for (int s = 0; s < V; ++s)
+#pragma unroll
+                for (int t = 0; t < VE; t += 4)
+                    __stcg(reinterpret_cast<float4 *>(slot + ln.vi[s] * VE + t),
+                           make_float4(acc[s][t], acc[s][t + 1], acc[s][t + 2], acc[s][t + 3]));
+        }
+        __threadfence();
+        __syncwarp();
+        int old = 0;
+        if (ln.lane == 0) old = atomicAdd(p.counters + hr, 1);
+        old = __shfl_sync(kFull, old, 0);
+        const int c0 = __ldg(p.chunk_start + hr), c1 = __ldg(p.chunk_start + hr + 1);
+        if (old != c1 - c0 - 1) return;  // not the row's last chunk
+        __threadfence();
+        zero();
+        for (int c = c0; c < c1; ++c) {
+            const float *slot = p.partials + (int64_t)c * p.slot_floats;
+#pragma unroll
+            for (int s = 0; s < V; ++s)
+#pragma unroll
+                for (int t = 0; t < VE; t += 4) {
+                    const float4 f = ld_cg_f4(slot + ln.vi[s] * VE + t);
+                    acc[s][t] += f.x;
+                    acc[s][t + 1] += f.y;
+                    acc[s][t + 2] += f.z;
+                    acc[s][t + 3] += f.w;
+                }
+        }
+        store_out(p, ln, row);
+        if (ln.lane == 0) p.counters[hr] = 0;  // ready for the next call
+    }
 };
 
-// Light rows (every row without a plan): persistent warps, warp w takes rows
-// w, w + W, ... While a row is processed, the next row's row_ptr entries
-// and then its first col_idx tile are already being fetched.
+// Persistent warps, warp w takes items w, w + W, ...: with a plan and a
+// workspace, the chunks of heavy rows first, then every row (heavy rows
+// skipped: their chunks or the heavy-row kernel do them). While an item is
+// processed, the next item's metadata and then its first col_idx tile are
+// already being fetched.
 constexpr int kSpmmThreads = 128;
 
 template <typename T, int V, int LE, int U>
-__global__ void __launch_bounds__(kSpmmThreads, 4)
+__global__ void __launch_bounds__(kSpmmThreads, V == 4 ? 4 : (V == 2 && sizeof(T) == 2 ? 6 : 8))
 spmm_rows_kernel(const EngineParams p) {
     using L = Lanes<T, V, LE>;
     const L ln(p.Dh);
     SpmmAcc<T, V, LE, U> st;
     const int64_t wpb = blockDim.x >> 5;
     const int64_t n_warps = (int64_t)gridDim.x * wpb;
-    int64_t row = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
-    if (row >= p.n_rows) return;
-    int ne0 = __ldg(p.row_ptr + row), ne1 = __ldg(p.row_ptr + row + 1);
+    const int64_t n_items = p.n_chunks + p.n_rows;
+    int64_t item = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
+    if (item >= n_items) return;
+    int4 meta = item_meta(p, item);
     int ci_tile = 0;
     bool ci_ready = false;
-    for (; row < p.n_rows; row += n_warps) {
-        const int e0 = ne0, e1 = ne1;
-        const int64_t nxt = row + n_warps;
-        const bool has_next = nxt < p.n_rows;
-        ne0 = has_next ? __ldg(p.row_ptr + nxt) : 0;
-        ne1 = has_next ? __ldg(p.row_ptr + nxt + 1) : 0;
-        if (e1 - e0 > p.heavy_threshold) {  // a heavy row: the heavy-row kernel's
+    for (; item < n_items; item += n_warps) {
+        const int4 cur = meta;  // {row, e0, e1, heavy index or -1}
+        const int64_t nxt = item + n_warps;
+        const bool has_next = nxt < n_items;
+        meta = has_next ? item_meta(p, nxt) : make_int4(0, 0, 0, -1);
+        const bool is_chunk = item < p.n_chunks;
+        if (!is_chunk && cur.z - cur.y > p.heavy_threshold) {
             ci_ready = false;
             continue;
         }
         const int first_ci =
-            ci_ready ? ci_tile : (ln.lane < e1 - e0 ? __ldg(p.col_idx + e0 + ln.lane) : 0);
+            ci_ready ? ci_tile : (ln.lane < cur.z - cur.y ? __ldg(p.col_idx + cur.y + ln.lane) : 0);
+        const int nn = meta.z - meta.y;
+        const bool want_next =
+            has_next && nn > 0 && (nxt < p.n_chunks || nn <= p.heavy_threshold);
         bool next_ready = false;
-        const bool want_next = has_next && ne1 > ne0 && ne1 - ne0 <= p.heavy_threshold;
         st.zero();
-        st.run(p, ln, e0, e1, 0, 1, first_ci, true, ne0, ne1, want_next, ci_tile, next_ready);
+        st.run(p, ln, cur.y, cur.z, 0, 1, first_ci, true, meta.y, meta.z, want_next, ci_tile,
+               next_ready);
         ci_ready = next_ready;
         st.merge_subgroups();
-        st.store_out(p, ln, row);
+        if (is_chunk)
+            st.chunk_epilogue(p, ln, cur.x, cur.w, item);
+        else
+            st.store_out(p, ln, cur.x);
     }
 }
 
@@ -223,7 +274,7 @@ spmm_heavy_kernel(const EngineParams p) {
 
 template <typename T, int V, int LE>
 static gat_status_t launch_spmm_fast(const EngineParams &p, cudaStream_t s) {
-    constexpr int U = V == 4 ? 2 : 8;  // edges in flight per warp (8 KB at V = 2)
+    constexpr int U = V == 4 ? 2 : 3;  // edges in flight per warp (3 KB at V = 2, fp32)
     auto kern = spmm_rows_kernel<T, V, LE, U>;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSpmmThreads, 0) !=
@@ -231,7 +282,7 @@ static gat_status_t launch_spmm_fast(const EngineParams &p, cudaStream_t s) {
         per_sm < 1)
         per_sm = 1;
     const int64_t wpb = kSpmmThreads / 32;
-    int64_t blocks = (p.n_rows + wpb - 1) / wpb;
+    int64_t blocks = (p.n_chunks + p.n_rows + wpb - 1) / wpb;
     const int64_t cap = (int64_t)sm_count() * per_sm;
     if (blocks > cap) blocks = cap;
     kern<<<(unsigned)blocks, kSpmmThreads, 0, s>>>(p);
@@ -276,11 +327,20 @@ static gat_status_t launch_spmm(EngineParams p, bool vec_ok, cudaStream_t s) {
 
 using namespace gat;
 
+extern "C" gat_status_t gat_spmm_weighted_workspace_size(gat_plan_t plan, int32_t H, int32_t Dh,
+                                                         size_t *bytes) {
+    if (!bytes || H < 1 || Dh < 1)
+        return fail(GAT_ERR_INVALID_ARG, "gat_spmm_weighted_workspace_size: bad arguments");
+    const int64_t slot = ((int64_t)H * Dh + 3) / 4 * 4;
+    *bytes = plan ? (size_t)plan->n_chunks * (size_t)slot * sizeof(float) : 0;
+    return GAT_OK;
+}
+
 extern "C" gat_status_t gat_spmm_weighted(const int32_t *row_ptr, const int32_t *col_idx,
                                           int64_t n_rows, int64_t n_src, int64_t n_edges,
                                           int32_t H, int32_t Dh, const float *w, const void *feat,
                                           gat_dtype_t dtype, void *out, gat_plan_t plan,
-                                          void *stream) {
+                                          void *workspace, size_t workspace_bytes, void *stream) {
     if (n_rows < 0 || n_src < 0 || n_edges < 0 || H < 1 || Dh < 1)
         return fail(GAT_ERR_INVALID_ARG, "gat_spmm_weighted: bad sizes");
     if (dtype != GAT_F32 && dtype != GAT_BF16)
@@ -302,13 +362,29 @@ extern "C" gat_status_t gat_spmm_weighted(const int32_t *row_ptr, const int32_t 
     p.H = H;
     p.Dh = Dh;
     p.heavy_threshold = INT_MAX;
+    p.slot_floats = ((int64_t)H * Dh + 3) / 4 * 4;
     const bool vec_ok = aligned16(out) && (n_edges == 0 || aligned16(feat));
     int V, LE;
     const int eb = dtype == GAT_F32 ? 4 : 2;
     if (plan && vec_ok && engine_shape(H, Dh, eb, V, LE) && plan->n_heavy > 0) {
         p.heavy_threshold = plan->heavy_threshold;
-        p.heavy_rows = plan->heavy_rows;
-        p.n_block_rows = plan->n_heavy;
+        const size_t need = (size_t)plan->n_chunks * (size_t)p.slot_floats * sizeof(float);
+        if (workspace && workspace_bytes >= need && aligned16(workspace)) {
+            // heavy rows as chunks in the same launch
+            p.n_chunks = plan->n_chunks;
+            p.chunk_desc = plan->chunk_desc;
+            p.chunk_start = plan->chunk_start;
+            p.counters = plan->counters;
+            p.partials = static_cast<float *>(workspace);
+        } else if (workspace) {
+            return fail(GAT_ERR_WORKSPACE,
+                        "gat_spmm_weighted: workspace needs %zu bytes (16-byte aligned), got %zu",
+                        need, workspace_bytes);
+        } else {
+            // no workspace: one thread block per heavy row, second launch
+            p.heavy_rows = plan->heavy_rows;
+            p.n_block_rows = plan->n_heavy;
+        }
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == GAT_F32) return launch_spmm<float>(p, vec_ok, s);

@@ -121,8 +121,11 @@ def test_spmm_shapes(gat, H, Dh, dtype):
         feat_d, feat_o = dev(f32), f32
     o, c = oracle.spmm_weighted(rp, ci, w.astype(np.float64), feat_o, H, Dh, want_cond=True)
     rpd = dev(rp)
-    for plan in (None, gat.Plan(rpd, heavy_threshold=64)):
-        out = gat.gat_spmm_weighted(rpd, dev(ci), dev(w), feat_d, H, Dh, plan=plan)
+    for plan, no_ws in ((None, False), (gat.Plan(rpd, heavy_threshold=64), False),
+                        (gat.Plan(rpd, heavy_threshold=64, chunk_edges=50), False),
+                        (gat.Plan(rpd, heavy_threshold=64), True)):
+        out = gat.gat_spmm_weighted(rpd, dev(ci), dev(w), feat_d, H, Dh, plan=plan,
+                                    no_workspace=no_ws)
         g = host(out)
         if dtype == "bf16":
             assert_bf16(g, o, c, name=f"spmm {H}x{Dh} bf16")
@@ -365,6 +368,26 @@ def test_spmm_heads_100k_elementwise(gat):
     deg = np.diff(d["row_ptr"]).astype(np.float64)
     rate = assert_fp32(host(out), o, c, deg[:, None, None], name="spmm 8x32 100k")
     assert rate > 0.99
+
+
+def test_spmm_heads_chunked_equals_block_path_and_is_deterministic(gat):
+    d = W.make_spmm_heads(n=50_000, seed=9)
+    H, Dh = d["H"], d["Dh"]
+    rp, ci, w, f = dev(d["row_ptr"]), dev(d["col_idx"]), dev(d["w"]), dev(d["feat"])
+    plan = gat.Plan(rp)
+    assert plan.info()["n_chunks"] > 0
+    a = gat.gat_spmm_weighted(rp, ci, w, f, H, Dh, plan=plan)
+    b = gat.gat_spmm_weighted(rp, ci, w, f, H, Dh, plan=plan)
+    assert torch.equal(a, b)
+    c = gat.gat_spmm_weighted(rp, ci, w, f, H, Dh, plan=plan, no_workspace=True)
+    o, cond = oracle.spmm_weighted(d["row_ptr"], d["col_idx"], d["w"].astype(np.float64),
+                                   d["feat"], H, Dh, want_cond=True)
+    deg = np.maximum(np.diff(d["row_ptr"]), 1).astype(np.float64)[:, None, None]
+    assert_fp32(host(a), o, cond, deg, name="spmm chunked")
+    assert_fp32(host(c), o, cond, deg, name="spmm block per heavy row")
+    small = torch.empty(16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(gat.GatError, match="GAT_ERR_WORKSPACE"):
+        gat.gat_spmm_weighted(rp, ci, w, f, H, Dh, plan=plan, workspace=small)
 
 
 def test_spmm_heads_full_size_sampled_rows(gat):
