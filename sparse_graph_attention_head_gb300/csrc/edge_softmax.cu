@@ -10,10 +10,14 @@
 // W = 4 (16-byte shared-memory accesses) when H % 4 == 0 and the pointers are
 // 16-byte aligned, else W = 1 with 4-byte copies and plain stores.
 //   light rows: a warp stages a run of consecutive light rows (up to 2048
-//     scores) and computes it with one thread per (row, group of W heads);
+//     scores) and computes its short rows with one thread per (row, group of
+//     W heads) and its longer rows (more than kWarpRowDeg edges) with the
+//     whole warp, one row at a time;
 //   heavy rows (with a plan): a block stages one row in chunks of up to
 //     12288 scores and reduces each head group over its threads.
-// A light row longer than a warp's buffer (possible without a plan) is read
+// Rows of a plan's heavy class that still fit a warp's buffer (up to 2048
+// scores) are done by the light-row kernel; a light row longer than the
+// buffer (possible without a plan, or with a large threshold) is read
 // straight from global memory by the whole warp. H > 32 takes the
 // head-at-a-time kernels further down.
 // out may alias scores: every score of a row is read before its first write.
@@ -29,6 +33,7 @@ constexpr int kSpanSmemBytes = kSoftmaxThreads / 32 * kSpanFloats * 4;
 constexpr int kHeavyThreads = 256;       // heavy-row kernel
 constexpr int kHeavySpanFloats = 12288;  // heavy-row staging buffer (48 KB)
 constexpr int kSoftmaxCache = 8;         // direct path: loads per thread per tile
+constexpr int kWarpRowDeg = 8;           // light rows longer than this: whole-warp softmax
 constexpr float kLog2e = 1.4426950408889634f;
 
 // exp(x) as exp2f(x * log2 e) (rarely taken paths)
@@ -97,6 +102,46 @@ __device__ __forceinline__ void segment_softmax(float *p, int d, int H) {
 #pragma unroll
         for (int w = 0; w < W; ++w) v[w] *= z[w];
         SVec<W>::st(p + e * H, v);
+    }
+}
+
+// In-place softmax of one row of d edges (H heads, H % 4 == 0, Q = H/4 a power
+// of two) by the whole warp: lane l takes float4s l, l+32, ... of the row, all
+// of head group l % Q, and the lanes of a head group merge their maxima and
+// sums with xor-shuffles over offsets 16 .. Q. Exact maximum, so no -inf guard
+// (an all -inf head gives NaN, as the two-pass definition).
+__device__ __forceinline__ void warp_row_softmax4(float *p, int d, int H, int lane) {
+    const int Q = H >> 2, n4 = d * Q;
+    float4 *p4 = reinterpret_cast<float4 *>(p);
+    float4 m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    for (int j = lane; j < n4; j += 32) {
+        const float4 v = p4[j];
+        m = make_float4(fmaxf(m.x, v.x), fmaxf(m.y, v.y), fmaxf(m.z, v.z), fmaxf(m.w, v.w));
+    }
+    for (int o = 16; o >= Q; o >>= 1) {
+        m.x = fmaxf(m.x, __shfl_xor_sync(kFull, m.x, o));
+        m.y = fmaxf(m.y, __shfl_xor_sync(kFull, m.y, o));
+        m.z = fmaxf(m.z, __shfl_xor_sync(kFull, m.z, o));
+        m.w = fmaxf(m.w, __shfl_xor_sync(kFull, m.w, o));
+    }
+    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = lane; j < n4; j += 32) {
+        float4 v = p4[j];
+        v = make_float4(ex2_approx((v.x - m.x) * kLog2e), ex2_approx((v.y - m.y) * kLog2e),
+                        ex2_approx((v.z - m.z) * kLog2e), ex2_approx((v.w - m.w) * kLog2e));
+        p4[j] = v;
+        z = make_float4(z.x + v.x, z.y + v.y, z.z + v.z, z.w + v.w);
+    }
+    for (int o = 16; o >= Q; o >>= 1) {
+        z.x += __shfl_xor_sync(kFull, z.x, o);
+        z.y += __shfl_xor_sync(kFull, z.y, o);
+        z.z += __shfl_xor_sync(kFull, z.z, o);
+        z.w += __shfl_xor_sync(kFull, z.w, o);
+    }
+    const float4 inv = make_float4(1.f / z.x, 1.f / z.y, 1.f / z.z, 1.f / z.w);
+    for (int j = lane; j < n4; j += 32) {
+        const float4 v = p4[j];
+        p4[j] = make_float4(v.x * inv.x, v.y * inv.y, v.z * inv.z, v.w * inv.w);
     }
 }
 
@@ -250,8 +295,10 @@ __global__ void __launch_bounds__(kSoftmaxThreads)
 softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t H,
                     const float *scores, float *out, int32_t heavy_threshold) {
     extern __shared__ __align__(16) float span_smem[];
+    __shared__ int order_smem[kSoftmaxThreads / 32][32];
     const int lane = threadIdx.x & 31;
     float *sb = span_smem + (threadIdx.x >> 5) * kSpanFloats;
+    int *order = order_smem[threadIdx.x >> 5];
     const int Q = H / W, R = 32 / Q;
     const int r = lane / Q, q = lane - r * Q;
     const int32_t cap_e = kSpanFloats / H;  // edges per buffer
@@ -266,7 +313,9 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
         const int32_t nxt = __shfl_down_sync(kFull, e0_lane, 1);
         const int32_t e1_lane = lane + 1 < nb ? nxt : rp_end;
         const int32_t deg_lane = e1_lane - e0_lane;
-        const bool fits = lane < nb && deg_lane <= heavy_threshold && deg_lane <= cap_e;
+        // a row the staging buffer holds is done here even when the plan
+        // counts it heavy (the heavy-row kernel skips such rows)
+        const bool fits = lane < nb && deg_lane <= cap_e;
         int i0 = 0;
         while (i0 < nb) {
             // the run: rows i0 .. i1-1, all light and within one buffer
@@ -277,7 +326,7 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
             if (i1 > nb) i1 = nb;
             if (i1 == i0) {  // a heavy row, or a light row longer than the buffer
                 const int32_t d = __shfl_sync(kFull, deg_lane, i0);
-                if (d <= heavy_threshold)
+                if (d <= heavy_threshold)  // light but too long: straight from global
                     softmax_row_direct(scores, out, (int64_t)base * H, (int64_t)(base + d) * H, H,
                                        lane);
                 ++i0;
@@ -291,14 +340,32 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
                 __syncwarp();
                 stage_in<W>(sb, scores + x0, n, lane, 32);
                 __syncwarp();
-                const int nr = i1 - i0;
-                for (int g0 = 0; g0 < nr; g0 += R) {
+                // rows of more than kWarpRowDeg edges (W = 4, Q a power of two):
+                // the whole warp, one row at a time; the rest one thread per
+                // (row, head group), R rows at a time, so a warp instruction
+                // never waits on one long row
+                const unsigned run_mask = (i1 - i0 == 32 ? 0xffffffffu : ((1u << (i1 - i0)) - 1u)) << i0;
+                const bool warp_ok = W == 4 && (Q & (Q - 1)) == 0;
+                const unsigned long_mask =
+                    __ballot_sync(kFull, warp_ok && deg_lane > kWarpRowDeg) & run_mask;
+                const unsigned short_mask = run_mask & ~long_mask;
+                if ((short_mask >> lane) & 1u) order[__popc(short_mask & ((1u << lane) - 1u))] = lane;
+                __syncwarp();
+                const int ns = __popc(short_mask);
+                for (int g0 = 0; g0 < ns; g0 += R) {
                     const int slot = g0 + r;
-                    const bool has = r < R && slot < nr;
-                    const int i = has ? i0 + slot : 0;
+                    const bool has = r < R && slot < ns;
+                    const int i = has ? order[slot] : 0;
                     const int32_t ri0 = __shfl_sync(kFull, e0_lane, i);
                     const int32_t ri1 = __shfl_sync(kFull, e1_lane, i);
                     if (has) segment_softmax<W>(sb + (ri0 - base) * H + q * W, ri1 - ri0, H);
+                }
+                for (unsigned lm = long_mask; lm; lm &= lm - 1u) {
+                    const int i = __ffs(lm) - 1;
+                    const int32_t ri0 = __shfl_sync(kFull, e0_lane, i);
+                    const int32_t ri1 = __shfl_sync(kFull, e1_lane, i);
+                    __syncwarp();
+                    warp_row_softmax4(sb + (ri0 - base) * H, ri1 - ri0, H, lane);
                 }
                 if (W == 4) {
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -369,7 +436,7 @@ template <int W>
 __global__ void __launch_bounds__(kHeavyThreads)
 softmax_heavy_rows_kernel(const int32_t *__restrict__ row_ptr,
                           const int32_t *__restrict__ heavy_rows, int64_t n_heavy, int32_t H,
-                          const float *scores, float *out) {
+                          const float *scores, float *out, int32_t light_cap) {
     extern __shared__ __align__(16) float hs[];
     __shared__ float red[kHeavyThreads * 4];
     const int t = threadIdx.x;
@@ -399,6 +466,7 @@ softmax_heavy_rows_kernel(const int32_t *__restrict__ row_ptr,
         const int64_t row = heavy_rows[b];
         const int64_t e0 = row_ptr[row];
         const int32_t deg = row_ptr[row + 1] - row_ptr[row];
+        if (deg <= light_cap) continue;  // the light-row kernel's
         float m[W], z[W], v[W];
 #pragma unroll
         for (int w = 0; w < W; ++w) m[w] = -INFINITY, z[w] = 0.f;
@@ -628,7 +696,7 @@ extern "C" gat_status_t gat_edge_softmax(const int32_t *row_ptr, int64_t n_rows,
             const int64_t hcap = (int64_t)sm_count() * per_sm;
             if (hb > hcap) hb = hcap;
             hk<<<(unsigned)hb, kHeavyThreads, smem, s>>>(row_ptr, plan->heavy_rows, plan->n_heavy,
-                                                         H, scores, out);
+                                                         H, scores, out, kSpanFloats / H);
         } else {
             const int64_t hcap = (int64_t)sm_count() * 8;
             if (hb > hcap) hb = hcap;
