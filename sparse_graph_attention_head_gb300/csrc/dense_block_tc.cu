@@ -19,9 +19,9 @@
 //          next chunk's global loads in flight in registers) and, through its
 //          first thread, issues each chunk's MMAs (commit -> one mbarrier per
 //          ring slot)
-//   all    relation-MLP bias of the node pairs with the edge mask folded in
-//          (-inf where masked), split over the four groups (the groups that
-//          start early take more pairs)
+//   k != 1 relation-MLP bias of the node pairs with the edge mask folded in
+//          (-inf where masked), split evenly over groups 0, 2 and 3 (group 1
+//          is streaming the Q|K|V weights meanwhile)
 //   k      attention for head k: Q, K, V rows from TMEM, K and V staged in the
 //          A region (idle once Q|K|V are in TMEM), scores + bias, softmax,
 //          context kept in registers until every warp has read its staging,
@@ -222,11 +222,14 @@ template <int P, int H>
 __device__ __forceinline__ void mlp_bias(const float *prow, const float *mrow, int j0, int j1,
                                          const float *w1, const float *bb1, const float *w2,
                                          const float *bb2, float *bias_g, int N, int n) {
-    float4 nxt[P / 4];
-    if (j0 < j1) {
+    // two pairs' features in flight ahead of the one being computed
+    float4 nxt[P / 4], nxt2[P / 4];
 #pragma unroll
-        for (int c4 = 0; c4 < P / 4; ++c4)
-            nxt[c4] = __ldg(reinterpret_cast<const float4 *>(prow + j0 * P) + c4);
+    for (int c4 = 0; c4 < P / 4; ++c4) {
+        nxt[c4] = j0 < j1 ? __ldg(reinterpret_cast<const float4 *>(prow + j0 * P) + c4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        nxt2[c4] = j0 + 1 < j1 ? __ldg(reinterpret_cast<const float4 *>(prow + (j0 + 1) * P) + c4)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     for (int j = j0; j < j1; ++j) {
         float pf[P];
@@ -236,27 +239,38 @@ __device__ __forceinline__ void mlp_bias(const float *prow, const float *mrow, i
             pf[4 * c4 + 1] = nxt[c4].y;
             pf[4 * c4 + 2] = nxt[c4].z;
             pf[4 * c4 + 3] = nxt[c4].w;
+            nxt[c4] = nxt2[c4];
         }
-        if (j + 1 < j1) {
+        if (j + 2 < j1) {
 #pragma unroll
             for (int c4 = 0; c4 < P / 4; ++c4)
-                nxt[c4] = __ldg(reinterpret_cast<const float4 *>(prow + (j + 1) * P) + c4);
+                nxt2[c4] = __ldg(reinterpret_cast<const float4 *>(prow + (j + 2) * P) + c4);
         }
         float r[H];
 #pragma unroll
         for (int h = 0; h < H; ++h) r[h] = bb2[h];
 #pragma unroll
         for (int u = 0; u < P; ++u) {
+            // W1 row u and W2 column u (stored transposed, w2t[u*H + h]) as
+            // 16-byte shared-memory reads; even and odd products summed
+            // apart, as before
+            const float4 *w1r = reinterpret_cast<const float4 *>(w1 + u * P);
             float a0 = bb1[u], a1 = 0.f;
 #pragma unroll
-            for (int c = 0; c < P; c += 2) {
-                a0 = fmaf(w1[u * P + c], pf[c], a0);
-                a1 = fmaf(w1[u * P + c + 1], pf[c + 1], a1);
+            for (int c4 = 0; c4 < P / 4; ++c4) {
+                const float4 w = w1r[c4];
+                a0 = fmaf(w.x, pf[4 * c4], a0);
+                a1 = fmaf(w.y, pf[4 * c4 + 1], a1);
+                a0 = fmaf(w.z, pf[4 * c4 + 2], a0);
+                a1 = fmaf(w.w, pf[4 * c4 + 3], a1);
             }
             const float a = a0 + a1;
             const float hid = __fdividef(a, 1.0f + __expf(-a));  // SiLU
-#pragma unroll
-            for (int h = 0; h < H; ++h) r[h] = fmaf(w2[h * P + u], hid, r[h]);
+            const float4 w2c = *reinterpret_cast<const float4 *>(w2 + u * H);
+            r[0] = fmaf(w2c.x, hid, r[0]);
+            r[1] = fmaf(w2c.y, hid, r[1]);
+            r[2] = fmaf(w2c.z, hid, r[2]);
+            r[3] = fmaf(w2c.w, hid, r[3]);
         }
         const bool masked = __ldg(mrow + j) < 0.5f;
 #pragma unroll
@@ -269,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
     using L = Smem<P, H, DH>;
     constexpr int D = L::D, n_qkv = 3 * D / kNB, n_out = D / kNB;
     static_assert(H == 4, "one attention head per role group");
+    static_assert(P % 4 == 0, "16-byte reads of the relation-MLP weights");
     static_assert(3 * D % kNB == 0 && D % kNB == 0 && DH % 8 == 0, "chunking");
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ uint64_t bar[2];
@@ -284,15 +299,15 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
     float *stage = reinterpret_cast<float *>(sm) + warp * 2 * N * DH;  // in the A region
     const uint32_t a_hi = smem_u32(sm + L::a_hi), a_lo = smem_u32(sm + L::a_lo);
     const float inv_sqrt_dh = 1.0f / sqrtf((float)DH);
-    // relation-MLP pair ranges: groups 2 and 3 start at once, group 0 after
-    // LayerNorm, group 1 after issuing Q|K|V
-    const int jb2 = 0, jb3 = (3 * N) / 8, jb0 = (6 * N) / 8, jb1 = min(N, (6 * N) / 8 + (N + 5) / 6);
-    const int j_lo = grp == 2 ? jb2 : grp == 3 ? jb3 : grp == 0 ? jb0 : jb1;
-    const int j_hi = grp == 2 ? jb3 : grp == 3 ? jb0 : grp == 0 ? jb1 : N;
+    // relation-MLP pair ranges: groups 0, 2 and 3 split the pairs evenly;
+    // group 1 streams the Q|K|V weight chunks meanwhile and takes none
+    const int jb2 = 0, jb3 = N / 3, jb0 = (2 * N) / 3;
+    const int j_lo = grp == 2 ? jb2 : grp == 3 ? jb3 : grp == 0 ? jb0 : N;
+    const int j_hi = grp == 2 ? jb3 : grp == 3 ? jb0 : N;
 
     for (int i = tid; i < P * P; i += kThreads) w1[i] = p.W1[i];
     for (int i = tid; i < P; i += kThreads) bb1[i] = p.b1[i];
-    for (int i = tid; i < H * P; i += kThreads) w2[i] = p.W2[i];
+    for (int i = tid; i < H * P; i += kThreads) w2[(i % P) * H + i / P] = p.W2[i];  // [u][h]
     for (int i = tid; i < H; i += kThreads) bb2[i] = p.b2[i];
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
