@@ -221,3 +221,25 @@ def test_backward_full_size_sampled(gat):
     assert_bf16(dq[rows], odq[pos], cq[pos], name="1e6 dq sampled rows")
     assert_bf16(dk[srcs], odk[srcs], ck[srcs], name="1e6 dk sampled sources")
     assert_bf16(dv[srcs], odv[srcs], cv[srcs], name="1e6 dv sampled sources")
+
+
+def test_backward_degenerate_graphs(gat):
+    H, Dh = 8, 64
+    rng = np.random.default_rng(81)
+    f = lambda m: W.bf16_bits_from_f32(rng.standard_normal((m, H, Dh)).astype(np.float32))  # noqa: E731
+    # no edges at all: dq = dk = dv = 0
+    rp = np.zeros(6, np.int32)
+    d = dict(q=f(5), k=f(4), v=f(4), dout=f(5), H=H, Dh=Dh, scale=0.125, dtype="bf16")
+    rpd, cid = dev(rp), dev(np.zeros(0, np.int32))
+    t = gat.Transpose(rpd, cid, 4)
+    dq, dk, dv = gat.gat_fused_layer_backward(rpd, cid, *(dev_feat(d[x]) for x in ("q", "k", "v", "dout")),
+                                              d["scale"], t, plan=gat.Plan(rpd, n_edges=0))
+    assert all((host(x) == 0).all() for x in (dq, dk, dv))
+    # every edge reads one source, one row holds them all (heavy row and heavy source)
+    deg = np.array([0, 700, 0, 1], np.int64)
+    rp = W.row_ptr_from_degrees(deg)
+    ci = np.zeros(int(rp[-1]), np.int32)
+    d = dict(q=f(4), k=f(3), v=f(3), dout=f(4), H=H, Dh=Dh, scale=0.125, dtype="bf16")
+    got, t = run_backward(gat, d, rp, ci, 3, {})
+    assert t.info()["n_heavy_src"] == 1
+    check_grads(got, d, 3, rp, ci, "single source")

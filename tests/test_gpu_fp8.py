@@ -133,3 +133,18 @@ def test_fused_fp8_full_size_quantised_on_device(gat):
     ob, cb = oracle.fused_layer(d["row_ptr"], d["col_idx"], d["q"], d["k"], d["v"], 8, 64,
                                 d["scale"], rows=rows, want_cond=True)
     assert np.abs(g[rows] - ob).max() <= 0.25 * cb.max()
+
+
+def test_fused_fp8_degenerate_graphs(gat):
+    H, Dh = 8, 64
+    rng = np.random.default_rng(97)
+    q = W.bf16_bits_from_f32(rng.standard_normal((5, H, Dh)).astype(np.float32))
+    k8, ks = oracle.fp8_quantize(rng.standard_normal((3, H, Dh)).astype(np.float32), H, Dh)
+    v8, vs = oracle.fp8_quantize(rng.standard_normal((3, H, Dh)).astype(np.float32), H, Dh)
+    rp = np.zeros(6, np.int32)  # no edges: zeros
+    out = gat.gat_fused_layer_fp8(dev(rp), dev(np.zeros(0, np.int32)), dev_feat(q), dev(k8), dev(ks),
+                                  dev(v8), dev(vs), 0.125, plan=gat.Plan(dev(rp), n_edges=0))
+    assert (host(out) == 0).all()
+    # an all-zero head quantises to scale 1 and zero codes; the layer then sees zeros
+    codes, scales = gat.gat_quantize_fp8(dev(np.zeros((2, H, Dh), np.float32)))
+    assert (host(codes) == 0).all() and (host(scales) == 1).all()
