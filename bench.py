@@ -485,9 +485,20 @@ def bench_small(name, args):
         # per row: row_ptr, q and out rows (bf16); per edge: col_idx, the k8 and
         # v8 rows (1 B per element) and their 2H scales
         alg_bytes = g["n_rows"] * (4 + 4 * hd) + g["n_edges"] * (4 + 2 * hd + 8 * g["H"])
+        # quantisation error of the layer: the fp8 output against the bf16
+        # layer's on the same inputs (both computed here, on the device)
+        fn()
+        ref = gat.gat_fused_layer(rp, ci, q, k, v, g["scale"], plan=plan,
+                                  workspace=torch.empty(max(1, gat.gat_fused_layer_workspace_size(
+                                      plan, g["H"], g["Dh"])), dtype=torch.uint8, device=dev))
+        diff = (out.float() - ref.float())
+        err = {"rel_rms": float(diff.pow(2).mean().sqrt() / ref.float().pow(2).mean().sqrt()),
+               "max_abs": float(diff.abs().max()), "ref_rms": float(ref.float().pow(2).mean().sqrt())}
+        del ref, diff
         extra = {"quantize_ms_both_tables": qa.elapsed_time(qb),
                  "bytes_vs_bf16_layer": alg_bytes / fused_bytes(g["n_rows"], g["n_edges"],
-                                                                 g["H"], g["Dh"])}
+                                                                 g["H"], g["Dh"]),
+                 "error_vs_bf16_layer": err}
     elif name == "edge_softmax_h8":
         # 8 heads on the 1e6-row power-law graph
         deg = W.zipf_degrees(np.random.default_rng(3), 1_000_000)
