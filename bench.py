@@ -507,7 +507,7 @@ def bench_small(name, args):
         out = torch.empty_like(s)
         plan = gat.Plan(rp)
         fn = lambda: gat.gat_edge_softmax(rp, s, g["H"], out=out, plan=plan)  # noqa: E731
-        units, launches = g["n_edges"] * g["H"], 2
+        units, launches = g["n_edges"] * g["H"], 1
         alg_bytes = 4 * (g["n_rows"] + 1) + 8 * g["n_edges"] * g["H"]
     elif name == "edge_softmax":
         rp, s = t(g["row_ptr"]), t(g["scores"])

@@ -38,8 +38,10 @@
  * - Results are deterministic: no floating-point atomics; every reduction
  *   runs in a fixed order, so repeated calls give bitwise-identical outputs.
  * - Thread safety: calls on different streams may run concurrently, except
- *   that one plan must not be used by two gat_fused_layer calls whose work
- *   overlaps on the GPU (it holds per-row arrival counters).
+ *   that one plan must not be used by two calls whose work overlaps on the
+ *   GPU: it holds per-row arrival counters and a work counter that the calls
+ *   taking a plan update and reset (order such calls on one stream, or give
+ *   each stream its own plan).
  */
 #ifndef GAT_H
 #define GAT_H
@@ -165,7 +167,9 @@ gat_status_t gat_sddmm(const int32_t *row_ptr, const int32_t *src_idx, const int
  * scores/out are fp32 [n_edges,H]; out may alias scores (in place). Rows of
  * degree 0 own no entries and write nothing. A row whose scores are all -inf
  * yields NaN, as the reference softmax does. `plan` may be NULL (every row is
- * handled by one warp) or a plan of this graph (heavy rows get a thread block).
+ * handled by one warp) or a plan of this graph (heavy rows get a thread block,
+ * and warps fetch batches of rows from the plan's work counter, so the plan
+ * must not be in use by another call at the same time).
  * Errors: GAT_ERR_INVALID_ARG, GAT_ERR_PLAN_MISMATCH.
  * ---------------------------------------------------------------------- */
 gat_status_t gat_edge_softmax(const int32_t *row_ptr, int64_t n_rows, int64_t n_edges, int32_t H,

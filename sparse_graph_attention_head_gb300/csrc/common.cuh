@@ -33,6 +33,7 @@ struct gat_plan_s {
     int32_t *chunk_row = nullptr;    // [n_chunks]
     int32_t *counters = nullptr;     // [n_heavy], arrival counters, zero between calls
     int4 *chunk_desc = nullptr;      // [n_chunks] {row, e0, e1, heavy index} of each chunk
+    int32_t *sched = nullptr;        // [4] work counters and finished-block count, zero between calls
     int device = 0;
 };
 

@@ -4,23 +4,31 @@
 //
 // scores/out are [E, H] with heads contiguous, so a row's scores form one
 // contiguous run of deg*H floats, and consecutive rows' runs are adjacent.
-// For H <= 32 runs are staged through shared memory (cp.async, every copy of
-// a run in flight at once), reduced there and written back with one bulk
-// copy (TMA engine) per run. Threads work on W consecutive heads at once:
-// W = 4 (16-byte shared-memory accesses) when H % 4 == 0 and the pointers are
-// 16-byte aligned, else W = 1 with 4-byte copies and plain stores.
-//   light rows: a warp stages a run of consecutive light rows (up to 2048
-//     scores) and computes its short rows with one thread per (row, group of
-//     W heads) and its longer rows (more than kWarpRowDeg edges) with the
-//     whole warp, one row at a time;
-//   heavy rows (with a plan): a block stages one row in chunks of up to
-//     12288 scores and reduces each head group over its threads.
-// Rows of a plan's heavy class that still fit a warp's buffer (up to 2048
-// scores) are done by the light-row kernel; a light row longer than the
-// buffer (possible without a plan, or with a large threshold) is read
-// straight from global memory by the whole warp. H > 32 takes the
-// head-at-a-time kernels further down.
-// out may alias scores: every score of a row is read before its first write.
+// H <= 32 is one launch of softmax_rows_kernel, a grid of the resident
+// blocks (8 warps, 64 KB of staging buffer each):
+//   phase 1 (with a plan): the plan's heavy rows longer than a warp buffer,
+//     fetched 8 list entries at a time from a counter in the plan, one block
+//     per row, streamed through two 32 KB halves of the block buffer (the
+//     next chunk's copies in flight while this one is computed); rows longer
+//     than a half are read twice (fold, then normalise);
+//   phase 2: batches of 32 consecutive rows, fetched from a second counter
+//     (static stride without a plan). A warp stages runs of consecutive rows
+//     (up to 2048 scores, cp.async with every copy in flight), computes them
+//     in shared memory / registers and writes each run back with one bulk
+//     copy (TMA engine).
+// Threads work on W consecutive heads at once: W = 4 (16-byte accesses) when
+// H % 4 == 0 and the pointers are 16-byte aligned, else W = 1 with 4-byte
+// copies and plain stores. With W = 4 and Q = H/4 a power of two, a light
+// row goes to a sub-warp of S lanes (S = Q .. 32, a power of two) holding up
+// to 4 float4s per lane in registers, or 8 per lane with the whole warp, or
+// past that to the whole warp through shared memory; other layouts use one
+// thread per (row, group of W heads). A light row longer than the buffer
+// (possible without a plan, or with a large threshold) is read straight from
+// global memory by the whole warp. H > 32 takes the head-at-a-time kernels
+// further down. The last block to finish resets the plan's counters, so a
+// plan serves one launch at a time.
+// out may alias scores: every score of a row (or chunk) is read before its
+// first write.
 #include <climits>
 
 #include "common.cuh"
@@ -29,11 +37,11 @@ namespace gat {
 
 constexpr int kSoftmaxThreads = 256;     // light-row kernels
 constexpr int kSpanFloats = 2048;        // light-row staging buffer per warp (8 KB)
-constexpr int kSpanSmemBytes = kSoftmaxThreads / 32 * kSpanFloats * 4;
-constexpr int kHeavyThreads = 256;       // heavy-row kernel
-constexpr int kHeavySpanFloats = 12288;  // heavy-row staging buffer (48 KB)
+constexpr int kSpanBlockFloats = kSoftmaxThreads / 32 * kSpanFloats;  // heavy rows: 2 chunks
+constexpr int kHeavyUnit = 8;            // heavy-list entries per fetch
+constexpr int kHeavyRegs = 8;            // heavy rows: float4s per thread and chunk
+constexpr int kSpanSmemBytes = kSpanBlockFloats * 4;
 constexpr int kSoftmaxCache = 8;         // direct path: loads per thread per tile
-constexpr int kWarpRowDeg = 8;           // light rows longer than this: whole-warp softmax
 constexpr float kLog2e = 1.4426950408889634f;
 
 // exp(x) as exp2f(x * log2 e) (rarely taken paths)
@@ -44,6 +52,15 @@ __device__ __forceinline__ float exp_e(float x) { return exp2f(x * kLog2e); }
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// 1/x by the hardware approximation (about 1 ulp). The softmax sums it
+// inverts are at least 1 (the maximum's own term) or NaN (a head of -inf
+// scores), so no denormal or zero input reaches it from a finite row.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
@@ -138,7 +155,7 @@ __device__ __forceinline__ void warp_row_softmax4(float *p, int d, int H, int la
         z.z += __shfl_xor_sync(kFull, z.z, o);
         z.w += __shfl_xor_sync(kFull, z.w, o);
     }
-    const float4 inv = make_float4(1.f / z.x, 1.f / z.y, 1.f / z.z, 1.f / z.w);
+    const float4 inv = make_float4(rcp_approx(z.x), rcp_approx(z.y), rcp_approx(z.z), rcp_approx(z.w));
     for (int j = lane; j < n4; j += 32) {
         const float4 v = p4[j];
         p4[j] = make_float4(v.x * inv.x, v.y * inv.y, v.z * inv.z, v.w * inv.w);
@@ -271,122 +288,97 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// copy n floats global -> shared with the calling threads (t of nt)
+// start copying n floats global -> shared with the calling threads (t of nt)
 template <int W>
-__device__ __forceinline__ void stage_in(float *dst, const float *src, int n, int t, int nt) {
+__device__ __forceinline__ void stage_issue(float *dst, const float *src, int n, int t, int nt) {
     if (W == 4) {
         for (int j = t; j < (n >> 2); j += nt) cp_async_16(dst + 4 * j, src + 4 * j);
     } else {
         for (int j = t; j < n; j += nt) cp_async_4(dst + j, src + j);
     }
+}
+// copy n floats global -> shared with the calling threads and wait for them
+template <int W>
+__device__ __forceinline__ void stage_in(float *dst, const float *src, int n, int t, int nt) {
+    stage_issue<W>(dst, src, n, t, nt);
     cp_async_wait_all();
 }
 
-// ---- light rows, H <= 32
+// ---- light rows in registers (W = 4, Q = H/4 a power of two)
 
-// A warp takes batches of 32 consecutive rows (one coalesced row_ptr load
-// per batch). Consecutive light rows of a batch own one contiguous run of
-// scores; the warp stages such a run (at most kSpanFloats scores) into its
-// buffer, computes it with one thread per (row, group of W heads) (Q = H/W
-// groups, R = 32/Q rows at a time, lane = r*Q + q) and writes it back. Heavy
-// rows are left to the heavy-row kernel.
-template <int W>
-__global__ void __launch_bounds__(kSoftmaxThreads)
-softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t H,
-                    const float *scores, float *out, int32_t heavy_threshold) {
-    extern __shared__ __align__(16) float span_smem[];
-    __shared__ int order_smem[kSoftmaxThreads / 32][32];
-    const int lane = threadIdx.x & 31;
-    float *sb = span_smem + (threadIdx.x >> 5) * kSpanFloats;
-    int *order = order_smem[threadIdx.x >> 5];
-    const int Q = H / W, R = 32 / Q;
-    const int r = lane / Q, q = lane - r * Q;
-    const int32_t cap_e = kSpanFloats / H;  // edges per buffer
-    const int64_t wpb = blockDim.x >> 5;
-    const int64_t n_warps = (int64_t)gridDim.x * wpb;
-    const int64_t n_batches = (n_rows + 31) / 32;
-    for (int64_t b = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5); b < n_batches; b += n_warps) {
-        const int64_t r0 = b * 32;
-        const int nb = n_rows - r0 < 32 ? (int)(n_rows - r0) : 32;
-        const int32_t e0_lane = row_ptr[r0 + (lane < nb ? lane : nb - 1)];
-        const int32_t rp_end = row_ptr[r0 + nb];
-        const int32_t nxt = __shfl_down_sync(kFull, e0_lane, 1);
-        const int32_t e1_lane = lane + 1 < nb ? nxt : rp_end;
-        const int32_t deg_lane = e1_lane - e0_lane;
-        // a row the staging buffer holds is done here even when the plan
-        // counts it heavy (the heavy-row kernel skips such rows)
-        const bool fits = lane < nb && deg_lane <= cap_e;
-        int i0 = 0;
-        while (i0 < nb) {
-            // the run: rows i0 .. i1-1, all light and within one buffer
-            const int32_t base = __shfl_sync(kFull, e0_lane, i0);
-            const bool ok = lane >= i0 && fits && e1_lane - base <= cap_e;
-            const unsigned bad = ~__ballot_sync(kFull, ok) & (0xffffffffu << i0);
-            int i1 = bad ? __ffs(bad) - 1 : 32;
-            if (i1 > nb) i1 = nb;
-            if (i1 == i0) {  // a heavy row, or a light row longer than the buffer
-                const int32_t d = __shfl_sync(kFull, deg_lane, i0);
-                if (d <= heavy_threshold)  // light but too long: straight from global
-                    softmax_row_direct(scores, out, (int64_t)base * H, (int64_t)(base + d) * H, H,
-                                       lane);
-                ++i0;
-                continue;
-            }
-            const int32_t end = __shfl_sync(kFull, e1_lane, i1 - 1);
-            const int64_t x0 = (int64_t)base * H;
-            const int n = (end - base) * H;
-            if (n > 0) {
-                if (W == 4 && lane == 0) bulk_wait_read();  // the buffer's last bulk store
-                __syncwarp();
-                stage_in<W>(sb, scores + x0, n, lane, 32);
-                __syncwarp();
-                // rows of more than kWarpRowDeg edges (W = 4, Q a power of two):
-                // the whole warp, one row at a time; the rest one thread per
-                // (row, head group), R rows at a time, so a warp instruction
-                // never waits on one long row
-                const unsigned run_mask = (i1 - i0 == 32 ? 0xffffffffu : ((1u << (i1 - i0)) - 1u)) << i0;
-                const bool warp_ok = W == 4 && (Q & (Q - 1)) == 0;
-                const unsigned long_mask =
-                    __ballot_sync(kFull, warp_ok && deg_lane > kWarpRowDeg) & run_mask;
-                const unsigned short_mask = run_mask & ~long_mask;
-                if ((short_mask >> lane) & 1u) order[__popc(short_mask & ((1u << lane) - 1u))] = lane;
-                __syncwarp();
-                const int ns = __popc(short_mask);
-                for (int g0 = 0; g0 < ns; g0 += R) {
-                    const int slot = g0 + r;
-                    const bool has = r < R && slot < ns;
-                    const int i = has ? order[slot] : 0;
-                    const int32_t ri0 = __shfl_sync(kFull, e0_lane, i);
-                    const int32_t ri1 = __shfl_sync(kFull, e1_lane, i);
-                    if (has) segment_softmax<W>(sb + (ri0 - base) * H + q * W, ri1 - ri0, H);
-                }
-                for (unsigned lm = long_mask; lm; lm &= lm - 1u) {
-                    const int i = __ffs(lm) - 1;
-                    const int32_t ri0 = __shfl_sync(kFull, e0_lane, i);
-                    const int32_t ri1 = __shfl_sync(kFull, e1_lane, i);
-                    __syncwarp();
-                    warp_row_softmax4(sb + (ri0 - base) * H, ri1 - ri0, H, lane);
-                }
-                if (W == 4) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
-                    if (lane == 0) bulk_store(out + x0, sb, (unsigned)n * 4u);
-                } else {
-                    __syncwarp();
-                    for (int j = lane; j < n; j += 32) out[x0 + j] = sb[j];
-                    __syncwarp();
-                }
-            }
-            i0 = i1;
+__device__ __forceinline__ float4 max4(float4 a, float4 b) {
+    return make_float4(fmaxf(a.x, b.x), fmaxf(a.y, b.y), fmaxf(a.z, b.z), fmaxf(a.w, b.w));
+}
+__device__ __forceinline__ float4 shfl_xor4(float4 a, int o) {
+    return make_float4(__shfl_xor_sync(kFull, a.x, o), __shfl_xor_sync(kFull, a.y, o),
+                       __shfl_xor_sync(kFull, a.z, o), __shfl_xor_sync(kFull, a.w, o));
+}
+
+// Softmax of the rows in `tm` (lanes of the batch whose rows lie in the
+// staged run at sb, first edge `base`; results written back in place), each
+// row on a sub-warp of S lanes
+// (Q <= S <= 32, powers of two), 32/S rows at a time. A row's run is d*Q
+// float4s; lane s of the sub-warp holds float4s s, s+S, ..., at most KV of
+// them, all of head group s % Q, in registers from one shared-memory read to
+// the one write of the result. Maximum and sum are merged over the lanes of
+// a head group with xor-shuffles over offsets S/2 .. Q. The sub-warps visit
+// their KV slots in rotated order, so that rows starting at equal bank
+// offsets do not meet in one wavefront. Exact maximum: a head whose scores
+// are all -inf gets NaN outputs, as the two-pass definition.
+template <int KV>
+__device__ __forceinline__ void softmax_tier4(float *sb, int32_t base, int H, int Q, int S,
+                                              unsigned tm, int32_t e0_lane, int32_t e1_lane,
+                                              int *order, int lane) {
+    if ((tm >> lane) & 1u) order[__popc(tm & ((1u << lane) - 1u))] = lane;
+    __syncwarp();
+    const int cnt = __popc(tm);
+    const int lg = __ffs(S) - 1;
+    const int slot = lane >> lg, s = lane & (S - 1), P = 32 >> lg;
+    const int rot = slot & (KV - 1);
+    const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    for (int p0 = 0; p0 < cnt; p0 += P) {
+        const int k = p0 + slot;
+        const bool has = k < cnt;
+        const int i = has ? order[k] : 0;
+        const int32_t ri0 = __shfl_sync(kFull, e0_lane, i);
+        const int32_t ri1 = __shfl_sync(kFull, e1_lane, i);
+        const int n4 = has ? (ri1 - ri0) * Q : 0;
+        float4 *p = reinterpret_cast<float4 *>(sb + (ri0 - base) * H);
+        float4 v[KV];
+        float4 m = ninf;
+#pragma unroll
+        for (int t = 0; t < KV; ++t) {
+            const int j = s + ((t + rot) & (KV - 1)) * S;
+            v[t] = j < n4 ? p[j] : ninf;
+            m = max4(m, v[t]);
+        }
+        for (int o = S >> 1; o >= Q; o >>= 1) m = max4(m, shfl_xor4(m, o));
+        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int t = 0; t < KV; ++t) {
+            v[t] = make_float4(ex2_approx((v[t].x - m.x) * kLog2e), ex2_approx((v[t].y - m.y) * kLog2e),
+                               ex2_approx((v[t].z - m.z) * kLog2e), ex2_approx((v[t].w - m.w) * kLog2e));
+            z = make_float4(z.x + v[t].x, z.y + v[t].y, z.z + v[t].z, z.w + v[t].w);
+        }
+        for (int o = S >> 1; o >= Q; o >>= 1) {
+            const float4 y = shfl_xor4(z, o);
+            z = make_float4(z.x + y.x, z.y + y.y, z.z + y.z, z.w + y.w);
+        }
+        const float4 inv = make_float4(rcp_approx(z.x), rcp_approx(z.y), rcp_approx(z.z), rcp_approx(z.w));
+#pragma unroll
+        for (int t = 0; t < KV; ++t) {
+            const int j = s + ((t + rot) & (KV - 1)) * S;
+            if (j < n4)
+                p[j] = make_float4(v[t].x * inv.x, v[t].y * inv.y, v[t].z * inv.z, v[t].w * inv.w);
         }
     }
-    if (W == 4 && lane == 0) bulk_wait_all();
+    __syncwarp();
 }
 
 // ---- heavy rows, H <= 32
 
 // reduction over the threads of a block that share a head group (W values
-// each); red holds kHeavyThreads * 4 floats; every thread gets its group's
+// each); red holds kSoftmaxThreads * 4 floats; every thread gets its group's
 // result
 template <bool IS_MAX, int W>
 __device__ __forceinline__ void head_reduce_block(float (&v)[W], const HeadLanes &hl, float *red) {
@@ -425,57 +417,198 @@ __device__ __forceinline__ void head_reduce_block(float (&v)[W], const HeadLanes
     __syncthreads();
 }
 
-// One block per heavy row. The row's run is staged through shared memory in
-// chunks of whole edges; thread t works on head group t % Q (W heads) and
-// edges t / Q, t / Q + S, ... of a chunk (S = floor(256 / Q)), so a warp
-// reads consecutive words. A run that fits one chunk is read once (maximum,
-// exp terms and scaling in shared memory, one bulk store); a longer run is
-// read twice: the first pass folds each chunk into a per-thread (max, sum of
-// exp), the second recomputes and writes.
+// One chunk task of a heavy row with the thread's (up to 8) float4s of the
+// chunk in registers (W = 4, Q a power of two). kind 0: the whole row in one
+// chunk (block maximum, exp terms, block sum, scaled write-back); kind 1: a
+// fold of the chunk into the running (m, z) = (maximum, sum of exp), merged
+// over the block after the row's last chunk into (m, z) = (row maximum,
+// 1 / row sum); kind 2: the chunk's outputs from that (m, z). Kinds 0 and 2
+// store the outputs from registers to gout, the chunk's place in the output.
+// Padding slots hold -inf, whose exp term is 0; a -inf score adds nothing to
+// a fold, so a head whose scores are all -inf ends with sum 0 and NaN
+// outputs, as the two-pass definition.
+__device__ __forceinline__ void heavy_task_regs(const float *cb, float *gout, int32_t d, int kind,
+                                                bool first, bool last, const HeadLanes &hl,
+                                                int32_t H, float *red, float (&m)[4],
+                                                float (&z)[4]) {
+    constexpr int KH = kHeavyRegs;
+    const int S = hl.G, col = hl.head * 4;
+    const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    float4 x[KH];
+#pragma unroll
+    for (int t = 0; t < KH; ++t) {
+        const int e = hl.grp + t * S;
+        x[t] = hl.active && e < d ? *reinterpret_cast<const float4 *>(cb + e * H + col) : ninf;
+    }
+    auto store = [&]() {
+#pragma unroll
+        for (int t = 0; t < KH; ++t) {
+            const int e = hl.grp + t * S;
+            if (hl.active && e < d) *reinterpret_cast<float4 *>(gout + (int64_t)e * H + col) = x[t];
+        }
+    };
+    if (kind == 0) {
+        float4 mx = ninf;
+#pragma unroll
+        for (int t = 0; t < KH; ++t) mx = max4(mx, x[t]);
+        float mv[4] = {mx.x, mx.y, mx.z, mx.w};
+        head_reduce_block<true, 4>(mv, hl, red);
+        float zv[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int t = 0; t < KH; ++t) {
+            x[t] = make_float4(ex2_approx((x[t].x - mv[0]) * kLog2e), ex2_approx((x[t].y - mv[1]) * kLog2e),
+                               ex2_approx((x[t].z - mv[2]) * kLog2e), ex2_approx((x[t].w - mv[3]) * kLog2e));
+            zv[0] += x[t].x;
+            zv[1] += x[t].y;
+            zv[2] += x[t].z;
+            zv[3] += x[t].w;
+        }
+        head_reduce_block<false, 4>(zv, hl, red);
+        const float4 inv = make_float4(rcp_approx(zv[0]), rcp_approx(zv[1]), rcp_approx(zv[2]), rcp_approx(zv[3]));
+#pragma unroll
+        for (int t = 0; t < KH; ++t)
+            x[t] = make_float4(x[t].x * inv.x, x[t].y * inv.y, x[t].z * inv.z, x[t].w * inv.w);
+        store();
+        return;
+    }
+    if (kind == 1) {
+        if (first)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) m[w] = -INFINITY, z[w] = 0.f;
+        float4 cm = ninf;
+#pragma unroll
+        for (int t = 0; t < KH; ++t) cm = max4(cm, x[t]);
+        const float cmv[4] = {cm.x, cm.y, cm.z, cm.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+            if (cmv[w] > m[w]) {
+                z[w] = z[w] == 0.f ? 0.f : z[w] * ex2_approx((m[w] - cmv[w]) * kLog2e);
+                m[w] = cmv[w];
+            }
+        // with m = -inf every score so far is -inf: the terms stay 0
+        const float mm[4] = {m[0] == -INFINITY ? 0.f : m[0], m[1] == -INFINITY ? 0.f : m[1],
+                             m[2] == -INFINITY ? 0.f : m[2], m[3] == -INFINITY ? 0.f : m[3]};
+#pragma unroll
+        for (int t = 0; t < KH; ++t) {
+            z[0] += ex2_approx((x[t].x - mm[0]) * kLog2e);
+            z[1] += ex2_approx((x[t].y - mm[1]) * kLog2e);
+            z[2] += ex2_approx((x[t].z - mm[2]) * kLog2e);
+            z[3] += ex2_approx((x[t].w - mm[3]) * kLog2e);
+        }
+        if (last) {
+            float mg[4] = {m[0], m[1], m[2], m[3]};
+            head_reduce_block<true, 4>(mg, hl, red);
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+                z[w] = z[w] == 0.f ? 0.f : z[w] * ex2_approx((m[w] - mg[w]) * kLog2e);
+            head_reduce_block<false, 4>(z, hl, red);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) m[w] = mg[w], z[w] = 1.f / z[w];
+        }
+        return;
+    }
+#pragma unroll
+    for (int t = 0; t < KH; ++t)
+        x[t] = make_float4(ex2_approx((x[t].x - m[0]) * kLog2e) * z[0], ex2_approx((x[t].y - m[1]) * kLog2e) * z[1],
+                           ex2_approx((x[t].z - m[2]) * kLog2e) * z[2], ex2_approx((x[t].w - m[3]) * kLog2e) * z[3]);
+    store();
+}
+
+// The block's heavy rows (first edges e0s[i], degrees degs[i], i < nh, in
+// shared memory) as one stream of chunk tasks through two buffers: the
+// copies of task k+1 are in flight while task k is computed. Thread t works
+// on head group t % Q (W heads) and edges t / Q, t / Q + S, ... of a chunk
+// (S = floor(blockDim / Q)), so a warp reads consecutive words. A row of at
+// most ce edges is one task, read once (maximum, exp terms and scaling in
+// shared memory, one bulk store). A longer row is read twice in chunks of
+// ce edges: fold tasks accumulate a per-thread (max, sum of exp), the block
+// merges them after the last one, and normalise tasks recompute and write.
+// Entered and left by all threads of the block; on return thread 0's last
+// bulk store may still be reading its buffer.
 template <int W>
-__global__ void __launch_bounds__(kHeavyThreads)
-softmax_heavy_rows_kernel(const int32_t *__restrict__ row_ptr,
-                          const int32_t *__restrict__ heavy_rows, int64_t n_heavy, int32_t H,
-                          const float *scores, float *out, int32_t light_cap) {
-    extern __shared__ __align__(16) float hs[];
-    __shared__ float red[kHeavyThreads * 4];
+__device__ __forceinline__ void softmax_heavy_rows(const int32_t *e0s, const int32_t *degs, int nh,
+                                                   int32_t H, const float *scores, float *out,
+                                                   float *buf0, float *buf1, int32_t ce,
+                                                   float *red) {
     const int t = threadIdx.x;
-    const HeadLanes hl(H / W, kHeavyThreads, t);
+    const HeadLanes hl(H / W, kSoftmaxThreads, t);
     const int S = hl.G;
     const int col = hl.head * W;
-    const int32_t ce = kHeavySpanFloats / H;  // edges per chunk
-    auto stage = [&](int64_t f0, int32_t d) {
-        if (W == 4 && t == 0) bulk_wait_read();
-        __syncthreads();
-        stage_in<W>(hs, scores + f0 * H, d * H, t, kHeavyThreads);
-        __syncthreads();
+    auto chunk_len = [&](int ii, int32_t cc) {
+        const int32_t dd = degs[ii] - cc;
+        return dd < ce ? dd : ce;
     };
-    auto flush = [&](int64_t f0, int32_t d) {
+    auto issue = [&](int ii, int32_t cc, float *dst) {
+        stage_issue<W>(dst, scores + ((int64_t)e0s[ii] + cc) * H, chunk_len(ii, cc) * H, t,
+                       kSoftmaxThreads);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    auto flush = [&](const float *src, int64_t f0, int32_t d) {
         const int n = d * H;
         if (W == 4) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncthreads();
-            if (t == 0) bulk_store(out + f0 * H, hs, (unsigned)n * 4u);
+            if (t == 0) bulk_store(out + f0 * H, src, (unsigned)n * 4u);
         } else {
             __syncthreads();
-            for (int j = t; j < n; j += kHeavyThreads) out[f0 * H + j] = hs[j];
+            for (int j = t; j < n; j += kSoftmaxThreads) out[f0 * H + j] = src[j];
             __syncthreads();
         }
     };
-    for (int64_t b = blockIdx.x; b < n_heavy; b += gridDim.x) {
-        const int64_t row = heavy_rows[b];
-        const int64_t e0 = row_ptr[row];
-        const int32_t deg = row_ptr[row + 1] - row_ptr[row];
-        if (deg <= light_cap) continue;  // the light-row kernel's
-        float m[W], z[W], v[W];
+    if (nh == 0) return;
+    // W = 4 with Q a power of two and at most 8 edges per thread in a chunk:
+    // a thread's float4s stay in registers from their one shared-memory read
+    // to their one write
+    const bool regs = W == 4 && (hl.H & (hl.H - 1)) == 0;
+    if (regs && ce > kHeavyRegs * S) ce = kHeavyRegs * S;
+    issue(0, 0, buf0);
+    float m[W], z[W], v[W];
 #pragma unroll
-        for (int w = 0; w < W; ++w) m[w] = -INFINITY, z[w] = 0.f;
+    for (int w = 0; w < W; ++w) m[w] = -INFINITY, z[w] = 0.f;
+    int i = 0, pass = 0;
+    int32_t c0 = 0;
+    for (int k = 0; i < nh; ++k) {
+        const int32_t deg = degs[i];
+        // the task after this one
+        int ni = i, np = pass;
+        int32_t nc = c0;
         if (deg <= ce) {
-            stage(e0, deg);
+            ni = i + 1;
+        } else if (c0 + ce < deg) {
+            nc = c0 + ce;
+        } else if (pass == 0) {
+            np = 1;
+            nc = 0;
+        } else {
+            ni = i + 1;
+            np = 0;
+            nc = 0;
+        }
+        float *cb = (k & 1) ? buf1 : buf0;
+        float *nb = (k & 1) ? buf0 : buf1;
+        cp_async_wait_all();                           // this task's copies
+        if (W == 4 && !regs && t == 0) bulk_wait_read();  // the previous task's store has left nb
+        __syncthreads();
+        if (ni < nh) issue(ni, nc, nb);
+        const int32_t d = chunk_len(i, c0);
+        const int64_t f0 = (int64_t)e0s[i] + c0;
+        if constexpr (W == 4) {
+            if (regs) {
+                heavy_task_regs(cb, out + f0 * H, d, deg <= ce ? 0 : (pass == 0 ? 1 : 2), c0 == 0,
+                                np == 1, hl, H, red, m, z);
+                i = ni;
+                pass = np;
+                c0 = nc;
+                continue;
+            }
+        }
+        if (deg <= ce) {
+#pragma unroll
+            for (int w = 0; w < W; ++w) m[w] = -INFINITY, z[w] = 0.f;
             if (hl.active)
 #pragma unroll 4
-                for (int e = hl.grp; e < deg; e += S) {
-                    SVec<W>::ld(hs + e * H + col, v);
+                for (int e = hl.grp; e < d; e += S) {
+                    SVec<W>::ld(cb + e * H + col, v);
 #pragma unroll
                     for (int w = 0; w < W; ++w) m[w] = fmaxf(m[w], v[w]);
                 }
@@ -484,41 +617,39 @@ softmax_heavy_rows_kernel(const int32_t *__restrict__ row_ptr,
             // -inf gets NaN terms and NaN outputs, as the two-pass definition
             if (hl.active)
 #pragma unroll 2
-                for (int e = hl.grp; e < deg; e += S) {
-                    SVec<W>::ld(hs + e * H + col, v);
+                for (int e = hl.grp; e < d; e += S) {
+                    SVec<W>::ld(cb + e * H + col, v);
 #pragma unroll
                     for (int w = 0; w < W; ++w) {
                         v[w] = ex2_approx((v[w] - m[w]) * kLog2e);
                         z[w] += v[w];
                     }
-                    SVec<W>::st(hs + e * H + col, v);
+                    SVec<W>::st(cb + e * H + col, v);
                 }
             head_reduce_block<false, W>(z, hl, red);
 #pragma unroll
             for (int w = 0; w < W; ++w) z[w] = 1.f / z[w];
             if (hl.active)
 #pragma unroll 4
-                for (int e = hl.grp; e < deg; e += S) {
-                    SVec<W>::ld(hs + e * H + col, v);
+                for (int e = hl.grp; e < d; e += S) {
+                    SVec<W>::ld(cb + e * H + col, v);
 #pragma unroll
                     for (int w = 0; w < W; ++w) v[w] *= z[w];
-                    SVec<W>::st(hs + e * H + col, v);
+                    SVec<W>::st(cb + e * H + col, v);
                 }
-            flush(e0, deg);
-            continue;
-        }
-        // first pass: per-thread (max, sum) folded chunk by chunk; a -inf
-        // score adds nothing, so an all -inf head ends with (-inf, 0) and
-        // gets 0 * (1/0) = NaN outputs
-        for (int32_t c0 = 0; c0 < deg; c0 += ce) {
-            const int32_t d = deg - c0 < ce ? deg - c0 : ce;
-            stage(e0 + c0, d);
+            flush(cb, f0, d);
+        } else if (pass == 0) {
+            // fold: a -inf score adds nothing, so an all -inf head ends with
+            // (-inf, 0) and gets 0 * (1/0) = NaN outputs
+            if (c0 == 0)
+#pragma unroll
+                for (int w = 0; w < W; ++w) m[w] = -INFINITY, z[w] = 0.f;
             float cm[W];
 #pragma unroll
             for (int w = 0; w < W; ++w) cm[w] = -INFINITY;
             if (hl.active)
                 for (int e = hl.grp; e < d; e += S) {
-                    SVec<W>::ld(hs + e * H + col, v);
+                    SVec<W>::ld(cb + e * H + col, v);
 #pragma unroll
                     for (int w = 0; w < W; ++w) cm[w] = fmaxf(cm[w], v[w]);
                 }
@@ -530,36 +661,228 @@ softmax_heavy_rows_kernel(const int32_t *__restrict__ row_ptr,
                 }
             if (hl.active)
                 for (int e = hl.grp; e < d; e += S) {
-                    SVec<W>::ld(hs + e * H + col, v);
+                    SVec<W>::ld(cb + e * H + col, v);
 #pragma unroll
                     for (int w = 0; w < W; ++w) z[w] += v[w] == -INFINITY ? 0.f : exp_e(v[w] - m[w]);
                 }
-        }
-        float mg[W];
+            if (np == 1) {  // the row's last chunk: merge over the block
+                float mg[W];
 #pragma unroll
-        for (int w = 0; w < W; ++w) mg[w] = m[w];
-        head_reduce_block<true, W>(mg, hl, red);
+                for (int w = 0; w < W; ++w) mg[w] = m[w];
+                head_reduce_block<true, W>(mg, hl, red);
 #pragma unroll
-        for (int w = 0; w < W; ++w)
-            z[w] = z[w] == 0.f ? 0.f : z[w] * (m[w] == mg[w] ? 1.f : exp_e(m[w] - mg[w]));
-        head_reduce_block<false, W>(z, hl, red);
+                for (int w = 0; w < W; ++w)
+                    z[w] = z[w] == 0.f ? 0.f : z[w] * (m[w] == mg[w] ? 1.f : exp_e(m[w] - mg[w]));
+                head_reduce_block<false, W>(z, hl, red);
 #pragma unroll
-        for (int w = 0; w < W; ++w) z[w] = 1.f / z[w];
-        // second pass: recompute and write
-        for (int32_t c0 = 0; c0 < deg; c0 += ce) {
-            const int32_t d = deg - c0 < ce ? deg - c0 : ce;
-            stage(e0 + c0, d);
+                for (int w = 0; w < W; ++w) m[w] = mg[w], z[w] = 1.f / z[w];
+            }
+        } else {
+            // normalise with the row's (maximum, 1 / sum) in (m, z)
             if (hl.active)
                 for (int e = hl.grp; e < d; e += S) {
-                    SVec<W>::ld(hs + e * H + col, v);
+                    SVec<W>::ld(cb + e * H + col, v);
 #pragma unroll
-                    for (int w = 0; w < W; ++w) v[w] = exp_e(v[w] - mg[w]) * z[w];
-                    SVec<W>::st(hs + e * H + col, v);
+                    for (int w = 0; w < W; ++w) v[w] = exp_e(v[w] - m[w]) * z[w];
+                    SVec<W>::st(cb + e * H + col, v);
                 }
-            flush(e0 + c0, d);
+            flush(cb, f0, d);
+        }
+        i = ni;
+        pass = np;
+        c0 = nc;
+    }
+}
+
+// ---- all rows, H <= 32, one launch
+//
+// Phase 1 (with a plan): the plan's heavy rows longer than a warp's buffer,
+// one block per row over the whole shared buffer (kSpanBlockFloats scores
+// at a time). Block b takes list entries b, b + grid, ...: its threads
+// read 256 of them at once and keep the ones above the buffer, so the rows
+// the light phase owns cost no serial round trips.
+// Phase 2: light rows. A warp takes batches of 32 consecutive rows (one
+// coalesced row_ptr load per batch), fetched from a global counter when the
+// plan provides one (so blocks that had more heavy work take fewer batches),
+// else by a static stride. Consecutive light rows of a batch own one
+// contiguous run of scores; the warp stages such a run (at most kSpanFloats
+// scores) into its buffer, computes it and writes it back with one bulk copy.
+// W = 4 with Q = H/4 a power of two: rows go to register tiers (up to 4 or 8
+// float4s per lane) or, past 8 per lane, to the whole-warp shared-memory
+// routine; otherwise one thread per (row, group of W heads) (Q = H/W groups,
+// R = 32/Q rows at a time, lane = r*Q + q). The last block to finish resets
+// the counters for the next launch on the stream.
+template <int W>
+__global__ void __launch_bounds__(kSoftmaxThreads, 3)
+softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t H,
+                    const float *scores, float *out, int32_t heavy_threshold,
+                    const int32_t *__restrict__ heavy_rows, int64_t n_heavy, int32_t *sched) {
+    extern __shared__ __align__(16) float span_smem[];
+    __shared__ int order_smem[kSoftmaxThreads / 32][32];
+    __shared__ float red[kSoftmaxThreads * 4];
+    __shared__ int32_t h_e0[kHeavyUnit], h_deg[kHeavyUnit];
+    __shared__ int hcount;
+    __shared__ int32_t s_unit;
+    const int t = threadIdx.x, lane = t & 31;
+    const int32_t cap_e = kSpanFloats / H;  // edges per warp buffer
+    if (n_heavy > 0) {
+        // units of kHeavyUnit list entries from the plan's second counter;
+        // the next unit's index is fetched while this one is computed
+        const int32_t ce = kSpanBlockFloats / 2 / H;  // edges per half buffer
+        const int64_t n_units = (n_heavy + kHeavyUnit - 1) / kHeavyUnit;
+        if (t == 0) s_unit = atomicAdd(sched + 1, 1);
+        __syncthreads();
+        int64_t unit = s_unit;
+        __syncthreads();  // every thread has read s_unit before thread 0 rewrites it
+        while (unit < n_units) {
+            if (t < 32) {
+                const int64_t k = unit * kHeavyUnit + t;
+                int32_t e0 = 0, deg = 0;
+                if (t < kHeavyUnit && k < n_heavy) {
+                    const int32_t row = heavy_rows[k];
+                    e0 = row_ptr[row];
+                    deg = row_ptr[row + 1] - e0;
+                }
+                const unsigned hb = __ballot_sync(kFull, deg > cap_e);
+                if (deg > cap_e) {
+                    const int slot = __popc(hb & ((1u << t) - 1u));
+                    h_e0[slot] = e0;
+                    h_deg[slot] = deg;
+                }
+                if (t == 0) {
+                    hcount = __popc(hb);
+                    s_unit = atomicAdd(sched + 1, 1);
+                }
+            }
+            __syncthreads();
+            unit = s_unit;
+            softmax_heavy_rows<W>(h_e0, h_deg, hcount, H, scores, out, span_smem,
+                                  span_smem + kSpanBlockFloats / 2, ce, red);
+            __syncthreads();
+        }
+        if (W == 4 && t == 0) bulk_wait_read();  // the shared buffer is the warps' again
+        __syncthreads();
+    }
+    float *sb = span_smem + (t >> 5) * kSpanFloats;
+    int *order = order_smem[t >> 5];
+    const int Q = H / W, R = 32 / Q;
+    const int r = lane / Q, q = lane - r * Q;
+    const bool tiers = W == 4 && (Q & (Q - 1)) == 0;
+    const int64_t n_batches = (n_rows + 31) / 32;
+    const int64_t n_warps = (int64_t)gridDim.x * (kSoftmaxThreads / 32);
+    const bool dyn = sched != nullptr;
+    auto fetch = [&]() -> int64_t {
+        int32_t b = 0;
+        if (lane == 0) b = atomicAdd(sched, 1);
+        return __shfl_sync(kFull, b, 0);
+    };
+    int64_t b = dyn ? fetch() : (int64_t)blockIdx.x * (kSoftmaxThreads / 32) + (t >> 5);
+    while (b < n_batches) {
+        // the next batch's index is fetched now and used after this one
+        const int64_t b_next = dyn ? fetch() : b + n_warps;
+        const int64_t r0 = b * 32;
+        const int nb = n_rows - r0 < 32 ? (int)(n_rows - r0) : 32;
+        const int32_t e0_lane = row_ptr[r0 + (lane < nb ? lane : nb - 1)];
+        const int32_t rp_end = row_ptr[r0 + nb];
+        const int32_t nxt = __shfl_down_sync(kFull, e0_lane, 1);
+        const int32_t e1_lane = lane + 1 < nb ? nxt : rp_end;
+        const int32_t deg_lane = e1_lane - e0_lane;
+        // a row the staging buffer holds is done here even when the plan
+        // counts it heavy (phase 1 skips such rows)
+        const bool fits = lane < nb && deg_lane <= cap_e;
+        int i0 = 0;
+        while (i0 < nb) {
+            // the run: rows i0 .. i1-1, all light and within one buffer
+            const int32_t base = __shfl_sync(kFull, e0_lane, i0);
+            const bool ok = lane >= i0 && fits && e1_lane - base <= cap_e;
+            const unsigned bad = ~__ballot_sync(kFull, ok) & (0xffffffffu << i0);
+            int i1 = bad ? __ffs(bad) - 1 : 32;
+            if (i1 > nb) i1 = nb;
+            if (i1 == i0) {  // a heavy row, or a light row longer than the buffer
+                const int32_t d = __shfl_sync(kFull, deg_lane, i0);
+                if (d <= heavy_threshold)  // light but too long: straight from global
+                    softmax_row_direct(scores, out, (int64_t)base * H, (int64_t)(base + d) * H, H,
+                                       lane);
+                ++i0;
+                continue;
+            }
+            const int32_t end = __shfl_sync(kFull, e1_lane, i1 - 1);
+            const int64_t x0 = (int64_t)base * H;
+            const int n = (end - base) * H;
+            if (n > 0) {
+                // the buffer's last bulk store has read it
+                if (W == 4 && lane == 0) bulk_wait_read();
+                __syncwarp();
+                stage_in<W>(sb, scores + x0, n, lane, 32);
+                __syncwarp();
+                const unsigned run_mask =
+                    (i1 - i0 == 32 ? 0xffffffffu : ((1u << (i1 - i0)) - 1u)) << i0;
+                const bool in_run = (run_mask >> lane) & 1u;
+                if (tiers) {
+                    const int n4 = deg_lane * Q;
+                    const int need = (n4 + 3) >> 2;  // lanes at 4 float4s each
+                    const int S_lane = need <= Q ? Q : 1 << (32 - __clz(need - 1));
+                    // more than 8 float4s per lane: the whole warp through shared memory
+                    for (unsigned lm = __ballot_sync(kFull, in_run && n4 > 256); lm; lm &= lm - 1u) {
+                        const int i = __ffs(lm) - 1;
+                        const int32_t ri0 = __shfl_sync(kFull, e0_lane, i);
+                        const int32_t ri1 = __shfl_sync(kFull, e1_lane, i);
+                        __syncwarp();
+                        warp_row_softmax4(sb + (ri0 - base) * H, ri1 - ri0, H, lane);
+                    }
+                    // 5 .. 8 float4s per lane: the whole warp, in registers
+                    const unsigned m8 = __ballot_sync(kFull, in_run && n4 > 128 && n4 <= 256);
+                    if (m8)
+                        softmax_tier4<8>(sb, base, H, Q, 32, m8, e0_lane, e1_lane, order, lane);
+                    // up to 4 float4s per lane: tiers of S lanes per row
+                    unsigned rest = __ballot_sync(kFull, in_run && n4 > 0 && n4 <= 128);
+                    while (rest) {
+                        const int S = __shfl_sync(kFull, S_lane, __ffs(rest) - 1);
+                        const unsigned tm = __ballot_sync(kFull, ((rest >> lane) & 1u) && S_lane == S);
+                        rest &= ~tm;
+                        softmax_tier4<4>(sb, base, H, Q, S, tm, e0_lane, e1_lane, order, lane);
+                    }
+                } else {
+                    if (in_run) order[lane - i0] = lane;
+                    __syncwarp();
+                    const int ns = i1 - i0;
+                    for (int g0 = 0; g0 < ns; g0 += R) {
+                        const int slot = g0 + r;
+                        const bool has = r < R && slot < ns;
+                        const int i = has ? order[slot] : 0;
+                        const int32_t ri0 = __shfl_sync(kFull, e0_lane, i);
+                        const int32_t ri1 = __shfl_sync(kFull, e1_lane, i);
+                        if (has) segment_softmax<W>(sb + (ri0 - base) * H + q * W, ri1 - ri0, H);
+                    }
+                }
+                if (W == 4) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) bulk_store(out + x0, sb, (unsigned)n * 4u);
+                } else {
+                    __syncwarp();
+                    for (int j = lane; j < n; j += 32) out[x0 + j] = sb[j];
+                    __syncwarp();
+                }
+            }
+            i0 = i1;
+        }
+        b = b_next;
+    }
+    if (W == 4 && lane == 0) bulk_wait_all();
+    if (dyn) {
+        // every warp of the block has taken its last batch index
+        __syncthreads();
+        if (t == 0) {
+            __threadfence();
+            if (atomicAdd(sched + 2, 1) == (int32_t)gridDim.x - 1) {
+                sched[0] = 0;
+                sched[1] = 0;
+                sched[2] = 0;
+                __threadfence();
+            }
         }
     }
-    if (W == 4 && t == 0) bulk_wait_all();
 }
 
 // H > 32: lanes over edges, one head at a time
@@ -658,6 +981,9 @@ extern "C" gat_status_t gat_edge_softmax(const int32_t *row_ptr, int64_t n_rows,
     // W = 4 heads per thread (16-byte accesses) when the layout allows it
     const bool vec4 = H % 4 == 0 && aligned16(scores) && aligned16(out);
     if (H <= 32) {
+        // one launch: the plan's heavy rows, then light batches; with a plan
+        // the grid is exactly the resident blocks and batches are fetched
+        // from the plan's counter
         auto kern = vec4 ? softmax_rows_kernel<4> : softmax_rows_kernel<1>;
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                kSpanSmemBytes);
@@ -668,10 +994,14 @@ extern "C" gat_status_t gat_edge_softmax(const int32_t *row_ptr, int64_t n_rows,
             per_sm < 1)
             per_sm = 1;
         const int64_t cap = (int64_t)sm_count() * per_sm;
-        if (blocks > cap) blocks = cap;
-        kern<<<(unsigned)blocks, kSoftmaxThreads, kSpanSmemBytes, s>>>(row_ptr, n_rows, H, scores,
-                                                                       out, T);
-    } else {
+        const int64_t n_heavy = plan ? plan->n_heavy : 0;
+        if (blocks > cap || (plan && n_heavy > 0)) blocks = cap;
+        kern<<<(unsigned)blocks, kSoftmaxThreads, kSpanSmemBytes, s>>>(
+            row_ptr, n_rows, H, scores, out, T, plan ? plan->heavy_rows : nullptr, n_heavy,
+            plan ? plan->sched : nullptr);
+        return check_launch("gat_edge_softmax: rows");
+    }
+    {
         const int64_t cap = (int64_t)sm_count() * 8;
         if (blocks > cap) blocks = cap;
         softmax_rows_generic_kernel<<<(unsigned)blocks, kSoftmaxThreads, 0, s>>>(
@@ -681,28 +1011,10 @@ extern "C" gat_status_t gat_edge_softmax(const int32_t *row_ptr, int64_t n_rows,
     if (st != GAT_OK) return st;
     if (plan && plan->n_heavy > 0) {
         int64_t hb = plan->n_heavy;
-        if (H <= 32) {
-            auto hk = vec4 ? softmax_heavy_rows_kernel<4> : softmax_heavy_rows_kernel<1>;
-            const int smem = kHeavySpanFloats * 4;
-            cudaError_t err =
-                cudaFuncSetAttribute(hk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            if (err != cudaSuccess)
-                return cuda_fail(err, "gat_edge_softmax: shared memory attribute");
-            int per_sm = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hk, kHeavyThreads, smem) !=
-                    cudaSuccess ||
-                per_sm < 1)
-                per_sm = 1;
-            const int64_t hcap = (int64_t)sm_count() * per_sm;
-            if (hb > hcap) hb = hcap;
-            hk<<<(unsigned)hb, kHeavyThreads, smem, s>>>(row_ptr, plan->heavy_rows, plan->n_heavy,
-                                                         H, scores, out, kSpanFloats / H);
-        } else {
-            const int64_t hcap = (int64_t)sm_count() * 8;
-            if (hb > hcap) hb = hcap;
-            softmax_heavy_kernel<<<(unsigned)hb, kSoftmaxThreads, 0, s>>>(
-                row_ptr, plan->heavy_rows, plan->n_heavy, H, scores, out);
-        }
+        const int64_t hcap = (int64_t)sm_count() * 8;
+        if (hb > hcap) hb = hcap;
+        softmax_heavy_kernel<<<(unsigned)hb, kSoftmaxThreads, 0, s>>>(
+            row_ptr, plan->heavy_rows, plan->n_heavy, H, scores, out);
         st = check_launch("gat_edge_softmax: heavy rows");
     }
     return st;

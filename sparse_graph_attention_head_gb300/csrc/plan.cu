@@ -297,6 +297,7 @@ extern "C" gat_status_t gat_plan_destroy(gat_plan_t p) {
     cudaFree(p->chunk_row);
     cudaFree(p->counters);
     cudaFree(p->chunk_desc);
+    cudaFree(p->sched);
     delete p;
     return GAT_OK;
 }
@@ -359,6 +360,8 @@ extern "C" gat_status_t gat_plan_create(const int32_t *row_ptr, int64_t n_rows, 
     if (e == cudaSuccess && p->n_heavy) e = cudaMalloc(&p->counters, p->n_heavy * sizeof(int32_t));
     if (e == cudaSuccess && p->n_chunks) e = cudaMalloc(&p->chunk_row, p->n_chunks * sizeof(int32_t));
     if (e == cudaSuccess && p->n_chunks) e = cudaMalloc(&p->chunk_desc, p->n_chunks * sizeof(int4));
+    if (e == cudaSuccess) e = cudaMalloc(&p->sched, 4 * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->sched, 0, 4 * sizeof(int32_t), s);
     if (e == cudaSuccess && p->n_heavy)
         e = cudaMemsetAsync(p->counters, 0, p->n_heavy * sizeof(int32_t), s);
     if (e != cudaSuccess) {
