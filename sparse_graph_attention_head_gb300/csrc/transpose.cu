@@ -9,10 +9,11 @@
 // Build (once per graph, on the device):
 //   count edges per source (integer atomics) -> exclusive scan = src_ptr
 //   scatter edge ids into their source's group (integer atomics: any order)
-//   order every group by edge id: log2(max group size) rank-merge passes, in
-//     which each element finds its place in the merged pair of runs by a
-//     binary search in the partner run (edge ids are distinct, so every
-//     place is unique)
+//   order every group by edge id: a warp sorts each run of 32 (bitonic, in
+//     registers), then log2(max group size / 32) rank-merge passes, in which
+//     each element finds its place in the merged pair of runs by a binary
+//     search in the partner run (edge ids are distinct, so every place is
+//     unique)
 //   dst[k] = the row owning edge perm[k]
 //   a degree plan over src_ptr for sources with many edges.
 #include <climits>
@@ -134,20 +135,57 @@ tr_fill_kernel(const int32_t *__restrict__ col_idx, int64_t E, int32_t *__restri
         perm[atomicAdd(cursor + col_idx[e], 1)] = (int32_t)e;
 }
 
-// seg[k] = the source owning position k; largest group size into *max_deg
+// seg[k] = the source owning position k
 __global__ void __launch_bounds__(kTrThreads)
-tr_seg_kernel(const int32_t *__restrict__ src_ptr, int64_t n_src, int32_t *__restrict__ seg,
-              int32_t *__restrict__ max_deg) {
+tr_seg_kernel(const int32_t *__restrict__ src_ptr, int64_t n_src, int32_t *__restrict__ seg) {
     const int lane = threadIdx.x & 31;
     const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    int32_t local_max = 0;
     for (int64_t j = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); j < n_src;
          j += n_warps) {
         const int32_t k0 = src_ptr[j], k1 = src_ptr[j + 1];
         for (int32_t k = k0 + lane; k < k1; k += 32) seg[k] = (int32_t)j;
-        local_max = max(local_max, k1 - k0);
     }
-    if (lane == 0 && local_max > 0) atomicMax(max_deg, local_max);
+}
+
+// largest count into *max_deg
+__global__ void __launch_bounds__(kTrThreads)
+tr_max_kernel(const int32_t *__restrict__ cnt, int64_t n, int32_t *__restrict__ max_deg) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int32_t m = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+        m = max(m, cnt[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(kFull, m, o));
+    if ((threadIdx.x & 31) == 0 && m > 0) atomicMax(max_deg, m);
+}
+
+// Every run of 32 positions of a group (from the group's start) sorted
+// ascending, one warp per group: a bitonic network over the lanes (lanes past
+// the group's end hold INT_MAX, above every edge id).
+__global__ void __launch_bounds__(kTrThreads)
+tr_sort32_kernel(int32_t *__restrict__ perm, const int32_t *__restrict__ src_ptr, int64_t n_src) {
+    const int lane = threadIdx.x & 31;
+    const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t j = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); j < n_src;
+         j += n_warps) {
+        const int32_t k0 = src_ptr[j], k1 = src_ptr[j + 1];
+        if (k1 - k0 < 2) continue;
+        for (int32_t r0 = k0; r0 < k1; r0 += 32) {
+            const int32_t k = r0 + lane;
+            int32_t v = k < k1 ? perm[k] : INT_MAX;
+#pragma unroll
+            for (int w = 2; w <= 32; w <<= 1)
+#pragma unroll
+                for (int o = w >> 1; o > 0; o >>= 1) {
+                    const int32_t x = __shfl_xor_sync(kFull, v, o);
+                    // ascending within blocks of w lanes with (lane & w) == 0, descending
+                    // in the others; the lower lane of a pair keeps the block's order
+                    const bool up = (lane & w) == 0, lower = (lane & o) == 0;
+                    v = (lower == up) ? min(v, x) : max(v, x);
+                }
+            if (k < k1) perm[k] = v;
+        }
+    }
 }
 
 // One merge pass: runs of length L inside every group are merged pairwise.
@@ -232,82 +270,96 @@ extern "C" gat_status_t gat_transpose_create(const int32_t *row_ptr, const int32
     t->n_src = n_src;
     t->n_edges = E;
     cudaGetDevice(&t->device);
-    int32_t *cnt = nullptr, *row_of = nullptr, *tmp = nullptr, *seg = nullptr, *flags = nullptr;
-    int64_t *sums = nullptr;
-    int32_t host_flags[2] = {0, 0};
+    // one scratch block: counts / cursors [n_src + 1], flags [2] (bad index,
+    // largest group), scan tile sums, and for E > 0 row_of, tmp and seg [E]
     const int64_t nb = (n_src + 1 + kScanTile - 1) / kScanTile;
+    const size_t o_flags = (size_t)(n_src + 1) * 4;
+    const size_t o_sums = (o_flags + 8 + 15) & ~(size_t)15;
+    const size_t o_row_of = (o_sums + (size_t)nb * 8 + 15) & ~(size_t)15;
+    const size_t o_tmp = o_row_of + (size_t)E * 4;
+    const size_t o_seg = o_tmp + (size_t)E * 4;
+    const size_t scratch_bytes = o_seg + (size_t)E * 4;
+    unsigned char *scratch = nullptr;
+    int32_t host_flags[2] = {0, 0};
     gat_status_t st = GAT_OK;
     cudaError_t e = cudaMalloc(&t->src_ptr, (n_src + 1) * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMalloc(&t->perm, (E > 0 ? E : 1) * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMalloc(&t->dst, (E > 0 ? E : 1) * sizeof(int32_t));
-    if (e == cudaSuccess) e = cudaMalloc(&cnt, (n_src + 1) * sizeof(int32_t));
-    if (e == cudaSuccess) e = cudaMalloc(&sums, nb * sizeof(int64_t));
-    if (e == cudaSuccess) e = cudaMalloc(&flags, 2 * sizeof(int32_t));
-    if (e == cudaSuccess && E > 0) e = cudaMalloc(&row_of, E * sizeof(int32_t));
-    if (e == cudaSuccess && E > 0) e = cudaMalloc(&tmp, E * sizeof(int32_t));
-    if (e == cudaSuccess && E > 0) e = cudaMalloc(&seg, E * sizeof(int32_t));
-    if (e == cudaSuccess) e = cudaMemsetAsync(cnt, 0, (n_src + 1) * sizeof(int32_t), s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(flags, 0, 2 * sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaMalloc(&scratch, scratch_bytes);
+    if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, o_flags + 8, s);  // counts and flags
     if (e != cudaSuccess) {
         st = cuda_fail(e, "gat_transpose_create: allocation");
         goto done;
     }
-    if (E > 0) {
-        // counts; an out-of-range column index stops the build here
-        tr_count_kernel<<<grid_for(E, kTrThreads), kTrThreads, 0, s>>>(col_idx, E, n_src, cnt,
-                                                                         flags);
-        if ((st = check_launch("gat_transpose_create: count")) != GAT_OK) goto done;
-        e = cudaMemcpyAsync(host_flags, flags, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    {
+        int32_t *cnt = reinterpret_cast<int32_t *>(scratch);
+        int32_t *flags = reinterpret_cast<int32_t *>(scratch + o_flags);
+        int64_t *sums = reinterpret_cast<int64_t *>(scratch + o_sums);
+        int32_t *row_of = reinterpret_cast<int32_t *>(scratch + o_row_of);
+        int32_t *tmp = reinterpret_cast<int32_t *>(scratch + o_tmp);
+        int32_t *seg = reinterpret_cast<int32_t *>(scratch + o_seg);
+        if (E > 0) {
+            // counts and the largest group; an out-of-range column index stops
+            // the build here
+            tr_count_kernel<<<grid_for(E, kTrThreads), kTrThreads, 0, s>>>(col_idx, E, n_src, cnt,
+                                                                             flags);
+            tr_max_kernel<<<grid_for(n_src, kTrThreads), kTrThreads, 0, s>>>(cnt, n_src, flags + 1);
+            if ((st = check_launch("gat_transpose_create: count")) != GAT_OK) goto done;
+            e = cudaMemcpyAsync(host_flags, flags, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+            if (e != cudaSuccess) {
+                st = cuda_fail(e, "gat_transpose_create: count");
+                goto done;
+            }
+            if (host_flags[0]) {
+                st = fail(GAT_ERR_INDEX_OUT_OF_RANGE,
+                          "gat_transpose_create: a column index is outside [0, n_src)");
+                goto done;
+            }
+            t->max_src_degree = host_flags[1];
+        }
+        e = exclusive_scan(cnt, t->src_ptr, n_src + 1, sums, s);
         if (e != cudaSuccess) {
-            st = cuda_fail(e, "gat_transpose_create: count");
+            st = cuda_fail(e, "gat_transpose_create: scan");
             goto done;
         }
-        if (host_flags[0]) {
-            st = fail(GAT_ERR_INDEX_OUT_OF_RANGE,
-                      "gat_transpose_create: a column index is outside [0, n_src)");
-            goto done;
+        if (E > 0) {
+            e = cudaMemcpyAsync(cnt, t->src_ptr, n_src * sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                                s);
+            if (e != cudaSuccess) {
+                st = cuda_fail(e, "gat_transpose_create: cursor copy");
+                goto done;
+            }
+            const unsigned rw = grid_for(n_rows * 32, kTrThreads);
+            tr_row_of_kernel<<<rw, kTrThreads, 0, s>>>(row_ptr, n_rows, row_of);
+            tr_fill_kernel<<<grid_for(E, kTrThreads), kTrThreads, 0, s>>>(col_idx, E, cnt, t->perm);
+            tr_sort32_kernel<<<grid_for(n_src * 32, kTrThreads), kTrThreads, 0, s>>>(
+                t->perm, t->src_ptr, n_src);
+            if ((st = check_launch("gat_transpose_create: fill")) != GAT_OK) goto done;
+            int32_t *a = t->perm, *b = tmp;
+            if (t->max_src_degree > 32) {
+                tr_seg_kernel<<<grid_for(n_src * 32, kTrThreads), kTrThreads, 0, s>>>(
+                    t->src_ptr, n_src, seg);
+                for (int64_t L = 32; L < t->max_src_degree; L <<= 1) {
+                    tr_merge_kernel<<<grid_for(E, kTrThreads), kTrThreads, 0, s>>>(
+                        a, b, seg, t->src_ptr, E, L);
+                    int32_t *c = a;
+                    a = b;
+                    b = c;
+                }
+                if ((st = check_launch("gat_transpose_create: merge")) != GAT_OK) goto done;
+            }
+            if (a != t->perm) {  // the sorted order ended in the scratch buffer
+                e = cudaMemcpyAsync(t->perm, a, E * sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
+                if (e != cudaSuccess) {
+                    st = cuda_fail(e, "gat_transpose_create: order copy");
+                    goto done;
+                }
+            }
+            tr_dst_kernel<<<grid_for(E, kTrThreads), kTrThreads, 0, s>>>(t->perm, row_of, E,
+                                                                         t->dst);
+            if ((st = check_launch("gat_transpose_create: dst")) != GAT_OK) goto done;
         }
-    }
-    e = exclusive_scan(cnt, t->src_ptr, n_src + 1, sums, s);
-    if (e != cudaSuccess) {
-        st = cuda_fail(e, "gat_transpose_create: scan");
-        goto done;
-    }
-    if (E > 0) {
-        e = cudaMemcpyAsync(cnt, t->src_ptr, n_src * sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
-        if (e != cudaSuccess) {
-            st = cuda_fail(e, "gat_transpose_create: cursor copy");
-            goto done;
-        }
-        const unsigned rw = grid_for(n_rows * 32, kTrThreads);
-        tr_row_of_kernel<<<rw, kTrThreads, 0, s>>>(row_ptr, n_rows, row_of);
-        tr_fill_kernel<<<grid_for(E, kTrThreads), kTrThreads, 0, s>>>(col_idx, E, cnt, t->perm);
-        tr_seg_kernel<<<grid_for(n_src * 32, kTrThreads), kTrThreads, 0, s>>>(t->src_ptr, n_src,
-                                                                              seg, flags + 1);
-        if ((st = check_launch("gat_transpose_create: fill")) != GAT_OK) goto done;
-        e = cudaMemcpyAsync(host_flags + 1, flags + 1, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-        if (e != cudaSuccess) {
-            st = cuda_fail(e, "gat_transpose_create: fill");
-            goto done;
-        }
-        t->max_src_degree = host_flags[1];
-        int32_t *a = t->perm, *b = tmp;
-        for (int64_t L = 1; L < t->max_src_degree; L <<= 1) {
-            tr_merge_kernel<<<grid_for(E, kTrThreads), kTrThreads, 0, s>>>(a, b, seg, t->src_ptr,
-                                                                           E, L);
-            int32_t *c = a;
-            a = b;
-            b = c;
-        }
-        if ((st = check_launch("gat_transpose_create: merge")) != GAT_OK) goto done;
-        if (a != t->perm) {  // the sorted order ended in the scratch buffer
-            tmp = t->perm;
-            t->perm = a;
-        }
-        tr_dst_kernel<<<grid_for(E, kTrThreads), kTrThreads, 0, s>>>(t->perm, row_of, E, t->dst);
-        if ((st = check_launch("gat_transpose_create: dst")) != GAT_OK) goto done;
     }
     st = gat_plan_create(t->src_ptr, n_src, E, 0, 0, stream, &t->src_plan);
 done:
@@ -317,12 +369,7 @@ done:
     } else {
         cudaStreamSynchronize(s);
     }
-    cudaFree(cnt);
-    cudaFree(sums);
-    cudaFree(flags);
-    cudaFree(row_of);
-    cudaFree(tmp);
-    cudaFree(seg);
+    cudaFree(scratch);
     if (st != GAT_OK) {
         gat_transpose_destroy(t);
         return st;

@@ -70,6 +70,30 @@ def test_edge_softmax_heads_in_place_and_long_rows(gat, H):
         assert_fp32(host(buf), o, name=f"edge_softmax H={H}")
 
 
+def test_edge_softmax_plan_reused_across_calls_and_head_counts(gat):
+    """One plan serves consecutive launches: its work counters are reset by
+    the last block of each launch. Every call writes into a NaN-filled
+    buffer, so a batch or heavy row skipped by a stale counter would show."""
+    deg = W.zipf_degrees(np.random.default_rng(21), 20_000, dmax=3000, mean=16.0)
+    deg[[5, 6, 7]] = [2500, 1100, 300]  # heavy rows: two-pass, one-pass, just past a warp buffer
+    rp_h = np.concatenate([[0], np.cumsum(deg)]).astype(np.int32)
+    rp = dev(rp_h)
+    plan = gat.Plan(rp)
+    first = {}
+    for H in (8, 4, 8, 16, 8):
+        d = W.make_edge_softmax(seed=70 + H, deg=deg, H=H)
+        s = dev(d["scores"])
+        out = torch.full_like(s, float("nan"))
+        gat.gat_edge_softmax(rp, s, H, out=out, plan=plan)
+        g = host(out)
+        if H not in first:
+            first[H] = g
+            assert_fp32(g, oracle.edge_softmax(d["row_ptr"], d["scores"], H),
+                        name=f"edge_softmax plan reuse H={H}")
+        else:  # deterministic: the same launch gives the same bits
+            assert np.array_equal(g, first[H])
+
+
 def test_edge_softmax_extreme_scores_and_neg_inf_row(gat):
     rp_h = np.array([0, 3, 5, 8], np.int32)
     s_h = np.array([[80.0], [-80.0], [79.0], [-np.inf], [-np.inf], [3.0], [3.0], [3.0]],
