@@ -6,8 +6,8 @@
 // contiguous run of deg*H floats, and consecutive rows' runs are adjacent.
 // H <= 32 is one launch of softmax_rows_kernel, a grid of the resident
 // blocks (8 warps, 64 KB of staging buffer each):
-//   phase 1 (with a plan): the plan's heavy rows longer than a warp buffer,
-//     fetched 8 list entries at a time from a counter in the plan, one block
+//   phase 1 (with a plan): the plan's heavy rows longer than two warp
+//     buffers, fetched 8 list entries at a time from a counter in the plan, one block
 //     per row, streamed through two 32 KB halves of the block buffer (the
 //     next chunk's copies in flight while this one is computed); rows longer
 //     than a half are read twice (fold, then normalise);
@@ -21,10 +21,11 @@
 // copies and plain stores. With W = 4 and Q = H/4 a power of two, a light
 // row goes to a sub-warp of S lanes (S = Q .. 32, a power of two) holding up
 // to 4 float4s per lane in registers, or 8 per lane with the whole warp, or
-// past that to the whole warp through shared memory; other layouts use one
-// thread per (row, group of W heads). A light row longer than the buffer
-// (possible without a plan, or with a large threshold) is read straight from
-// global memory by the whole warp. H > 32 takes the head-at-a-time kernels
+// past that to the whole warp through shared memory; a row of up to two
+// buffers streams through the warp's buffer twice (fold, then normalise);
+// other layouts use one thread per (row, group of W heads). A light row
+// longer than that (possible without a plan, or with a large threshold) is
+// read straight from global memory by the whole warp. H > 32 takes the head-at-a-time kernels
 // further down. The last block to finish resets the plan's counters, so a
 // plan serves one launch at a time.
 // out may alias scores: every score of a row (or chunk) is read before its
@@ -40,6 +41,7 @@ constexpr int kSpanFloats = 2048;        // light-row staging buffer per warp (8
 constexpr int kSpanBlockFloats = kSoftmaxThreads / 32 * kSpanFloats;  // heavy rows: 2 chunks
 constexpr int kHeavyUnit = 8;            // heavy-list entries per fetch
 constexpr int kHeavyRegs = 8;            // heavy rows: float4s per thread and chunk
+constexpr int kMediumChunks = 2;         // rows up to this many warp buffers: one warp
 constexpr int kSpanSmemBytes = kSpanBlockFloats * 4;
 constexpr int kSoftmaxCache = 8;         // direct path: loads per thread per tile
 constexpr float kLog2e = 1.4426950408889634f;
@@ -373,6 +375,90 @@ __device__ __forceinline__ void softmax_tier4(float *sb, int32_t base, int H, in
         }
     }
     __syncwarp();
+}
+
+// A row of d edges (first edge e0) longer than the warp buffer by the warp
+// alone (W = 4, Q a power of two): its run streams through the buffer sb in
+// chunks of cap_e edges twice. Fold pass: lane l holds float4s l, l+32, ...
+// of a chunk (head group l % Q); per chunk the lane's maximum, then its exp
+// terms against the running maximum (the running sum rescaled when the
+// maximum grows); the lanes of a head group then merge their (max, sum)
+// pairs with xor-shuffles. Normalise pass: the chunk again (the second read
+// of a run the warp has just read), exp terms scaled by 1/sum, written back
+// with one bulk copy per chunk. A head whose scores are all -inf keeps sum 0
+// and gets NaN outputs, as the two-pass definition.
+__device__ __noinline__ void softmax_row_medium4(const float *scores, float *out, float *sb,
+                                                 int64_t e0, int32_t d, int32_t H, int32_t cap_e,
+                                                 int lane) {
+    const int Q = H >> 2;
+    float4 m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 *p4 = reinterpret_cast<const float4 *>(sb);
+    auto stage = [&](int32_t c0, int32_t dc) {
+        if (lane == 0) bulk_wait_read();  // the buffer's last bulk store has read it
+        __syncwarp();
+        stage_in<4>(sb, scores + (e0 + c0) * H, dc * H, lane, 32);
+        __syncwarp();
+    };
+    auto fold1 = [](float &mw, float &zw, float cm) {
+        if (cm > mw) {
+            zw = zw == 0.f ? 0.f : zw * ex2_approx((mw - cm) * kLog2e);
+            mw = cm;
+        }
+    };
+    for (int32_t c0 = 0; c0 < d; c0 += cap_e) {
+        const int32_t dc = d - c0 < cap_e ? d - c0 : cap_e;
+        const int n4 = dc * Q;
+        stage(c0, dc);
+        float4 cm = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        for (int j = lane; j < n4; j += 32) cm = max4(cm, p4[j]);
+        fold1(m.x, z.x, cm.x);
+        fold1(m.y, z.y, cm.y);
+        fold1(m.z, z.z, cm.z);
+        fold1(m.w, z.w, cm.w);
+        // with m = -inf every score so far is -inf: the terms stay 0
+        const float4 mm = make_float4(m.x == -INFINITY ? 0.f : m.x, m.y == -INFINITY ? 0.f : m.y,
+                                      m.z == -INFINITY ? 0.f : m.z, m.w == -INFINITY ? 0.f : m.w);
+        for (int j = lane; j < n4; j += 32) {
+            const float4 v = p4[j];
+            z.x += ex2_approx((v.x - mm.x) * kLog2e);
+            z.y += ex2_approx((v.y - mm.y) * kLog2e);
+            z.z += ex2_approx((v.z - mm.z) * kLog2e);
+            z.w += ex2_approx((v.w - mm.w) * kLog2e);
+        }
+    }
+    // merge the head group's lanes (offsets 16 .. Q keep l % Q)
+    auto merge1 = [](float &mw, float &zw, float mo, float zo) {
+        const float mx = fmaxf(mw, mo);
+        const float a = zw == 0.f ? 0.f : zw * ex2_approx((mw - mx) * kLog2e);
+        const float b = zo == 0.f ? 0.f : zo * ex2_approx((mo - mx) * kLog2e);
+        mw = mx;
+        zw = a + b;
+    };
+    for (int o = 16; o >= Q; o >>= 1) {
+        const float4 mo = shfl_xor4(m, o), zo = shfl_xor4(z, o);
+        merge1(m.x, z.x, mo.x, zo.x);
+        merge1(m.y, z.y, mo.y, zo.y);
+        merge1(m.z, z.z, mo.z, zo.z);
+        merge1(m.w, z.w, mo.w, zo.w);
+    }
+    const float4 inv = make_float4(rcp_approx(z.x), rcp_approx(z.y), rcp_approx(z.z), rcp_approx(z.w));
+    float4 *q4 = reinterpret_cast<float4 *>(sb);
+    for (int32_t c0 = 0; c0 < d; c0 += cap_e) {
+        const int32_t dc = d - c0 < cap_e ? d - c0 : cap_e;
+        const int n4 = dc * Q;
+        stage(c0, dc);
+        for (int j = lane; j < n4; j += 32) {
+            const float4 v = q4[j];
+            q4[j] = make_float4(ex2_approx((v.x - m.x) * kLog2e) * inv.x,
+                                ex2_approx((v.y - m.y) * kLog2e) * inv.y,
+                                ex2_approx((v.z - m.z) * kLog2e) * inv.z,
+                                ex2_approx((v.w - m.w) * kLog2e) * inv.w);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) bulk_store(out + (e0 + c0) * H, sb, (unsigned)(dc * H) * 4u);
+    }
 }
 
 // ---- heavy rows, H <= 32
@@ -725,6 +811,10 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
     __shared__ int32_t s_unit;
     const int t = threadIdx.x, lane = t & 31;
     const int32_t cap_e = kSpanFloats / H;  // edges per warp buffer
+    // rows up to cap_m edges are the warps' (two passes through the buffer,
+    // W = 4 with Q a power of two); longer ones phase 1's
+    const bool tiers = W == 4 && ((H / W) & (H / W - 1)) == 0;
+    const int32_t cap_m = tiers ? kMediumChunks * cap_e : cap_e;
     if (n_heavy > 0) {
         // units of kHeavyUnit list entries from the plan's second counter;
         // the next unit's index is fetched while this one is computed
@@ -743,8 +833,8 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
                     e0 = row_ptr[row];
                     deg = row_ptr[row + 1] - e0;
                 }
-                const unsigned hb = __ballot_sync(kFull, deg > cap_e);
-                if (deg > cap_e) {
+                const unsigned hb = __ballot_sync(kFull, deg > cap_m);
+                if (deg > cap_m) {
                     const int slot = __popc(hb & ((1u << t) - 1u));
                     h_e0[slot] = e0;
                     h_deg[slot] = deg;
@@ -767,7 +857,6 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
     int *order = order_smem[t >> 5];
     const int Q = H / W, R = 32 / Q;
     const int r = lane / Q, q = lane - r * Q;
-    const bool tiers = W == 4 && (Q & (Q - 1)) == 0;
     const int64_t n_batches = (n_rows + 31) / 32;
     const int64_t n_warps = (int64_t)gridDim.x * (kSoftmaxThreads / 32);
     const bool dyn = sched != nullptr;
@@ -800,7 +889,9 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
             if (i1 > nb) i1 = nb;
             if (i1 == i0) {  // a heavy row, or a light row longer than the buffer
                 const int32_t d = __shfl_sync(kFull, deg_lane, i0);
-                if (d <= heavy_threshold)  // light but too long: straight from global
+                if (tiers && d <= cap_m)  // up to kMediumChunks buffers: the warp, two passes
+                    softmax_row_medium4(scores, out, sb, base, d, H, cap_e, lane);
+                else if (d <= heavy_threshold)  // light but too long: straight from global
                     softmax_row_direct(scores, out, (int64_t)base * H, (int64_t)(base + d) * H, H,
                                        lane);
                 ++i0;
