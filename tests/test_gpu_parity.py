@@ -94,6 +94,61 @@ def test_edge_softmax_plan_reused_across_calls_and_head_counts(gat):
             assert np.array_equal(g, first[H])
 
 
+@pytest.mark.parametrize("H", [8, 4, 32])
+def test_edge_softmax_neg_inf_heads_on_every_row_path(gat, H):
+    """-inf scores on every row path of the 8-head kernel (thread tiers, the
+    8-per-lane warp tier, the whole-warp shared-memory rows, rows streamed
+    twice through a warp buffer, one-chunk and multi-chunk block rows; the
+    warp-from-global rows without a plan): head 0 of every row all -inf (NaN,
+    as the two-pass definition), head 1 -inf but for one edge (that edge 1,
+    the rest 0), head 2 -inf on every other edge; scores ~ N(0, 30^2)."""
+    deg = np.array([3, 8, 9, 100, 200, 300, 600, 1500, 3000, 0, 2, 40], np.int32)
+    rng = np.random.default_rng(11 + H)
+    rp_h = np.concatenate([[0], np.cumsum(deg)]).astype(np.int32)
+    E = int(rp_h[-1])
+    s_h = rng.normal(0.0, 30.0, size=(E, H)).astype(np.float32)
+    for r in range(deg.size):
+        e0, e1 = rp_h[r], rp_h[r + 1]
+        if e1 == e0:
+            continue
+        s_h[e0:e1, 0] = -np.inf
+        keep = e0 + (e1 - e0) // 2
+        s_h[e0:e1, 1] = -np.inf
+        s_h[keep, 1] = 5.0
+        s_h[e0:e1:2, 2] = -np.inf
+    o = oracle.edge_softmax(rp_h, s_h, H)
+    rp = dev(rp_h)
+    for plan in (None, gat.Plan(rp)):
+        buf = dev(s_h)
+        gat.gat_edge_softmax(rp, buf, H, out=buf, plan=plan)  # in place
+        g = host(buf)
+        assert_fp32(g, o, name=f"edge_softmax -inf heads H={H} plan={plan is not None}")
+        for r in range(deg.size):
+            e0, e1 = rp_h[r], rp_h[r + 1]
+            if e1 > e0:
+                assert np.isnan(g[e0:e1, 0]).all()
+                assert abs(g[e0 + (e1 - e0) // 2, 1] - 1.0) <= 1e-6
+
+
+def test_edge_softmax_unaligned_buffers(gat):
+    """Scores and output 4 bytes off a 16-byte boundary (H = 8): the 4-byte
+    copy path, with and without a plan, against the oracle."""
+    deg = np.array([5, 0, 300, 40, 2000, 7, 129, 1], np.int32)
+    d = W.make_edge_softmax(seed=91, deg=deg, H=8)
+    rp = dev(d["row_ptr"])
+    o = oracle.edge_softmax(d["row_ptr"], d["scores"], 8)
+    E = d["scores"].shape[0]
+    for plan in (None, gat.Plan(rp)):
+        sbuf = torch.empty(E * 8 + 1, device=DEV)
+        obuf = torch.empty(E * 8 + 1, device=DEV)
+        s = sbuf[1:].view(E, 8)
+        s.copy_(dev(d["scores"]))
+        out = obuf[1:].view(E, 8)
+        assert s.data_ptr() % 16 != 0 and out.data_ptr() % 16 != 0
+        gat.gat_edge_softmax(rp, s, 8, out=out, plan=plan)
+        assert_fp32(host(out), o, name="edge_softmax unaligned")
+
+
 def test_edge_softmax_extreme_scores_and_neg_inf_row(gat):
     rp_h = np.array([0, 3, 5, 8], np.int32)
     s_h = np.array([[80.0], [-80.0], [79.0], [-np.inf], [-np.inf], [3.0], [3.0], [3.0]],
