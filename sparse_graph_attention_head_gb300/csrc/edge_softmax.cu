@@ -6,8 +6,8 @@
 // contiguous run of deg*H floats, and consecutive rows' runs are adjacent.
 // H <= 32 is one launch of softmax_rows_kernel, a grid of the resident
 // blocks (8 warps, 64 KB of staging buffer each):
-//   phase 1 (with a plan): the plan's heavy rows longer than two warp
-//     buffers, fetched 8 list entries at a time from a counter in the plan, one block
+//   phase 1 (with a plan): the plan's heavy rows longer than a warp buffer,
+//     fetched 8 list entries at a time from a counter in the plan, one block
 //     per row, streamed through two 32 KB halves of the block buffer (the
 //     next chunk's copies in flight while this one is computed); rows longer
 //     than a half are read twice (fold, then normalise);
@@ -21,8 +21,9 @@
 // copies and plain stores. With W = 4 and Q = H/4 a power of two, a light
 // row goes to a sub-warp of S lanes (S = Q .. 32, a power of two) holding up
 // to 4 float4s per lane in registers, or 8 per lane with the whole warp, or
-// past that to the whole warp through shared memory; a row of up to two
-// buffers streams through the warp's buffer twice (fold, then normalise);
+// past that to the whole warp through shared memory; a row the plan does not
+// call heavy (any row without a plan) of up to two buffers streams through
+// the warp's buffer twice (fold, then normalise);
 // other layouts use one thread per (row, group of W heads). A light row
 // longer than that (possible without a plan, or with a large threshold) is
 // read straight from global memory by the whole warp. H > 32 takes the head-at-a-time kernels
@@ -811,8 +812,9 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
     __shared__ int32_t s_unit;
     const int t = threadIdx.x, lane = t & 31;
     const int32_t cap_e = kSpanFloats / H;  // edges per warp buffer
-    // rows up to cap_m edges are the warps' (two passes through the buffer,
-    // W = 4 with Q a power of two); longer ones phase 1's
+    // light rows up to cap_m edges that the buffer does not hold are the
+    // warps' (two passes through the buffer, W = 4 with Q a power of two);
+    // the plan's heavy rows beyond the buffer are phase 1's
     const bool tiers = W == 4 && ((H / W) & (H / W - 1)) == 0;
     const int32_t cap_m = tiers ? kMediumChunks * cap_e : cap_e;
     if (n_heavy > 0) {
@@ -833,8 +835,8 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
                     e0 = row_ptr[row];
                     deg = row_ptr[row + 1] - e0;
                 }
-                const unsigned hb = __ballot_sync(kFull, deg > cap_m);
-                if (deg > cap_m) {
+                const unsigned hb = __ballot_sync(kFull, deg > cap_e);
+                if (deg > cap_e) {
                     const int slot = __popc(hb & ((1u << t) - 1u));
                     h_e0[slot] = e0;
                     h_deg[slot] = deg;
@@ -889,7 +891,7 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
             if (i1 > nb) i1 = nb;
             if (i1 == i0) {  // a heavy row, or a light row longer than the buffer
                 const int32_t d = __shfl_sync(kFull, deg_lane, i0);
-                if (tiers && d <= cap_m)  // up to kMediumChunks buffers: the warp, two passes
+                if (tiers && d <= cap_m && d <= heavy_threshold)  // the warp, two passes
                     softmax_row_medium4(scores, out, sb, base, d, H, cap_e, lane);
                 else if (d <= heavy_threshold)  // light but too long: straight from global
                     softmax_row_direct(scores, out, (int64_t)base * H, (int64_t)(base + d) * H, H,
