@@ -784,21 +784,25 @@ __device__ __forceinline__ void softmax_heavy_rows(const int32_t *e0s, const int
 // ---- all rows, H <= 32, one launch
 //
 // Phase 1 (with a plan): the plan's heavy rows longer than a warp's buffer,
-// one block per row over the whole shared buffer (kSpanBlockFloats scores
-// at a time). Block b takes list entries b, b + grid, ...: its threads
-// read 256 of them at once and keep the ones above the buffer, so the rows
-// the light phase owns cost no serial round trips.
+// one block per row. A block takes kHeavyUnit list entries at a time from
+// the plan's heavy counter (the next unit's index requested while this one
+// runs); its first warp reads the unit's entries at once and keeps the rows
+// above the buffer, so rows the light phase owns cost no serial round trips.
+// The kept rows stream through the two halves of the block's buffer
+// (softmax_heavy_rows).
 // Phase 2: light rows. A warp takes batches of 32 consecutive rows (one
-// coalesced row_ptr load per batch), fetched from a global counter when the
-// plan provides one (so blocks that had more heavy work take fewer batches),
-// else by a static stride. Consecutive light rows of a batch own one
-// contiguous run of scores; the warp stages such a run (at most kSpanFloats
-// scores) into its buffer, computes it and writes it back with one bulk copy.
-// W = 4 with Q = H/4 a power of two: rows go to register tiers (up to 4 or 8
-// float4s per lane) or, past 8 per lane, to the whole-warp shared-memory
-// routine; otherwise one thread per (row, group of W heads) (Q = H/W groups,
-// R = 32/Q rows at a time, lane = r*Q + q). The last block to finish resets
-// the counters for the next launch on the stream.
+// coalesced row_ptr load per batch), fetched from the plan's batch counter
+// when there is a plan (so blocks that had more heavy work take fewer
+// batches), else by a static stride. Consecutive light rows of a batch own
+// one contiguous run of scores; the warp stages such a run (at most
+// kSpanFloats scores) into its buffer, computes it and writes it back with
+// one bulk copy. W = 4 with Q = H/4 a power of two: rows go to register
+// tiers (up to 4 or 8 float4s per lane) or, past 8 per lane, to the
+// whole-warp shared-memory routine, and a row beyond the buffer that the
+// plan does not call heavy (up to kMediumChunks buffers) streams through
+// the warp's buffer twice; otherwise one thread per (row, group of W heads)
+// (Q = H/W groups, R = 32/Q rows at a time, lane = r*Q + q). The last block
+// to finish resets the counters for the next launch on the stream.
 template <int W>
 __global__ void __launch_bounds__(kSoftmaxThreads, 3)
 softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t H,
