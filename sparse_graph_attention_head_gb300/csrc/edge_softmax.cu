@@ -21,14 +21,15 @@
 // copies and plain stores. With W = 4 and Q = H/4 a power of two, a light
 // row goes to a sub-warp of S lanes (S = Q .. 32, a power of two) holding up
 // to 4 float4s per lane in registers, or 8 per lane with the whole warp, or
-// past that to the whole warp through shared memory; a row the plan does not
-// call heavy (any row without a plan) of up to two buffers streams through
-// the warp's buffer twice (fold, then normalise);
-// other layouts use one thread per (row, group of W heads). A light row
-// longer than that (possible without a plan, or with a large threshold) is
-// read straight from global memory by the whole warp. H > 32 takes the head-at-a-time kernels
-// further down. The last block to finish resets the plan's counters, so a
-// plan serves one launch at a time.
+// past that to the whole warp through shared memory; a row beyond the buffer
+// that the plan does not call heavy (any such row without a plan) streams
+// through the warp's buffer twice (fold, then normalise). Other layouts use
+// one thread per (row, group of W heads), and read a light row longer than
+// the buffer straight from global memory with the whole warp. The launch
+// serves H <= 32, and H = 64 or 128 with W = 4 (Q = 16 or 32 head groups,
+// still at most one per lane); other head counts take the head-at-a-time
+// kernels further down. The last block to finish resets the plan's
+// counters, so a plan serves one launch at a time.
 // out may alias scores: every score of a row (or chunk) is read before its
 // first write.
 #include <climits>
@@ -42,7 +43,6 @@ constexpr int kSpanFloats = 2048;        // light-row staging buffer per warp (8
 constexpr int kSpanBlockFloats = kSoftmaxThreads / 32 * kSpanFloats;  // heavy rows: 2 chunks
 constexpr int kHeavyUnit = 8;            // heavy-list entries per fetch
 constexpr int kHeavyRegs = 8;            // heavy rows: float4s per thread and chunk
-constexpr int kMediumChunks = 2;         // rows up to this many warp buffers: one warp
 constexpr int kSpanSmemBytes = kSpanBlockFloats * 4;
 constexpr int kSoftmaxCache = 8;         // direct path: loads per thread per tile
 constexpr float kLog2e = 1.4426950408889634f;
@@ -799,8 +799,8 @@ __device__ __forceinline__ void softmax_heavy_rows(const int32_t *e0s, const int
 // one bulk copy. W = 4 with Q = H/4 a power of two: rows go to register
 // tiers (up to 4 or 8 float4s per lane) or, past 8 per lane, to the
 // whole-warp shared-memory routine, and a row beyond the buffer that the
-// plan does not call heavy (up to kMediumChunks buffers) streams through
-// the warp's buffer twice; otherwise one thread per (row, group of W heads)
+// plan does not call heavy streams through the warp's buffer twice;
+// otherwise one thread per (row, group of W heads)
 // (Q = H/W groups, R = 32/Q rows at a time, lane = r*Q + q). The last block
 // to finish resets the counters for the next launch on the stream.
 template <int W>
@@ -816,11 +816,10 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
     __shared__ int32_t s_unit;
     const int t = threadIdx.x, lane = t & 31;
     const int32_t cap_e = kSpanFloats / H;  // edges per warp buffer
-    // light rows up to cap_m edges that the buffer does not hold are the
-    // warps' (two passes through the buffer, W = 4 with Q a power of two);
+    // light rows the buffer does not hold are the warps' (two passes through
+    // the buffer with W = 4 and Q a power of two, else straight from global);
     // the plan's heavy rows beyond the buffer are phase 1's
     const bool tiers = W == 4 && ((H / W) & (H / W - 1)) == 0;
-    const int32_t cap_m = tiers ? kMediumChunks * cap_e : cap_e;
     if (n_heavy > 0) {
         // units of kHeavyUnit list entries from the plan's second counter;
         // the next unit's index is fetched while this one is computed
@@ -895,9 +894,9 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
             if (i1 > nb) i1 = nb;
             if (i1 == i0) {  // a heavy row, or a light row longer than the buffer
                 const int32_t d = __shfl_sync(kFull, deg_lane, i0);
-                if (tiers && d <= cap_m && d <= heavy_threshold)  // the warp, two passes
+                if (tiers && d <= heavy_threshold)  // light but too long: the warp, two passes
                     softmax_row_medium4(scores, out, sb, base, d, H, cap_e, lane);
-                else if (d <= heavy_threshold)  // light but too long: straight from global
+                else if (d <= heavy_threshold)  // the same, straight from global
                     softmax_row_direct(scores, out, (int64_t)base * H, (int64_t)(base + d) * H, H,
                                        lane);
                 ++i0;
@@ -1072,12 +1071,16 @@ extern "C" gat_status_t gat_edge_softmax(const int32_t *row_ptr, int64_t n_rows,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int32_t T = plan ? plan->heavy_threshold : INT_MAX;
     const int64_t wpb = kSoftmaxThreads / 32;
-    // a warp per batch of 32 rows (H <= 32) or per row (H > 32)
-    const int64_t warps = H <= 32 ? (n_rows + 31) / 32 : n_rows;
-    int64_t blocks = (warps + wpb - 1) / wpb;
     // W = 4 heads per thread (16-byte accesses) when the layout allows it
     const bool vec4 = H % 4 == 0 && aligned16(scores) && aligned16(out);
-    if (H <= 32) {
+    // H = 64 or 128 with 16-byte groups of four heads: Q = H/4 <= 32 head
+    // groups, a power of two, as the one-launch kernel needs
+    const bool wide4 = vec4 && (H == 64 || H == 128);
+    const bool one_launch = H <= 32 || wide4;
+    // a warp per batch of 32 rows (one launch) or per row (the others)
+    const int64_t warps = one_launch ? (n_rows + 31) / 32 : n_rows;
+    int64_t blocks = (warps + wpb - 1) / wpb;
+    if (one_launch) {
         // one launch: the plan's heavy rows, then light batches; with a plan
         // the grid is exactly the resident blocks and batches are fetched
         // from the plan's counter

@@ -57,7 +57,7 @@ def test_edge_softmax_workload(gat, use_plan):
     assert_fp32(host(out), o, name="edge_softmax")
 
 
-@pytest.mark.parametrize("H", [1, 3, 4, 5, 8, 12, 32, 40])
+@pytest.mark.parametrize("H", [1, 3, 4, 5, 8, 12, 32, 40, 64, 128])
 def test_edge_softmax_heads_in_place_and_long_rows(gat, H):
     deg = np.array([0, 1, 2, 31, 32, 33, 300, 0, 5000, 7])
     d = W.make_edge_softmax(seed=40 + H, deg=deg, H=H)
@@ -94,7 +94,7 @@ def test_edge_softmax_plan_reused_across_calls_and_head_counts(gat):
             assert np.array_equal(g, first[H])
 
 
-@pytest.mark.parametrize("H", [8, 4, 32])
+@pytest.mark.parametrize("H", [8, 4, 32, 64, 128])
 def test_edge_softmax_neg_inf_heads_on_every_row_path(gat, H):
     """-inf scores on every row path of the 8-head kernel (thread tiers, the
     8-per-lane warp tier, the whole-warp shared-memory rows, rows streamed
