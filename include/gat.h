@@ -212,7 +212,9 @@ gat_status_t gat_spmm_weighted(const int32_t *row_ptr, const int32_t *col_idx, i
  *     out[i,h,:] = sum_e softmax_e(s[.,h])[e] * v[col_idx[e],h,:]
  *     out[i,:,:] = 0 for a zero-degree row i
  * q/out are [n_rows,H,Dh], k/v are [n_src,H,Dh], all in `dtype` (fp32
- * arithmetic, bf16 results rounded to nearest even).
+ * arithmetic, bf16 results rounded to nearest even). Shapes the vector
+ * kernel does not take whole run as groups of heads it takes (one launch
+ * per group); shapes with no such group take a scalar kernel (no chunks).
  * plan: NULL (every row by one warp; workspace unused) or a plan of this
  * graph (heavy rows split into chunks whose partial softmax states go to
  * `workspace` and are merged by the last chunk to finish).

@@ -1,7 +1,8 @@
 // fused_layer.cu - gat_fused_layer: SDDMM -> segmented softmax -> weighted
 // SpMM in one pass over the CSR graph (see row_engine.cuh for the layout and
-// the online-softmax recurrence). This file holds the launch logic and the
-// scalar fallback used for shapes the vector engine does not cover.
+// the online-softmax recurrence). This file holds the launch logic (a shape
+// the vector engine does not cover whole runs as groups of heads it does
+// cover, one launch per group) and the scalar fallback for the rest.
 #include <climits>
 
 #include "row_engine.cuh"
@@ -115,6 +116,16 @@ static gat_status_t launch_fused(EngineParams p, bool vec_ok, cudaStream_t s) {
     return check_launch("gat_fused_layer (scalar)");
 }
 
+// The widest head group g (g divides H) whose (g, Dh) the vector engine
+// covers; 0 when there is none. Heads are independent in the layer, so a row
+// is computed group by group, each group a slice of every q/k/v/out row.
+static int engine_group(int H, int Dh, int elem_bytes) {
+    int V, LE;
+    for (int g = H; g >= 1; --g)
+        if (H % g == 0 && engine_shape(g, Dh, elem_bytes, V, LE)) return g;
+    return 0;
+}
+
 int64_t slot_floats(int H, int Dh) {
     const int64_t f = (int64_t)H * Dh + 2 * (int64_t)H;
     return (f + 3) / 4 * 4;
@@ -158,14 +169,15 @@ extern "C" gat_status_t gat_fused_layer(const int32_t *row_ptr, const int32_t *c
     p.n_rows = n_rows;
     p.H = H;
     p.Dh = Dh;
+    p.row_elems = (int64_t)H * Dh;
     p.qscale = scale * kLog2e;
     p.heavy_threshold = INT_MAX;
     p.chunk_edges = 1;
     p.slot_floats = slot_floats(H, Dh);
     const int eb = dtype == GAT_F32 ? 4 : 2;
     const bool vec_ok = aligned16(q) && aligned16(out) && (n_edges == 0 || (aligned16(k) && aligned16(v)));
-    int V, LE;
-    const bool fast = vec_ok && engine_shape(H, Dh, eb, V, LE);
+    const int Hg = vec_ok ? engine_group(H, Dh, eb) : 0;
+    const bool fast = Hg > 0;
     if (plan && fast) {
         p.heavy_threshold = plan->heavy_threshold;
         p.chunk_edges = plan->chunk_edges;
@@ -185,6 +197,28 @@ extern "C" gat_status_t gat_fused_layer(const int32_t *row_ptr, const int32_t *c
         }
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (fast && Hg < H) {
+        // one launch per group of Hg heads over the slices of the rows at
+        // head h0 (Dh * elem_bytes is a multiple of 16, so every slice keeps
+        // the 16-byte alignment); the chunk states of a launch fit the
+        // workspace sized for all H heads, and each launch leaves the plan's
+        // arrival counters at zero for the next
+        for (int h0 = 0; h0 < H; h0 += Hg) {
+            EngineParams pg = p;
+            const size_t off = (size_t)h0 * Dh * eb;
+            pg.H = Hg;
+            pg.q = static_cast<const char *>(q) + off;
+            pg.out = static_cast<char *>(out) + off;
+            if (n_edges > 0) {
+                pg.k = static_cast<const char *>(k) + off;
+                pg.v = static_cast<const char *>(v) + off;
+            }
+            const gat_status_t st = dtype == GAT_F32 ? launch_fused<float>(pg, true, s)
+                                                     : launch_fused<__nv_bfloat16>(pg, true, s);
+            if (st != GAT_OK) return st;
+        }
+        return GAT_OK;
+    }
     if (dtype == GAT_F32) return launch_fused<float>(p, vec_ok, s);
     return launch_fused<__nv_bfloat16>(p, vec_ok, s);
 }

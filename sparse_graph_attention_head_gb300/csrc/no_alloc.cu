@@ -170,6 +170,7 @@ extern "C" gat_status_t gat_fused_layer_no_alloc(const int32_t *row_ptr, const i
     p.n_rows = n_rows;
     p.H = H;
     p.Dh = Dh;
+    p.row_elems = (int64_t)H * Dh;
     p.qscale = scale * kLog2eNA;
     p.heavy_threshold = kNoAllocThreshold;
     p.chunk_edges = kNoAllocChunk;

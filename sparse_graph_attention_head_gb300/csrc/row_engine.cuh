@@ -46,6 +46,7 @@ struct EngineParams {
     void *out;        // [n_rows, H, Dh]
     int64_t n_rows;
     int32_t H, Dh;
+    int64_t row_elems;  // fused: elements per q/k/v/out row (H * Dh, or more for a head group)
     float qscale;     // fused: scale * log2(e)
     // light/heavy split (no plan: heavy_threshold = INT_MAX, n_chunks = 0)
     int32_t heavy_threshold;
@@ -154,7 +155,7 @@ struct FusedRow {
     float m[V], l[V];
 
     __device__ __forceinline__ void load_q(const EngineParams &p, const L &ln, int64_t row) {
-        const char *qrow = static_cast<const char *>(p.q) + row * (int64_t)p.H * p.Dh * sizeof(T);
+        const char *qrow = static_cast<const char *>(p.q) + row * p.row_elems * (int64_t)sizeof(T);
 #pragma unroll
         for (int s = 0; s < V; ++s) {
             uint4 u = ld_stream16(qrow + ln.vi[s] * 16);
@@ -179,7 +180,7 @@ struct FusedRow {
 #pragma unroll
             for (int t = 0; t < VE; ++t) acc[s][t] = 0.f;
         }
-        const int64_t row_bytes = (int64_t)p.H * p.Dh * sizeof(T);
+        const int64_t row_bytes = p.row_elems * (int64_t)sizeof(T);
         const char *kb = static_cast<const char *>(p.k);
         const char *vb = static_cast<const char *>(p.v);
         for (int base = e0; base < e1; base += 32) {
@@ -281,7 +282,7 @@ struct FusedRow {
 
     __device__ __forceinline__ void store_out(const EngineParams &p, const L &ln, int64_t row) {
         if (ln.sub != 0) return;
-        char *orow = static_cast<char *>(p.out) + row * (int64_t)p.H * p.Dh * sizeof(T);
+        char *orow = static_cast<char *>(p.out) + row * p.row_elems * (int64_t)sizeof(T);
 #pragma unroll
         for (int s = 0; s < V; ++s) {
             const float inv = l[s] > 0.f ? 1.f / l[s] : 0.f;

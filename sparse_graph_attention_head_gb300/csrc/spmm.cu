@@ -361,6 +361,7 @@ extern "C" gat_status_t gat_spmm_weighted(const int32_t *row_ptr, const int32_t 
     p.n_rows = n_rows;
     p.H = H;
     p.Dh = Dh;
+    p.row_elems = (int64_t)H * Dh;
     p.heavy_threshold = INT_MAX;
     p.slot_floats = ((int64_t)H * Dh + 3) / 4 * 4;
     const bool vec_ok = aligned16(out) && (n_edges == 0 || aligned16(feat));

@@ -308,7 +308,10 @@ def test_fused_small_power_law(gat, use_plan):
 
 @pytest.mark.parametrize("H,Dh,dtype", [(8, 64, "f32"), (4, 64, "bf16"), (2, 64, "bf16"),
                                          (1, 64, "bf16"), (1, 32, "bf16"), (4, 32, "f32"),
-                                         (1, 64, "f32"), (3, 24, "f32"), (2, 40, "bf16")])
+                                         (1, 64, "f32"), (3, 24, "f32"), (2, 40, "bf16"),
+                                         # head groups: 3 x 4, 2 x 8, 2 x 16, 3 x 2, 2 x 8 heads
+                                         (12, 64, "bf16"), (16, 128, "bf16"), (32, 64, "bf16"),
+                                         (6, 32, "f32"), (16, 64, "f32")])
 def test_fused_shapes(gat, H, Dh, dtype):
     deg = W.zipf_degrees(np.random.default_rng(90 + Dh), 1500, dmax=700)
     d, rp, ci, q, k, v = fused_case(1500, 91 + H, H=H, Dh=Dh, dtype=dtype, deg=deg)
