@@ -42,7 +42,8 @@ struct EngineParams {
     const void *q;    // fused: [n_rows, H, Dh]
     const void *k;    // fused: [n_src, H, Dh]
     const void *v;    // [n_src, H, Dh] (fused: values; spmm: features)
-    const float *w;   // spmm: [n_edges, H]
+    const float *w;   // spmm: [n_edges, w_stride], this call's heads from column 0
+    int32_t w_stride; // spmm: weights per edge (H, or more for a head group)
     void *out;        // [n_rows, H, Dh]
     int64_t n_rows;
     int32_t H, Dh;

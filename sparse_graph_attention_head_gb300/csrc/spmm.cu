@@ -4,7 +4,8 @@
 // metadata prefetched. Heavy rows of a plan: with a workspace, cut into
 // chunks in the same launch and summed by the last chunk in chunk order;
 // without one, one 8-warp block per row in a second launch, warps summed in
-// warp order. Lane layout: row_engine.cuh.
+// warp order. Lane layout: row_engine.cuh. A shape the vector kernels do not
+// take whole runs as groups of heads they take, one launch per group.
 #include <climits>
 
 #include "row_engine.cuh"
@@ -74,7 +75,7 @@ struct SpmmAcc {
                                         int tile0, int tile_step, int first_ci, bool have_first,
                                         int ne0, int ne1, bool want_next, int &next_ci,
                                         bool &next_ready) {
-        const int64_t row_bytes = (int64_t)p.H * p.Dh * sizeof(T);
+        const int64_t row_bytes = p.row_elems * (int64_t)sizeof(T);
         const char *fb = static_cast<const char *>(p.v);
         const int first = e0 + tile0 * 32;
         for (int base = first; base < e1; base += tile_step * 32) {
@@ -94,7 +95,7 @@ struct SpmmAcc {
                     for (int s = 0; s < V; ++s) {
                         if (valid) {
                             vr[u][s] = ld_stream16(fb + src * row_bytes + ln.vi[s] * 16);
-                            wv[u][s] = __ldg(p.w + (int64_t)(base + j) * p.H + ln.head[s]);
+                            wv[u][s] = __ldg(p.w + (int64_t)(base + j) * p.w_stride + ln.head[s]);
                         } else {
                             vr[u][s] = make_uint4(0, 0, 0, 0);
                             wv[u][s] = 0.f;
@@ -131,7 +132,7 @@ struct SpmmAcc {
 
     __device__ __forceinline__ void store_out(const EngineParams &p, const L &ln, int64_t row) {
         if (ln.sub != 0) return;
-        char *orow = static_cast<char *>(p.out) + row * (int64_t)p.H * p.Dh * sizeof(T);
+        char *orow = static_cast<char *>(p.out) + row * p.row_elems * (int64_t)sizeof(T);
 #pragma unroll
         for (int s = 0; s < V; ++s) st_stream16(orow + ln.vi[s] * 16, Vec<T>::pack(acc[s]));
     }
@@ -272,6 +273,17 @@ spmm_heavy_kernel(const EngineParams p) {
     }
 }
 
+// The widest head group g (g divides H) whose (g, Dh) the vector kernels
+// cover; 0 when there is none. Heads are independent, so a row is summed
+// group by group, each group a slice of every feature / output row and of
+// every edge's weights.
+static int spmm_group(int H, int Dh, int elem_bytes) {
+    int V, LE;
+    for (int g = H; g >= 1; --g)
+        if (H % g == 0 && engine_shape(g, Dh, elem_bytes, V, LE)) return g;
+    return 0;
+}
+
 template <typename T, int V, int LE>
 static gat_status_t launch_spmm_fast(const EngineParams &p, cudaStream_t s) {
     constexpr int U = V == 4 ? 2 : 3;  // edges in flight per warp (3 KB at V = 2, fp32)
@@ -362,12 +374,13 @@ extern "C" gat_status_t gat_spmm_weighted(const int32_t *row_ptr, const int32_t 
     p.H = H;
     p.Dh = Dh;
     p.row_elems = (int64_t)H * Dh;
+    p.w_stride = H;
     p.heavy_threshold = INT_MAX;
     p.slot_floats = ((int64_t)H * Dh + 3) / 4 * 4;
     const bool vec_ok = aligned16(out) && (n_edges == 0 || aligned16(feat));
-    int V, LE;
     const int eb = dtype == GAT_F32 ? 4 : 2;
-    if (plan && vec_ok && engine_shape(H, Dh, eb, V, LE) && plan->n_heavy > 0) {
+    const int Hg = vec_ok ? spmm_group(H, Dh, eb) : 0;
+    if (plan && Hg > 0 && plan->n_heavy > 0) {
         p.heavy_threshold = plan->heavy_threshold;
         const size_t need = (size_t)plan->n_chunks * (size_t)p.slot_floats * sizeof(float);
         if (workspace && workspace_bytes >= need && aligned16(workspace)) {
@@ -388,6 +401,26 @@ extern "C" gat_status_t gat_spmm_weighted(const int32_t *row_ptr, const int32_t 
         }
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (Hg > 0 && Hg < H) {
+        // one launch (or two, with block-per-row heavy rows) per group of Hg
+        // heads over the slices at head h0: rows keep their full stride
+        // (row_elems), weights theirs (w_stride = H); Dh * elem_bytes is a
+        // multiple of 16, so every slice stays 16-byte aligned
+        for (int h0 = 0; h0 < H; h0 += Hg) {
+            EngineParams pg = p;
+            const size_t off = (size_t)h0 * Dh * eb;
+            pg.H = Hg;
+            pg.out = static_cast<char *>(out) + off;
+            if (n_edges > 0) {
+                pg.v = static_cast<const char *>(feat) + off;
+                pg.w = w + h0;
+            }
+            const gat_status_t st = dtype == GAT_F32 ? launch_spmm<float>(pg, true, s)
+                                                     : launch_spmm<__nv_bfloat16>(pg, true, s);
+            if (st != GAT_OK) return st;
+        }
+        return GAT_OK;
+    }
     if (dtype == GAT_F32) return launch_spmm<float>(p, vec_ok, s);
     return launch_spmm<__nv_bfloat16>(p, vec_ok, s);
 }

@@ -184,7 +184,9 @@ def test_aggregate_workload(gat, use_plan):
 
 @pytest.mark.parametrize("H,Dh,dtype", [(1, 64, "f32"), (4, 32, "f32"), (8, 64, "f32"),
                                          (8, 64, "bf16"), (2, 64, "bf16"), (1, 32, "bf16"),
-                                         (3, 24, "f32"), (5, 6, "bf16")])
+                                         (3, 24, "f32"), (5, 6, "bf16"),
+                                         # head groups: 2 x 8, 3 x 4, 2 x 16 heads
+                                         (16, 64, "f32"), (12, 32, "bf16"), (32, 32, "f32")])
 def test_spmm_shapes(gat, H, Dh, dtype):
     rng = np.random.default_rng(50 + H * Dh)
     deg = np.concatenate([rng.integers(0, 40, 300), [0, 65, 64, 200, 1500]])
