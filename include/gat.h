@@ -250,9 +250,9 @@ gat_status_t gat_fused_layer(const int32_t *row_ptr, const int32_t *col_idx, int
  * q and out [n_rows,H,Dh] in `dtype`, fp32 arithmetic. Same plan and
  * workspace rules as gat_fused_layer (size from
  * gat_fused_layer_workspace_size). The vector kernel takes H*Dh of 512 or
- * 1024 with Dh a power-of-two multiple of 16 and 16-byte aligned pointers;
- * other shapes (Dh <= 256) take a scalar kernel (no chunks, workspace
- * unused). Errors: as gat_fused_layer; GAT_ERR_UNSUPPORTED for Dh > 256.
+ * 1024 with Dh a power-of-two multiple of 16 and 16-byte aligned pointers,
+ * wider rows as groups of heads of that size (one launch per group); other
+ * shapes (Dh <= 256) take a scalar kernel (no chunks, workspace unused). Errors: as gat_fused_layer; GAT_ERR_UNSUPPORTED for Dh > 256.
  * ---------------------------------------------------------------------- */
 gat_status_t gat_quantize_fp8(const void *x, gat_dtype_t dtype, int64_t n, int32_t H, int32_t Dh,
                               uint8_t *codes, float *scales, void *stream);

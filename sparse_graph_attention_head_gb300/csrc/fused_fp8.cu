@@ -19,7 +19,9 @@
 //     s = scale * ks[src,h] * <q, decode(k8[src])>, online softmax in log2
 //     units, acc += p * vs[src,h] * decode(v8[src]). Heavy rows of a plan are
 //     cut into chunks whose states merge exactly as in gat_fused_layer.
-//     Other shapes take a scalar kernel (one warp per row, heads in turn).
+//     Wider rows run as groups of heads of 512 or 1024 codes, one launch per
+//     group; other shapes take a scalar kernel (one warp per row, heads in
+//     turn).
 #include <climits>
 #include <cuda_fp8.h>
 
@@ -38,6 +40,8 @@ struct Fp8Params {
     void *out;               // [n_rows,H,Dh], T
     int64_t n_rows;
     int32_t H, Dh;
+    int32_t Hs;    // heads per row of q, out, the code tables and the scales (H, or
+                   // more for a head group whose slices start at head 0 of each row)
     float qscale;  // scale * log2(e)
     int32_t heavy_threshold;
     int64_t n_chunks;
@@ -98,7 +102,7 @@ struct Fp8Row {
     }
 
     __device__ __forceinline__ void begin(const Fp8Params &p, int64_t row) {
-        const T *qrow = static_cast<const T *>(p.q) + row * (int64_t)p.H * p.Dh;
+        const T *qrow = static_cast<const T *>(p.q) + row * (int64_t)p.Hs * p.Dh;
 #pragma unroll
         for (int s = 0; s < V; ++s) {
             load16(qrow + vi[s] * 16, qf[s]);
@@ -113,7 +117,7 @@ struct Fp8Row {
     }
 
     __device__ __forceinline__ void run(const Fp8Params &p, int e0, int e1) {
-        const int64_t HD = (int64_t)p.H * p.Dh;
+        const int64_t HD = (int64_t)p.Hs * p.Dh;
         for (int base = e0; base < e1; base += 32) {
             const int n = min(32, e1 - base);
             const int my_ci = lane < n ? __ldg(p.col_idx + base + lane) : 0;
@@ -128,8 +132,8 @@ struct Fp8Row {
                         if (j0 + u < n) {
                             kr[u][s] = ld_stream16(p.k8 + src * HD + vi[s] * 16);
                             vr[u][s] = ld_stream16(p.v8 + src * HD + vi[s] * 16);
-                            kss[u][s] = __ldg(p.ks + src * p.H + head[s]);
-                            vss[u][s] = __ldg(p.vs + src * p.H + head[s]);
+                            kss[u][s] = __ldg(p.ks + src * p.Hs + head[s]);
+                            vss[u][s] = __ldg(p.vs + src * p.Hs + head[s]);
                         } else {
                             kr[u][s] = vr[u][s] = make_uint4(0, 0, 0, 0);
                             kss[u][s] = vss[u][s] = 0.f;
@@ -184,7 +188,7 @@ struct Fp8Row {
     }
 
     __device__ __forceinline__ void store_out(const Fp8Params &p, int64_t row) {
-        T *orow = static_cast<T *>(p.out) + row * (int64_t)p.H * p.Dh;
+        T *orow = static_cast<T *>(p.out) + row * (int64_t)p.Hs * p.Dh;
 #pragma unroll
         for (int s = 0; s < V; ++s) {
             const float inv = l[s] > 0.f ? 1.f / l[s] : 0.f;
@@ -519,17 +523,21 @@ extern "C" gat_status_t gat_fused_layer_fp8(const int32_t *row_ptr, const int32_
     p.n_rows = n_rows;
     p.H = H;
     p.Dh = Dh;
+    p.Hs = H;
     p.qscale = scale * kLog2e8;
     p.heavy_threshold = INT_MAX;
     p.slot_floats = slot_floats(H, Dh);
     // vector path: rows of 512 or 1024 codes (32 or 64 16-byte vectors), a
-    // head a power-of-two number of whole vectors
-    const int64_t HD = (int64_t)H * Dh;
+    // head a power-of-two number of whole vectors; wider rows as groups of
+    // heads of that size (the widest group dividing H), one launch each
     const int G = Dh / 16;
-    const bool shape_ok = Dh % 16 == 0 && (G & (G - 1)) == 0 && (HD == 512 || HD == 1024);
-    const bool fast = shape_ok && aligned16(q) && aligned16(out) &&
+    int Hg = 0;
+    if (Dh % 16 == 0 && (G & (G - 1)) == 0)
+        for (int g = H; g >= 1 && !Hg; --g)
+            if (H % g == 0 && ((int64_t)g * Dh == 512 || (int64_t)g * Dh == 1024)) Hg = g;
+    const bool fast = Hg > 0 && aligned16(q) && aligned16(out) &&
                       (n_edges == 0 || (aligned16(k8) && aligned16(v8)));
-    const int V = (int)(HD / 512);
+    const int V = fast ? (int)((int64_t)Hg * Dh / 512) : 1;
     if (plan && fast) {
         p.heavy_threshold = plan->heavy_threshold;
         p.n_chunks = plan->n_chunks;
@@ -546,6 +554,28 @@ extern "C" gat_status_t gat_fused_layer_fp8(const int32_t *row_ptr, const int32_
         }
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (fast && Hg < H) {
+        // the slices at head h0 of every row: q/out rows (16-byte multiples
+        // of Dh elements), code rows (Dh bytes, a multiple of 16) and scale
+        // rows; the chunk states of a group fit the workspace sized for H
+        const int eb = dtype == GAT_F32 ? 4 : 2;
+        for (int h0 = 0; h0 < H; h0 += Hg) {
+            Fp8Params pg = p;
+            pg.H = Hg;
+            pg.q = static_cast<const char *>(q) + (size_t)h0 * Dh * eb;
+            pg.out = static_cast<char *>(out) + (size_t)h0 * Dh * eb;
+            if (n_edges > 0) {
+                pg.k8 = k8 + (size_t)h0 * Dh;
+                pg.v8 = v8 + (size_t)h0 * Dh;
+                pg.ks = k_scale + h0;
+                pg.vs = v_scale + h0;
+            }
+            const gat_status_t st = dtype == GAT_F32 ? launch_fp8<float>(pg, true, V, s)
+                                                     : launch_fp8<__nv_bfloat16>(pg, true, V, s);
+            if (st != GAT_OK) return st;
+        }
+        return GAT_OK;
+    }
     if (dtype == GAT_F32) return launch_fp8<float>(p, fast, V, s);
     return launch_fp8<__nv_bfloat16>(p, fast, V, s);
 }

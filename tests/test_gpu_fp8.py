@@ -88,7 +88,9 @@ def check(gat, rp, ci, q, k8, ks, v8, vs, H, Dh, scale, plan_kw, name, rows=None
 
 @pytest.mark.parametrize("H,Dh,dtype", [(8, 64, "bf16"), (8, 64, "f32"), (16, 64, "bf16"),
                                          (4, 256, "f32"), (4, 32, "bf16"), (3, 24, "f32"),
-                                         (2, 200, "bf16")])
+                                         (2, 200, "bf16"),
+                                         # head groups of 1024 codes: 2 x 16, 2 x 8 heads
+                                         (32, 64, "bf16"), (16, 128, "f32")])
 def test_fused_fp8_shapes(gat, H, Dh, dtype):
     rng = np.random.default_rng(95 + H * Dh)
     deg = np.concatenate([rng.integers(0, 40, 300), [0, 129, 700, 2000]])
