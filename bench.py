@@ -50,6 +50,19 @@ def dist_env():
     return rank, world, local
 
 
+def relaunch_ranks(n: int) -> int:
+    """Run this same command as n ranks, one per GPU of this node, under
+    torch.distributed.run (rendezvous on 127.0.0.1); returns its exit code."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def dist_init(world, backend):
     import torch.distributed as dist
     if world > 1 and not dist.is_initialized():
@@ -197,26 +210,85 @@ def to_dev(torch, a, dev):
     return t.view(torch.bfloat16) if a.dtype == np.uint16 else t
 
 
-def cpu_baseline_fused(d, budget_s=10.0, block=20000, start_row=0):
-    """The oracle timed on consecutive row blocks until budget_s elapses."""
+def host_cpu():
+    """The host's CPU model name and logical core count (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith(("model name", "cpu model")):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    return {"cpu_model": model or "unknown", "nproc": os.cpu_count() or 1}
+
+
+def oracle_rows_timed(d, budget_s, block, threads, start_row=0):
+    """The oracle (unchanged) on consecutive row blocks until budget_s elapses,
+    driven from `threads` host threads at once; each call takes its own block
+    and ctypes releases the GIL for the call, so the threads run in parallel.
+    Returns (edges, rows, seconds)."""
+    from concurrent.futures import ThreadPoolExecutor
     import oracle
     oracle.build()
     rp = d["row_ptr"]
     n = rp.size - 1
+    lock = threading.Lock()
+    state = {"next": start_row, "edges": 0, "rows": 0}
     t0 = time.perf_counter()
-    edges = rows = 0
-    r = start_row
-    while time.perf_counter() - t0 < budget_s and rows < n:
-        sel = np.arange(r, min(n, r + block))
-        oracle.fused_layer(rp, d["col_idx"], d["q"], d["k"], d["v"], d["H"], d["Dh"],
-                           d["scale"], rows=sel)
-        edges += int(rp[sel[-1] + 1] - rp[sel[0]])
-        rows += sel.size
-        r = (r + block) % n
-    dt = time.perf_counter() - t0
-    return {"value": edges * d["H"] / dt, "unit": "edge-heads/s", "cores": 1, "kind": "oracle",
-            "sample": f"{rows} consecutive rows ({edges} edges, {edges * d['H']} edge-heads) "
-                      f"of the same graph, fp64 C loops, single thread, {dt:.1f} s"}
+
+    def worker():
+        while time.perf_counter() - t0 < budget_s:
+            with lock:
+                if state["rows"] >= n:
+                    return
+                r = state["next"]
+                state["next"] = (r + block) % n
+                state["rows"] += min(n, r + block) - r
+            sel = np.arange(r, min(n, r + block))
+            oracle.fused_layer(rp, d["col_idx"], d["q"], d["k"], d["v"], d["H"], d["Dh"],
+                               d["scale"], rows=sel)
+            with lock:
+                state["edges"] += int(rp[sel[-1] + 1] - rp[sel[0]])
+
+    with ThreadPoolExecutor(threads) as ex:
+        for f in [ex.submit(worker) for _ in range(threads)]:
+            f.result()
+    return state["edges"], state["rows"], time.perf_counter() - t0
+
+
+def cpu_baseline_fused(d, budget_s=10.0, block=20000):
+    """The oracle timed on the host's cores: once on one thread, once on every
+    core (threads over row blocks); `value` is the all-core rate."""
+    host = host_cpu()
+    cores = host["nproc"]
+    e1, r1, t1 = oracle_rows_timed(d, budget_s / 2, block, 1)
+    ea, ra, ta = oracle_rows_timed(d, budget_s / 2, max(1000, block // 4), cores,
+                                   start_row=r1 % (d["row_ptr"].size - 1))
+    v1, va = e1 * d["H"] / t1, ea * d["H"] / ta
+    return {"value": va, "unit": "edge-heads/s", "cores": cores, "kind": "oracle",
+            "value_all_cores": va, "cores_all": cores, "value_single_thread": v1,
+            "cpu_model": host["cpu_model"], "nproc": host["nproc"],
+            "sample": f"all cores: {ra} rows ({ea} edges) in consecutive blocks over {cores} "
+                      f"threads, {ta:.1f} s; one thread: {r1} consecutive rows ({e1} edges), "
+                      f"{t1:.1f} s; fp64 C loops of the same graph"}
+
+
+def spread(ms):
+    """Median and 10th / 90th percentiles of per-call times (ms)."""
+    a = np.asarray(ms, dtype=np.float64)
+    return {"median_ms": float(np.median(a)), "p10_ms": float(np.percentile(a, 10)),
+            "p90_ms": float(np.percentile(a, 90)), "reps": int(a.size)}
 
 
 def bench_fused(args, rank, world, local, dist):
@@ -272,6 +344,7 @@ def bench_fused(args, rank, world, local, dist):
     per_launch = [a.elapsed_time(b) for a, b in ev]
     ms_step = dist_max(dist, total_ms / args.steps, None)
     kern_ms = statistics.mean(per_launch)
+    sp = spread(per_launch)
 
     # end to end: every step copies its inputs from pinned host memory, runs the
     # layer and copies the output back. Steps are software-pipelined over two
@@ -335,6 +408,7 @@ def bench_fused(args, rank, world, local, dist):
         "unit": "edge-heads/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step,
+        "median_ms": sp["median_ms"], "p10_ms": sp["p10_ms"], "p90_ms": sp["p90_ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "fused GAT layer: 1e6 rows, Zipf(2.1) in-degrees clipped to "
@@ -366,25 +440,38 @@ def bench_fused(args, rank, world, local, dist):
 
 def bench_reference(args, rank, world):
     """--impl reference: the fp64 oracle, timed per step on a bounded sample."""
+    from concurrent.futures import ThreadPoolExecutor
     d = W.make_fused(seed=3)
     import oracle
     oracle.build()
     rp = d["row_ptr"]
-    block = args.ref_rows
+    host = host_cpu()
+    cores = host["nproc"]
+    block = args.ref_rows  # rows per step, split over every core
+    sub = max(1, (block + cores - 1) // cores)
     n = rp.size - 1
+    pool = ThreadPoolExecutor(cores)
 
-    def step(i):
-        r0 = (i * block) % n
-        sel = np.arange(r0, min(n, r0 + block))
+    def part(r0, r1):
+        sel = np.arange(r0, r1)
         oracle.fused_layer(rp, d["col_idx"], d["q"], d["k"], d["v"], d["H"], d["Dh"],
                            d["scale"], rows=sel)
-        return int(rp[sel[-1] + 1] - rp[sel[0]])
+        return int(rp[r1] - rp[r0])
+
+    def step(i):
+        # one step: `block` consecutive rows, cut into one sub-block per core
+        # (ctypes releases the GIL, so the oracle calls run in parallel)
+        r0 = (i * block) % n
+        r1 = min(n, r0 + block)
+        futs = [pool.submit(part, a, min(r1, a + sub)) for a in range(r0, r1, sub)]
+        return sum(f.result() for f in futs)
 
     for i in range(args.warmup):
         step(i)
     t0 = time.perf_counter()
     edges = sum(step(args.warmup + i) for i in range(args.steps))
     dt = time.perf_counter() - t0
+    pool.shutdown()
     value = edges * d["H"] / dt
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "edge-heads/s",
@@ -395,9 +482,11 @@ def bench_reference(args, rank, world):
                                "[1,4096] rescaled to mean 16, col_idx uniform sorted in-row, "
                                "H=8, Dh=64, q/k/v bf16 N(0,1), seed 3",
                    "sample_rows_per_step": block},
-        "cpu_baseline": {"value": value, "unit": "edge-heads/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "edge-heads/s", "cores": cores,
+                         "kind": "oracle", "cpu_model": host["cpu_model"],
                          "sample": f"{args.steps} steps of {block} consecutive rows each "
-                                   f"({edges} edges), fp64 C loops, single thread"},
+                                   f"({edges} edges), fp64 C loops, {cores} threads "
+                                   f"(one sub-block of the step's rows each)"},
         "e2e": {"value": value, "unit": "edge-heads/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -559,16 +648,20 @@ def bench_small(name, args):
     for _ in range(max(3, args.warmup)):
         fn()
     torch.cuda.synchronize()
+    # 50 calls, each bracketed by its own events; rates use the median call
     reps = 50
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record()
-    for _ in range(reps):
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for a, b in evs:
+        a.record()
         fn()
-    ev1.record()
+        b.record()
     torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1) / reps
+    sp = spread([a.elapsed_time(b) for a, b in evs])
+    ms = sp["median_ms"]
     hbm_peak, bf16_peak, kind = measured_peaks()
-    res = {"ms_per_step": ms, "units_per_s": units / (ms * 1e-3), "launches_per_step": launches,
+    res = {"ms_per_step": ms, "p10_ms": sp["p10_ms"], "p90_ms": sp["p90_ms"], "reps": reps,
+           "units_per_s": units / (ms * 1e-3), "launches_per_step": launches,
            "warm": True, "algorithmic_bytes": alg_bytes,
            "achieved_gbs": alg_bytes / (ms * 1e-3) / 1e9,
            "hbm_frac": alg_bytes / (ms * 1e-3) / 1e9 / hbm_peak}
@@ -598,8 +691,9 @@ def main():
     ap.add_argument("--workload", default="fused",
                     choices=["fused", "edge_softmax", "aggregate", "sddmm", "dense", "spmm_heads",
                              "edge_softmax_h8", "fused_backward", "fused_fp8"])
-    ap.add_argument("--ref-rows", type=int, default=5000,
-                    help="--impl reference: consecutive rows per step (~0.2 s of oracle work)")
+    ap.add_argument("--ref-rows", type=int, default=40000,
+                    help="--impl reference: consecutive rows per step, split over the host's "
+                         "cores (~0.2 s of oracle work on 16 cores)")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for cpu_baseline (0: skip)")
     ap.add_argument("--n-rows", type=int, default=1_000_000,
@@ -607,7 +701,14 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the smaller workloads")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU: relaunch this command under the torch launcher
+        sys.exit(relaunch_ranks(args.gpus))
     rank, world, local = dist_env()
+    if world != args.gpus:
+        print(json.dumps({"error": f"--gpus {args.gpus} but the launcher started {world} ranks "
+                                   "(WORLD_SIZE); they must agree"}), flush=True)
+        sys.exit(2)
 
     if args.impl == "reference":
         if rank != 0:

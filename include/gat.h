@@ -368,8 +368,10 @@ gat_status_t gat_fused_layer_backward(const int32_t *row_ptr, const int32_t *col
  * (each call clears what must start at zero); calls whose work overlaps on
  * the GPU race on it and must be serialised by the caller.
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture. Every call synchronises `stream` once to read the plan's size.
+ * device, with that device current). Every call copies the plan's size back
+ * to the host and synchronises `stream` to read it, so this entry point
+ * cannot be used inside stream capture at all (not even after a first
+ * uncaptured call); call it on an uncaptured stream.
  * ---------------------------------------------------------------------- */
 gat_status_t gat_fused_layer_no_alloc(const int32_t *row_ptr, const int32_t *col_idx,
                                       int64_t n_rows, int64_t n_src, int64_t n_edges, int32_t H,

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "gat.h"
 
 namespace gat {
@@ -141,18 +143,64 @@ __device__ __forceinline__ void store_elem(__nv_bfloat16 *p, int64_t i, float x)
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Multiprocessor count of the current device (cached per device ordinal).
-inline int sm_count() {
-    static int cache[64] = {0};
+// Launch quantities are cached per device ordinal (attributes and occupancy
+// belong to a device context), in atomics so host threads making their first
+// calls at the same time are safe: a race only computes the same value twice.
+constexpr int kMaxDevices = 64;
+
+inline int current_device() {
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (cache[dev] == 0) {
-        int n = 0;
+    return (dev < 0 || dev >= kMaxDevices) ? 0 : dev;
+}
+
+// Multiprocessor count of the current device.
+inline int sm_count() {
+    static std::atomic<int> cache[kMaxDevices];
+    const int dev = current_device();
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cache[dev] = n > 0 ? n : 1;
+        if (n < 1) n = 1;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
+}
+
+// Resident blocks of `kernel` on the whole current device (blocks per SM at
+// this block size and dynamic shared memory, times the SM count), computed
+// once per device into `cache` (a static array of kMaxDevices atomics owned
+// by the call site, one per kernel instance and launch shape).
+template <typename Kernel>
+inline int64_t device_blocks(std::atomic<int64_t> *cache, Kernel kernel, int threads,
+                             size_t smem) {
+    const int dev = current_device();
+    int64_t cap = cache[dev].load(std::memory_order_relaxed);
+    if (cap == 0) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) !=
+                cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        cap = (int64_t)sm_count() * per_sm;
+        cache[dev].store(cap, std::memory_order_relaxed);
+    }
+    return cap;
+}
+
+// Allow `kernel` up to `bytes` of dynamic shared memory on the current device
+// (the attribute is per device context), once per device into `done` (a
+// static array of kMaxDevices atomic flags owned by the call site). Pass the
+// largest amount the kernel is ever launched with, so concurrent first calls
+// all set the same value.
+template <typename Kernel>
+inline cudaError_t allow_dynamic_smem(std::atomic<int> *done, Kernel kernel, int bytes) {
+    const int dev = current_device();
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
+    return e;
 }
 
 }  // namespace gat

@@ -189,13 +189,16 @@ extern "C" gat_status_t gat_dense_masked_attention(
                   Wq, Wk, Wv, W1, b1, W2, b2, Wout, out};
     const int DS = D + 1;
     const size_t smem = (size_t)(6 * N * DS + H * N * N + P * P + P + H * P + H) * sizeof(float);
-    static size_t configured = 0;
-    if (smem > configured) {
-        cudaError_t e = cudaFuncSetAttribute(dense_block_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return cuda_fail(e, "gat_dense_masked_attention: smem attribute");
-        configured = smem;
-    }
+    // the attribute is set once per device, to the device's opt-in maximum, so
+    // every shape (and concurrent first calls with different shapes) fits it
+    static std::atomic<int> smem_set[kMaxDevices];
+    int optin = 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, current_device());
+    if (smem > (size_t)optin)
+        return fail(GAT_ERR_UNSUPPORTED, "gat_dense_masked_attention: %zu bytes of shared memory "
+                    "needed, %d available", smem, optin);
+    cudaError_t e = allow_dynamic_smem(smem_set, dense_block_kernel, optin);
+    if (e != cudaSuccess) return cuda_fail(e, "gat_dense_masked_attention: smem attribute");
     int per_sm = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dense_block_kernel, kDenseThreads, smem);
     if (per_sm < 1) per_sm = 1;

@@ -107,8 +107,8 @@ static gat_status_t launch_fused(EngineParams p, bool vec_ok, cudaStream_t s) {
     // the scalar path handles every row whole: no chunks, no workspace
     p.n_chunks = 0;
     p.heavy_threshold = INT_MAX;
-    static int64_t cap = 0;
-    if (cap == 0) cap = persistent_blocks(fused_generic_kernel<T>, INT64_MAX);
+    static std::atomic<int64_t> caps[kMaxDevices];
+    const int64_t cap = device_blocks(caps, fused_generic_kernel<T>, kEngineThreads, 0);
     const int64_t wpb = kEngineThreads / 32;
     int64_t blocks = (p.n_rows + wpb - 1) / wpb;
     if (blocks > cap) blocks = cap;

@@ -13,38 +13,26 @@
 // (kNoAllocScratchBytes, 32 MiB). Every GPU that loads the library holds that
 // array until the process exits. Its device address is looked up once per
 // device (cudaGetSymbolAddress, with that device current) on the first call
-// made on the device; make that first call before any stream capture.
-// The kernels are the library's own plan and fused-layer kernels, unchanged.
+// made on the device. The kernels are the library's own plan and fused-layer
+// kernels, unchanged.
 //
 // The array is shared by every call and keeps the previous call's contents:
 // each call clears the arrival counters it needs. Calls whose work overlaps
 // on the GPU (other streams, other host threads) race on the array; serialise
-// them. Each call synchronises `stream` once, to read the plan's size.
+// them. Every call copies the plan's size back into host memory and
+// synchronises `stream` to read it, so no call of this entry point can be
+// recorded by stream capture into a CUDA graph (the first call's address
+// lookup is a further reason); call it on an uncaptured stream.
 #include <mutex>
 
+#include "plan.cuh"
 #include "row_engine.cuh"
 
 namespace gat {
 
-// Layout of the plan kernels' scan records (defined with the kernels).
-struct Counts {
-    long long heavy, chunks, edges;
-};
-__global__ void plan_count_kernel(const int32_t *row_ptr, int64_t n_rows, int32_t T, int32_t C,
-                                  Counts *block_counts);
-__global__ void plan_scan_kernel(const Counts *block_counts, int64_t nb, Counts *offsets,
-                                 Counts *totals);
-__global__ void plan_fill_kernel(const int32_t *row_ptr, int64_t n_rows, int32_t T, int32_t C,
-                                 const Counts *offsets, const Counts *totals,
-                                 int32_t *heavy_rows, int32_t *chunk_start, int32_t *chunk_row);
-__global__ void plan_desc_kernel(const int32_t *row_ptr, const int32_t *heavy_rows,
-                                 const int32_t *chunk_start, int64_t n_heavy, int32_t C,
-                                 int4 *desc);
-
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 constexpr int32_t kNoAllocThreshold = 64;  // heavy rows: degree > 64
 constexpr int32_t kNoAllocChunk = 64;      // edges per chunk
-constexpr int64_t kPlanRowsPerBlockNA = 256 * 8;  // rows per plan block (plan kernels' tiling)
 constexpr float kLog2eNA = 1.4426950408889634f;
 
 static __device__ __align__(256) unsigned char g_no_alloc_scratch[kNoAllocScratchBytes];
@@ -115,7 +103,7 @@ extern "C" gat_status_t gat_fused_layer_no_alloc(const int32_t *row_ptr, const i
                     "shape (H=%d, Dh=%d)", (int)H, (int)Dh);
 
     // the scan records must fit before anything is launched
-    const int64_t nb = (n_rows + kPlanRowsPerBlockNA - 1) / kPlanRowsPerBlockNA;
+    const int64_t nb = plan_blocks(n_rows);
     const size_t counts_bytes = align256((size_t)(2 * nb + 1) * sizeof(Counts));
     if (counts_bytes > kNoAllocScratchBytes)
         return fail(GAT_ERR_WORKSPACE,
@@ -129,9 +117,9 @@ extern "C" gat_status_t gat_fused_layer_no_alloc(const int32_t *row_ptr, const i
     Counts *counts = reinterpret_cast<Counts *>(sc);
 
     // plan sizes (one read-back)
-    plan_count_kernel<<<(unsigned)nb, 256, 0, s>>>(row_ptr, n_rows, kNoAllocThreshold,
+    plan_count_kernel<<<(unsigned)nb, kPlanThreads, 0, s>>>(row_ptr, n_rows, kNoAllocThreshold,
                                                   kNoAllocChunk, counts);
-    plan_scan_kernel<<<1, 1024, 0, s>>>(counts, nb, counts + nb, counts + 2 * nb);
+    plan_scan_kernel<<<1, kPlanScanThreads, 0, s>>>(counts, nb, counts + nb, counts + 2 * nb);
     if ((st = check_launch("gat_fused_layer_no_alloc: plan count")) != GAT_OK) return st;
     Counts tot{0, 0, 0};
     cudaError_t e =
@@ -186,16 +174,16 @@ extern "C" gat_status_t gat_fused_layer_no_alloc(const int32_t *row_ptr, const i
         e = cudaMemsetAsync(p.counters, 0, (size_t)tot.heavy * 4, s);
         if (e != cudaSuccess) return cuda_fail(e, "gat_fused_layer_no_alloc: clearing counters");
     }
-    plan_fill_kernel<<<(unsigned)nb, 256, 0, s>>>(row_ptr, n_rows, kNoAllocThreshold, kNoAllocChunk,
+    plan_fill_kernel<<<(unsigned)nb, kPlanThreads, 0, s>>>(row_ptr, n_rows, kNoAllocThreshold, kNoAllocChunk,
                                                  counts + nb, counts + 2 * nb,
                                                  const_cast<int32_t *>(p.heavy_rows),
                                                  const_cast<int32_t *>(p.chunk_start),
                                                  const_cast<int32_t *>(p.chunk_row));
     if ((st = check_launch("gat_fused_layer_no_alloc: plan fill")) != GAT_OK) return st;
     if (tot.heavy > 0) {
-        int64_t db = (tot.heavy + 255) / 256;
+        int64_t db = (tot.heavy + kPlanThreads - 1) / kPlanThreads;
         if (db > 4096) db = 4096;
-        plan_desc_kernel<<<(unsigned)db, 256, 0, s>>>(row_ptr, p.heavy_rows, p.chunk_start,
+        plan_desc_kernel<<<(unsigned)db, kPlanThreads, 0, s>>>(row_ptr, p.heavy_rows, p.chunk_start,
                                                      tot.heavy, kNoAllocChunk,
                                                      const_cast<int4 *>(p.chunk_desc));
         if ((st = check_launch("gat_fused_layer_no_alloc: chunk descriptors")) != GAT_OK) return st;

@@ -9,7 +9,7 @@
 #include <cstdarg>
 #include <cstdio>
 
-#include "common.cuh"
+#include "plan.cuh"
 
 namespace gat {
 
@@ -39,14 +39,6 @@ gat_status_t check_launch(const char *what) {
 // ---------------------------------------------------------------------------
 // plan kernels
 // ---------------------------------------------------------------------------
-constexpr int kPlanThreads = 256;
-constexpr int kPlanRounds = 8;  // rows per block = kPlanThreads * kPlanRounds
-constexpr int64_t kPlanRowsPerBlock = (int64_t)kPlanThreads * kPlanRounds;
-
-struct Counts {
-    long long heavy, chunks, edges;
-};
-
 __device__ __forceinline__ void row_class(const int32_t *__restrict__ row_ptr, int64_t r,
                                           int64_t n_rows, int32_t T, int32_t C, int &is_heavy,
                                           int &chunks, int &deg) {
@@ -137,7 +129,7 @@ plan_count_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t T
 }
 
 // Exclusive scan of the per-block counts (one block, sequential tiles).
-__global__ void __launch_bounds__(1024)
+__global__ void __launch_bounds__(kPlanScanThreads)
 plan_scan_kernel(const Counts *__restrict__ block_counts, int64_t nb, Counts *__restrict__ offsets,
                  Counts *__restrict__ totals) {
     __shared__ long long sh[3][32];
@@ -329,7 +321,7 @@ extern "C" gat_status_t gat_plan_create(const int32_t *row_ptr, int64_t n_rows, 
         *out = p;
         return GAT_OK;
     }
-    const int64_t nb = (n_rows + kPlanRowsPerBlock - 1) / kPlanRowsPerBlock;
+    const int64_t nb = plan_blocks(n_rows);
     Counts *scratch = nullptr;  // [nb] counts, [nb] offsets, [1] totals
     cudaError_t e = cudaMalloc(&scratch, (2 * nb + 1) * sizeof(Counts));
     Counts host_tot{0, 0, 0};
@@ -340,7 +332,7 @@ extern "C" gat_status_t gat_plan_create(const int32_t *row_ptr, int64_t n_rows, 
     }
     plan_count_kernel<<<(unsigned)nb, kPlanThreads, 0, s>>>(row_ptr, n_rows, p->heavy_threshold,
                                                             p->chunk_edges, scratch);
-    plan_scan_kernel<<<1, 1024, 0, s>>>(scratch, nb, scratch + nb, scratch + 2 * nb);
+    plan_scan_kernel<<<1, kPlanScanThreads, 0, s>>>(scratch, nb, scratch + nb, scratch + 2 * nb);
     if ((st = check_launch("gat_plan_create: count/scan")) != GAT_OK) goto out_fail;
     e = cudaMemcpyAsync(&host_tot, scratch + 2 * nb, sizeof(Counts), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);

@@ -408,15 +408,8 @@ template <typename T, int V, int LE>
 inline gat_status_t launch_fused_engine(const EngineParams &p, cudaStream_t s) {
     constexpr int U = V == 1 ? 4 : (V == 2 ? 3 : 1);
     auto kern = fused_engine_kernel<T, V, LE, U, 5>;
-    static int64_t cap = 0;
-    if (cap == 0) {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFusedThreads, 0) !=
-                cudaSuccess ||
-            per_sm < 1)
-            per_sm = 1;
-        cap = (int64_t)sm_count() * per_sm;
-    }
+    static std::atomic<int64_t> caps[kMaxDevices];
+    const int64_t cap = device_blocks(caps, kern, kFusedThreads, 0);
     const int64_t items = p.n_chunks + p.n_rows;
     const int64_t wpb = kFusedThreads / 32;
     int64_t blocks = (items + wpb - 1) / wpb;

@@ -326,8 +326,8 @@ static gat_status_t launch_spmm(EngineParams p, bool vec_ok, cudaStream_t s) {
         if (V == 2) return launch_spmm_fast<T, 2, 32>(p, s);
         if (V == 4) return launch_spmm_fast<T, 4, 32>(p, s);
     }
-    static int64_t cap = 0;
-    if (cap == 0) cap = persistent_blocks(spmm_generic_kernel<T>, INT64_MAX);
+    static std::atomic<int64_t> caps[kMaxDevices];
+    const int64_t cap = device_blocks(caps, spmm_generic_kernel<T>, kEngineThreads, 0);
     const int64_t wpb = kEngineThreads / 32;
     int64_t blocks = (p.n_rows + wpb - 1) / wpb;
     if (blocks > cap) blocks = cap;

@@ -14,7 +14,20 @@ o = 0 with a 10x margin over the worst-case bound of a 4096-term row.
 Both return the fraction that meets the strict relative form (no c term), so
 tests can report it alongside.
 """
+import json
+import os
+
 import numpy as np
+
+
+def _log(name, strict, n):
+    """Append the strict-allclose pass fraction of one comparison to the JSON
+    lines file named by GAT_PARITY_LOG (nothing when it is unset), so a run
+    records how far each case is from the plain rtol/atol criterion."""
+    path = os.environ.get("GAT_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": name, "strict_fraction": strict, "n": int(n)}) + "\n")
 
 
 def _report(name, g, o, tol):
@@ -41,7 +54,9 @@ def assert_fp32(g, o, cond=None, n_terms=None, name="fp32"):
     assert (np.isnan(g) == nan_o).all(), f"{name}: NaN pattern differs"
     _report(name, np.where(nan_o, 0, g), np.where(nan_o, 0, o), tol)
     strict = np.abs(g - o) <= 1e-6 + 1e-5 * np.abs(o)
-    return float(np.mean(strict[~nan_o])) if (~nan_o).any() else 1.0
+    rate = float(np.mean(strict[~nan_o])) if (~nan_o).any() else 1.0
+    _log(name, rate, (~nan_o).sum())
+    return rate
 
 
 def assert_bf16(g, o, cond, name="bf16"):
@@ -51,4 +66,6 @@ def assert_bf16(g, o, cond, name="bf16"):
     tol = 1e-2 * np.abs(o) + 1e-4 * np.asarray(cond)
     _report(name, g, o, tol)
     strict = np.abs(g - o) <= 1e-2 * np.abs(o)
-    return float(np.mean(strict))
+    rate = float(np.mean(strict))
+    _log(name, rate, g.size)
+    return rate

@@ -417,9 +417,18 @@ def test_full_size_fused_sampled_rows(gat, full_fused):
     deg = np.diff(d["row_ptr"])
     rng = np.random.default_rng(7)
     heaviest = np.argsort(deg)[-12:]
-    at_thr = np.flatnonzero((deg >= 63) & (deg <= 66))[:8]
-    rows = np.unique(np.concatenate([heaviest, at_thr, rng.integers(0, deg.size, 300),
+    # rows at the plan's class edges: the light / heavy cut (degree T vs T + 1)
+    # and one or two whole chunks (degree C, C + 1, 2C, 2C + 1)
+    inf = plan.info()
+    T, C = inf["heavy_threshold"], inf["chunk_edges"]
+    edges = []
+    for lo, hi in ((T - 1, T + 2), (C - 1, C + 2), (2 * C - 1, 2 * C + 2)):
+        sel = np.flatnonzero((deg >= lo) & (deg <= hi))
+        assert sel.size, f"no row of degree {lo}..{hi} in the workload"
+        edges.append(sel[:8])
+    rows = np.unique(np.concatenate([heaviest, *edges, rng.integers(0, deg.size, 300),
                                      [0, deg.size - 1]]))
+    assert {T, T + 1, C, C + 1} <= set(deg[rows].tolist())
     check_fused(d, g, rows=rows)
     assert np.isfinite(g).all()
 

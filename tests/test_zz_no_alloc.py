@@ -2,8 +2,9 @@
 device memory (a framework owning all memory through its own pool, an
 allocator callback, a spent allocation budget). Its plan and chunk states live
 in the library's static device scratch; this checks, through the C ABI, that
-two calls in a row both match gat_fused_layer with an allocated plan and
-workspace, and that a graph too large for the scratch is refused up front.
+two calls in a row both match the fp64 oracle and gat_fused_layer with an
+allocated plan and workspace, and that a graph too large for the scratch is
+refused up front.
 
 Kept in its own file, collected last, so a failure here never hides the rest
 of the suite; it passes alone in a fresh process as well as after the others.
@@ -47,19 +48,20 @@ def test_no_alloc_matches_allocating_entry_point_twice(gat, H, Dh, dtype):
     ref = gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], plan=plan)
     torch.cuda.synchronize()
     ref_h = ref.float().cpu().numpy().astype(np.float64)
-    _, cond = oracle.fused_layer(d["row_ptr"], d["col_idx"], d["q"], d["k"], d["v"], H, Dh,
+    o, cond = oracle.fused_layer(d["row_ptr"], d["col_idx"], d["q"], d["k"], d["v"], H, Dh,
                                  d["scale"], want_cond=True)
+    deg_n = np.diff(d["row_ptr"]).astype(np.float64)[:, None, None]
     for _ in range(2):  # the scratch keeps the previous call's contents
         out = torch.full_like(q, float("nan"))
         gat.gat_fused_layer_no_alloc(rp, ci, q, k, v, d["scale"], out)
         torch.cuda.synchronize()
         got = out.float().cpu().numpy().astype(np.float64)
         assert (got[9] == 0).all()
-        if dtype == "bf16":
-            assert_bf16(got, ref_h, cond, name="no_alloc vs gat_fused_layer")
-        else:
-            deg_n = np.diff(d["row_ptr"]).astype(np.float64)[:, None, None]
-            assert_fp32(got, ref_h, cond, deg_n, name="no_alloc vs gat_fused_layer")
+        for want, what in ((o, "oracle"), (ref_h, "gat_fused_layer")):
+            if dtype == "bf16":
+                assert_bf16(got, want, cond, name=f"no_alloc vs {what}")
+            else:
+                assert_fp32(got, want, cond, deg_n, name=f"no_alloc vs {what}")
 
 
 def test_no_alloc_refuses_graphs_beyond_its_scratch(gat):
