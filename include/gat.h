@@ -390,15 +390,38 @@ gat_status_t gat_fused_layer_no_alloc(const int32_t *row_ptr, const int32_t *col
  * nodes/out [B,N,D], pair_feats [B,N,N,P], edge_mask [B,N,N] (float 0/1).
  * Head h owns feature dims [h*D/H, (h+1)*D/H). out must not alias nodes.
  * Supported: 1 <= N <= 32, D % H == 0, D/H <= 32, D <= 128, D % 4 == 0,
- * 1 <= P <= 32, 16-byte aligned pointers; else GAT_ERR_UNSUPPORTED.
+ * 1 <= P <= 32, 16-byte aligned nodes, out and weight matrices; else
+ * GAT_ERR_UNSUPPORTED.
+ * The block page's module shape (P = 16, H = 4, D = 96, N <= 24, 16-byte
+ * aligned pair_feats) runs on the tensor cores: its weights are first split
+ * into scaled fp16 halves in `workspace` (caller device memory, 16-byte
+ * aligned, at least gat_dense_masked_attention_workspace_size bytes; its
+ * contents on entry are ignored), then one kernel computes the block (fp32
+ * accuracy from three fp16 products per product, see the kernel). Other
+ * shapes run a SIMT kernel and take no workspace (NULL allowed).
+ * The tensor-core kernel never traps: a wait on its pipeline that gives up
+ * (never expected) sets a flag in the workspace and the affected outputs are
+ * NaN; gat_dense_masked_attention_status turns that flag into a status.
+ * Concurrent calls must use different workspaces.
+ * Errors: GAT_ERR_INVALID_ARG, GAT_ERR_UNSUPPORTED, GAT_ERR_WORKSPACE (the
+ * tensor-core shape with a missing, small or misaligned workspace).
  * ---------------------------------------------------------------------- */
+gat_status_t gat_dense_masked_attention_workspace_size(int32_t N, int32_t D, int32_t H,
+                                                       int32_t P, size_t *bytes);
+
 gat_status_t gat_dense_masked_attention(int32_t B, int32_t N, int32_t D, int32_t H, int32_t P,
                                         const float *nodes, const float *pair_feats,
                                         const float *edge_mask, const float *ln_w,
                                         const float *ln_b, float ln_eps, const float *Wq,
                                         const float *Wk, const float *Wv, const float *W1,
                                         const float *b1, const float *W2, const float *b2,
-                                        const float *Wout, float *out, void *stream);
+                                        const float *Wout, float *out, void *workspace,
+                                        size_t workspace_bytes, void *stream);
+
+/* Synchronise `stream` and report whether the last tensor-core call that used
+ * `workspace` completed its pipeline: GAT_OK, or GAT_ERR_CUDA when one of its
+ * bounded waits gave up (its outputs were then written as NaN). */
+gat_status_t gat_dense_masked_attention_status(const void *workspace, void *stream);
 
 #ifdef __cplusplus
 }

@@ -34,6 +34,7 @@ EXPORTS = (
     "gat_transpose_create", "gat_transpose_destroy", "gat_transpose_info", "gat_transpose_export",
     "gat_fused_layer_backward_workspace_size", "gat_fused_layer_backward",
     "gat_quantize_fp8", "gat_fused_layer_fp8", "gat_spmm_weighted_workspace_size",
+    "gat_dense_masked_attention_workspace_size", "gat_dense_masked_attention_status",
 )
 
 
@@ -71,8 +72,10 @@ def _load() -> ctypes.CDLL:
         "gat_fused_layer_workspace_size": ([P, I32, I32, P], ctypes.c_int),
         "gat_fused_layer": ([P, P, I64, I64, I64, I32, I32, F, P, P, P, ctypes.c_int, P, P, P, SZ,
                              P], ctypes.c_int),
-        "gat_dense_masked_attention": ([I32] * 5 + [P] * 5 + [F] + [P] * 8 + [P, P],
+        "gat_dense_masked_attention": ([I32] * 5 + [P] * 5 + [F] + [P] * 8 + [P, P, SZ, P],
                                        ctypes.c_int),
+        "gat_dense_masked_attention_workspace_size": ([I32, I32, I32, I32, P], ctypes.c_int),
+        "gat_dense_masked_attention_status": ([P, P], ctypes.c_int),
         "gat_fused_layer_no_alloc": ([P, P, I64, I64, I64, I32, I32, F, P, P, P, ctypes.c_int, P,
                                       P], ctypes.c_int),
         "gat_transpose_create": ([P, P, I64, I64, I64, P, P], ctypes.c_int),
@@ -436,18 +439,38 @@ def gat_fused_layer_backward(row_ptr, col_idx, q, k, v, dout, scale, transpose, 
     return dq, dk, dv
 
 
+def gat_dense_masked_attention_workspace_size(N, D, H, P) -> int:
+    n = ctypes.c_size_t()
+    _check("gat_dense_masked_attention_workspace_size",
+           _lib.gat_dense_masked_attention_workspace_size(N, D, H, P, ctypes.byref(n)))
+    return n.value
+
+
 def gat_dense_masked_attention(nodes, pair_feats, edge_mask, ln_w, ln_b, ln_eps, Wq, Wk, Wv,
-                               W1, b1, W2, b2, Wout, H, out=None, stream=None):
-    """Dense-masked small-graph attention block (fp32). nodes [B,N,D]."""
+                               W1, b1, W2, b2, Wout, H, out=None, workspace=None, stream=None):
+    """Dense-masked small-graph attention block (fp32). nodes [B,N,D]. The
+    tensor-core shape needs ``workspace`` (allocated here when None)."""
     B, N, D = nodes.shape
     P = pair_feats.shape[-1]
     if out is None:
         out = torch.empty_like(nodes)
+    if workspace is None:
+        need = gat_dense_masked_attention_workspace_size(N, D, H, P)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=nodes.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("gat_dense_masked_attention", _lib.gat_dense_masked_attention(
         B, N, D, H, P, _ptr(nodes), _ptr(pair_feats), _ptr(edge_mask), _ptr(ln_w), _ptr(ln_b),
         float(ln_eps), _ptr(Wq), _ptr(Wk), _ptr(Wv), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2),
-        _ptr(Wout), _ptr(out), _stream(stream)))
+        _ptr(Wout), _ptr(out), _ptr(workspace), ws_bytes, _stream(stream)))
     return out
+
+
+def gat_dense_masked_attention_status(workspace, stream=None) -> None:
+    """Raise GatError when the last tensor-core call with ``workspace`` gave up
+    a bounded wait (synchronises the stream)."""
+    _check("gat_dense_masked_attention_status",
+           _lib.gat_dense_masked_attention_status(_ptr(workspace), _stream(stream)))
 
 
 def version() -> int:

@@ -147,12 +147,15 @@ dense_block_kernel(const DenseParams p) {
 }
 
 // tensor-core path (dense_block_tc.cu); GAT_ERR_UNSUPPORTED outside its shapes
+bool dense_block_tc_shape(int32_t N, int32_t D, int32_t H, int32_t P);
+size_t dense_block_tc_workspace();
 gat_status_t dense_block_tc(int32_t B, int32_t N, int32_t D, int32_t H, int32_t P,
                             const float *nodes, const float *pair, const float *mask,
                             const float *ln_w, const float *ln_b, float ln_eps, const float *Wq,
                             const float *Wk, const float *Wv, const float *W1, const float *b1,
                             const float *W2, const float *b2, const float *Wout, float *out,
-                            cudaStream_t s);
+                            void *workspace, size_t workspace_bytes, cudaStream_t s);
+gat_status_t dense_block_tc_status(const void *workspace, cudaStream_t s);
 
 }  // namespace gat
 
@@ -163,7 +166,7 @@ extern "C" gat_status_t gat_dense_masked_attention(
     const float *pair_feats, const float *edge_mask, const float *ln_w, const float *ln_b,
     float ln_eps, const float *Wq, const float *Wk, const float *Wv, const float *W1,
     const float *b1, const float *W2, const float *b2, const float *Wout, float *out,
-    void *stream) {
+    void *workspace, size_t workspace_bytes, void *stream) {
     if (B < 0 || N < 1 || D < 1 || H < 1 || P < 1)
         return fail(GAT_ERR_INVALID_ARG, "gat_dense_masked_attention: bad sizes");
     if (N > 32 || D % H || D / H > 32 || D > 128 || D % 4 || P > 32 || H > kDenseMaxH)
@@ -179,12 +182,10 @@ extern "C" gat_status_t gat_dense_masked_attention(
         return fail(GAT_ERR_UNSUPPORTED, "gat_dense_masked_attention: pointers must be 16-byte aligned");
     // the module shape of the block page runs its projections on the tensor
     // cores (dense_block_tc.cu); every other shape runs the SIMT kernel below
-    if (aligned16(pair_feats) && aligned16(ln_w) && aligned16(ln_b)) {
-        const gat_status_t st =
-            dense_block_tc(B, N, D, H, P, nodes, pair_feats, edge_mask, ln_w, ln_b, ln_eps, Wq,
-                           Wk, Wv, W1, b1, W2, b2, Wout, out, static_cast<cudaStream_t>(stream));
-        if (st != GAT_ERR_UNSUPPORTED) return st;
-    }
+    if (aligned16(pair_feats) && dense_block_tc_shape(N, D, H, P))
+        return dense_block_tc(B, N, D, H, P, nodes, pair_feats, edge_mask, ln_w, ln_b, ln_eps, Wq,
+                              Wk, Wv, W1, b1, W2, b2, Wout, out, workspace, workspace_bytes,
+                              static_cast<cudaStream_t>(stream));
     DenseParams p{B, N, D, H, P, nodes, pair_feats, edge_mask, ln_w, ln_b, ln_eps,
                   Wq, Wk, Wv, W1, b1, W2, b2, Wout, out};
     const int DS = D + 1;
@@ -206,4 +207,18 @@ extern "C" gat_status_t gat_dense_masked_attention(
     if (blocks > B) blocks = B;
     dense_block_kernel<<<(unsigned)blocks, kDenseThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
     return check_launch("gat_dense_masked_attention");
+}
+
+extern "C" gat_status_t gat_dense_masked_attention_workspace_size(int32_t N, int32_t D, int32_t H,
+                                                                  int32_t P, size_t *bytes) {
+    if (!bytes || N < 1 || D < 1 || H < 1 || P < 1)
+        return fail(GAT_ERR_INVALID_ARG, "gat_dense_masked_attention_workspace_size: bad arguments");
+    *bytes = dense_block_tc_shape(N, D, H, P) ? dense_block_tc_workspace() : 0;
+    return GAT_OK;
+}
+
+extern "C" gat_status_t gat_dense_masked_attention_status(const void *workspace, void *stream) {
+    if (!workspace)
+        return fail(GAT_ERR_INVALID_ARG, "gat_dense_masked_attention_status: workspace is NULL");
+    return dense_block_tc_status(workspace, static_cast<cudaStream_t>(stream));
 }

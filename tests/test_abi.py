@@ -71,11 +71,22 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.gat_fused_layer(None, None, 0, 0, 0, 8, 64, 0.125, None, None, None, 1, None,
                                None, None, 0, None) == 0
     # unsupported dense shapes
-    lib.gat_dense_masked_attention.argtypes = [I32] * 5 + [P] * 5 + [ctypes.c_float] + [P] * 11
-    args = [None] * 5 + [1e-5] + [None] * 11
+    lib.gat_dense_masked_attention.argtypes = ([I32] * 5 + [P] * 5 + [ctypes.c_float] +
+                                               [P] * 10 + [ctypes.c_size_t, P])
+    args = [None] * 5 + [1e-5] + [None] * 10 + [0, None]
     assert lib.gat_dense_masked_attention(4, 40, 96, 4, 16, *args) == 2   # N > 32
     assert lib.gat_dense_masked_attention(4, 24, 90, 4, 16, *args) == 2   # D % H
     assert lib.gat_dense_masked_attention(-1, 24, 96, 4, 16, *args) == 1
+    # the tensor-core shape needs a workspace; other shapes none
+    lib.gat_dense_masked_attention_workspace_size.argtypes = [I32] * 4 + [P]
+    n = ctypes.c_size_t(123)
+    assert lib.gat_dense_masked_attention_workspace_size(24, 96, 4, 16, ctypes.byref(n)) == 0
+    assert n.value >= 8 * 48 * 96 * 4  # the split Q|K|V|out weight images at least
+    assert lib.gat_dense_masked_attention_workspace_size(7, 12, 3, 5, ctypes.byref(n)) == 0
+    assert n.value == 0
+    assert lib.gat_dense_masked_attention_workspace_size(0, 96, 4, 16, ctypes.byref(n)) == 1
+    lib.gat_dense_masked_attention_status.argtypes = [P, P]
+    assert lib.gat_dense_masked_attention_status(None, None) == 1
     # plan creation without an output handle
     lib.gat_plan_create.argtypes = [P, I64, I64, I32, I32, P, P]
     assert lib.gat_plan_create(None, 4, 4, 0, 0, None, None) == 1

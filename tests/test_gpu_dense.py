@@ -22,13 +22,31 @@ def gat():
     return g
 
 
-def run(gat, w):
+def run(gat, w, workspace=None):
     t = {k: torch.from_numpy(np.ascontiguousarray(w[k])).cuda() for k in NAMES + WEIGHTS}
     out = gat.gat_dense_masked_attention(t["nodes"], t["pair_feats"], t["edge_mask"], t["ln_w"],
                                          t["ln_b"], w["ln_eps"], *[t[k] for k in WEIGHTS],
-                                         H=w["H"])
+                                         H=w["H"], workspace=workspace)
     torch.cuda.synchronize()
     return out.cpu().numpy().astype(np.float64)
+
+
+def fp32_block(w):
+    """The block evaluated in plain float32 on the CPU (PyTorch modules and
+    matmuls): the error floor of ordinary fp32 arithmetic on these inputs."""
+    f = {k: torch.from_numpy(np.ascontiguousarray(w[k])) for k in NAMES + WEIGHTS}
+    B, N, D, H = w["B"], w["N"], w["D"], w["H"]
+    dh = D // H
+    x = f["nodes"]
+    xn = torch.nn.functional.layer_norm(x, (D,), f["ln_w"], f["ln_b"], w["ln_eps"])
+    q, k, v = (xn @ f[n].T for n in ("Wq", "Wk", "Wv"))
+    hid = f["pair_feats"] @ f["W1"].T + f["b1"]
+    r = torch.nn.functional.silu(hid) @ f["W2"].T + f["b2"]
+    q, k, v = (a.view(B, N, H, dh).transpose(1, 2) for a in (q, k, v))
+    lg = q @ k.transpose(-1, -2) / np.sqrt(dh) + r.permute(0, 3, 1, 2)
+    lg = lg.masked_fill((f["edge_mask"] < 0.5)[:, None], float("-inf"))
+    ctx = (torch.softmax(lg, -1) @ v).transpose(1, 2).reshape(B, N, D)
+    return (x + ctx @ f["Wout"].T).double().numpy()
 
 
 @pytest.mark.parametrize("wstd,affine", [(0.02, False), (0.05, True)])
@@ -41,16 +59,45 @@ def test_dense_block_small_batch(gat, wstd, affine):
 
 
 def test_dense_block_sharp_attention_stress(gat):
-    """Weights ~ N(0, 0.3^2) make logits ~ +-10, so fp32 rounding of q and k
-    (relative 1e-7 over 96-term projections) moves logits by ~1e-4 and the
-    softmax weights by as much relatively: fp32 cannot meet 1e-5 here, the
-    check is 1e-3 of the output's conditioning scale (catches any real error,
-    which is O(1))."""
+    """Weights ~ N(0, 0.3^2) make logits ~ +-10 (sharp softmax). Plain fp32 on
+    the CPU lands at ~0.1 of the fp32 tolerance on these inputs (measured
+    here), so the kernel is held to the same fp32 tolerance as every other
+    case, and also to 10x the measured fp32 error."""
     w = W.make_dense(seed=4, B=32, wstd=0.3, affine_ln=True)
     g = run(gat, w)
     o, c = oracle.dense_block(w, want_cond=True)
-    err = np.abs(g - o)
-    assert (err <= 1e-3 * np.maximum(c, np.abs(o)) + 1e-6).all(), err.max()
+    scale = np.maximum(np.abs(o), c)
+    floor = float(np.max(np.abs(fp32_block(w) - o) / scale))
+    gerr = float(np.max(np.abs(g - o) / scale))
+    assert floor < 1e-5  # plain fp32 meets the tolerance here
+    assert_fp32(g, o, c, name="dense block stress")
+    assert gerr <= 10 * floor + 1e-7, (gerr, floor)
+
+
+@pytest.mark.parametrize("B,N", [(1, 24), (3, 24), (97, 24), (6, 13), (5, 1), (9, 5)])
+def test_dense_block_tensor_core_ragged(gat, B, N):
+    """The tensor-core shape (P=16, H=4, D=96) with a partial last tile and
+    fewer than 24 nodes; one node that attends to nothing gives NaN."""
+    w = W.make_dense(seed=40 + B + N, B=B, N=N, wstd=0.05, affine_ln=True)
+    w["edge_mask"][B - 1, N - 1, :] = 0.0
+    g = run(gat, w)
+    o, c = oracle.dense_block(w, want_cond=True)
+    assert np.isnan(g[B - 1, N - 1]).all()
+    assert_fp32(g, o, c, name=f"dense block B={B} N={N}")
+
+
+def test_dense_block_workspace_rules(gat):
+    w = W.make_dense(seed=41, B=8)
+    need = gat.gat_dense_masked_attention_workspace_size(w["N"], w["D"], w["H"], w["P"])
+    assert need > 0
+    small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(gat.GatError, match="GAT_ERR_WORKSPACE"):
+        run(gat, w, workspace=small)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    a = run(gat, w, workspace=ws)
+    gat.gat_dense_masked_attention_status(ws)  # completed: no bounded wait gave up
+    b = run(gat, w, workspace=ws)
+    assert np.array_equal(a, b)  # deterministic, workspace reused
 
 
 def test_dense_block_full_size_sampled_graphs(gat):
