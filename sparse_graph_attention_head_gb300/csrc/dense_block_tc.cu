@@ -347,7 +347,7 @@ struct Smem {
     __host__ __device__ static uint32_t nodes_bytes(int N) { return kGraphs * N * kNodeStride * 4; }
     // W1 transposed [c][u], b1, W2 transposed [u][h], b2, gamma, beta
     __host__ __device__ static uint32_t params(int N) { return nodes(N) + nodes_bytes(N); }
-    static constexpr uint32_t params_bytes = (P * P + P + P * H + H + 2 * D) * 4;
+    static constexpr uint32_t params_bytes = (P * P + P + P * H + H + 2 * D + 4) * 4;
     __host__ __device__ static uint32_t rscale(int N) { return params(N) + params_bytes; }
     __host__ __device__ static uint32_t total(int N) { return rscale(N) + 128 * 4; }
 };
@@ -487,14 +487,8 @@ __device__ __forceinline__ void layer_norm(const Params &p, const float *nodes_s
     const float var = ((red[512 + row] + red[640 + row]) + (red[768 + row] + red[896 + row])) / (float)D;
     const float dmax = fmaxf(fmaxf(red[1024 + row], red[1152 + row]), fmaxf(red[1280 + row], red[1408 + row]));
     const float rstd = 1.0f / sqrtf(var + p.ln_eps);
-    float gmax = 0.f, bmax = 0.f;  // |gamma|, |beta| maxima (16-lane broadcast reads)
-#pragma unroll 4
-    for (int i = 0; i < D; ++i) {
-        gmax = fmaxf(gmax, fabsf(gam[i]));
-        bmax = fmaxf(bmax, fabsf(bet[i]));
-    }
-    // an upper bound of |x_n| over the row picks its scale
-    const int sr = valid ? scale_exp(dmax * rstd * gmax + bmax) : 0;
+    // an upper bound of |x_n| over the row (gamma, beta maxima follow beta) picks its scale
+    const int sr = valid ? scale_exp(dmax * rstd * bet[D] + bet[D + 1]) : 0;
     if (k == 0) rscale[row] = sr;
     const float sc = exp2i(sr);
     uint32_t hi[12], lo[12];
@@ -545,6 +539,19 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
     for (int i = tid; i < D; i += kThreads) {
         gam[i] = p.ln_w[i];
         bet[i] = p.ln_b[i];
+    }
+    if (warp == 1) {  // max |gamma|, max |beta| after beta
+        float gm = 0.f, bm = 0.f;
+        for (int i = lane; i < D; i += 32) {
+            gm = fmaxf(gm, fabsf(p.ln_w[i]));
+            bm = fmaxf(bm, fabsf(p.ln_b[i]));
+        }
+        gm = warp_max(gm);
+        bm = warp_max(bm);
+        if (lane == 0) {
+            bet[D] = gm;
+            bet[D + 1] = bm;
+        }
     }
     if (tid < 4) sw_s[tid] = hd->sw[tid];
     if (warp == 0) {
