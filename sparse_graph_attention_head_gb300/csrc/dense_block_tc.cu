@@ -25,11 +25,15 @@
 //   control warp (lane 0): streams the pre-split weight chunks (Q K V O,
 //       96 rows each) through a 2-slot shared-memory ring with bulk copies,
 //       issues Q|K|V once LayerNorm(t) is in TMEM and tile t-1's readers of
-//       those columns are done, and the out-projection once the context is;
-//   A (16 warps): the relation MLP in fp32, one thread per node pair
-//       (features prefetched into shared memory by cp.async, W1 and W2 read
-//       as shared-memory broadcasts, packed f32x2 FMAs): b1, SiLU, W2, b2 and
-//       the edge mask (-inf where masked) give the bias of all heads;
+//       those columns are done, each relation-MLP block once its features
+//       are in TMEM, and the out-projection once the context is;
+//   A (quad q = warps 4q..4q+3): the relation MLP, one thread per node pair
+//       of 128-pair blocks q, q + 4, ...: the pair's 16 features (prefetched
+//       into shared memory by cp.async) go, split and scaled, to its TMEM lane
+//       as the A operand of W1 (128 x 16 x 16 MMAs, in TMEM columns idle
+//       until the next tile's LayerNorm); the same thread reads the hidden
+//       values back and applies b1, SiLU, W2, b2 (packed f32x2 FMAs) and the
+//       edge mask (-inf where masked), giving the bias of all heads;
 //   B (warp (g, h) = (w % 4, w / 4)): attention of head h in graph g, one
 //       thread per query node: Q row from TMEM, K and V rows staged in shared
 //       memory, scores + bias in log2 units, two-pass softmax with ex2,
@@ -60,21 +64,28 @@ constexpr int kChunks = 4;                        // weight chunks per tile: Q K
 constexpr int kRing = 2;
 constexpr uint32_t kChunkHalf = D * D * 2;        // one of hi / lo, fp16
 constexpr uint32_t kChunkBytes = 2 * kChunkHalf;
+constexpr uint32_t kW1Half = P * P * 2;           // W1 image, one of hi / lo
 constexpr int kNodeStride = 100;                  // floats per staged node row
 // TMEM columns (32-bit): fp32 accumulators, or fp16 pairs for A operands
 // A operands (x_n, then the context) at column 288 (even tiles) or 384 (odd)
 // (hi: kAHalf columns of fp16 pairs for the D inputs, then lo)
 __host__ __device__ constexpr uint32_t col_a(int t) { return (t & 1) ? 384u : 288u; }
 constexpr uint32_t kAHalf = D / 2;
+// relation-MLP slot of quad q in tile t: A hi (8) | A lo (8) | D (16) columns,
+// in the next tile's A region (idle until its LayerNorm) or columns 480-511
+__host__ __device__ constexpr uint32_t mlp_col(int t, int q) {
+    return q < 3 ? col_a(t + 1) + 32u * q : 480u;
+}
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 1000000000ull;       // a wait gives up after 1 s (never expected)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Workspace written by the prep kernel: header, then the weight images.
 constexpr size_t kWsChunks = 256;
-constexpr size_t kWsBytes = kWsChunks + (size_t)kChunks * kChunkBytes;
+constexpr size_t kWsW1 = kWsChunks + (size_t)kChunks * kChunkBytes;
+constexpr size_t kWsBytes = kWsW1 + 2 * kW1Half;
 struct WsHeader {
-    int32_t sw[4];  // scale exponents of Wq, Wk, Wv, Wout
+    int32_t sw[5];  // scale exponents of Wq, Wk, Wv, Wout, W1
     int32_t err;    // set when a bounded wait gives up
 };
 
@@ -277,16 +288,17 @@ __device__ __forceinline__ float ex2(float x) {
 // ---------------------------------------------------------------------------
 constexpr int kPrepThreads = 256;
 
-// Block m: matrix m of (Wq, Wk, Wv, Wout), all D rows.
+// Block m: matrix m of (Wq, Wk, Wv, Wout, W1), all rows.
 __global__ void __launch_bounds__(kPrepThreads)
 dense_prep_kernel(const float *__restrict__ Wq, const float *__restrict__ Wk,
                   const float *__restrict__ Wv, const float *__restrict__ Wout,
-                  unsigned char *__restrict__ ws) {
+                  const float *__restrict__ W1, unsigned char *__restrict__ ws) {
     __shared__ float red[kPrepThreads / 32];
     const int m = blockIdx.x, tid = threadIdx.x;
-    const float *W = m == 0 ? Wq : m == 1 ? Wk : m == 2 ? Wv : Wout;
+    const float *W = m == 0 ? Wq : m == 1 ? Wk : m == 2 ? Wv : m == 3 ? Wout : W1;
+    const int K = m < 4 ? D : P;  // square matrices
     float mx = 0.f;
-    for (int i = tid; i < D * D; i += kPrepThreads) mx = fmaxf(mx, fabsf(__ldg(W + i)));
+    for (int i = tid; i < K * K; i += kPrepThreads) mx = fmaxf(mx, fabsf(__ldg(W + i)));
     mx = warp_max(mx);
     if ((tid & 31) == 0) red[tid >> 5] = mx;
     __syncthreads();
@@ -300,15 +312,16 @@ dense_prep_kernel(const float *__restrict__ Wq, const float *__restrict__ Wk,
         if (m == 0) hd->err = 0;
     }
     const float sc = exp2i(s);
-    unsigned char *dst = ws + kWsChunks + (size_t)m * kChunkBytes;
-    for (int i = tid; i < D * D / 2; i += kPrepThreads) {
-        const int n = i / (D / 2), k = 2 * (i % (D / 2));
-        const float *src = W + (int64_t)n * D + k;
+    unsigned char *dst = ws + (m < 4 ? kWsChunks + (size_t)m * kChunkBytes : kWsW1);
+    const uint32_t half = m < 4 ? kChunkHalf : kW1Half;
+    for (int i = tid; i < K * K / 2; i += kPrepThreads) {
+        const int n = i / (K / 2), k = 2 * (i % (K / 2));
+        const float *src = W + (int64_t)n * K + k;
         uint32_t hi, lo;
         split2(__ldg(src) * sc, __ldg(src + 1) * sc, hi, lo);
-        const uint32_t off = kmaj16(n, k, D);
+        const uint32_t off = kmaj16(n, k, K);
         *reinterpret_cast<uint32_t *>(dst + off) = hi;
-        *reinterpret_cast<uint32_t *>(dst + kChunkHalf + off) = lo;
+        *reinterpret_cast<uint32_t *>(dst + half + off) = lo;
     }
 }
 
@@ -345,7 +358,8 @@ struct Smem {
     }
     __host__ __device__ static uint32_t nodes(int N) { return stage(N) + stage_bytes(N); }
     __host__ __device__ static uint32_t nodes_bytes(int N) { return kGraphs * N * kNodeStride * 4; }
-    // W1 transposed [c][u], b1, W2 transposed [u][h], b2, gamma, beta
+    // W1 image (fp16 hi | lo, the MMA's B operand), b1, W2 transposed [u][h], b2,
+    // gamma, beta, max |gamma|, max |beta|
     __host__ __device__ static uint32_t params(int N) { return nodes(N) + nodes_bytes(N); }
     static constexpr uint32_t params_bytes = (P * P + P + P * H + H + 2 * D + 4) * 4;
     __host__ __device__ static uint32_t rscale(int N) { return params(N) + params_bytes; }
@@ -353,14 +367,15 @@ struct Smem {
 };
 
 struct Barriers {
-    uint64_t wfull[kRing], wdone[kRing], xfull, edone, qkv, cfull, ofull, drain;
+    uint64_t wfull[kRing], wdone[kRing], afull[4], dfull[4], xfull, edone, qkv, cfull, ofull, drain;
 };
 
 // Control thread: weight ring and every MMA issue, driven by mbarriers.
 __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, uint32_t tmem,
-                             int n_my, int32_t *err) {
+                             int n_my, int nblk, const float *w1img, int32_t *err) {
     const int total = kChunks * n_my;
     uint32_t ph_wfull = 0, ph_wdone = 0;  // expected parity per ring slot, one bit each
+    uint32_t ph_afull = 0;                // and per relation-MLP slot
     const unsigned char *src0 = p.ws + kWsChunks;
     const uint32_t ring0 = smem_u32(sm + Smem::ring);
     auto load = [&](int r) {
@@ -377,17 +392,34 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
     };
     int loaded = 0, issued = 0, refill = 0;
     for (; loaded < total && loaded < kRing; ++loaded) load(loaded);
-    constexpr uint32_t idesc = idesc_f16(D, 128);
+    constexpr uint32_t idesc = idesc_f16(D, 128), idesc_m = idesc_f16(P, 128);
+    const uint32_t w1h = smem_u32(w1img);
+    const uint64_t w1dh = smem_desc(w1h, 128, 256), w1dl = smem_desc(w1h + kW1Half, 128, 256);
     bool bail = false;
     for (int t = 0; t < n_my && !bail; ++t) {
         // Q|K|V(t) overwrite columns [0, 288) that tile t-1's attention and
         // epilogue read: wait for LayerNorm(t) and for tile t-1's readers
         bool x_ok = false, e_ok = t == 0, c_ok = false;
+        int mlp_left = nblk;
         uint64_t idle_since = 0;
         uint32_t idle = 0;
         const uint32_t acol = col_a(t);
-        while (issued < kChunks * (t + 1)) {
+        while (issued < kChunks * (t + 1) || mlp_left > 0) {
             bool progress = false;
+            // relation-MLP blocks whose features are in TMEM
+            for (int q = 0; q < 4 && mlp_left > 0; ++q) {
+                if (mbar_test(&br.afull[q], (ph_afull >> q) & 1u)) {
+                    ph_afull ^= 1u << q;
+                    fence_after();
+                    const uint32_t base = tmem + mlp_col(t, q);
+                    mma_ts(base + 16, base, w1dh, idesc_m, 0);
+                    mma_ts(base + 16, base, w1dl, idesc_m, 1);
+                    mma_ts(base + 16, base + 8, w1dh, idesc_m, 1);
+                    mma_commit(&br.dfull[q]);
+                    --mlp_left;
+                    progress = true;
+                }
+            }
             if (refill < issued && loaded < total) {
                 const int s = refill % kRing;
                 if (mbar_test(&br.wdone[s], (ph_wdone >> s) & 1u)) {
@@ -397,6 +429,8 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
                     progress = true;
                 }
             }
+            if (issued == kChunks * (t + 1)) goto next;  // only relation-MLP blocks left
+            {
             const int c = issued % kChunks, s = issued % kRing;
             if (!x_ok) x_ok = mbar_test(&br.xfull, (uint32_t)t & 1u);
             if (!e_ok) e_ok = mbar_test(&br.edone, (uint32_t)(t - 1) & 1u);
@@ -422,6 +456,8 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
                 ++issued;
                 progress = true;
             }
+            }
+        next:
             if (progress) {
                 idle = 0;
             } else if ((++idle & 63) == 0) {
@@ -516,14 +552,14 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ Barriers br;
     __shared__ uint32_t tmem_slot;
-    __shared__ int32_t sw_s[4];
+    __shared__ int32_t sw_s[5];
     __shared__ int32_t vmax_s[kGraphs];
     const int N = p.N, NN = N * N, NS = N + 1;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const WsHeader *hd = reinterpret_cast<const WsHeader *>(p.ws);
     int32_t *err = const_cast<int32_t *>(&hd->err);
     float *prm = reinterpret_cast<float *>(sm + Smem::params(N));
-    float *w1t = prm, *b1s = w1t + P * P, *w2t = b1s + P, *b2s = w2t + P * H, *gam = b2s + H,
+    float *w1img = prm, *b1s = w1img + P * P, *w2t = b1s + P, *b2s = w2t + P * H, *gam = b2s + H,
           *bet = gam + D;
     float *red = reinterpret_cast<float *>(sm + Smem::bias);  // LayerNorm statistics (phase C)
     int32_t *rscale = reinterpret_cast<int32_t *>(sm + Smem::rscale(N));
@@ -532,7 +568,12 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
     float *stage_base = reinterpret_cast<float *>(sm + Smem::stage(N));
 
     // ---- set-up: parameters, barriers, TMEM
-    for (int i = tid; i < P * P; i += kThreads) w1t[(i % P) * P + i / P] = p.W1[i];  // [c][u]
+    {
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(p.ws + kWsW1);
+        uint32_t *dst = reinterpret_cast<uint32_t *>(w1img);
+        for (int i = tid; i < (int)(2 * kW1Half / 4); i += kThreads) dst[i] = src[i];
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // read by the tensor cores
+    }
     for (int i = tid; i < P; i += kThreads) b1s[i] = p.b1[i];
     for (int i = tid; i < H * P; i += kThreads) w2t[(i % P) * H + i / P] = p.W2[i];  // [u][h]
     for (int i = tid; i < H; i += kThreads) b2s[i] = p.b2[i];
@@ -553,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             bet[D + 1] = bm;
         }
     }
-    if (tid < 4) sw_s[tid] = hd->sw[tid];
+    if (tid < 5) sw_s[tid] = hd->sw[tid];
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&tmem_slot)),
@@ -564,6 +605,10 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         for (int s = 0; s < kRing; ++s) {
             mbar_init(&br.wfull[s], 1);
             mbar_init(&br.wdone[s], 1);
+        }
+        for (int q = 0; q < 4; ++q) {
+            mbar_init(&br.afull[q], 128);
+            mbar_init(&br.dfull[q], 1);
         }
         mbar_init(&br.xfull, kComputeThreads);
         mbar_init(&br.edone, kComputeThreads);
@@ -581,13 +626,14 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
     const int n_my = blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
     if (warp == kComputeWarps) {
-        if (lane == 0) control_loop(p, sm, br, tmem, n_my, err);
+        if (lane == 0) control_loop(p, sm, br, tmem, n_my, (kGraphs * NN + 127) / 128, w1img, err);
         __syncwarp();
     } else {
         const int g = warp & 3, h = warp >> 2, n = lane;  // graph (lane quarter), head, node
         const uint32_t lane_q = (uint32_t)(32 * g) << 16;
         const float qk_scale = kLog2e / sqrtf((float)DH);  // scores in log2 units
-        const int nwb = (kGraphs * NN + 31) / 32;           // 32-pair relation-MLP blocks per tile
+        const int nblk = (kGraphs * NN + 127) / 128;        // 128-pair relation-MLP blocks per tile
+        const int quad = warp >> 2;                         // relation-MLP blocks quad, quad + 4, ...
         uint32_t ph_qkv = 0, ph_of = 0;
 
         // node rows of tile `tl` into the staging buffer (all compute threads)
@@ -605,8 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         // this thread's relation-MLP prefetch slot: 16 features and the mask value
         const float4 *pslot = reinterpret_cast<const float4 *>(stage_base + tid * P);
         const float *mslot = stage_base + kComputeThreads * P + tid;
-        auto fetch_pairs = [&](int tl, int wb) {
-            const int pi = 32 * wb + lane;
+        auto fetch_pairs = [&](int tl, int blk) {
+            const int pi = 128 * blk + 32 * g + lane;
             const int64_t pg = (int64_t)tl * kGraphs * NN + pi;
             if (pi < kGraphs * NN && (int64_t)tl * kGraphs + pi / NN < p.B) {
 #pragma unroll
@@ -622,14 +668,14 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         // prologue: LayerNorm of the first tile; its relation-MLP prefetch
         if (n_my > 0) {
             fetch_nodes(blockIdx.x);
-            if (warp < nwb) fetch_pairs(blockIdx.x, warp);
+            if (quad < nblk) fetch_pairs(blockIdx.x, quad);
             asm volatile("cp.async.wait_all;" ::: "memory");
             named_sync(1, kComputeThreads);
             layer_norm(p, nodes_s, red, rscale, gam, bet, tmem, col_a(0), blockIdx.x, warp, lane);
             mbar_arrive(&br.xfull);
             named_sync(1, kComputeThreads);  // statistics read: the bias region is free
         }
-        uint32_t ph_ed = 0;
+        uint32_t ph_ed = 0, ph_df = 0;
 
         for (int it = 0; it < n_my; ++it) {
             const int tile = blockIdx.x + it * gridDim.x;
@@ -638,51 +684,62 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             const bool rvalid = b < p.B && n < N;
             if (tid < kGraphs) vmax_s[tid] = 0;
 
-            // ======== phase A: relation MLP, thread = pair (warp-blocks w, w + 16, ...)
+            // ======== phase A: relation MLP, thread = pair 32 g + n of 128-pair blocks
+            // quad, quad + 4, ...: the first layer on the tensor cores (its features,
+            // scaled and split, are the A operand in this quad's TMEM slot)
             bool guard = it > 0;  // the last LayerNorm's statistics share the bias region
-            for (int wb = warp; wb < nwb; wb += kComputeWarps) {
-                const int pi = 32 * wb + lane;
+            const uint32_t mslot_t = tmem + lane_q + mlp_col(it, quad);
+            for (int blk = quad; blk < nblk; blk += 4) {
+                const int pi = 128 * blk + 32 * g + lane;
                 const bool valid = pi < kGraphs * NN && (int64_t)tile * kGraphs + pi / NN < p.B;
                 asm volatile("cp.async.wait_all;" ::: "memory");
-                float2 x2[P / 2];
+                float pf[P];
 #pragma unroll
                 for (int c = 0; c < P / 4; ++c) {
                     const float4 v = valid ? pslot[c] : make_float4(0.f, 0.f, 0.f, 0.f);
-                    x2[2 * c] = make_float2(v.x, v.y);
-                    x2[2 * c + 1] = make_float2(v.z, v.w);
+                    pf[4 * c] = v.x;
+                    pf[4 * c + 1] = v.y;
+                    pf[4 * c + 2] = v.z;
+                    pf[4 * c + 3] = v.w;
                 }
                 const float mask_v = *mslot;
-                if (wb + kComputeWarps < nwb) fetch_pairs(tile, wb + kComputeWarps);
-                // hidden = W1 x + b1 as 8 unit pairs (u, u + 1)
-                float2 hid[P / 2];
+                if (blk + 4 < nblk) fetch_pairs(tile, blk + 4);
+                float mx = 0.f;
 #pragma unroll
-                for (int i = 0; i < P / 4; ++i) {
-                    const float4 bq = reinterpret_cast<const float4 *>(b1s)[i];
-                    hid[2 * i] = make_float2(bq.x, bq.y);
-                    hid[2 * i + 1] = make_float2(bq.z, bq.w);
+                for (int u = 0; u < P; ++u) mx = fmaxf(mx, fabsf(pf[u]));
+                const int sp = scale_exp(mx);
+                {
+                    const float sc = exp2i(sp);
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) split2(pf[2 * c] * sc, pf[2 * c + 1] * sc, hi[c], lo[c]);
+                    tmem_st8(mslot_t, hi);
+                    tmem_st8(mslot_t + 8, lo);
                 }
-#pragma unroll
-                for (int c = 0; c < P; ++c) {
-                    const float xc = (c & 1) ? x2[c >> 1].y : x2[c >> 1].x;
-                    const float2 xx = make_float2(xc, xc);
-                    const float4 *wr = reinterpret_cast<const float4 *>(w1t + c * P);
-#pragma unroll
-                    for (int i = 0; i < P / 4; ++i) {
-                        const float4 w = wr[i];
-                        hid[2 * i] = ffma2(make_float2(w.x, w.y), xx, hid[2 * i]);
-                        hid[2 * i + 1] = ffma2(make_float2(w.z, w.w), xx, hid[2 * i + 1]);
-                    }
-                }
-                // SiLU, then r = W2 silu + b2 as head pairs (0, 1), (2, 3)
+                tmem_st_done();
+                mbar_arrive(&br.afull[quad]);
+                mbar_wait(&br.dfull[quad], ph_df, err);
+                ph_df ^= 1u;
+                fence_after();
+                float hid[P];
+                tmem_ld16(mslot_t + 16, hid);
+                const float unsc = exp2i(-sp) * exp2i(-sw_s[4]);
+                // b1, SiLU, then r = W2 silu + b2 as head pairs (0, 1), (2, 3)
                 float2 r01 = make_float2(b2s[0], b2s[1]), r23 = make_float2(b2s[2], b2s[3]);
 #pragma unroll
-                for (int u = 0; u < P; ++u) {
-                    const float a = (u & 1) ? hid[u >> 1].y : hid[u >> 1].x;
-                    const float sl = __fdividef(a, 1.0f + __expf(-a));
-                    const float2 ss = make_float2(sl, sl);
-                    const float4 w = reinterpret_cast<const float4 *>(w2t)[u];
-                    r01 = ffma2(make_float2(w.x, w.y), ss, r01);
-                    r23 = ffma2(make_float2(w.z, w.w), ss, r23);
+                for (int u4 = 0; u4 < P / 4; ++u4) {
+                    const float4 bq = reinterpret_cast<const float4 *>(b1s)[u4];
+                    const float bb[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int u = 4 * u4 + i;
+                        const float a = fmaf(hid[u], unsc, bb[i]);
+                        const float sl = __fdividef(a, 1.0f + __expf(-a));
+                        const float2 ss = make_float2(sl, sl);
+                        const float4 w = reinterpret_cast<const float4 *>(w2t)[u];
+                        r01 = ffma2(make_float2(w.x, w.y), ss, r01);
+                        r23 = ffma2(make_float2(w.z, w.w), ss, r23);
+                    }
                 }
                 if (guard) {  // every thread is past that LayerNorm once tile it-1 is done
                     mbar_wait(&br.edone, ph_ed, err);
@@ -781,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                                     : make_float2(0.f, 0.f);
             }
             named_sync(1, kComputeThreads);  // every graph's largest |V| known; staging free
-            if (it + 1 < n_my && warp < nwb) fetch_pairs(tile + gridDim.x, warp);
+            if (it + 1 < n_my && quad < nblk) fetch_pairs(tile + gridDim.x, quad);
             // the context (|ctx| <= max |V| of the graph) as the out-projection's A operand
             const int sc_g = scale_exp(__int_as_float(vmax_s[g]));
             {
@@ -869,7 +926,7 @@ gat_status_t dense_block_tc(int32_t B, int32_t N, int32_t D, int32_t H, int32_t 
                     "gat_dense_masked_attention: this shape needs a 16-byte aligned workspace of "
                     "%zu bytes (got %zu)", tc::kWsBytes, workspace_bytes);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
-    tc::dense_prep_kernel<<<4, tc::kPrepThreads, 0, s>>>(Wq, Wk, Wv, Wout, ws);
+    tc::dense_prep_kernel<<<5, tc::kPrepThreads, 0, s>>>(Wq, Wk, Wv, Wout, W1, ws);
     gat_status_t st = check_launch("gat_dense_masked_attention (weight prep)");
     if (st != GAT_OK) return st;
     const uint32_t smem = tc::Smem::total(N);
