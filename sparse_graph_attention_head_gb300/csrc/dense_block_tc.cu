@@ -65,7 +65,7 @@ constexpr int kRing = 2;
 constexpr uint32_t kChunkHalf = D * D * 2;        // one of hi / lo, fp16
 constexpr uint32_t kChunkBytes = 2 * kChunkHalf;
 constexpr uint32_t kW1Half = P * P * 2;           // W1 image, one of hi / lo
-constexpr int kNodeStride = 100;                  // floats per staged node row
+constexpr int kNodeStride = D;                    // staged node rows are contiguous (one bulk copy)
 // TMEM columns (32-bit): fp32 accumulators, or fp16 pairs for A operands
 // A operands (x_n, then the context) at column 288 (even tiles) or 384 (odd)
 // (hi: kAHalf columns of fp16 pairs for the D inputs, then lo)
@@ -367,15 +367,14 @@ struct Smem {
 };
 
 struct Barriers {
-    uint64_t wfull[kRing], wdone[kRing], afull[4], dfull[4], xfull, edone, qkv, cfull, ofull, drain;
+    uint64_t wfull[kRing], wdone[kRing], dfull[4], nfull, xfull, edone, qkv, cfull, ofull, drain;
 };
 
 // Control thread: weight ring and every MMA issue, driven by mbarriers.
 __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, uint32_t tmem,
-                             int n_my, int nblk, const float *w1img, int32_t *err) {
+                             int n_my, const float *nodes_s, int32_t *err) {
     const int total = kChunks * n_my;
     uint32_t ph_wfull = 0, ph_wdone = 0;  // expected parity per ring slot, one bit each
-    uint32_t ph_afull = 0;                // and per relation-MLP slot
     const unsigned char *src0 = p.ws + kWsChunks;
     const uint32_t ring0 = smem_u32(sm + Smem::ring);
     auto load = [&](int r) {
@@ -392,34 +391,32 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
     };
     int loaded = 0, issued = 0, refill = 0;
     for (; loaded < total && loaded < kRing; ++loaded) load(loaded);
-    constexpr uint32_t idesc = idesc_f16(D, 128), idesc_m = idesc_f16(P, 128);
-    const uint32_t w1h = smem_u32(w1img);
-    const uint64_t w1dh = smem_desc(w1h, 128, 256), w1dl = smem_desc(w1h + kW1Half, 128, 256);
+    constexpr uint32_t idesc = idesc_f16(D, 128);
+    // a tile's node rows (contiguous graphs) into the staging buffer, one bulk copy
+    auto load_nodes = [&](int tl) {
+        const int64_t b0 = (int64_t)tl * kGraphs;
+        const int64_t ng = p.B - b0 < kGraphs ? p.B - b0 : kGraphs;
+        const uint32_t bytes = (uint32_t)(ng * p.N * D * 4);
+        const uint32_t bar = smem_u32(&br.nfull);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                     : "memory");
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+            "[%3];" ::"r"(smem_u32(nodes_s)),
+            "l"(p.nodes + b0 * p.N * D), "r"(bytes), "r"(bar)
+            : "memory");
+    };
+    if (n_my > 0) load_nodes(blockIdx.x);
     bool bail = false;
     for (int t = 0; t < n_my && !bail; ++t) {
         // Q|K|V(t) overwrite columns [0, 288) that tile t-1's attention and
         // epilogue read: wait for LayerNorm(t) and for tile t-1's readers
         bool x_ok = false, e_ok = t == 0, c_ok = false;
-        int mlp_left = nblk;
         uint64_t idle_since = 0;
         uint32_t idle = 0;
         const uint32_t acol = col_a(t);
-        while (issued < kChunks * (t + 1) || mlp_left > 0) {
+        while (issued < kChunks * (t + 1)) {
             bool progress = false;
-            // relation-MLP blocks whose features are in TMEM
-            for (int q = 0; q < 4 && mlp_left > 0; ++q) {
-                if (mbar_test(&br.afull[q], (ph_afull >> q) & 1u)) {
-                    ph_afull ^= 1u << q;
-                    fence_after();
-                    const uint32_t base = tmem + mlp_col(t, q);
-                    mma_ts(base + 16, base, w1dh, idesc_m, 0);
-                    mma_ts(base + 16, base, w1dl, idesc_m, 1);
-                    mma_ts(base + 16, base + 8, w1dh, idesc_m, 1);
-                    mma_commit(&br.dfull[q]);
-                    --mlp_left;
-                    progress = true;
-                }
-            }
             if (refill < issued && loaded < total) {
                 const int s = refill % kRing;
                 if (mbar_test(&br.wdone[s], (ph_wdone >> s) & 1u)) {
@@ -429,10 +426,13 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
                     progress = true;
                 }
             }
-            if (issued == kChunks * (t + 1)) goto next;  // only relation-MLP blocks left
             {
             const int c = issued % kChunks, s = issued % kRing;
-            if (!x_ok) x_ok = mbar_test(&br.xfull, (uint32_t)t & 1u);
+            if (!x_ok) {
+                x_ok = mbar_test(&br.xfull, (uint32_t)t & 1u);
+                // LayerNorm(t) has read the staged rows: the next tile's go there
+                if (x_ok && t + 1 < n_my) load_nodes(blockIdx.x + (t + 1) * gridDim.x);
+            }
             if (!e_ok) e_ok = mbar_test(&br.edone, (uint32_t)(t - 1) & 1u);
             if (c == kChunks - 1 && !c_ok) c_ok = mbar_test(&br.cfull, (uint32_t)t & 1u);
             const bool ready = c < kChunks - 1 ? (x_ok && e_ok) : c_ok;
@@ -457,7 +457,6 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
                 progress = true;
             }
             }
-        next:
             if (progress) {
                 idle = 0;
             } else if ((++idle & 63) == 0) {
@@ -606,10 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             mbar_init(&br.wfull[s], 1);
             mbar_init(&br.wdone[s], 1);
         }
-        for (int q = 0; q < 4; ++q) {
-            mbar_init(&br.afull[q], 128);
-            mbar_init(&br.dfull[q], 1);
-        }
+        for (int q = 0; q < 4; ++q) mbar_init(&br.dfull[q], 1);
+        mbar_init(&br.nfull, 1);
         mbar_init(&br.xfull, kComputeThreads);
         mbar_init(&br.edone, kComputeThreads);
         mbar_init(&br.qkv, 1);
@@ -626,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
     const int n_my = blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
     if (warp == kComputeWarps) {
-        if (lane == 0) control_loop(p, sm, br, tmem, n_my, (kGraphs * NN + 127) / 128, w1img, err);
+        if (lane == 0) control_loop(p, sm, br, tmem, n_my, nodes_s, err);
         __syncwarp();
     } else {
         const int g = warp & 3, h = warp >> 2, n = lane;  // graph (lane quarter), head, node
@@ -636,18 +633,6 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         const int quad = warp >> 2;                         // relation-MLP blocks quad, quad + 4, ...
         uint32_t ph_qkv = 0, ph_of = 0;
 
-        // node rows of tile `tl` into the staging buffer (all compute threads)
-        auto fetch_nodes = [&](int tl) {
-            const int rows = kGraphs * N;
-            for (int i = tid; i < rows * (D / 4); i += kComputeThreads) {
-                const int r = i / (D / 4), c = i % (D / 4), gg = r / N;
-                const int64_t b = (int64_t)tl * kGraphs + gg;
-                if (b < p.B)
-                    cp_async16(smem_u32(nodes_s + r * kNodeStride + 4 * c),
-                               p.nodes + (b * N + (r - gg * N)) * (int64_t)D + 4 * c);
-            }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-        };
         // this thread's relation-MLP prefetch slot: 16 features and the mask value
         const float4 *pslot = reinterpret_cast<const float4 *>(stage_base + tid * P);
         const float *mslot = stage_base + kComputeThreads * P + tid;
@@ -667,10 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
 
         // prologue: LayerNorm of the first tile; its relation-MLP prefetch
         if (n_my > 0) {
-            fetch_nodes(blockIdx.x);
             if (quad < nblk) fetch_pairs(blockIdx.x, quad);
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            named_sync(1, kComputeThreads);
+            mbar_wait(&br.nfull, 0, err);  // the first tile's node rows
             layer_norm(p, nodes_s, red, rscale, gam, bet, tmem, col_a(0), blockIdx.x, warp, lane);
             mbar_arrive(&br.xfull);
             named_sync(1, kComputeThreads);  // statistics read: the bias region is free
@@ -685,11 +668,16 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             if (tid < kGraphs) vmax_s[tid] = 0;
 
             // ======== phase A: relation MLP, thread = pair 32 g + n of 128-pair blocks
-            // quad, quad + 4, ...: the first layer on the tensor cores (its features,
-            // scaled and split, are the A operand in this quad's TMEM slot)
+            // quad, quad + 4, ...: the first layer on the tensor cores (the pair's
+            // features, scaled and split, are the A operand in this quad's TMEM slot;
+            // the quad's first thread issues its MMAs). Software-pipelined: block i's
+            // hidden values are read back, block i + 1 is split and issued, then block
+            // i's epilogue runs while the tensor cores work.
             bool guard = it > 0;  // the last LayerNorm's statistics share the bias region
-            const uint32_t mslot_t = tmem + lane_q + mlp_col(it, quad);
-            for (int blk = quad; blk < nblk; blk += 4) {
+            const uint32_t slot_col = mlp_col(it, quad);
+            const uint32_t mslot_t = tmem + lane_q + slot_col;
+            const bool issuer = (warp & 3) == 0 && lane == 0;
+            auto split_issue = [&](int blk, int &sp, float &mk) {
                 const int pi = 128 * blk + 32 * g + lane;
                 const bool valid = pi < kGraphs * NN && (int64_t)tile * kGraphs + pi / NN < p.B;
                 asm volatile("cp.async.wait_all;" ::: "memory");
@@ -702,28 +690,47 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                     pf[4 * c + 2] = v.z;
                     pf[4 * c + 3] = v.w;
                 }
-                const float mask_v = *mslot;
+                mk = valid ? *mslot : 1.f;
                 if (blk + 4 < nblk) fetch_pairs(tile, blk + 4);
                 float mx = 0.f;
 #pragma unroll
                 for (int u = 0; u < P; ++u) mx = fmaxf(mx, fabsf(pf[u]));
-                const int sp = scale_exp(mx);
-                {
-                    const float sc = exp2i(sp);
-                    uint32_t hi[8], lo[8];
+                sp = scale_exp(mx);
+                const float sc = exp2i(sp);
+                uint32_t hi[8], lo[8];
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) split2(pf[2 * c] * sc, pf[2 * c + 1] * sc, hi[c], lo[c]);
-                    tmem_st8(mslot_t, hi);
-                    tmem_st8(mslot_t + 8, lo);
-                }
+                for (int c = 0; c < 8; ++c) split2(pf[2 * c] * sc, pf[2 * c + 1] * sc, hi[c], lo[c]);
+                tmem_st8(mslot_t, hi);
+                tmem_st8(mslot_t + 8, lo);
                 tmem_st_done();
-                mbar_arrive(&br.afull[quad]);
+                named_sync(2 + quad, 128);  // the block's 128 rows are in TMEM
+                if (issuer) {
+                    fence_after();
+                    const uint32_t base = tmem + slot_col;
+                    constexpr uint32_t idesc_m = idesc_f16(P, 128);
+                    const uint32_t w1h = smem_u32(w1img);
+                    const uint64_t w1dh = smem_desc(w1h, 128, 256);
+                    const uint64_t w1dl = smem_desc(w1h + kW1Half, 128, 256);
+                    mma_ts(base + 16, base, w1dh, idesc_m, 0);
+                    mma_ts(base + 16, base, w1dl, idesc_m, 1);
+                    mma_ts(base + 16, base + 8, w1dh, idesc_m, 1);
+                    mma_commit(&br.dfull[quad]);
+                }
+            };
+            int sp = 0;
+            float mk = 1.f;
+            if (quad < nblk) split_issue(quad, sp, mk);
+            for (int blk = quad; blk < nblk; blk += 4) {
+                const int pi = 128 * blk + 32 * g + lane;
+                const bool valid = pi < kGraphs * NN && (int64_t)tile * kGraphs + pi / NN < p.B;
                 mbar_wait(&br.dfull[quad], ph_df, err);
                 ph_df ^= 1u;
                 fence_after();
                 float hid[P];
                 tmem_ld16(mslot_t + 16, hid);
                 const float unsc = exp2i(-sp) * exp2i(-sw_s[4]);
+                const float mask_v = mk;
+                if (blk + 4 < nblk) split_issue(blk + 4, sp, mk);
                 // b1, SiLU, then r = W2 silu + b2 as head pairs (0, 1), (2, 3)
                 float2 r01 = make_float2(b2s[0], b2s[1]), r23 = make_float2(b2s[2], b2s[3]);
 #pragma unroll
@@ -757,9 +764,6 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 }
             }
             named_sync(1, kComputeThreads);  // every pair's bias written
-            // the next tile's node rows (the buffer's rows were normalised in the
-            // last phase C), for its LayerNorm in this tile's phase C
-            if (it + 1 < n_my) fetch_nodes(tile + gridDim.x);
             mbar_wait(&br.qkv, ph_qkv, err);
             ph_qkv ^= 1u;
             fence_after();
@@ -863,8 +867,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 xres[c] = rvalid ? __ldg(reinterpret_cast<const float4 *>(x) + c)
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
             if (it + 1 < n_my) {
-                asm volatile("cp.async.wait_all;" ::: "memory");
-                named_sync(1, kComputeThreads);  // every thread's node rows landed
+                mbar_wait(&br.nfull, (uint32_t)(it + 1) & 1u, err);  // the next tile's node rows
                 layer_norm(p, nodes_s, red, rscale, gam, bet, tmem, col_a(it + 1),
                            tile + gridDim.x, warp, lane);
                 mbar_arrive(&br.xfull);
