@@ -588,6 +588,22 @@ def bench_small(name, args):
                  "bytes_vs_bf16_layer": alg_bytes / fused_bytes(g["n_rows"], g["n_edges"],
                                                                  g["H"], g["Dh"]),
                  "error_vs_bf16_layer": err}
+    elif name == "sddmm_csr":
+        # per-edge scores of the fused workload's graph: out[e,h] = q[row]·k[col]/8,
+        # 1e6 rows, Zipf(2.1) degrees, H=8, Dh=64, bf16 q/k, fp32 [E,8] out
+        g = W.make_fused(seed=3, n=args.n_rows)
+        bt = lambda a: t(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+        rp, ci = t(g["row_ptr"]), t(g["col_idx"])
+        q, k = bt(g["q"]), bt(g["k"])
+        out = torch.empty((g["n_edges"], g["H"]), dtype=torch.float32, device=dev)
+        fn = lambda: gat.gat_sddmm(ci, k, q, g["H"], g["Dh"], scale=g["scale"],  # noqa: E731
+                                   row_ptr=rp, out=out)
+        units, launches = g["n_edges"] * g["H"], 1
+        rb = 2 * g["H"] * g["Dh"]
+        # per row: row_ptr entry and q row; per edge: col_idx entry, k row of the
+        # source, H fp32 scores out
+        alg_bytes = g["n_rows"] * (4 + rb) + g["n_edges"] * (4 + rb + 4 * g["H"])
+        flops = 2.0 * g["n_edges"] * g["H"] * g["Dh"]
     elif name == "edge_softmax_h8":
         # 8 heads on the 1e6-row power-law graph
         deg = W.zipf_degrees(np.random.default_rng(3), 1_000_000)
@@ -690,7 +706,7 @@ def main():
     ap.add_argument("--impl", default="gat", choices=["gat", "reference"])
     ap.add_argument("--workload", default="fused",
                     choices=["fused", "edge_softmax", "aggregate", "sddmm", "dense", "spmm_heads",
-                             "edge_softmax_h8", "fused_backward", "fused_fp8"])
+                             "edge_softmax_h8", "fused_backward", "fused_fp8", "sddmm_csr"])
     ap.add_argument("--ref-rows", type=int, default=40000,
                     help="--impl reference: consecutive rows per step, split over the host's "
                          "cores (~0.2 s of oracle work on 16 cores)")
@@ -726,7 +742,7 @@ def main():
         if not args.no_extras:
             res["other_workloads"] = {}
             for nm in ("edge_softmax", "aggregate", "sddmm", "dense", "spmm_heads",
-                       "edge_softmax_h8", "fused_backward", "fused_fp8"):
+                       "edge_softmax_h8", "fused_backward", "fused_fp8", "sddmm_csr"):
                 try:
                     res["other_workloads"][nm] = bench_small(nm, args)
                 except Exception as exc:  # keep the headline line if a side workload fails

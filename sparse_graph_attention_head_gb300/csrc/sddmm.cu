@@ -7,9 +7,15 @@
 // warp-per-edge idea of the page's drafts narrowed to the head width) and the
 // group finishes with a xor-shuffle sum. Consecutive pairs of a warp are
 // consecutive heads of the same edge, so a warp reads whole feature rows.
-// CSR form: the destination row of an edge is found by binary search on
-// row_ptr.
-#include "common.cuh"
+// CSR form, row layouts the vector engine covers (sddmm_rows_kernel): each
+// warp takes an equal contiguous span of edges (balanced whatever the degree
+// distribution), finds the row of its first edge by one binary search on
+// row_ptr and walks the rows of its span; the destination row's features stay
+// in registers, spread over the lanes in 16-byte vectors as in the fused
+// layer, while U source rows per warp are in flight; a head is G adjacent
+// lanes (G-lane xor-shuffle sum) and one store per edge writes all its heads.
+// Other CSR layouts find each edge's row by binary search (sddmm_kernel).
+#include "row_engine.cuh"
 
 namespace gat {
 
@@ -72,12 +78,121 @@ sddmm_kernel(const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ sr
     }
 }
 
+// CSR SDDMM over equal edge spans per warp. V 16-byte vectors per lane (the
+// row is V * 32 vectors), G = Dh / VE lanes per head (G >= V), U edges in
+// flight per warp, MINB resident blocks per SM (the register budget).
+constexpr int kSddmmRowsThreads = 256;
+
+template <typename T, int V, int U, int MINB>
+__global__ void __launch_bounds__(kSddmmRowsThreads, MINB)
+sddmm_rows_kernel(const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
+                  int64_t n_rows, int64_t n_edges, const T *__restrict__ a,
+                  const T *__restrict__ b, int32_t H, int32_t Dh, float scale,
+                  float *__restrict__ out) {
+    constexpr int VE = Vec<T>::N;
+    const int lane = threadIdx.x & 31;
+    const int64_t n_warps = (int64_t)gridDim.x * (kSddmmRowsThreads / 32);
+    const int64_t w = (int64_t)blockIdx.x * (kSddmmRowsThreads / 32) + (threadIdx.x >> 5);
+    const int64_t e_begin = n_edges * w / n_warps, e_end = n_edges * (w + 1) / n_warps;
+    if (e_begin >= e_end) return;
+    const int G = Dh / VE;                          // lanes per head
+    const int64_t row_bytes = (int64_t)H * Dh * sizeof(T);
+    // the lane that stores head (s * 32 + lane) / G of this edge: lane % G == s
+    const int my_slot = lane % G;
+    const int my_head = my_slot < V ? (my_slot * 32 + lane) / G : 0;
+    const char *ab = reinterpret_cast<const char *>(a);
+    const char *bb = reinterpret_cast<const char *>(b);
+    int64_t r = row_of_edge(row_ptr, n_rows, e_begin);
+    int64_t e = e_begin;
+    while (e < e_end) {
+        int64_t rend = __ldg(row_ptr + r + 1);
+        while (rend <= e) {  // rows of degree 0
+            ++r;
+            rend = __ldg(row_ptr + r + 1);
+        }
+        float qf[V][VE];
+#pragma unroll
+        for (int s = 0; s < V; ++s) {
+            Vec<T>::unpack(ld_stream16(bb + r * row_bytes + (s * 32 + lane) * 16), qf[s]);
+#pragma unroll
+            for (int t = 0; t < VE; ++t) qf[s][t] *= scale;
+        }
+        const int64_t seg_end = rend < e_end ? rend : e_end;
+        for (int64_t base = e; base < seg_end; base += 32) {
+            const int n = (int)(seg_end - base < 32 ? seg_end - base : 32);
+            const int my_ci = lane < n ? __ldg(col_idx + base + lane) : 0;
+            for (int j0 = 0; j0 < n; j0 += U) {
+                uint4 kr[U][V];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t src = __shfl_sync(kFull, my_ci, (j0 + u) & 31);
+                    if (j0 + u < n) {
+#pragma unroll
+                        for (int s = 0; s < V; ++s)
+                            kr[u][s] = ld_stream16(ab + src * row_bytes + (s * 32 + lane) * 16);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    float part[V];
+#pragma unroll
+                    for (int s = 0; s < V; ++s) {
+                        float kf[VE];
+                        Vec<T>::unpack(kr[u][s], kf);
+                        float acc = 0.f;
+#pragma unroll
+                        for (int t = 0; t < VE; ++t) acc = fmaf(qf[s][t], kf[t], acc);
+                        part[s] = acc;
+                    }
+                    for (int o = 1; o < G; o <<= 1) {
+#pragma unroll
+                        for (int s = 0; s < V; ++s) part[s] += __shfl_xor_sync(kFull, part[s], o);
+                    }
+                    if (j0 + u < n && my_slot < V) {
+                        float val = part[0];
+#pragma unroll
+                        for (int s = 1; s < V; ++s) val = my_slot == s ? part[s] : val;
+                        out[(base + j0 + u) * H + my_head] = val;
+                    }
+                }
+            }
+        }
+        e = seg_end;
+    }
+}
+
+template <typename T, int V>
+static gat_status_t launch_sddmm_rows(const int32_t *row_ptr, const int32_t *ci, int64_t n_rows,
+                                      int64_t E, const void *a, const void *b, int32_t H,
+                                      int32_t Dh, float scale, float *out, cudaStream_t s) {
+    // 2 KB of source rows in flight per warp at 5 blocks of 8 warps per SM:
+    // a sweep on the 1e6-row workload (H=8, Dh=64, bf16) over 1-8 edges in
+    // flight x 1-8 blocks per SM put this at 2.84 ms, the rest at 2.9-4.5 ms
+    constexpr int U = V == 1 ? 4 : (V == 2 ? 2 : 1);
+    auto kern = sddmm_rows_kernel<T, V, U, 5>;
+    static std::atomic<int64_t> caps[kMaxDevices];
+    int64_t blocks = device_blocks(caps, kern, kSddmmRowsThreads, 0);
+    // at least ~32 edges per warp
+    const int64_t want = (E + 32 * (kSddmmRowsThreads / 32) - 1) / (32 * (kSddmmRowsThreads / 32));
+    if (blocks > want) blocks = want < 1 ? 1 : want;
+    kern<<<(unsigned)blocks, kSddmmRowsThreads, 0, s>>>(row_ptr, ci, n_rows, E,
+                                                       static_cast<const T *>(a),
+                                                       static_cast<const T *>(b), H, Dh, scale, out);
+    return check_launch("gat_sddmm (CSR rows)");
+}
+
 template <typename T>
 static gat_status_t launch_sddmm(const int32_t *row_ptr, const int32_t *si, const int32_t *di,
                                  int64_t n_rows, int64_t E, const void *a, const void *b,
                                  int32_t H, int32_t Dh, float scale, float *out, cudaStream_t s) {
     constexpr int VE = Vec<T>::N;
     const bool vec = (Dh % VE == 0) && aligned16(a) && aligned16(b);
+    int V = 0, LE = 0;
+    if (row_ptr && vec && engine_shape(H, Dh, sizeof(T), V, LE) && LE == 32 && Dh / VE >= V) {
+        if (V == 1) return launch_sddmm_rows<T, 1>(row_ptr, si, n_rows, E, a, b, H, Dh, scale, out, s);
+        if (V == 2) return launch_sddmm_rows<T, 2>(row_ptr, si, n_rows, E, a, b, H, Dh, scale, out, s);
+        if (V == 4) return launch_sddmm_rows<T, 4>(row_ptr, si, n_rows, E, a, b, H, Dh, scale, out, s);
+    }
     const int nv = vec ? Dh / VE : Dh;
     int G = 1;
     while (G < 32 && G * 2 <= nv) G *= 2;

@@ -393,6 +393,28 @@ def test_validate_graph(gat):
 # ----------------------------------------------------------------------------
 # full-size fused workload: 1e6 rows, Zipf(2.1) mean 16, H=8, Dh=64, bf16
 # ----------------------------------------------------------------------------
+@pytest.mark.parametrize("H,Dh,dtype", [(8, 64, "bf16"), (4, 64, "f32"), (16, 64, "bf16"),
+                                         (2, 32, "f32")])
+def test_sddmm_csr_row_walk_every_edge(gat, H, Dh, dtype):
+    """CSR SDDMM on a power-law graph with empty rows and one 3000-edge row,
+    every (edge, head) compared: the edge spans of the warps cut rows anywhere."""
+    rng = np.random.default_rng(70 + H)
+    deg = W.zipf_degrees(rng, 4000, dmax=600)
+    deg[[5, 6, 7, 100]] = [0, 0, 3000, 0]
+    rp, ci = W.make_csr(rng, deg, 2500, sort_within_rows=True)
+    n = deg.size
+    k32 = rng.standard_normal((2500, H, Dh)).astype(np.float32)
+    q32 = rng.standard_normal((n, H, Dh)).astype(np.float32)
+    if dtype == "bf16":
+        kb, qb = W.bf16_bits_from_f32(k32), W.bf16_bits_from_f32(q32)
+        kd, qd, ko, qo = dev_bf16(kb), dev_bf16(qb), kb, qb
+    else:
+        kd, qd, ko, qo = dev(k32), dev(q32), k32, q32
+    out = gat.gat_sddmm(dev(ci), kd, qd, H, Dh, scale=0.125, row_ptr=dev(rp))
+    o, c = oracle.sddmm(ci, ko, qo, H, Dh, scale=0.125, row_ptr=rp, want_cond=True)
+    assert_fp32(host(out), o, c, Dh, name=f"sddmm csr {H}x{Dh} {dtype}")
+
+
 @pytest.fixture(scope="module")
 def full_fused(gat):
     d, rp, ci, q, k, v = fused_case(1_000_000, 3)
@@ -408,6 +430,26 @@ def test_full_size_plan_bit_exact(gat, full_fused):
     np.testing.assert_array_equal(hr, ohr)
     np.testing.assert_array_equal(cs, ocs)
     np.testing.assert_array_equal(cr, ocr)
+
+
+def test_full_size_sddmm_csr_sampled_edges(gat, full_fused):
+    """The CSR SDDMM of the benchmark's sddmm_csr workload (the fused workload's
+    graph and q, k: 1e6 rows, H=8, Dh=64, bf16, scale 1/8): the edges of the
+    heaviest rows, of rows around zero-degree... every degree class, and random
+    edges against the oracle (COO form of the same edges)."""
+    d, rp, ci, q, k, v, _ = full_fused
+    out = host(gat.gat_sddmm(ci, k, q, d["H"], d["Dh"], scale=d["scale"], row_ptr=rp))
+    deg = np.diff(d["row_ptr"])
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([np.argsort(deg)[-6:], rng.integers(0, deg.size, 400),
+                                     [0, deg.size - 1]]))
+    edges = np.concatenate([np.arange(d["row_ptr"][r], d["row_ptr"][r + 1]) for r in rows])
+    edges = np.unique(np.concatenate([edges, rng.integers(0, d["n_edges"], 20000)]))
+    dst = np.searchsorted(d["row_ptr"], edges, side="right") - 1
+    o, c = oracle.sddmm(d["col_idx"][edges], d["k"], d["q"], d["H"], d["Dh"], scale=d["scale"],
+                        dst_idx=dst, want_cond=True)
+    assert_fp32(out[edges], o, c, d["Dh"], name="sddmm csr 1e6 rows")
+    assert np.isfinite(out).all()
 
 
 def test_full_size_fused_sampled_rows(gat, full_fused):
