@@ -438,6 +438,89 @@ def bench_fused(args, rank, world, local, dist):
     return res, d
 
 
+def shard_bounds(row_begin, row_ptr, rank):
+    """Rows [r0, r1) and edges [e0, e1) of a rank's row range."""
+    r0, r1 = int(row_begin[rank]), int(row_begin[rank + 1])
+    return r0, r1, int(row_ptr[r0]), int(row_ptr[r1])
+
+
+def node_shard(n, world, rank):
+    """Node rows [a, b) whose k / v a rank owns before the all-gather: equal
+    contiguous blocks of ceil(n / world) rows (the last may be short)."""
+    per = (n + world - 1) // world
+    return min(n, rank * per), min(n, (rank + 1) * per), per
+
+
+def bench_rowshard(args, rank, world, local, dist):
+    """--mode rowshard: the graph's rows cut into `world` contiguous ranges of
+    about equal traffic (gat_partition_rows); each rank owns the k / v rows of
+    an equal node block, and one step is an all-gather of k and of v into full
+    local tables, then the fused layer over the rank's own rows (the shard as
+    a graph of its own: gat_rebase_row_ptr, its own plan). The whole job is one
+    graph (strong scaling); value = all edge-heads / the slowest rank's step."""
+    import torch
+    import sparse_graph_attention_head_gb300 as gat
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    d = W.make_fused(seed=3, n=args.n_rows)
+    n, E, H, Dh = d["n_rows"], d["n_edges"], d["H"], d["Dh"]
+    rb = gat.gat_partition_rows(d["row_ptr"], world)
+    r0, r1, e0, e1 = shard_bounds(rb, d["row_ptr"], rank)
+    a, b, per = node_shard(n, world, rank)
+    rp_all = to_dev(torch, d["row_ptr"], dev)
+    rp = gat.gat_rebase_row_ptr(rp_all, r0, r1)
+    ci = to_dev(torch, d["col_idx"][e0:e1], dev)
+    q = to_dev(torch, d["q"][r0:r1], dev)
+    kv_shard = [to_dev(torch, d[x][a:b], dev) for x in ("k", "v")]
+    kv_full = [torch.empty((per * world, H, Dh), dtype=torch.bfloat16, device=dev)
+               for _ in range(2 if dist is not None else 0)]
+    kv_pad = [torch.zeros((per, H, Dh), dtype=torch.bfloat16, device=dev)
+              for _ in range(2 if dist is not None else 0)]
+    out = torch.empty_like(q)
+    plan = gat.Plan(rp)
+    ws = torch.empty(max(1, gat.gat_fused_layer_workspace_size(plan, H, Dh)), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        if dist is not None:
+            for sh, pad, full in zip(kv_shard, kv_pad, kv_full):
+                pad[: sh.shape[0]].copy_(sh)
+                dist.all_gather_into_tensor(full, pad)
+        # (one rank owns every node: its shards are the full tables)
+        k, v = (kv_full[0][:n], kv_full[1][:n]) if dist is not None else kv_shard
+        gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], out=out, plan=plan, workspace=ws,
+                            stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    dist_barrier(dist)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    dist_barrier(dist)
+    ms = dist_max(dist, t0.elapsed_time(t1) / args.steps, dev)
+    return {
+        "metric": METRIC, "value": E * H / (ms * 1e-3), "unit": "edge-heads/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "fused GAT layer, row-sharded: 1e6 rows, Zipf(2.1) in-degrees, "
+                               "H=8, Dh=64, bf16, seed 3; per step an all-gather of the "
+                               "node-sharded k and v, then the fused layer on each rank's rows",
+                   "n_rows": n, "n_edges": E, "parallelism": f"{world} row shards",
+                   "rank0_rows": [r0, r1], "rank0_edges": e1 - e0},
+        "gpu_launches": args.steps, "clocks": clk.summary(),
+    }
+
+
 def bench_reference(args, rank, world):
     """--impl reference: the fp64 oracle, timed per step on a bounded sample."""
     from concurrent.futures import ThreadPoolExecutor
@@ -715,6 +798,9 @@ def main():
     ap.add_argument("--n-rows", type=int, default=1_000_000,
                     help="rows of the fused workload (smaller only for profiling captures)")
     ap.add_argument("--no-extras", action="store_true", help="skip the smaller workloads")
+    ap.add_argument("--mode", default="replicas", choices=["replicas", "rowshard"],
+                    help="N > 1: independent full problems per rank (replicas, weak scaling) "
+                         "or one graph cut into row shards (rowshard, strong scaling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
@@ -733,6 +819,13 @@ def main():
         return
 
     dist = dist_init(world, "nccl")
+    if args.mode == "rowshard":
+        res = bench_rowshard(args, rank, world, local, dist)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     if args.workload != "fused":
         if rank == 0:
             print(json.dumps({"workload": args.workload, **bench_small(args.workload, args)}))

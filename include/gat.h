@@ -141,6 +141,34 @@ gat_status_t gat_validate_graph(const int32_t *row_ptr, const int32_t *col_idx,
                                 int32_t *flag, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Row shards (one process per GPU). Rows are independent in every operation
+ * here [softmax page, reference model: a softmax per node's own edge range;
+ * spmm page: one output row per destination], so a graph splits into
+ * contiguous row ranges that different GPUs compute alone, each needing the
+ * source rows its edges read (all of k / v for uniform sources).
+ *
+ * gat_partition_rows: HOST function (no GPU work, row_ptr in host memory):
+ * cuts rows [0, n_rows) into `parts` contiguous ranges
+ * [row_begin[p], row_begin[p+1]) of about equal weight, the weight of a row
+ * being 1 + its degree (its q and out rows and one gathered source row per
+ * edge: the fused layer's traffic). row_begin has parts + 1 entries,
+ * row_begin[0] = 0, row_begin[parts] = n_rows, non-decreasing (a part may be
+ * empty). Deterministic. Errors: GAT_ERR_INVALID_ARG, and
+ * GAT_ERR_INDEX_OUT_OF_RANGE for a decreasing row_ptr.
+ *
+ * gat_rebase_row_ptr: out[i] = row_ptr[r0 + i] - row_ptr[r0] for
+ * i in [0, r1 - r0] (device arrays, enqueued on `stream`): the row pointer of
+ * rows [r0, r1) as a graph of its own, whose edges are col_idx + row_ptr[r0],
+ * queries q + r0 * H * Dh and outputs out + r0 * H * Dh. Errors:
+ * GAT_ERR_INVALID_ARG, GAT_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+gat_status_t gat_partition_rows(const int32_t *row_ptr, int64_t n_rows, int32_t parts,
+                                int64_t *row_begin);
+
+gat_status_t gat_rebase_row_ptr(const int32_t *row_ptr, int64_t r0, int64_t r1, int32_t *out,
+                                void *stream);
+
+/* ------------------------------------------------------------------------
  * SDDMM [sddmm page, reference model: gather both endpoint feature rows of
  * every edge, multiply elementwise, sum over the feature dimension],
  * generalised to heads and a scale:

@@ -35,6 +35,7 @@ EXPORTS = (
     "gat_fused_layer_backward_workspace_size", "gat_fused_layer_backward",
     "gat_quantize_fp8", "gat_fused_layer_fp8", "gat_spmm_weighted_workspace_size",
     "gat_dense_masked_attention_workspace_size", "gat_dense_masked_attention_status",
+    "gat_partition_rows", "gat_rebase_row_ptr",
 )
 
 
@@ -76,6 +77,8 @@ def _load() -> ctypes.CDLL:
                                        ctypes.c_int),
         "gat_dense_masked_attention_workspace_size": ([I32, I32, I32, I32, P], ctypes.c_int),
         "gat_dense_masked_attention_status": ([P, P], ctypes.c_int),
+        "gat_partition_rows": ([P, I64, I32, P], ctypes.c_int),
+        "gat_rebase_row_ptr": ([P, I64, I64, P, P], ctypes.c_int),
         "gat_fused_layer_no_alloc": ([P, P, I64, I64, I64, I32, I32, F, P, P, P, ctypes.c_int, P,
                                       P], ctypes.c_int),
         "gat_transpose_create": ([P, P, I64, I64, I64, P, P], ctypes.c_int),
@@ -471,6 +474,29 @@ def gat_dense_masked_attention_status(workspace, stream=None) -> None:
     a bounded wait (synchronises the stream)."""
     _check("gat_dense_masked_attention_status",
            _lib.gat_dense_masked_attention_status(_ptr(workspace), _stream(stream)))
+
+
+def gat_partition_rows(row_ptr, parts: int):
+    """Contiguous row ranges of about equal fused-layer traffic (host call on a
+    host int32 row_ptr, numpy or CPU tensor); returns row_begin (int64,
+    parts + 1 entries)."""
+    import numpy as np
+    rp = np.ascontiguousarray(row_ptr.numpy() if isinstance(row_ptr, torch.Tensor) else row_ptr,
+                              dtype=np.int32)
+    out = np.empty(parts + 1, dtype=np.int64)
+    _check("gat_partition_rows", _lib.gat_partition_rows(
+        rp.ctypes.data, rp.size - 1, parts, out.ctypes.data))
+    return out
+
+
+def gat_rebase_row_ptr(row_ptr, r0: int, r1: int, out=None, stream=None):
+    """row_ptr[r0:r1+1] - row_ptr[r0] on the device (rows [r0, r1) as a graph)."""
+    _idx(row_ptr, "row_ptr")
+    if out is None:
+        out = torch.empty(r1 - r0 + 1, dtype=torch.int32, device=row_ptr.device)
+    _check("gat_rebase_row_ptr", _lib.gat_rebase_row_ptr(_ptr(row_ptr), r0, r1, _ptr(out),
+                                                         _stream(stream)))
+    return out
 
 
 def version() -> int:

@@ -255,9 +255,65 @@ __global__ void validate_kernel(const int32_t *__restrict__ row_ptr,
     if (__any_sync(kFull, bad) && (threadIdx.x & 31) == 0) atomicOr(flag, 1);
 }
 
+// ---------------------------------------------------------------------------
+// row shards: a contiguous row range as a graph of its own
+// ---------------------------------------------------------------------------
+__global__ void rebase_row_ptr_kernel(const int32_t *__restrict__ row_ptr, int64_t r0, int64_t n,
+                                      int32_t *__restrict__ out) {
+    const int32_t base = __ldg(row_ptr + r0);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i <= n; i += stride)
+        out[i] = __ldg(row_ptr + r0 + i) - base;
+}
+
 }  // namespace gat
 
 using namespace gat;
+
+// ---------------------------------------------------------------------------
+// C ABI: row partition (host) and shard row pointers (device)
+// ---------------------------------------------------------------------------
+extern "C" gat_status_t gat_partition_rows(const int32_t *row_ptr, int64_t n_rows,
+                                           int32_t parts, int64_t *row_begin) {
+    if (!row_ptr || !row_begin || n_rows < 0 || parts < 1)
+        return fail(GAT_ERR_INVALID_ARG, "gat_partition_rows: bad arguments");
+    for (int64_t i = 0; i < n_rows; ++i)
+        if (row_ptr[i + 1] < row_ptr[i])
+            return fail(GAT_ERR_INDEX_OUT_OF_RANGE, "gat_partition_rows: row_ptr decreases at %lld",
+                        (long long)i);
+    // weight of rows [0, r): r + row_ptr[r] - row_ptr[0] (a row's q and out rows plus
+    // one gathered source row per edge), non-decreasing in r; boundary p is the
+    // first r whose prefix weight reaches p / parts of the total
+    const int64_t total = n_rows + (int64_t)row_ptr[n_rows] - row_ptr[0];
+    row_begin[0] = 0;
+    for (int32_t q = 1; q < parts; ++q) {
+        const int64_t target = (total * q + parts - 1) / parts;
+        int64_t lo = row_begin[q - 1], hi = n_rows;  // first r in [lo, hi] with weight >= target
+        while (lo < hi) {
+            const int64_t mid = lo + (hi - lo) / 2;
+            if (mid + (int64_t)row_ptr[mid] - row_ptr[0] >= target)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        row_begin[q] = lo;
+    }
+    row_begin[parts] = n_rows;
+    return GAT_OK;
+}
+
+extern "C" gat_status_t gat_rebase_row_ptr(const int32_t *row_ptr, int64_t r0, int64_t r1,
+                                           int32_t *out, void *stream) {
+    if (!row_ptr || !out || r0 < 0 || r1 < r0)
+        return fail(GAT_ERR_INVALID_ARG, "gat_rebase_row_ptr: bad arguments");
+    const int64_t n = r1 - r0;
+    int64_t blocks = (n + 1 + 255) / 256;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    rebase_row_ptr_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        row_ptr, r0, n, out);
+    return check_launch("gat_rebase_row_ptr");
+}
 
 // ---------------------------------------------------------------------------
 // C ABI: status / version
