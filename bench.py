@@ -187,6 +187,49 @@ def profiled_traffic(kernel: str):
 
 
 # ----------------------------------------------------------------------------
+# L2 persistence (A/B switch; the library itself sets no access policy)
+# ----------------------------------------------------------------------------
+def l2_persist(torch, stream, tensors, target):
+    """--l2-persist: `off` leaves the device as it is; otherwise the context's
+    persisting-L2 carve-out is set to the device maximum (a per-context limit,
+    gone with the process) and, unless target is `none`, an access-policy
+    window (persisting hits, streaming misses, hit ratio = carve-out / window)
+    is put on `stream` over tensors[target]. Returns a description."""
+    if target == "off":
+        return None
+    import ctypes
+    import glob
+    libs = sorted(glob.glob(os.path.join(os.path.dirname(torch.__file__), "lib", "libcudart.so*")) +
+                  glob.glob("/usr/local/cuda/lib64/libcudart.so*"))
+    rt = ctypes.CDLL(libs[0])
+
+    class Window(ctypes.Structure):  # cudaStreamAttrValue.accessPolicyWindow, padded
+        _fields_ = [("base_ptr", ctypes.c_void_p), ("num_bytes", ctypes.c_size_t),
+                    ("hitRatio", ctypes.c_float), ("hitProp", ctypes.c_int),
+                    ("missProp", ctypes.c_int), ("pad", ctypes.c_char * 40)]
+    dev = torch.cuda.current_device()
+    maxp, maxw = ctypes.c_int(), ctypes.c_int()
+    rt.cudaDeviceGetAttribute(ctypes.byref(maxp), 108, dev)  # max persisting L2 bytes
+    rt.cudaDeviceGetAttribute(ctypes.byref(maxw), 109, dev)  # max access-policy window bytes
+    if rt.cudaDeviceSetLimit(6, ctypes.c_size_t(maxp.value)) != 0:  # persisting L2 limit
+        raise RuntimeError("cudaDeviceSetLimit(persisting L2) failed")
+    desc = {"carve_out_bytes": maxp.value, "window": target}
+    if target != "none":
+        if target not in tensors:
+            raise ValueError(f"--l2-persist {target}: this workload has {sorted(tensors)}")
+        t = tensors[target]
+        w = Window()
+        w.base_ptr = t.data_ptr()
+        w.num_bytes = min(t.numel() * t.element_size(), maxw.value)
+        w.hitRatio = min(1.0, maxp.value / w.num_bytes)
+        w.hitProp, w.missProp = 2, 1  # persisting, streaming
+        if rt.cudaStreamSetAttribute(ctypes.c_void_p(stream.cuda_stream), 1, ctypes.byref(w)) != 0:
+            raise RuntimeError("cudaStreamSetAttribute(access policy window) failed")
+        desc.update(window_bytes=w.num_bytes, hit_ratio=w.hitRatio)
+    return desc
+
+
+# ----------------------------------------------------------------------------
 # fused workload
 # ----------------------------------------------------------------------------
 def fused_bytes(n_rows, n_edges, H, Dh, esize=2):
@@ -317,6 +360,8 @@ def bench_fused(args, rank, world, local, dist):
     ws = torch.empty(max(1, gat.gat_fused_layer_workspace_size(plan, H, Dh)), dtype=torch.uint8,
                      device=dev)
 
+    l2 = l2_persist(torch, stream, {"q": q, "k": k, "v": v}, args.l2_persist)
+
     def step():
         gat.gat_fused_layer(rp, ci, q, k, v, d["scale"], out=out, plan=plan, workspace=ws,
                             stream=stream)
@@ -417,7 +462,7 @@ def bench_fused(args, rank, world, local, dist):
                    "n_rows": n, "n_edges": E, "H": H, "Dh": Dh,
                    "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (q/k/v 3.07 GB vs 126 MB L2), no flush",
-                   "plan": info, "plan_ms": round(plan_ms, 3),
+                   "plan": info, "plan_ms": round(plan_ms, 3), "l2_persist": l2,
                    "generate_s": round(t_gen, 1)},
         "hbm_gbs": achieved,
         "hbm_frac_of_peak": achieved / hbm_peak,
@@ -617,6 +662,8 @@ def bench_small(name, args):
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         ws = torch.empty(gat.gat_fused_layer_backward_workspace_size(
             plan, g["n_rows"], g["n_edges"], g["H"], g["Dh"]), dtype=torch.uint8, device=dev)
+        extra_l2 = l2_persist(torch, torch.cuda.current_stream(), {"q": q, "k": k, "v": v,
+                                                                 "dout": go}, args.l2_persist)
         fn = lambda: gat.gat_fused_layer_backward(rp, ci, q, k, v, go, g["scale"], tr,  # noqa: E731
                                                   plan=plan, dq=dq, dk=dk, dv=dv, workspace=ws)
         units, launches = g["n_edges"] * g["H"], 4
@@ -628,7 +675,7 @@ def bench_small(name, args):
         alg_bytes = (g["n_edges"] * (4 + 2 * rb + 16 * g["H"] + 8 + 2 * rb)
                      + g["n_rows"] * (4 + 3 * rb + 8 * g["H"]) + g["n_src"] * (4 + 2 * rb))
         flops = 2.0 * g["n_edges"] * g["H"] * g["Dh"] * 6
-        extra = {"transpose_build_ms": transpose_ms, "transpose": tr.info()}
+        extra = {"transpose_build_ms": transpose_ms, "transpose": tr.info(), "l2_persist": extra_l2}
     elif name == "fused_fp8":
         # the fused workload (1e6 rows, Zipf, H=8, Dh=64) with k/v quantised to
         # E4M3 + per (node, head) scales on the device; q/out bf16
@@ -694,6 +741,8 @@ def bench_small(name, args):
         rp, s = t(g["row_ptr"]), t(g["scores"])
         out = torch.empty_like(s)
         plan = gat.Plan(rp)
+        extra = {"l2_persist": l2_persist(torch, torch.cuda.current_stream(), {"scores": s},
+                                          args.l2_persist)}
         fn = lambda: gat.gat_edge_softmax(rp, s, g["H"], out=out, plan=plan)  # noqa: E731
         units, launches = g["n_edges"] * g["H"], 1
         alg_bytes = 4 * (g["n_rows"] + 1) + 8 * g["n_edges"] * g["H"]
@@ -798,6 +847,12 @@ def main():
     ap.add_argument("--n-rows", type=int, default=1_000_000,
                     help="rows of the fused workload (smaller only for profiling captures)")
     ap.add_argument("--no-extras", action="store_true", help="skip the smaller workloads")
+    ap.add_argument("--l2-persist", default="off",
+                    choices=["off", "none", "q", "k", "v", "dout", "scores"],
+                    help="A/B of L2 persistence: off (default, device untouched), or the "
+                         "device's persisting-L2 carve-out with a window on this table "
+                         "(none: carve-out, no window); fused, fused_backward, "
+                         "edge_softmax_h8 workloads")
     ap.add_argument("--mode", default="replicas", choices=["replicas", "rowshard"],
                     help="N > 1: independent full problems per rank (replicas, weak scaling) "
                          "or one graph cut into row shards (rowshard, strong scaling)")
