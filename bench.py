@@ -757,15 +757,29 @@ def bench_small(name, args):
         vals = t(g["values"]).reshape(g["n_src"], 1, g["F"])
         w = torch.empty_like(s)
         out = torch.empty((g["n_rows"], 1, g["F"]), device=dev)
+        # one pass: the softmax of the given scores and the weighted sum together
+        fn = lambda: gat.gat_softmax_aggregate(rp, ci, s, vals, 1, g["F"], out=out)  # noqa: E731
+        units, launches = g["n_edges"], 1
+        # row_ptr; per edge its col_idx, its score and one gathered value row;
+        # one output row per row
+        alg_bytes = 4 * (g["n_rows"] + 1) + g["n_edges"] * (4 + 4 + 4 * g["F"]) + \
+            4 * g["F"] * g["n_rows"]
 
-        def fn():
+        def two():
             gat.gat_edge_softmax(rp, s, 1, out=w)
             gat.gat_spmm_weighted(rp, ci, w, vals, 1, g["F"], out=out)
-        units, launches = g["n_edges"], 2
-        # softmax: row_ptr + scores in + weights out; spmm: row_ptr, col_idx,
-        # weights, one gathered value row per edge, one output row per row
-        alg_bytes = (4 * (g["n_rows"] + 1) + 8 * g["n_edges"]) + \
-            (4 * (g["n_rows"] + 1) + g["n_edges"] * (4 + 4 + 4 * g["F"]) + 4 * g["F"] * g["n_rows"])
+        for _ in range(max(3, args.warmup)):
+            two()
+        torch.cuda.synchronize()
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(50)]
+        for a, b in ev2:
+            a.record()
+            two()
+            b.record()
+        torch.cuda.synchronize()
+        extra["two_launch_median_ms"] = spread([a.elapsed_time(b) for a, b in ev2])["median_ms"]
+        extra["two_launch"] = "gat_edge_softmax then gat_spmm_weighted, weights through memory"
     elif name == "sddmm":
         si, di, a, b = t(g["src_idx"]), t(g["dst_idx"]), t(g["src_feat"]), t(g["dst_feat"])
         out = torch.empty((g["n_edges"], 1), device=dev)

@@ -232,6 +232,31 @@ gat_status_t gat_spmm_weighted(const int32_t *row_ptr, const int32_t *col_idx, i
                                void *stream);
 
 /* ------------------------------------------------------------------------
+ * Softmax + neighbourhood aggregation in one pass [aggregate page, reference
+ * model: a softmax over each destination's edge scores, then the
+ * softmax-weighted sum of the source rows; a zero-degree destination stays
+ * zero]:
+ *     out[i,h,:] = sum_{e in row i} softmax_e(scores[.,h])[e] * feat[col_idx[e],h,:]
+ * scores fp32 [n_edges,H] (given, not computed); feat [n_src,H,Dh] and out
+ * [n_rows,H,Dh] share `dtype` (fp32 arithmetic). One launch (per group of
+ * heads the vector engine takes) with an online softmax: no weight reaches
+ * memory. Same plan / workspace rules as gat_fused_layer (size from
+ * gat_fused_layer_workspace_size). Needs 16-byte aligned feat / out and a
+ * vector-engine shape (Dh * element size a multiple of 16 with Dh / (16 /
+ * element size) a power of two); else GAT_ERR_UNSUPPORTED (compose
+ * gat_edge_softmax and gat_spmm_weighted instead). A non-empty row whose
+ * scores are all -inf for a head gives NaN for that head, as the softmax of
+ * the composition does; a zero-degree row gives zeros.
+ * Errors: GAT_ERR_INVALID_ARG, GAT_ERR_UNSUPPORTED, GAT_ERR_PLAN_MISMATCH,
+ * GAT_ERR_WORKSPACE.
+ * ---------------------------------------------------------------------- */
+gat_status_t gat_softmax_aggregate(const int32_t *row_ptr, const int32_t *col_idx,
+                                   int64_t n_rows, int64_t n_src, int64_t n_edges, int32_t H,
+                                   int32_t Dh, const float *scores, const void *feat,
+                                   gat_dtype_t dtype, void *out, gat_plan_t plan, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * Fused multi-head graph-attention layer: SDDMM -> segmented softmax ->
  * weighted SpMM in one pass (the composition of the sddmm, softmax and spmm
  * pages' operations), with the softmax kept online so no score or weight

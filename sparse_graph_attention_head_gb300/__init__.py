@@ -35,7 +35,7 @@ EXPORTS = (
     "gat_fused_layer_backward_workspace_size", "gat_fused_layer_backward",
     "gat_quantize_fp8", "gat_fused_layer_fp8", "gat_spmm_weighted_workspace_size",
     "gat_dense_masked_attention_workspace_size", "gat_dense_masked_attention_status",
-    "gat_partition_rows", "gat_rebase_row_ptr",
+    "gat_partition_rows", "gat_rebase_row_ptr", "gat_softmax_aggregate",
 )
 
 
@@ -78,6 +78,8 @@ def _load() -> ctypes.CDLL:
         "gat_dense_masked_attention_workspace_size": ([I32, I32, I32, I32, P], ctypes.c_int),
         "gat_dense_masked_attention_status": ([P, P], ctypes.c_int),
         "gat_partition_rows": ([P, I64, I32, P], ctypes.c_int),
+        "gat_softmax_aggregate": ([P, P, I64, I64, I64, I32, I32, P, P, ctypes.c_int, P, P, P, SZ,
+                                   P], ctypes.c_int),
         "gat_rebase_row_ptr": ([P, I64, I64, P, P], ctypes.c_int),
         "gat_fused_layer_no_alloc": ([P, P, I64, I64, I64, I32, I32, F, P, P, P, ctypes.c_int, P,
                                       P], ctypes.c_int),
@@ -280,6 +282,29 @@ def gat_spmm_weighted(row_ptr, col_idx, w, feat, H, Dh, n_rows=None, out=None, p
     _check("gat_spmm_weighted", _lib.gat_spmm_weighted(
         _ptr(row_ptr), _ptr(col_idx) if E else None, n_rows, feat.numel() // (H * Dh), E, H, Dh,
         _ptr(w) if E else None, _ptr(feat), _dtype(feat), _ptr(out), _plan_handle(plan),
+        _ptr(workspace), ws_bytes, _stream(stream)))
+    return out
+
+
+def gat_softmax_aggregate(row_ptr, col_idx, scores, feat, H, Dh, n_rows=None, out=None,
+                          plan=None, workspace=None, stream=None):
+    """out[i,h,:] = sum_e softmax_e(scores[:,h]) feat[col_idx[e],h,:], one pass;
+    scores fp32 [E,H], feat [n_src,H,Dh], out has feat's dtype."""
+    _idx(row_ptr, "row_ptr")
+    _idx(col_idx, "col_idx")
+    n_rows = row_ptr.numel() - 1 if n_rows is None else n_rows
+    E = col_idx.numel()
+    if out is None:
+        out = torch.empty((n_rows, H, Dh), dtype=feat.dtype, device=feat.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if plan is not None and workspace is None:
+        need = gat_fused_layer_workspace_size(plan, H, Dh)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=feat.device)
+            ws_bytes = need
+    _check("gat_softmax_aggregate", _lib.gat_softmax_aggregate(
+        _ptr(row_ptr), _ptr(col_idx) if E else None, n_rows, feat.numel() // (H * Dh), E, H, Dh,
+        _ptr(scores) if E else None, _ptr(feat), _dtype(feat), _ptr(out), _plan_handle(plan),
         _ptr(workspace), ws_bytes, _stream(stream)))
     return out
 

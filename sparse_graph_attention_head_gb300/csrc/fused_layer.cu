@@ -222,3 +222,99 @@ extern "C" gat_status_t gat_fused_layer(const int32_t *row_ptr, const int32_t *c
     if (dtype == GAT_F32) return launch_fused<float>(p, vec_ok, s);
     return launch_fused<__nv_bfloat16>(p, vec_ok, s);
 }
+
+// ---------------------------------------------------------------------------
+// softmax of given edge scores + aggregation, one launch
+// ---------------------------------------------------------------------------
+namespace gat {
+
+template <typename T>
+static gat_status_t launch_given(const EngineParams &p, cudaStream_t s) {
+    int V = 0, LE = 0;
+    if (!engine_shape(p.H, p.Dh, sizeof(T), V, LE))
+        return fail(GAT_ERR_UNSUPPORTED, "gat_softmax_aggregate: shape H=%d Dh=%d", (int)p.H,
+                    (int)p.Dh);
+    if (V == 1 && LE == 4) return launch_fused_engine<T, 1, 4, true>(p, s);
+    if (V == 1 && LE == 8) return launch_fused_engine<T, 1, 8, true>(p, s);
+    if (V == 1 && LE == 16) return launch_fused_engine<T, 1, 16, true>(p, s);
+    if (V == 1 && LE == 32) return launch_fused_engine<T, 1, 32, true>(p, s);
+    if (V == 2) return launch_fused_engine<T, 2, 32, true>(p, s);
+    return launch_fused_engine<T, 4, 32, true>(p, s);
+}
+
+}  // namespace gat
+
+extern "C" gat_status_t gat_softmax_aggregate(const int32_t *row_ptr, const int32_t *col_idx,
+                                              int64_t n_rows, int64_t n_src, int64_t n_edges,
+                                              int32_t H, int32_t Dh, const float *scores,
+                                              const void *feat, gat_dtype_t dtype, void *out,
+                                              gat_plan_t plan, void *workspace,
+                                              size_t workspace_bytes, void *stream) {
+    if (n_rows < 0 || n_src < 0 || n_edges < 0 || H < 1 || Dh < 1)
+        return fail(GAT_ERR_INVALID_ARG, "gat_softmax_aggregate: bad sizes");
+    if (dtype != GAT_F32 && dtype != GAT_BF16)
+        return fail(GAT_ERR_UNSUPPORTED, "gat_softmax_aggregate: unknown dtype %d", (int)dtype);
+    if (n_rows == 0) return GAT_OK;
+    if (!row_ptr || !out || (n_edges > 0 && (!col_idx || !scores || !feat)))
+        return fail(GAT_ERR_INVALID_ARG, "gat_softmax_aggregate: NULL pointer");
+    if (plan && (plan->n_rows != n_rows || plan->n_edges != n_edges))
+        return fail(GAT_ERR_PLAN_MISMATCH,
+                    "gat_softmax_aggregate: plan is for n_rows=%lld n_edges=%lld",
+                    (long long)plan->n_rows, (long long)plan->n_edges);
+    const int eb = dtype == GAT_F32 ? 4 : 2;
+    const bool vec_ok = aligned16(out) && (n_edges == 0 || aligned16(feat));
+    const int Hg = vec_ok ? engine_group(H, Dh, eb) : 0;
+    if (Hg == 0)
+        return fail(GAT_ERR_UNSUPPORTED,
+                    "gat_softmax_aggregate: needs 16-byte aligned rows and a vector-engine shape "
+                    "(H=%d, Dh=%d); use gat_edge_softmax + gat_spmm_weighted", (int)H, (int)Dh);
+    EngineParams p{};
+    p.row_ptr = row_ptr;
+    p.col_idx = col_idx;
+    p.v = feat;
+    p.w = scores;
+    p.w_stride = H;
+    p.out = out;
+    p.n_rows = n_rows;
+    p.H = Hg;
+    p.Dh = Dh;
+    p.row_elems = (int64_t)H * Dh;
+    p.qscale = kLog2e;
+    p.heavy_threshold = INT_MAX;
+    p.chunk_edges = 1;
+    p.slot_floats = slot_floats(H, Dh);
+    if (plan) {
+        p.heavy_threshold = plan->heavy_threshold;
+        p.chunk_edges = plan->chunk_edges;
+        p.n_chunks = plan->n_chunks;
+        p.heavy_rows = plan->heavy_rows;
+        p.chunk_start = plan->chunk_start;
+        p.chunk_row = plan->chunk_row;
+        p.chunk_desc = plan->chunk_desc;
+        p.counters = plan->counters;
+        if (p.n_chunks > 0) {
+            const size_t need = (size_t)p.n_chunks * (size_t)p.slot_floats * sizeof(float);
+            if (!workspace || workspace_bytes < need || !aligned16(workspace))
+                return fail(GAT_ERR_WORKSPACE,
+                            "gat_softmax_aggregate: workspace needs %zu bytes (16-byte aligned), "
+                            "got %zu", need, workspace_bytes);
+            p.partials = static_cast<float *>(workspace);
+        }
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // one launch per group of Hg heads (a slice of every feature / out row and
+    // the group's columns of the scores)
+    for (int h0 = 0; h0 < H; h0 += Hg) {
+        EngineParams pg = p;
+        const size_t off = (size_t)h0 * Dh * eb;
+        pg.out = static_cast<char *>(out) + off;
+        if (n_edges > 0) {
+            pg.v = static_cast<const char *>(feat) + off;
+            pg.w = scores + h0;
+        }
+        const gat_status_t st = dtype == GAT_F32 ? launch_given<float>(pg, s)
+                                                 : launch_given<__nv_bfloat16>(pg, s);
+        if (st != GAT_OK) return st;
+    }
+    return GAT_OK;
+}

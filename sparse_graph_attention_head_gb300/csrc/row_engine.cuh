@@ -20,6 +20,8 @@
 // per head: m' = max(m, s), c = 2^(m-m'), l = l c + 2^(s-m'),
 // acc = acc c + 2^(s-m') v. Scores are pre-scaled by log2(e) so the
 // exponentials are exp2. Nothing per edge ever reaches memory.
+// Given-score mode (gat_softmax_aggregate): the same online softmax over
+// scores read from w[e,h] (scaled by qscale = log2(e)) instead of q.k.
 // SpMM mode (spmm.cu): acc += w[e,h] * feat[src].
 //
 // Heavy rows (fused mode, with a plan) arrive as chunks; each chunk warp
@@ -171,6 +173,8 @@ struct FusedRow {
     // tile of the warp's next item [ne0, ne1) is fetched into next_ci
     // (next_ready), so the next item can start gathering at once; a next
     // item that is a light-row slot beyond the threshold is not fetched.
+    // GIVEN: the edges' scores are read from w (no k rows, no q).
+    template <bool GIVEN>
     __device__ __forceinline__ void run(const EngineParams &p, const L &ln, int e0, int e1,
                                         int first_ci, int ne0, int ne1, bool next_is_row,
                                         int &next_ci, bool &next_ready) {
@@ -199,7 +203,7 @@ struct FusedRow {
                     if (valid[u]) {
 #pragma unroll
                         for (int s = 0; s < V; ++s) {
-                            kr[u][s] = ld_stream16(kb + src * row_bytes + ln.vi[s] * 16);
+                            if (!GIVEN) kr[u][s] = ld_stream16(kb + src * row_bytes + ln.vi[s] * 16);
                             vr[u][s] = ld_stream16(vb + src * row_bytes + ln.vi[s] * 16);
                         }
                     } else {
@@ -218,23 +222,36 @@ struct FusedRow {
                     }
                 }
                 float sc[U][V];
+                if constexpr (GIVEN) {
+                    // every lane of a head reads the edge's score of that head
 #pragma unroll
-                for (int u = 0; u < U; ++u)
+                    for (int u = 0; u < U; ++u) {
+                        const int64_t e = base + j0 + u * ES + ln.sub;
 #pragma unroll
-                    for (int s = 0; s < V; ++s) {
-                        float kf[VE];
-                        Vec<T>::unpack(kr[u][s], kf);
-                        float d = 0.f;
-#pragma unroll
-                        for (int t = 0; t < VE; ++t) d = fmaf(qf[s][t], kf[t], d);
-                        sc[u][s] = d;
+                        for (int s = 0; s < V; ++s)
+                            sc[u][s] = valid[u] ? __ldg(p.w + e * p.w_stride + ln.head[s]) * p.qscale
+                                                : 0.f;
                     }
-                // per-head sums over the head's G lanes (uniform across the warp)
-                for (int o = 1; o < ln.G; o <<= 1) {
+                } else {
 #pragma unroll
                     for (int u = 0; u < U; ++u)
 #pragma unroll
-                        for (int s = 0; s < V; ++s) sc[u][s] += __shfl_xor_sync(kFull, sc[u][s], o);
+                        for (int s = 0; s < V; ++s) {
+                            float kf[VE];
+                            Vec<T>::unpack(kr[u][s], kf);
+                            float d = 0.f;
+#pragma unroll
+                            for (int t = 0; t < VE; ++t) d = fmaf(qf[s][t], kf[t], d);
+                            sc[u][s] = d;
+                        }
+                    // per-head sums over the head's G lanes (uniform across the warp)
+                    for (int o = 1; o < ln.G; o <<= 1) {
+#pragma unroll
+                        for (int u = 0; u < U; ++u)
+#pragma unroll
+                            for (int s = 0; s < V; ++s)
+                                sc[u][s] += __shfl_xor_sync(kFull, sc[u][s], o);
+                    }
                 }
 #pragma unroll
                 for (int s = 0; s < V; ++s) {
@@ -281,12 +298,15 @@ struct FusedRow {
         }
     }
 
-    __device__ __forceinline__ void store_out(const EngineParams &p, const L &ln, int64_t row) {
+    // masked_nan: the row has edges, so a head with no finite score (l = 0,
+    // possible only with given scores of -inf) is NaN, as the two-pass softmax
+    __device__ __forceinline__ void store_out(const EngineParams &p, const L &ln, int64_t row,
+                                              bool masked_nan = false) {
         if (ln.sub != 0) return;
         char *orow = static_cast<char *>(p.out) + row * p.row_elems * (int64_t)sizeof(T);
 #pragma unroll
         for (int s = 0; s < V; ++s) {
-            const float inv = l[s] > 0.f ? 1.f / l[s] : 0.f;
+            const float inv = l[s] > 0.f ? 1.f / l[s] : (masked_nan ? NAN : 0.f);
             float o[VE];
 #pragma unroll
             for (int t = 0; t < VE; ++t) o[t] = acc[s][t] * inv;
@@ -296,7 +316,7 @@ struct FusedRow {
 
     // chunk of a heavy row: publish the state; the last chunk merges the row
     __device__ __forceinline__ void chunk_epilogue(const EngineParams &p, const L &ln, int64_t row,
-                                                   int hr, int64_t chunk) {
+                                                   int hr, int64_t chunk, bool masked_nan = false) {
         const int HD = p.H * p.Dh;
         if (ln.sub == 0) {
             float *slot = p.partials + chunk * p.slot_floats;
@@ -353,7 +373,7 @@ struct FusedRow {
                 m[s] = mx;
             }
         }
-        store_out(p, ln, row);
+        store_out(p, ln, row, masked_nan);
         if (ln.lane == 0) p.counters[hr] = 0;  // ready for the next call
     }
 };
@@ -364,7 +384,7 @@ struct FusedRow {
 // Blocks of 4 warps, MINB resident per SM (5 -> 96 registers, 20 warps/SM).
 constexpr int kFusedThreads = 128;
 
-template <typename T, int V, int LE, int U, int MINB>
+template <typename T, int V, int LE, int U, int MINB, bool GIVEN = false>
 __global__ void __launch_bounds__(kFusedThreads, MINB)
 fused_engine_kernel(const EngineParams p) {
     using L = Lanes<T, V, LE>;
@@ -391,23 +411,23 @@ fused_engine_kernel(const EngineParams p) {
         const int first_ci =
             ci_ready ? ci_tile : (ln.lane < cur.z - cur.y ? __ldg(p.col_idx + cur.y + ln.lane) : 0);
         bool next_ready = false;
-        st.load_q(p, ln, cur.x);
-        st.run(p, ln, cur.y, cur.z, first_ci, has_next ? meta.y : 0, has_next ? meta.z : 0,
+        if (!GIVEN) st.load_q(p, ln, cur.x);
+        st.template run<GIVEN>(p, ln, cur.y, cur.z, first_ci, has_next ? meta.y : 0, has_next ? meta.z : 0,
                nxt >= p.n_chunks, ci_tile, next_ready);
         ci_ready = next_ready;
         if (!is_chunk)
-            st.store_out(p, ln, cur.x);
+            st.store_out(p, ln, cur.x, GIVEN && cur.z > cur.y);
         else
-            st.chunk_epilogue(p, ln, cur.x, cur.w, item);
+            st.chunk_epilogue(p, ln, cur.x, cur.w, item, GIVEN);
     }
 }
 
 // Host-side launch of the fused engine for one (T, V, LE): U edges in flight
 // per warp (V=1: 4, V=2: 3, V=4: 1), five resident 4-warp blocks per SM.
-template <typename T, int V, int LE>
+template <typename T, int V, int LE, bool GIVEN = false>
 inline gat_status_t launch_fused_engine(const EngineParams &p, cudaStream_t s) {
     constexpr int U = V == 1 ? 4 : (V == 2 ? 3 : 1);
-    auto kern = fused_engine_kernel<T, V, LE, U, 5>;
+    auto kern = fused_engine_kernel<T, V, LE, U, 5, GIVEN>;
     static std::atomic<int64_t> caps[kMaxDevices];
     const int64_t cap = device_blocks(caps, kern, kFusedThreads, 0);
     const int64_t items = p.n_chunks + p.n_rows;

@@ -182,6 +182,80 @@ def test_aggregate_workload(gat, use_plan):
     assert rate > 0.99
 
 
+@pytest.mark.parametrize("use_plan", [False, True])
+def test_softmax_aggregate_workload_one_launch(gat, use_plan):
+    """The same operation (softmax of given scores, then the weighted sum) in
+    one pass: the 384-row workload against the oracle's softmax followed by
+    its aggregation."""
+    d = W.make_aggregate()
+    rp, ci = dev(d["row_ptr"]), dev(d["col_idx"])
+    plan = gat.Plan(rp, heavy_threshold=24, chunk_edges=8) if use_plan else None
+    if use_plan:
+        assert plan.info()["n_chunks"] > 0
+    out = gat.gat_softmax_aggregate(rp, ci, dev(d["scores"]).reshape(-1, 1),
+                                    dev(d["values"]).reshape(384, 1, 64), 1, 64, plan=plan)
+    w_o = oracle.edge_softmax(d["row_ptr"], d["scores"], 1)
+    o, c = oracle.spmm_weighted(d["row_ptr"], d["col_idx"], w_o, d["values"], 1, 64,
+                                want_cond=True)
+    n = np.maximum(np.diff(d["row_ptr"]), 1).astype(np.float64)[:, None, None]
+    g = host(out)
+    assert (g[np.diff(d["row_ptr"]) == 0] == 0).all()
+    rate = assert_fp32(g, o, c, n, name="aggregate one pass")
+    assert rate > 0.99
+
+
+@pytest.mark.parametrize("H,Dh,dtype", [(8, 64, "bf16"), (4, 32, "f32"), (12, 64, "bf16"),
+                                         (1, 64, "f32"), (2, 8, "f32")])
+def test_softmax_aggregate_heads_heavy_rows_masked_head(gat, H, Dh, dtype):
+    """Multi-head one-pass softmax + aggregation on a power-law graph with a
+    chunked heavy row, an empty row, and a row whose head 0 is all -inf (NaN
+    there, as the softmax of the composition gives)."""
+    rng = np.random.default_rng(80 + H * Dh)
+    deg = W.zipf_degrees(rng, 3000, dmax=500)
+    deg[[4, 9, 20]] = [2500, 0, 7]
+    rp, ci = W.make_csr(rng, deg, 2000, sort_within_rows=False)
+    E = int(rp[-1])
+    sc = (2.0 * rng.standard_normal((E, H))).astype(np.float32)
+    sc[rp[20]:rp[21], 0] = -np.inf
+    f32 = rng.standard_normal((2000, H, Dh)).astype(np.float32)
+    if dtype == "bf16":
+        fb = W.bf16_bits_from_f32(f32)
+        fd, fo = dev_bf16(fb), fb
+    else:
+        fd, fo = dev(f32), f32
+    rpd = dev(rp)
+    plan = gat.Plan(rpd)
+    assert plan.info()["n_chunks"] > 0
+    w_o = oracle.edge_softmax(rp, sc, H)
+    o, c = oracle.spmm_weighted(rp, ci, w_o, fo, H, Dh, want_cond=True)
+    assert np.isnan(o[20, 0]).all()
+    keep = np.ones(o.shape, dtype=bool)
+    keep[20, 0] = False
+    for pl in (None, plan):
+        g = host(gat.gat_softmax_aggregate(rpd, dev(ci), dev(sc), fd, H, Dh, plan=pl))
+        assert np.isnan(g[20, 0]).all() and not np.isnan(g[keep]).any()
+        assert (g[9] == 0).all()
+        if dtype == "bf16":
+            assert_bf16(g[keep], o[keep], c[keep], name=f"aggregate one pass {H}x{Dh} bf16")
+        else:
+            n = np.broadcast_to(np.maximum(deg, 1).astype(np.float64)[:, None, None], o.shape)
+            assert_fp32(g[keep], o[keep], c[keep], n[keep], name=f"aggregate one pass {H}x{Dh}")
+
+
+def test_softmax_aggregate_errors(gat):
+    """Shapes outside the vector engine are refused (the two-launch
+    composition covers them); a plan for another graph is refused."""
+    rp = dev(np.array([0, 2, 3], np.int32))
+    ci = dev(np.array([0, 1, 1], np.int32))
+    sc = dev(np.zeros((3, 1), np.float32))
+    with pytest.raises(gat.GatError, match="GAT_ERR_UNSUPPORTED"):
+        gat.gat_softmax_aggregate(rp, ci, sc, dev(np.zeros((2, 1, 5), np.float32)), 1, 5)
+    other = gat.Plan(dev(np.array([0, 1, 2, 3], np.int32)))
+    with pytest.raises(gat.GatError, match="GAT_ERR_PLAN_MISMATCH"):
+        gat.gat_softmax_aggregate(rp, ci, sc, dev(np.zeros((2, 1, 8), np.float32)), 1, 8,
+                                  plan=other)
+
+
 @pytest.mark.parametrize("H,Dh,dtype", [(1, 64, "f32"), (4, 32, "f32"), (8, 64, "f32"),
                                          (8, 64, "bf16"), (2, 64, "bf16"), (1, 32, "bf16"),
                                          (3, 24, "f32"), (5, 6, "bf16"),
