@@ -7,10 +7,14 @@
 // H <= 32 is one launch of softmax_rows_kernel, a grid of the resident
 // blocks (8 warps, 64 KB of staging buffer each):
 //   phase 1 (with a plan): the plan's heavy rows longer than a warp buffer,
-//     fetched 8 list entries at a time from a counter in the plan, one block
-//     per row, streamed through two 32 KB halves of the block buffer (the
+//     one block per row. With W = 4 and H <= 32 the block takes list entries
+//     blockIdx.x, blockIdx.x + gridDim.x, ... and streams their chunks
+//     through a ring of eight 8 KB slots (softmax_heavy_ring: up to seven
+//     chunks in flight, no barrier per chunk, two per row); otherwise it
+//     fetches 8 list entries at a time from a counter in the plan and
+//     streams each row through two 32 KB halves of the block buffer (the
 //     next chunk's copies in flight while this one is computed); rows longer
-//     than a half are read twice (fold, then normalise);
+//     than the resident limit are read twice (fold, then normalise);
 //   phase 2: batches of 32 consecutive rows, fetched from a second counter
 //     (static stride without a plan). A warp stages runs of consecutive rows
 //     (up to 2048 scores, cp.async with every copy in flight), computes them
@@ -781,6 +785,246 @@ __device__ __forceinline__ void softmax_heavy_rows(const int32_t *e0s, const int
     }
 }
 
+// ---- heavy rows, W = 4 and Q = H/4 a power of two: a ring of chunk loads
+//
+// The block buffer is kRing slots of kSpanFloats scores, one chunk of cap_e
+// = kSpanFloats / H edges each. The block's heavy rows form one stream of
+// chunk loads: a row of at most kResident chunks is loaded once and stays in
+// its slots until it is written; a longer row is loaded twice (fold pass,
+// then normalise pass; the second read of a row the block has just read is
+// served by L2). Thread t copies (cp.async) and later reads float4 positions
+// t + 256 i of every slot and no others, so a chunk needs no block barrier:
+// the thread's own cp.async.wait_group covers it. Up to kRing - 1 chunks are
+// in flight while one is computed; the block synchronises only in each row's
+// merge of its per-thread (maximum, sum) pairs. Serves Q = H/4 <= 8 head
+// groups (H = 4, 8, 16, 32).
+constexpr int kRing = kSpanBlockFloats / kSpanFloats;       // 8 slots
+constexpr int kResident = 4;                                // rows read once: <= 4 chunks
+constexpr int kRingPer = kSpanFloats / 4 / kSoftmaxThreads;  // float4s per thread and slot
+
+// wait until at most `pending` (0 .. kRing - 1) of the thread's most recent
+// cp.async groups are still in flight
+__device__ __forceinline__ void cp_async_wait_upto(int pending) {
+    switch (pending) {
+        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+        case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+        case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+        case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+    }
+}
+
+// The issuing side of the stream: rows are the set bits of `left` (lanes of
+// every warp hold the same rows' first edge and degree), each row's loads
+// in order (resident: one pass; otherwise two).
+struct ChunkIssuer {
+    unsigned left;
+    int32_t e0, deg, nc, c;
+    int pass;
+    bool have;
+    int issued;
+
+    // issue loads while fewer than kRing are unconsumed (loads before `freed`
+    // are consumed); block-uniform control flow
+    __device__ __forceinline__ void pump(const float *scores, float *buf, int32_t H, int32_t cap_e,
+                                         int32_t e0_lane, int32_t deg_lane, int freed, int t) {
+        while (issued - freed < kRing) {
+            if (!have) {
+                if (!left) return;
+                const int l = __ffs(left) - 1;
+                left &= left - 1u;
+                e0 = __shfl_sync(kFull, e0_lane, l);
+                deg = __shfl_sync(kFull, deg_lane, l);
+                nc = (deg + cap_e - 1) / cap_e;
+                c = 0;
+                pass = 0;
+                have = true;
+            }
+            const int32_t c0 = c * cap_e;
+            const int32_t dc = deg - c0 < cap_e ? deg - c0 : cap_e;
+            const int n4 = dc * (H >> 2);
+            float *slot = buf + (issued % kRing) * kSpanFloats;
+            const float *src = scores + ((int64_t)e0 + c0) * H;
+#pragma unroll
+            for (int i = 0; i < kRingPer; ++i) {
+                const int j = t + i * kSoftmaxThreads;
+                if (j < n4) cp_async_16(slot + 4 * j, src + 4 * j);
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");  // one group per load, maybe empty
+            ++issued;
+            if (++c == nc) {
+                c = 0;
+                if (nc > kResident && pass == 0)
+                    pass = 1;
+                else
+                    have = false;
+            }
+        }
+    }
+};
+
+// fold the thread's float4s of one chunk into its running (m, z) of 4 heads
+__device__ __forceinline__ void ring_fold(const float *slot, int n4, int t, float4 &m, float4 &z) {
+    const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    float4 v[kRingPer];
+    float4 cm = ninf;
+#pragma unroll
+    for (int i = 0; i < kRingPer; ++i) {
+        const int j = t + i * kSoftmaxThreads;
+        v[i] = j < n4 ? reinterpret_cast<const float4 *>(slot)[j] : ninf;
+        cm = max4(cm, v[i]);
+    }
+    auto rescale = [](float &mw, float &zw, float cw) {
+        if (cw > mw) {
+            zw = zw == 0.f ? 0.f : zw * ex2_approx((mw - cw) * kLog2e);
+            mw = cw;
+        }
+    };
+    rescale(m.x, z.x, cm.x);
+    rescale(m.y, z.y, cm.y);
+    rescale(m.z, z.z, cm.z);
+    rescale(m.w, z.w, cm.w);
+    // a -inf score adds nothing (also while the running maximum is -inf)
+    auto term = [](float x, float mw) { return x == -INFINITY ? 0.f : ex2_approx((x - mw) * kLog2e); };
+#pragma unroll
+    for (int i = 0; i < kRingPer; ++i) {
+        z.x += term(v[i].x, m.x);
+        z.y += term(v[i].y, m.y);
+        z.z += term(v[i].z, m.z);
+        z.w += term(v[i].w, m.w);
+    }
+}
+
+// write the thread's float4s of one chunk as 2^((x - m) log2 e) * inv
+__device__ __forceinline__ void ring_write(const float *slot, int n4, int t, float4 m, float4 inv,
+                                           float *gout) {
+#pragma unroll
+    for (int i = 0; i < kRingPer; ++i) {
+        const int j = t + i * kSoftmaxThreads;
+        if (j < n4) {
+            const float4 v = reinterpret_cast<const float4 *>(slot)[j];
+            reinterpret_cast<float4 *>(gout)[j] =
+                make_float4(ex2_approx((v.x - m.x) * kLog2e) * inv.x,
+                            ex2_approx((v.y - m.y) * kLog2e) * inv.y,
+                            ex2_approx((v.z - m.z) * kLog2e) * inv.z,
+                            ex2_approx((v.w - m.w) * kLog2e) * inv.w);
+        }
+    }
+}
+
+// The row's (maximum, sum) of each of the thread's 4 heads from every
+// thread's running (m, z), Q = H/4 <= 8 head groups: xor-shuffles inside the
+// warps, then two barriers (maxima; sums rescaled to the row maximum)
+// through the two regions of red. A warp writes a region again only after
+// the next barrier, which every warp reaches after its reads, so no barrier
+// follows the reads.
+__device__ __forceinline__ void ring_merge(float4 &m, float4 &z, int Q, float *red) {
+    constexpr int NW = kSoftmaxThreads / 32;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int q = lane & (Q - 1);  // = t % Q, the thread's head group
+    float4 *rm = reinterpret_cast<float4 *>(red);   // [NW][Q] warp maxima
+    float4 *rz = rm + NW * 8;                       // [NW][Q] warp sums
+    float4 mw = m;
+    for (int o = 16; o >= Q; o >>= 1) mw = max4(mw, shfl_xor4(mw, o));
+    if (lane < Q) rm[warp * Q + lane] = mw;
+    __syncthreads();
+    float4 M = rm[q];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) M = max4(M, rm[w * Q + q]);
+    // a zero sum stays zero (its maximum may be -inf)
+    auto sc = [](float zz, float mm, float MM) {
+        return zz == 0.f ? 0.f : zz * ex2_approx((mm - MM) * kLog2e);
+    };
+    float4 zs = make_float4(sc(z.x, m.x, M.x), sc(z.y, m.y, M.y), sc(z.z, m.z, M.z),
+                            sc(z.w, m.w, M.w));
+    for (int o = 16; o >= Q; o >>= 1) {
+        const float4 y = shfl_xor4(zs, o);
+        zs = make_float4(zs.x + y.x, zs.y + y.y, zs.z + y.z, zs.w + y.w);
+    }
+    if (lane < Q) rz[warp * Q + lane] = zs;
+    __syncthreads();
+    float4 Z = rz[q];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) {
+        const float4 y = rz[w * Q + q];
+        Z = make_float4(Z.x + y.x, Z.y + y.y, Z.z + y.z, Z.w + y.w);
+    }
+    m = M;
+    z = Z;
+}
+
+// The plan's heavy rows longer than cap_e edges, entries blockIdx.x,
+// blockIdx.x + gridDim.x, ... of its list (interleaved, so every warp of the
+// block knows the block's upcoming rows without a hand-off; the light
+// batches that follow are fetched dynamically and even out the load).
+// Entered and left by all threads of the block, every copy waited for.
+__device__ __forceinline__ void softmax_heavy_ring(const int32_t *__restrict__ row_ptr,
+                                                   const int32_t *__restrict__ heavy_rows,
+                                                   int64_t n_heavy, int32_t H, int32_t cap_e,
+                                                   const float *scores, float *out, float *buf,
+                                                   float *red) {
+    const int t = threadIdx.x, lane = t & 31;
+    const int Q = H >> 2;
+    const int64_t G = gridDim.x;
+    for (int64_t g0 = 0; (int64_t)blockIdx.x + g0 * G < n_heavy; g0 += 32) {
+        // 32 list entries at a time, one per lane (every warp the same)
+        const int64_t k = (int64_t)blockIdx.x + (g0 + lane) * G;
+        int32_t e0_lane = 0, deg_lane = 0;
+        if (k < n_heavy) {
+            const int32_t row = __ldg(heavy_rows + k);
+            e0_lane = __ldg(row_ptr + row);
+            deg_lane = __ldg(row_ptr + row + 1) - e0_lane;
+        }
+        const unsigned rows = __ballot_sync(kFull, deg_lane > cap_e);
+        ChunkIssuer is{rows, 0, 0, 0, 0, 0, false, 0};
+        int freed = 0, kc = 0;  // loads consumed and freed; next load to consume
+        is.pump(scores, buf, H, cap_e, e0_lane, deg_lane, freed, t);
+        for (unsigned left = rows; left; left &= left - 1u) {
+            const int l = __ffs(left) - 1;
+            const int32_t e0 = __shfl_sync(kFull, e0_lane, l);
+            const int32_t deg = __shfl_sync(kFull, deg_lane, l);
+            const int32_t nc = (deg + cap_e - 1) / cap_e;
+            const bool resident = nc <= kResident;
+            float4 m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            const int k_row = kc;
+            for (int32_t c = 0; c < nc; ++c) {
+                const int32_t dc = deg - c * cap_e < cap_e ? deg - c * cap_e : cap_e;
+                cp_async_wait_upto(is.issued - 1 - kc);
+                ring_fold(buf + (kc % kRing) * kSpanFloats, dc * Q, t, m, z);
+                ++kc;
+                if (!resident) {
+                    ++freed;
+                    is.pump(scores, buf, H, cap_e, e0_lane, deg_lane, freed, t);
+                }
+            }
+            // merge over the block; an all -inf head: maximum -inf, sum 0,
+            // NaN outputs (two-pass definition)
+            ring_merge(m, z, Q, red);
+            const float4 mg = m;
+            const float4 inv = make_float4(rcp_approx(z.x), rcp_approx(z.y), rcp_approx(z.z),
+                                           rcp_approx(z.w));
+            for (int32_t c = 0; c < nc; ++c) {
+                const int32_t dc = deg - c * cap_e < cap_e ? deg - c * cap_e : cap_e;
+                int kk;
+                if (resident) {
+                    kk = k_row + c;  // still in its slot
+                } else {
+                    kk = kc++;
+                    cp_async_wait_upto(is.issued - 1 - kk);
+                }
+                ring_write(buf + (kk % kRing) * kSpanFloats, dc * Q, t, mg, inv,
+                           out + ((int64_t)e0 + c * cap_e) * H);
+                ++freed;
+                is.pump(scores, buf, H, cap_e, e0_lane, deg_lane, freed, t);
+            }
+        }
+    }
+}
+
 // ---- all rows, H <= 32, one launch
 //
 // Phase 1 (with a plan): the plan's heavy rows longer than a warp's buffer,
@@ -820,7 +1064,11 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
     // the buffer with W = 4 and Q a power of two, else straight from global);
     // the plan's heavy rows beyond the buffer are phase 1's
     const bool tiers = W == 4 && ((H / W) & (H / W - 1)) == 0;
-    if (n_heavy > 0) {
+    if (n_heavy > 0 && tiers && H <= 32) {
+        softmax_heavy_ring(row_ptr, heavy_rows, n_heavy, H, cap_e, scores, out, span_smem, red);
+        cp_async_wait_all();
+        __syncthreads();  // the buffer is the warps' again
+    } else if (n_heavy > 0) {
         // units of kHeavyUnit list entries from the plan's second counter;
         // the next unit's index is fetched while this one is computed
         const int32_t ce = kSpanBlockFloats / 2 / H;  // edges per half buffer
