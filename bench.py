@@ -377,16 +377,16 @@ def bench_fused(args, rank, world, local, dist):
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for a, b in ev:
-            a.record(stream)
+        for ev_a, ev_b in ev:
+            ev_a.record(stream)
             step()
-            b.record(stream)
+            ev_b.record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
     dist_barrier(dist)
     torch.cuda.synchronize()
     total_ms = t0.elapsed_time(t1)
-    per_launch = [a.elapsed_time(b) for a, b in ev]
+    per_launch = [x.elapsed_time(y) for x, y in ev]
     ms_step = dist_max(dist, total_ms / args.steps, None)
     kern_ms = statistics.mean(per_launch)
     sp = spread(per_launch)
@@ -773,12 +773,12 @@ def bench_small(name, args):
         torch.cuda.synchronize()
         ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(50)]
-        for a, b in ev2:
-            a.record()
+        for ev_a, ev_b in ev2:
+            ev_a.record()
             two()
-            b.record()
+            ev_b.record()
         torch.cuda.synchronize()
-        extra["two_launch_median_ms"] = spread([a.elapsed_time(b) for a, b in ev2])["median_ms"]
+        extra["two_launch_median_ms"] = spread([x.elapsed_time(y) for x, y in ev2])["median_ms"]
         extra["two_launch"] = "gat_edge_softmax then gat_spmm_weighted, weights through memory"
     elif name == "sddmm":
         si, di, a, b = t(g["src_idx"]), t(g["dst_idx"]), t(g["src_feat"]), t(g["dst_feat"])
@@ -814,12 +814,14 @@ def bench_small(name, args):
     reps = 50
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(reps)]
-    for a, b in evs:
-        a.record()
+    # (the workload closures above may capture names such as a and b: the
+    # events get names of their own)
+    for ev_a, ev_b in evs:
+        ev_a.record()
         fn()
-        b.record()
+        ev_b.record()
     torch.cuda.synchronize()
-    sp = spread([a.elapsed_time(b) for a, b in evs])
+    sp = spread([x.elapsed_time(y) for x, y in evs])
     ms = sp["median_ms"]
     hbm_peak, bf16_peak, kind = measured_peaks()
     res = {"ms_per_step": ms, "p10_ms": sp["p10_ms"], "p90_ms": sp["p90_ms"], "reps": reps,
