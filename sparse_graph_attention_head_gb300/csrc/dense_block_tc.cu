@@ -65,7 +65,9 @@ constexpr int kRing = 2;
 constexpr uint32_t kChunkHalf = D * D * 2;        // one of hi / lo, fp16
 constexpr uint32_t kChunkBytes = 2 * kChunkHalf;
 constexpr uint32_t kW1Half = P * P * 2;           // W1 image, one of hi / lo
-constexpr int kNodeStride = D;                    // staged node rows are contiguous (one bulk copy)
+// staged node rows: stride 100 floats, so the 16-byte loads of 8 lanes
+// (8 consecutive rows) fall in 8 distinct bank quads (one bulk copy per row)
+constexpr int kNodeStride = D + 4;
 // TMEM columns (32-bit): fp32 accumulators, or fp16 pairs for A operands
 // A operands (x_n, then the context) at column 288 (even tiles) or 384 (odd)
 // (hi: kAHalf columns of fp16 pairs for the D inputs, then lo)
@@ -392,19 +394,24 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
     int loaded = 0, issued = 0, refill = 0;
     for (; loaded < total && loaded < kRing; ++loaded) load(loaded);
     constexpr uint32_t idesc = idesc_f16(D, 128);
-    // a tile's node rows (contiguous graphs) into the staging buffer, one bulk copy
+    // a tile's node rows (contiguous graphs) into the staging buffer, one
+    // bulk copy per row (rows kNodeStride floats apart)
     auto load_nodes = [&](int tl) {
         const int64_t b0 = (int64_t)tl * kGraphs;
         const int64_t ng = p.B - b0 < kGraphs ? p.B - b0 : kGraphs;
-        const uint32_t bytes = (uint32_t)(ng * p.N * D * 4);
+        const int rows = (int)(ng * p.N);
         const uint32_t bar = smem_u32(&br.nfull);
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                     "r"((uint32_t)(rows * D * 4))
                      : "memory");
-        asm volatile(
-            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-            "[%3];" ::"r"(smem_u32(nodes_s)),
-            "l"(p.nodes + b0 * p.N * D), "r"(bytes), "r"(bar)
-            : "memory");
+        const float *src = p.nodes + b0 * p.N * D;
+        const uint32_t dst = smem_u32(nodes_s);
+        for (int r = 0; r < rows; ++r)
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+                "[%3];" ::"r"(dst + (uint32_t)(r * kNodeStride * 4)),
+                "l"(src + (int64_t)r * D), "r"((uint32_t)(D * 4)), "r"(bar)
+                : "memory");
     };
     if (n_my > 0) load_nodes(blockIdx.x);
     bool bail = false;
@@ -633,8 +640,10 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         const int quad = warp >> 2;                         // relation-MLP blocks quad, quad + 4, ...
         uint32_t ph_qkv = 0, ph_of = 0;
 
-        // this thread's relation-MLP prefetch slot: 16 features and the mask value
-        const float4 *pslot = reinterpret_cast<const float4 *>(stage_base + tid * P);
+        // this thread's relation-MLP prefetch slot: 16 features (quarter c at
+        // float4 index c * 512 + tid, so a warp's 16-byte accesses are
+        // consecutive) and the mask value
+        const float4 *pslot = reinterpret_cast<const float4 *>(stage_base) + tid;
         const float *mslot = stage_base + kComputeThreads * P + tid;
         auto fetch_pairs = [&](int tl, int blk) {
             const int pi = 128 * blk + 32 * g + lane;
@@ -642,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             if (pi < kGraphs * NN && (int64_t)tl * kGraphs + pi / NN < p.B) {
 #pragma unroll
                 for (int c = 0; c < P / 4; ++c)
-                    cp_async16(smem_u32(pslot + c), p.pair + pg * P + 4 * c);
+                    cp_async16(smem_u32(pslot + c * kComputeThreads), p.pair + pg * P + 4 * c);
                 asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(mslot)),
                              "l"(p.mask + pg)
                              : "memory");
@@ -684,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 float pf[P];
 #pragma unroll
                 for (int c = 0; c < P / 4; ++c) {
-                    const float4 v = valid ? pslot[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 v = valid ? pslot[c * kComputeThreads] : make_float4(0.f, 0.f, 0.f, 0.f);
                     pf[4 * c] = v.x;
                     pf[4 * c + 1] = v.y;
                     pf[4 * c + 2] = v.z;
