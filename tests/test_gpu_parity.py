@@ -130,6 +130,40 @@ def test_edge_softmax_neg_inf_heads_on_every_row_path(gat, H):
                 assert abs(g[e0 + (e1 - e0) // 2, 1] - 1.0) <= 1e-6
 
 
+@pytest.mark.parametrize("H", [8, 4])
+def test_edge_softmax_heavy_ring_boundaries_and_many_heavy_rows(gat, H):
+    """The heavy rows' chunk ring: 20,000 plan-heavy rows at H = 8 (more than
+    32 list entries per block of the grid, so blocks take several 32-entry
+    groups; 6,000 at H = 4) cycling through the ring's boundaries in chunks
+    of 2048/H edges: one
+    edge past a warp buffer, exactly 2 and 4 chunks (the largest row kept in
+    its slots), 4 chunks + 1 (the first row read twice), and long rows; an
+    all -inf head on some rows. Every element against the oracle."""
+    ce = 2048 // H
+    cyc = np.array([ce + 1, 2 * ce, 2 * ce + 1, 4 * ce, 4 * ce + 1, 9 * ce + 3, ce + 7, 3 * ce])
+    deg = np.tile(cyc, 20000 // cyc.size + 1)[:20000].astype(np.int64)
+    if H == 4:  # keep the edge count moderate at the wider chunks
+        deg = deg[:6000]
+    rng = np.random.default_rng(90 + H)
+    rp_h = np.concatenate([[0], np.cumsum(deg)]).astype(np.int32)
+    E = int(rp_h[-1])
+    s_h = (2.0 * rng.standard_normal((E, H))).astype(np.float32)
+    for r in range(0, deg.size, 997):
+        s_h[rp_h[r]:rp_h[r + 1], 0] = -np.inf
+    rp = dev(rp_h)
+    plan = gat.Plan(rp)
+    assert plan.info()["n_heavy"] == deg.size
+    o = oracle.edge_softmax(rp_h, s_h, H)
+    g = host(gat.gat_edge_softmax(rp, dev(s_h), H, plan=plan))
+    nan_rows = np.zeros(E, dtype=bool)
+    for r in range(0, deg.size, 997):
+        nan_rows[rp_h[r]:rp_h[r + 1]] = True
+    assert np.isnan(g[nan_rows, 0]).all()
+    keep = np.ones(g.shape, dtype=bool)
+    keep[nan_rows, 0] = False
+    assert_fp32(g[keep], o[keep], name=f"edge_softmax heavy ring H={H}")
+
+
 def test_edge_softmax_unaligned_buffers(gat):
     """Scores and output 4 bytes off a 16-byte boundary (H = 8): the 4-byte
     copy path, with and without a plan, against the oracle."""
