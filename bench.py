@@ -816,7 +816,13 @@ def bench_small(name, args):
            for _ in range(reps)]
     # (the workload closures above may capture names such as a and b: the
     # events get names of their own)
+    cold = getattr(args, "cold_l2", False)
+    if cold:
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
     for ev_a, ev_b in evs:
+        if cold:
+            flush.fill_(1)  # outside the events: evicts the workload's lines from L2
         ev_a.record()
         fn()
         ev_b.record()
@@ -826,7 +832,7 @@ def bench_small(name, args):
     hbm_peak, bf16_peak, kind = measured_peaks()
     res = {"ms_per_step": ms, "p10_ms": sp["p10_ms"], "p90_ms": sp["p90_ms"], "reps": reps,
            "units_per_s": units / (ms * 1e-3), "launches_per_step": launches,
-           "warm": True, "algorithmic_bytes": alg_bytes,
+           "warm": not cold, "algorithmic_bytes": alg_bytes,
            "achieved_gbs": alg_bytes / (ms * 1e-3) / 1e9,
            "hbm_frac": alg_bytes / (ms * 1e-3) / 1e9 / hbm_peak}
     if flops:
@@ -840,6 +846,8 @@ def bench_small(name, args):
         res["tf32_peak_tflops"] = tf32_peak
         res["peak_kind"] = kind
     res.update(extra)
+    res["l2"] = ("flushed before each call (twice the L2 size written)" if cold else
+                 "warm (inputs may stay in L2 between calls)")
     if name in ("edge_softmax", "aggregate", "sddmm"):
         res["note"] = "L2-resident and launch-latency bound at this size; fractions are not a roofline claim"
     return res
@@ -855,6 +863,13 @@ def main():
     ap.add_argument("--workload", default="fused",
                     choices=["fused", "edge_softmax", "aggregate", "sddmm", "dense", "spmm_heads",
                              "edge_softmax_h8", "fused_backward", "fused_fp8", "sddmm_csr"])
+    ap.add_argument("--config", type=int, choices=[1, 2, 3, 4, 5],
+                    help="the workload by its configuration number: 1 edge softmax (384 rows), "
+                         "2 softmax + aggregation, 3 COO SDDMM, 4 the fused layer on the "
+                         "1e6-row graph (the default), 5 the dense-masked block")
+    ap.add_argument("--cold-l2", action="store_true",
+                    help="smaller workloads: write a buffer of twice the L2 size before each "
+                         "timed call (cold-cache times; by default they are timed warm)")
     ap.add_argument("--ref-rows", type=int, default=40000,
                     help="--impl reference: consecutive rows per step, split over the host's "
                          "cores (~0.2 s of oracle work on 16 cores)")
@@ -874,6 +889,9 @@ def main():
                          "or one graph cut into row shards (rowshard, strong scaling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.config is not None:
+        args.workload = {1: "edge_softmax", 2: "aggregate", 3: "sddmm", 4: "fused",
+                         5: "dense"}[args.config]
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         # one process per GPU: relaunch this command under the torch launcher
         sys.exit(relaunch_ranks(args.gpus))
