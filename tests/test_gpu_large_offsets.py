@@ -144,3 +144,35 @@ def test_backward_past_32bit_offsets(gat, big):
         assert int(torch.count_nonzero(grad).item()) == int(torch.count_nonzero(grad[tt]).item())
     del k, v, dk, dv, tr
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("use_plan", [True, False])
+def test_edge_softmax_scores_past_2_31_elements(gat, use_plan):
+    """Scores [E, 8] with E * 8 past 2^31: 290,000 rows of 1,000 edges (the
+    heavy-row path with a plan, rows streamed twice through a warp buffer
+    without one), then 100,000 light rows of 1..40 edges whose scores all
+    lie past the 2^31st element. Sampled row ranges (across the boundary and
+    at the end) against the oracle on the same scores."""
+    Hs = 8
+    deg = np.concatenate([np.full(290_000, 1000),
+                          np.random.default_rng(12).integers(1, 41, 100_000)]).astype(np.int64)
+    rp = np.concatenate([[0], np.cumsum(deg)]).astype(np.int64)
+    assert rp[290_000] * Hs > 2**31 and rp[-1] < 2**31
+    rp32 = rp.astype(np.int32)
+    E = int(rp[-1])
+    g = torch.Generator(device="cuda").manual_seed(77)
+    s = torch.randn((E, Hs), device="cuda", generator=g) * 2.0
+    out = torch.empty_like(s)
+    rpd = dev(rp32)
+    plan = gat.Plan(rpd) if use_plan else None
+    gat.gat_edge_softmax(rpd, s, Hs, out=out, plan=plan)
+    torch.cuda.synchronize()
+    boundary = int(np.searchsorted(rp, 2**31 // Hs, side="right")) - 1
+    for r0, r1 in ((boundary - 3, boundary + 3), (289_990, 290_010), (389_000, 390_000)):
+        e0, e1 = int(rp[r0]), int(rp[r1])
+        sub = s[e0:e1].cpu().numpy()
+        o = oracle.edge_softmax((rp[r0:r1 + 1] - e0).astype(np.int32), sub, Hs)
+        assert_fp32(out[e0:e1].cpu().numpy().astype(np.float64), o,
+                    name=f"edge softmax rows {r0}..{r1}, scores past 2^31")
+    del s, out
+    torch.cuda.empty_cache()
