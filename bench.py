@@ -805,6 +805,16 @@ def bench_small(name, args):
         mlp = 2.0 * N_ * N_ * (P_ * P_ + H_ * P_)            # relation MLP
         flops = B_ * (proj + attn + mlp)
         tensor_flops = B_ * proj
+        # the kernel reads the pair features of unmasked pairs only (a masked
+        # pair's logit is -inf whatever its relation-MLP bias): the bytes it
+        # has to move on this mask, beside the nominal count above
+        unmasked = int((g["edge_mask"] >= 0.5).sum())
+        need = B_ * 4 * (2 * N_ * D_ + N_ * N_) + 4 * P_ * unmasked + 4 * (4 * D_ * D_)
+        extra["required_bytes"] = need
+        extra["unmasked_pair_frac"] = unmasked / float(B_ * N_ * N_)
+        extra["bytes_note"] = ("algorithmic_bytes / hbm_frac: every pair's features (the "
+                               "workload's definition); required_bytes / hbm_frac_required: "
+                               "the unmasked pairs' features only, as the kernel reads them")
     else:
         raise ValueError(name)
     for _ in range(max(3, args.warmup)):
@@ -846,6 +856,8 @@ def bench_small(name, args):
         res["tf32_peak_tflops"] = tf32_peak
         res["peak_kind"] = kind
     res.update(extra)
+    if "required_bytes" in extra:
+        res["hbm_frac_required"] = extra["required_bytes"] / (ms * 1e-3) / 1e9 / hbm_peak
     res["l2"] = ("flushed before each call (twice the L2 size written)" if cold else
                  "warm (inputs may stay in L2 between calls)")
     if name in ("edge_softmax", "aggregate", "sddmm"):

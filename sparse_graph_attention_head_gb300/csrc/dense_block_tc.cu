@@ -27,21 +27,28 @@
 //       issues Q|K|V once LayerNorm(t) is in TMEM and tile t-1's readers of
 //       those columns are done, each relation-MLP block once its features
 //       are in TMEM, and the out-projection once the context is;
-//   A (quad q = warps 4q..4q+3): the relation MLP, one thread per node pair
-//       of 128-pair blocks q, q + 4, ...: the pair's 16 features (prefetched
-//       into shared memory by cp.async) go, split and scaled, to its TMEM lane
-//       as the A operand of W1 (128 x 16 x 16 MMAs, in TMEM columns idle
-//       until the next tile's LayerNorm); the same thread reads the hidden
-//       values back and applies b1, SiLU, W2, b2 (packed f32x2 FMAs) and the
-//       edge mask (-inf where masked), giving the bias of all heads;
+//   A (quad q = warps 4q..4q+3): the relation MLP over the tile's unmasked
+//       pairs only (a masked pair's logit is -inf whatever its bias, so its
+//       features are never read): per (graph, query row) a word of unmasked
+//       keys and a prefix of their counts, built from the mask in shared
+//       memory the tile before; one thread per unmasked pair of 128-pair
+//       blocks q, q + 4, ...: the pair's 16 features (prefetched into shared
+//       memory by cp.async) go, split and scaled, to its TMEM lane as the A
+//       operand of W1 (128 x 16 x 16 MMAs, in TMEM columns idle until the
+//       next tile's LayerNorm); the same thread reads the hidden values back
+//       and applies b1, SiLU, W2, b2 (packed f32x2 FMAs), giving the bias of
+//       all heads;
 //   B (warp (g, h) = (w % 4, w / 4)): attention of head h in graph g, one
 //       thread per query node: Q row from TMEM, K and V rows staged in shared
-//       memory, scores + bias in log2 units, two-pass softmax with ex2,
+//       memory, scores + bias in log2 units (-inf for the query's masked
+//       keys, from its word), two-pass softmax with ex2,
 //       context (packed f32x2 FMAs); the context becomes the out-projection's
 //       A operand (scaled per graph by the largest |V|, which bounds it);
 //   C: LayerNorm of tile t+1 into the other A region of TMEM (warp (g, k):
 //       columns [24k, 24k + 24) of graph g's rows, row statistics combined
-//       through shared memory), then out-projection columns [24h, 24h + 24)
+//       through shared memory), tile t+1's unmasked-pair words and prefix
+//       (its mask copied in by cp.async since the end of B) and its first
+//       relation-MLP prefetch, then out-projection columns [24h, 24h + 24)
 //       + the residual.
 // Every mbarrier wait is bounded; a wait that gives up sets the call's error
 // flag in the workspace (readable with gat_dense_masked_attention_status) and
@@ -352,10 +359,11 @@ struct Smem {
         return b > lnred_bytes ? b : lnred_bytes;
     }
     __host__ __device__ static uint32_t stage(int N) { return bias + bias_bytes(N); }
-    // K / V staging of the attention, or (during the relation MLP) one
-    // prefetch slot of 16 features per compute thread plus its mask value
+    // K / V staging of the attention, or (outside it) one prefetch slot of
+    // 16 features per compute thread and the next tile's mask values
     __host__ __device__ static uint32_t stage_bytes(int N) {
-        const uint32_t kv = kComputeWarps * 2 * N * DH * 4, mlp = kComputeThreads * (P + 1) * 4;
+        const uint32_t kv = kComputeWarps * 2 * N * DH * 4,
+                       mlp = kComputeThreads * P * 4 + kGraphs * N * N * 4;
         return kv > mlp ? kv : mlp;
     }
     __host__ __device__ static uint32_t nodes(int N) { return stage(N) + stage_bytes(N); }
@@ -365,7 +373,12 @@ struct Smem {
     __host__ __device__ static uint32_t params(int N) { return nodes(N) + nodes_bytes(N); }
     static constexpr uint32_t params_bytes = (P * P + P + P * H + H + 2 * D + 4) * 4;
     __host__ __device__ static uint32_t rscale(int N) { return params(N) + params_bytes; }
-    __host__ __device__ static uint32_t total(int N) { return rscale(N) + 128 * 4; }
+    // the tile's unmasked pairs: per (graph, query row) a word of unmasked
+    // keys (bit j), and the exclusive prefix of their counts over the 128
+    // rows (graph-major), [128] = the tile's total
+    __host__ __device__ static uint32_t umask(int N) { return rscale(N) + 128 * 4; }
+    __host__ __device__ static uint32_t rpre(int N) { return umask(N) + 128 * 4; }
+    __host__ __device__ static uint32_t total(int N) { return rpre(N) + 132 * 4; }
 };
 
 struct Barriers {
@@ -569,6 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
           *bet = gam + D;
     float *red = reinterpret_cast<float *>(sm + Smem::bias);  // LayerNorm statistics (phase C)
     int32_t *rscale = reinterpret_cast<int32_t *>(sm + Smem::rscale(N));
+    uint32_t *um_s = reinterpret_cast<uint32_t *>(sm + Smem::umask(N));
+    int32_t *rpre_s = reinterpret_cast<int32_t *>(sm + Smem::rpre(N));
     float *bias = reinterpret_cast<float *>(sm + Smem::bias);
     float *nodes_s = reinterpret_cast<float *>(sm + Smem::nodes(N));
     float *stage_base = reinterpret_cast<float *>(sm + Smem::stage(N));
@@ -636,32 +651,93 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         const int g = warp & 3, h = warp >> 2, n = lane;  // graph (lane quarter), head, node
         const uint32_t lane_q = (uint32_t)(32 * g) << 16;
         const float qk_scale = kLog2e / sqrtf((float)DH);  // scores in log2 units
-        const int nblk = (kGraphs * NN + 127) / 128;        // 128-pair relation-MLP blocks per tile
         const int quad = warp >> 2;                         // relation-MLP blocks quad, quad + 4, ...
         uint32_t ph_qkv = 0, ph_of = 0;
 
-        // this thread's relation-MLP prefetch slot: 16 features (quarter c at
-        // float4 index c * 512 + tid, so a warp's 16-byte accesses are
-        // consecutive) and the mask value
+        // Relation-MLP pairs: only the unmasked ones. A masked pair's logit is
+        // -inf whatever its relation MLP gives, so its features are never read;
+        // the unmasked pairs of a tile are numbered in (graph, query, key)
+        // order and taken in 128-pair blocks.
+        // mask_copy(tl): tile tl's mask values into the staging region above
+        // the prefetch slots (cp.async, issued while the staging region is
+        // free and long before use); compact(tl): the unmasked-key words (a
+        // thread per (graph, row)) and their row prefix (every compute
+        // thread; three barriers)
+        float *mask_s = stage_base + kComputeThreads * P;
+        auto mask_copy = [&](int tl) {
+            const int64_t g0 = (int64_t)tl * kGraphs;
+            const int np = (int)((p.B - g0 < kGraphs ? p.B - g0 : kGraphs) * NN);
+            for (int pi = tid; pi < np; pi += kComputeThreads)
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(mask_s + pi)),
+                             "l"(p.mask + g0 * NN + pi)
+                             : "memory");
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        auto compact = [&](int tl) {
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            named_sync(1, kComputeThreads);  // every thread's mask copies landed
+            if (tid < 128) {
+                const int gg = tid >> 5, nn = tid & 31;
+                uint32_t w = 0;
+                if (nn < N && (int64_t)tl * kGraphs + gg < p.B) {
+                    const float *mr = mask_s + gg * NN + nn * N;
+                    for (int j = 0; j < N; ++j) w |= (mr[j] < 0.5f ? 0u : 1u) << j;
+                }
+                um_s[tid] = w;
+            }
+            named_sync(1, kComputeThreads);
+            if (warp == 0) {
+                int cr[4], sum = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    cr[k] = __popc(um_s[4 * lane + k]);
+                    sum += cr[k];
+                }
+                int incl = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                int ex = incl - sum;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    rpre_s[4 * lane + k] = ex;
+                    ex += cr[k];
+                }
+                if (lane == 31) rpre_s[128] = incl;
+            }
+            named_sync(1, kComputeThreads);
+        };
+        // the idx-th unmasked pair of the tile (idx < its count): the row by a
+        // binary search of the prefix, the key as that row's k-th unmasked bit
+        auto pair_of = [&](int idx) -> int {
+            int r = 0;
+#pragma unroll
+            for (int st = 64; st > 0; st >>= 1)
+                if (rpre_s[r + st] <= idx) r += st;
+            const int j = (int)__fns(um_s[r], 0, idx - rpre_s[r] + 1);
+            return (r >> 5) * NN + (r & 31) * N + j;
+        };
+        // this thread's relation-MLP prefetch slot: 16 features, quarter c at
+        // float4 index c * 512 + tid (a warp's 16-byte accesses consecutive)
         const float4 *pslot = reinterpret_cast<const float4 *>(stage_base) + tid;
-        const float *mslot = stage_base + kComputeThreads * P + tid;
         auto fetch_pairs = [&](int tl, int blk) {
-            const int pi = 128 * blk + 32 * g + lane;
-            const int64_t pg = (int64_t)tl * kGraphs * NN + pi;
-            if (pi < kGraphs * NN && (int64_t)tl * kGraphs + pi / NN < p.B) {
+            const int idx = 128 * blk + 32 * g + lane;
+            if (idx < rpre_s[128]) {
+                const int64_t pg = (int64_t)tl * kGraphs * NN + pair_of(idx);
 #pragma unroll
                 for (int c = 0; c < P / 4; ++c)
                     cp_async16(smem_u32(pslot + c * kComputeThreads), p.pair + pg * P + 4 * c);
-                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(mslot)),
-                             "l"(p.mask + pg)
-                             : "memory");
             }
             asm volatile("cp.async.commit_group;" ::: "memory");
         };
 
         // prologue: LayerNorm of the first tile; its relation-MLP prefetch
         if (n_my > 0) {
-            if (quad < nblk) fetch_pairs(blockIdx.x, quad);
+            mask_copy(blockIdx.x);
+            compact(blockIdx.x);
+            if (128 * quad < rpre_s[128]) fetch_pairs(blockIdx.x, quad);
             mbar_wait(&br.nfull, 0, err);  // the first tile's node rows
             layer_norm(p, nodes_s, red, rscale, gam, bet, tmem, col_a(0), blockIdx.x, warp, lane);
             mbar_arrive(&br.xfull);
@@ -683,12 +759,13 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             // hidden values are read back, block i + 1 is split and issued, then block
             // i's epilogue runs while the tensor cores work.
             bool guard = it > 0;  // the last LayerNorm's statistics share the bias region
+            const int npairs = rpre_s[128];            // the tile's unmasked pairs
+            const int nblk = (npairs + 127) >> 7;       // in 128-pair blocks
             const uint32_t slot_col = mlp_col(it, quad);
             const uint32_t mslot_t = tmem + lane_q + slot_col;
             const bool issuer = (warp & 3) == 0 && lane == 0;
-            auto split_issue = [&](int blk, int &sp, float &mk) {
-                const int pi = 128 * blk + 32 * g + lane;
-                const bool valid = pi < kGraphs * NN && (int64_t)tile * kGraphs + pi / NN < p.B;
+            auto split_issue = [&](int blk, int &sp) {
+                const bool valid = 128 * blk + 32 * g + lane < npairs;
                 asm volatile("cp.async.wait_all;" ::: "memory");
                 float pf[P];
 #pragma unroll
@@ -699,7 +776,6 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                     pf[4 * c + 2] = v.z;
                     pf[4 * c + 3] = v.w;
                 }
-                mk = valid ? *mslot : 1.f;
                 if (blk + 4 < nblk) fetch_pairs(tile, blk + 4);
                 float mx = 0.f;
 #pragma unroll
@@ -727,19 +803,17 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 }
             };
             int sp = 0;
-            float mk = 1.f;
-            if (quad < nblk) split_issue(quad, sp, mk);
+            if (quad < nblk) split_issue(quad, sp);
             for (int blk = quad; blk < nblk; blk += 4) {
-                const int pi = 128 * blk + 32 * g + lane;
-                const bool valid = pi < kGraphs * NN && (int64_t)tile * kGraphs + pi / NN < p.B;
+                const int idx = 128 * blk + 32 * g + lane;
+                const bool valid = idx < npairs;
                 mbar_wait(&br.dfull[quad], ph_df, err);
                 ph_df ^= 1u;
                 fence_after();
                 float hid[P];
                 tmem_ld16(mslot_t + 16, hid);
                 const float unsc = exp2i(-sp) * exp2i(-sw_s[4]);
-                const float mask_v = mk;
-                if (blk + 4 < nblk) split_issue(blk + 4, sp, mk);
+                if (blk + 4 < nblk) split_issue(blk + 4, sp);
                 // b1, SiLU, then r = W2 silu + b2 as head pairs (0, 1), (2, 3)
                 float2 r01 = make_float2(b2s[0], b2s[1]), r23 = make_float2(b2s[2], b2s[3]);
 #pragma unroll
@@ -763,16 +837,21 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                     guard = false;
                 }
                 if (valid) {
+                    const int pi = pair_of(idx);
                     const int gg = pi / NN, rem = pi - gg * NN, nn = rem / N, j = rem - nn * N;
-                    const bool masked = mask_v < 0.5f;
                     float *bw = bias + (gg * H * N + j) * NS + nn;  // head stride N * NS
-                    bw[0] = masked ? -INFINITY : r01.x * kLog2e;
-                    bw[N * NS] = masked ? -INFINITY : r01.y * kLog2e;
-                    bw[2 * N * NS] = masked ? -INFINITY : r23.x * kLog2e;
-                    bw[3 * N * NS] = masked ? -INFINITY : r23.y * kLog2e;
+                    bw[0] = r01.x * kLog2e;
+                    bw[N * NS] = r01.y * kLog2e;
+                    bw[2 * N * NS] = r23.x * kLog2e;
+                    bw[3 * N * NS] = r23.y * kLog2e;
                 }
             }
-            named_sync(1, kComputeThreads);  // every pair's bias written
+            if (guard) {  // this thread had no block: the barrier phase is still consumed
+                mbar_wait(&br.edone, ph_ed, err);
+                ph_ed ^= 1u;
+                guard = false;
+            }
+            named_sync(1, kComputeThreads);  // every unmasked pair's bias written
             mbar_wait(&br.qkv, ph_qkv, err);
             ph_qkv ^= 1u;
             fence_after();
@@ -814,6 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 // the score of (n, j) replaces its bias entry, which only this
                 // lane reads: the two softmax passes keep no score registers
                 float *brow = bias + (g * H + h) * N * NS + n;
+                const uint32_t unm = rvalid ? um_s[32 * g + n] : 0u;  // this query's unmasked keys
                 float m = -INFINITY;
                 const int nj = rvalid ? N : 0;  // lanes past the graph's nodes touch nothing
 #pragma unroll 2
@@ -825,7 +905,8 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                         a = ffma2(q2[2 * c], make_float2(k4.x, k4.y), a);
                         bb = ffma2(q2[2 * c + 1], make_float2(k4.z, k4.w), bb);
                     }
-                    const float s = ((a.x + a.y) + (bb.x + bb.y)) + brow[j * NS];
+                    const float s = (unm >> j) & 1u ? ((a.x + a.y) + (bb.x + bb.y)) + brow[j * NS]
+                                                    : -INFINITY;
                     brow[j * NS] = s;
                     m = fmaxf(m, s);
                 }
@@ -851,7 +932,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                                     : make_float2(0.f, 0.f);
             }
             named_sync(1, kComputeThreads);  // every graph's largest |V| known; staging free
-            if (it + 1 < n_my && quad < nblk) fetch_pairs(tile + gridDim.x, quad);
+            if (it + 1 < n_my) mask_copy(tile + gridDim.x);  // read after the next LayerNorm
             // the context (|ctx| <= max |V| of the graph) as the out-projection's A operand
             const int sc_g = scale_exp(__int_as_float(vmax_s[g]));
             {
@@ -880,6 +961,10 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 layer_norm(p, nodes_s, red, rscale, gam, bet, tmem, col_a(it + 1),
                            tile + gridDim.x, warp, lane);
                 mbar_arrive(&br.xfull);
+                // the next tile's unmasked pairs (this tile's attention has read
+                // its words) and its first relation-MLP block
+                compact(tile + gridDim.x);
+                if (128 * quad < rpre_s[128]) fetch_pairs(tile + gridDim.x, quad);
             }
             mbar_wait(&br.ofull, ph_of, err);
             ph_of ^= 1u;

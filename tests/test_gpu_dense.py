@@ -123,3 +123,38 @@ def test_dense_block_n32_d128(gat):
     w = W.make_dense(seed=23, B=40, N=32, D=128, H=8, P=32, wstd=0.05)
     o, c = oracle.dense_block(w, want_cond=True)
     assert_fp32(run(gat, w), o, c, name="dense block 32x128")
+
+
+def test_dense_block_mask_densities_and_unread_masked_pairs(gat):
+    """The tensor-core block runs the relation MLP on the unmasked pairs only
+    (a masked pair's logit is -inf whatever its bias): masks from all
+    unmasked to all masked per graph and per 4-graph tile (a tile with no
+    unmasked pair, a tile of 2,304), a partial last tile; every masked pair's
+    features are NaN or +inf, so a kernel that read them would show it.
+    Rows with every key masked are NaN (as the reference); the rest match
+    the oracle."""
+    B, N = 37, 24
+    w = W.make_dense(seed=51, B=B, wstd=0.05, affine_ln=True)
+    rng = np.random.default_rng(52)
+    m = w["edge_mask"]
+    dens = {0: 1.0, 1: 0.0, 2: 0.05, 3: 0.95, 4: 0.5, 5: 0.3, 6: -1, 7: 0.3}
+    for b, d in dens.items():
+        if d < 0:  # the diagonal only
+            m[b] = np.eye(N, dtype=np.float32)
+        else:
+            m[b] = (rng.random((N, N)) < d).astype(np.float32)
+            if b != 1:
+                np.fill_diagonal(m[b], 1.0)
+    m[8:12] = 0.0  # a tile without one unmasked pair
+    m[12:16] = 1.0  # a tile of unmasked pairs only
+    masked = m < 0.5
+    pf = w["pair_feats"]
+    pf[masked] = np.nan
+    pf[masked & (rng.random(masked.shape) < 0.3)] = np.inf
+    g = run(gat, w)
+    o, c = oracle.dense_block(w, want_cond=True)
+    empty = ~(m >= 0.5).any(axis=2)  # [B, N]: queries with every key masked
+    assert empty[1].all() and empty[8:12].all() and not empty[12:16].any()
+    assert np.isnan(g[empty]).all()
+    assert np.isfinite(g[~empty]).all()
+    assert_fp32(g[~empty], o[~empty], c[~empty], name="dense block mask densities")
