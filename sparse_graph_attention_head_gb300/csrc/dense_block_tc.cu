@@ -386,6 +386,13 @@ struct Barriers {
 };
 
 // Control thread: weight ring and every MMA issue, driven by mbarriers.
+// Per tile the weight chunks stream as K, V, Q, O (workspace images 1, 2, 0,
+// 3): K and V (TMEM columns 96-287) go as soon as the tile's LayerNorm is in
+// TMEM, since the previous tile's attention - their only other reader - is
+// over by then; Q (columns 0-95) waits for the previous tile's epilogue to
+// read the out-projection there; O for the context.
+__host__ __device__ constexpr int chunk_of(int pos) { return pos == 0 ? 1 : pos == 1 ? 2 : pos == 2 ? 0 : 3; }
+
 __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, uint32_t tmem,
                              int n_my, const float *nodes_s, int32_t *err) {
     const int total = kChunks * n_my;
@@ -401,7 +408,7 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
         asm volatile(
             "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
             "[%3];" ::"r"(ring0 + (uint32_t)s * kChunkBytes),
-            "l"(src0 + (size_t)(r % kChunks) * kChunkBytes), "r"(kChunkBytes), "r"(bar)
+            "l"(src0 + (size_t)chunk_of(r % kChunks) * kChunkBytes), "r"(kChunkBytes), "r"(bar)
             : "memory");
     };
     int loaded = 0, issued = 0, refill = 0;
@@ -429,8 +436,10 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
     if (n_my > 0) load_nodes(blockIdx.x);
     bool bail = false;
     for (int t = 0; t < n_my && !bail; ++t) {
-        // Q|K|V(t) overwrite columns [0, 288) that tile t-1's attention and
-        // epilogue read: wait for LayerNorm(t) and for tile t-1's readers
+        // K, V(t) overwrite columns [96, 288) that tile t-1's attention read
+        // (over: its context was signalled before O(t-1) was issued) and Q(t)
+        // columns [0, 96) that its epilogue reads: LayerNorm(t) for all
+        // three, tile t-1's epilogue for Q
         bool x_ok = false, e_ok = t == 0, c_ok = false;
         uint64_t idle_since = 0;
         uint32_t idle = 0;
@@ -447,7 +456,7 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
                 }
             }
             {
-            const int c = issued % kChunks, s = issued % kRing;
+            const int pos = issued % kChunks, c = chunk_of(pos), s = issued % kRing;
             if (!x_ok) {
                 x_ok = mbar_test(&br.xfull, (uint32_t)t & 1u);
                 // LayerNorm(t) has read the staged rows: the next tile's go there
@@ -455,7 +464,7 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
             }
             if (!e_ok) e_ok = mbar_test(&br.edone, (uint32_t)(t - 1) & 1u);
             if (c == kChunks - 1 && !c_ok) c_ok = mbar_test(&br.cfull, (uint32_t)t & 1u);
-            const bool ready = c < kChunks - 1 ? (x_ok && e_ok) : c_ok;
+            const bool ready = c == kChunks - 1 ? c_ok : (c == 0 ? x_ok && e_ok : x_ok);
             if (ready && mbar_test(&br.wfull[s], (ph_wfull >> s) & 1u)) {
                 ph_wfull ^= 1u << s;
                 fence_after();
@@ -471,7 +480,7 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
                     mma_ts(d, al, dh, idesc, 1);
                 }
                 mma_commit(&br.wdone[s]);
-                if (c == kChunks - 2) mma_commit(&br.qkv);
+                if (c == 0) mma_commit(&br.qkv);  // Q, the last of the three
                 if (c == kChunks - 1) mma_commit(&br.ofull);
                 ++issued;
                 progress = true;
@@ -660,8 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         // order and taken in 128-pair blocks.
         // mask_copy(tl): tile tl's mask values into the staging region above
         // the prefetch slots (cp.async, issued while the staging region is
-        // free and long before use); compact(tl): the unmasked-key words (a
-        // thread per (graph, row)) and their row prefix (every compute
+        // free and long before use); compact(tl): the unmasked-key words (four
+        // threads per (graph, row)) and their row prefix (every compute
         // thread; three barriers)
         float *mask_s = stage_base + kComputeThreads * P;
         auto mask_copy = [&](int tl) {
@@ -676,14 +685,22 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         auto compact = [&](int tl) {
             asm volatile("cp.async.wait_all;" ::: "memory");
             named_sync(1, kComputeThreads);  // every thread's mask copies landed
-            if (tid < 128) {
-                const int gg = tid >> 5, nn = tid & 31;
+            {
+                // word r = tid / 4 (graph r / 32, row r % 32), keys
+                // [6 (tid % 4), 6 (tid % 4) + 6) from this thread, OR-ed over the 4
+                const int r = tid >> 2, part = tid & 3, gg = r >> 5, nn = r & 31;
                 uint32_t w = 0;
                 if (nn < N && (int64_t)tl * kGraphs + gg < p.B) {
                     const float *mr = mask_s + gg * NN + nn * N;
-                    for (int j = 0; j < N; ++j) w |= (mr[j] < 0.5f ? 0u : 1u) << j;
+#pragma unroll
+                    for (int k = 0; k < kMaxN / 4; ++k) {
+                        const int j = (kMaxN / 4) * part + k;
+                        if (j < N) w |= (mr[j] < 0.5f ? 0u : 1u) << j;
+                    }
                 }
-                um_s[tid] = w;
+                w |= __shfl_xor_sync(kFull, w, 1);
+                w |= __shfl_xor_sync(kFull, w, 2);
+                if (part == 0) um_s[r] = w;
             }
             named_sync(1, kComputeThreads);
             if (warp == 0) {
