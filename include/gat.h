@@ -450,8 +450,11 @@ gat_status_t gat_fused_layer_no_alloc(const int32_t *row_ptr, const int32_t *col
  * into scaled fp16 halves in `workspace` (caller device memory, 16-byte
  * aligned, at least gat_dense_masked_attention_workspace_size bytes; its
  * contents on entry are ignored), then one kernel computes the block (fp32
- * accuracy from three fp16 products per product, see the kernel). Other
- * shapes run a SIMT kernel and take no workspace (NULL allowed).
+ * accuracy from three fp16 products per product, see the kernel). That
+ * kernel evaluates the relation MLP for unmasked pairs only: the features
+ * of a pair whose edge_mask is < 0.5 are never read (its logit is -inf
+ * whatever they hold, NaN included). Other shapes run a SIMT kernel and
+ * take no workspace (NULL allowed).
  * The tensor-core kernel never traps: a wait on its pipeline that gives up
  * (never expected) sets a flag in the workspace and the affected outputs are
  * NaN; gat_dense_masked_attention_status turns that flag into a status.
