@@ -52,20 +52,26 @@ struct Fp8Params {
     int64_t slot_floats;
 };
 
-// 16 E4M3 codes -> 16 floats (exact: every E4M3 value is a half)
-__device__ __forceinline__ void decode16(const uint4 &u, float *f) {
+// 16 E4M3 codes -> 8 float pairs (elements 2i, 2i + 1); exact: every E4M3 value is a half
+__device__ __forceinline__ void decode16x2(const uint4 &u, float2 *f) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)(w[i] >> (16 * j));
-            const __half2 h = __half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3));
-            const float2 v = __half22float2(h);
-            f[4 * i + 2 * j] = v.x;
-            f[4 * i + 2 * j + 1] = v.y;
+            f[2 * i + j] = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
         }
-    }
+}
+
+// packed fp32 FMA on a pair, (a.x b.x + c.x, a.y b.y + c.y), each rounded once
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)),
+          "l"(*reinterpret_cast<uint64_t *>(&c)));
+    return *reinterpret_cast<float2 *>(&r);
 }
 
 // 16 consecutive elements of a T row, as floats
@@ -87,7 +93,7 @@ __device__ __forceinline__ void store16(T *p, const float *f) {
 
 template <typename T, int V, int U>
 struct Fp8Row {
-    float qf[V][16], acc[V][16];
+    float2 qf[V][8], acc[V][8];  // element pairs (packed fp32 arithmetic)
     float m[V], l[V];
     int lane, G, vi[V], head[V];
 
@@ -105,11 +111,12 @@ struct Fp8Row {
         const T *qrow = static_cast<const T *>(p.q) + row * (int64_t)p.Hs * p.Dh;
 #pragma unroll
         for (int s = 0; s < V; ++s) {
-            load16(qrow + vi[s] * 16, qf[s]);
+            float qv[16];
+            load16(qrow + vi[s] * 16, qv);
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                qf[s][t] *= p.qscale;
-                acc[s][t] = 0.f;
+            for (int t = 0; t < 8; ++t) {
+                qf[s][t] = make_float2(qv[2 * t] * p.qscale, qv[2 * t + 1] * p.qscale);
+                acc[s][t] = make_float2(0.f, 0.f);
             }
             m[s] = -INFINITY;
             l[s] = 0.f;
@@ -145,12 +152,12 @@ struct Fp8Row {
                 for (int u = 0; u < U; ++u)
 #pragma unroll
                     for (int s = 0; s < V; ++s) {
-                        float kf[16];
-                        decode16(kr[u][s], kf);
-                        float d = 0.f;
+                        float2 kf[8];
+                        decode16x2(kr[u][s], kf);
+                        float2 d = make_float2(0.f, 0.f);
 #pragma unroll
-                        for (int t = 0; t < 16; ++t) d = fmaf(qf[s][t], kf[t], d);
-                        sc[u][s] = d;
+                        for (int t = 0; t < 8; ++t) d = fma2(qf[s][t], kf[t], d);
+                        sc[u][s] = d.x + d.y;
                     }
                 for (int o = 1; o < G; o <<= 1) {
 #pragma unroll
@@ -169,17 +176,19 @@ struct Fp8Row {
                     if (mx == -INFINITY) continue;
                     const float c = fast_exp2(m[s] - mx);
                     l[s] *= c;
+                    const float2 c2 = make_float2(c, c), z2 = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) acc[s][t] *= c;
+                    for (int t = 0; t < 8; ++t) acc[s][t] = fma2(acc[s][t], c2, z2);
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
                         const float pe = j0 + u < n ? fast_exp2(sc[u][s] - mx) : 0.f;
                         l[s] += pe;
                         const float w = pe * vss[u][s];
-                        float vf[16];
-                        decode16(vr[u][s], vf);
+                        const float2 w2 = make_float2(w, w);
+                        float2 vf[8];
+                        decode16x2(vr[u][s], vf);
 #pragma unroll
-                        for (int t = 0; t < 16; ++t) acc[s][t] = fmaf(w, vf[t], acc[s][t]);
+                        for (int t = 0; t < 8; ++t) acc[s][t] = fma2(w2, vf[t], acc[s][t]);
                     }
                     m[s] = mx;
                 }
@@ -194,7 +203,10 @@ struct Fp8Row {
             const float inv = l[s] > 0.f ? 1.f / l[s] : 0.f;
             float o[16];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) o[t] = acc[s][t] * inv;
+            for (int t = 0; t < 8; ++t) {
+                o[2 * t] = acc[s][t].x * inv;
+                o[2 * t + 1] = acc[s][t].y * inv;
+            }
             store16(orow + vi[s] * 16, o);
         }
     }
@@ -208,9 +220,9 @@ struct Fp8Row {
 #pragma unroll
         for (int s = 0; s < V; ++s) {
 #pragma unroll
-            for (int t = 0; t < 16; t += 4)
-                __stcg(reinterpret_cast<float4 *>(slot + vi[s] * 16 + t),
-                       make_float4(acc[s][t], acc[s][t + 1], acc[s][t + 2], acc[s][t + 3]));
+            for (int t = 0; t < 8; t += 2)
+                __stcg(reinterpret_cast<float4 *>(slot + vi[s] * 16 + 2 * t),
+                       make_float4(acc[s][t].x, acc[s][t].y, acc[s][t + 1].x, acc[s][t + 1].y));
             if (vi[s] % G == 0) {
                 __stcg(slot + HD + head[s], m[s]);
                 __stcg(slot + HD + p.H + head[s], l[s]);
@@ -229,7 +241,7 @@ struct Fp8Row {
             m[s] = -INFINITY;
             l[s] = 0.f;
 #pragma unroll
-            for (int t = 0; t < 16; ++t) acc[s][t] = 0.f;
+            for (int t = 0; t < 8; ++t) acc[s][t] = make_float2(0.f, 0.f);
         }
         for (int c = c0; c < c1; ++c) {
             const float *sl = p.partials + (int64_t)c * p.slot_floats;
@@ -242,12 +254,12 @@ struct Fp8Row {
                 const float a1 = fast_exp2(m[s] - mx), a2 = fast_exp2(mc - mx);
                 l[s] = l[s] * a1 + lc * a2;
 #pragma unroll
-                for (int t = 0; t < 16; t += 4) {
-                    const float4 f = ld_cg_f4(sl + vi[s] * 16 + t);
-                    acc[s][t] = acc[s][t] * a1 + f.x * a2;
-                    acc[s][t + 1] = acc[s][t + 1] * a1 + f.y * a2;
-                    acc[s][t + 2] = acc[s][t + 2] * a1 + f.z * a2;
-                    acc[s][t + 3] = acc[s][t + 3] * a1 + f.w * a2;
+                for (int t = 0; t < 8; t += 2) {
+                    const float4 f = ld_cg_f4(sl + vi[s] * 16 + 2 * t);
+                    acc[s][t].x = acc[s][t].x * a1 + f.x * a2;
+                    acc[s][t].y = acc[s][t].y * a1 + f.y * a2;
+                    acc[s][t + 1].x = acc[s][t + 1].x * a1 + f.z * a2;
+                    acc[s][t + 1].y = acc[s][t + 1].y * a1 + f.w * a2;
                 }
                 m[s] = mx;
             }
