@@ -124,27 +124,6 @@ __device__ __forceinline__ int4 item_meta(const EngineParams &p, int64_t item) {
     return make_int4((int)row, __ldg(p.row_ptr + row), __ldg(p.row_ptr + row + 1), -1);
 }
 
-// Edge range of one work item; returns false when the item is skipped.
-__device__ __forceinline__ bool item_range(const EngineParams &p, int64_t item, int64_t &row,
-                                           int &e0, int &e1, int &hr, int64_t &chunk) {
-    if (item < p.n_chunks) {
-        chunk = item;
-        hr = __ldg(p.chunk_row + chunk);
-        row = __ldg(p.heavy_rows + hr);
-        const int j = (int)(chunk - __ldg(p.chunk_start + hr));
-        const int rs = __ldg(p.row_ptr + row), re = __ldg(p.row_ptr + row + 1);
-        e0 = rs + j * p.chunk_edges;
-        e1 = min(e0 + p.chunk_edges, re);
-        return true;
-    }
-    chunk = -1;
-    hr = -1;
-    row = item - p.n_chunks;
-    e0 = __ldg(p.row_ptr + row);
-    e1 = __ldg(p.row_ptr + row + 1);
-    return (e1 - e0) <= p.heavy_threshold;
-}
-
 // ---------------------------------------------------------------------------
 // fused mode
 // ---------------------------------------------------------------------------
