@@ -933,7 +933,9 @@ def main():
         return
     res, d = bench_fused(args, rank, world, local, dist)
     if rank == 0:
-        if not args.no_extras:
+        # the side workloads and the CPU baseline are single-GPU measurements:
+        # taken at N = 1 only (at N > 1 every rank ends with the headline)
+        if not args.no_extras and world == 1:
             res["other_workloads"] = {}
             for nm in ("edge_softmax", "aggregate", "sddmm", "dense", "spmm_heads",
                        "edge_softmax_h8", "fused_backward", "fused_fp8", "sddmm_csr"):
@@ -941,7 +943,7 @@ def main():
                     res["other_workloads"][nm] = bench_small(nm, args)
                 except Exception as exc:  # keep the headline line if a side workload fails
                     res["other_workloads"][nm] = {"error": repr(exc)}
-        if args.cpu_budget > 0:
+        if args.cpu_budget > 0 and world == 1:
             res["cpu_baseline"] = cpu_baseline_fused(d, budget_s=args.cpu_budget)
         print(json.dumps(res), flush=True)
     if dist is not None:
