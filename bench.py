@@ -735,8 +735,8 @@ def bench_small(name, args):
         alg_bytes = g["n_rows"] * (4 + rb) + g["n_edges"] * (4 + rb + 4 * g["H"])
         flops = 2.0 * g["n_edges"] * g["H"] * g["Dh"]
     elif name == "edge_softmax_h8":
-        # 8 heads on the 1e6-row power-law graph
-        deg = W.zipf_degrees(np.random.default_rng(3), 1_000_000)
+        # 8 heads on the 1e6-row power-law graph (--n-rows: smaller, for captures)
+        deg = W.zipf_degrees(np.random.default_rng(3), args.n_rows)
         g = W.make_edge_softmax(seed=6, deg=deg, H=8)
         rp, s = t(g["row_ptr"]), t(g["scores"])
         out = torch.empty_like(s)
@@ -888,7 +888,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for cpu_baseline (0: skip)")
     ap.add_argument("--n-rows", type=int, default=1_000_000,
-                    help="rows of the fused workload (smaller only for profiling captures)")
+                    help="rows of the 1e6-row workloads (fused, fused_backward, fused_fp8, "
+                         "sddmm_csr, edge_softmax_h8; smaller only for profiling captures)")
     ap.add_argument("--no-extras", action="store_true", help="skip the smaller workloads")
     ap.add_argument("--l2-persist", default="off",
                     choices=["off", "none", "q", "k", "v", "dout", "scores"],
