@@ -633,7 +633,7 @@ def bench_small(name, args):
     extra = {}
     if name == "spmm_heads":
         # head_dim 32, 8 heads, fp32 weights and features, 1e6-row power-law graph
-        g = W.make_spmm_heads()
+        g = W.make_spmm_heads(n=args.n_rows)
         rp, ci, w, feat = t(g["row_ptr"]), t(g["col_idx"]), t(g["w"]), t(g["feat"])
         out = torch.empty_like(feat)
         plan = gat.Plan(rp)
@@ -889,7 +889,8 @@ def main():
                     help="seconds of oracle time for cpu_baseline (0: skip)")
     ap.add_argument("--n-rows", type=int, default=1_000_000,
                     help="rows of the 1e6-row workloads (fused, fused_backward, fused_fp8, "
-                         "sddmm_csr, edge_softmax_h8; smaller only for profiling captures)")
+                         "sddmm_csr, edge_softmax_h8, spmm_heads; smaller only for profiling "
+                         "captures)")
     ap.add_argument("--no-extras", action="store_true", help="skip the smaller workloads")
     ap.add_argument("--l2-persist", default="off",
                     choices=["off", "none", "q", "k", "v", "dout", "scores"],
