@@ -516,11 +516,14 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
 // w / 4) takes columns [24k, 24k + 24) of graph g's rows (thread = row), the
 // row statistics are summed over the four column quarters through `red`.
 // Writes the row scale exponents and returns after this thread's TMEM stores
-// are complete and fenced.
+// are complete and fenced. Its first barrier also covers this thread's
+// cp.async copies (the tile's mask values), and `mid` runs between its two
+// barriers (whatever it writes is visible to all compute threads on return).
+template <typename Mid>
 __device__ __forceinline__ void layer_norm(const Params &p, const float *nodes_s, float *red,
                                            int32_t *rscale, const float *gam, const float *bet,
                                            uint32_t tmem, uint32_t acol, int tile, int warp,
-                                           int lane) {
+                                           int lane, Mid &&mid) {
     const int g = warp & 3, k = warp >> 2, n = lane, N = p.N;
     const bool valid = (int64_t)tile * kGraphs + g < p.B && n < N;
     const int row = 32 * g + n;
@@ -533,7 +536,9 @@ __device__ __forceinline__ void layer_norm(const Params &p, const float *nodes_s
 #pragma unroll
     for (int c = 0; c < 6; ++c) s1 += (x[c].x + x[c].y) + (x[c].z + x[c].w);
     red[k * 128 + row] = s1;
+    asm volatile("cp.async.wait_all;" ::: "memory");
     named_sync(1, kComputeThreads);
+    mid();
     const float mean = ((red[row] + red[128 + row]) + (red[256 + row] + red[384 + row])) / (float)D;
     float v2 = 0.f, dm = 0.f;
 #pragma unroll
@@ -669,9 +674,9 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         // order and taken in 128-pair blocks.
         // mask_copy(tl): tile tl's mask values into the staging region above
         // the prefetch slots (cp.async, issued while the staging region is
-        // free and long before use); compact(tl): the unmasked-key words (four
-        // threads per (graph, row)) and their row prefix (every compute
-        // thread; three barriers)
+        // free and long before use); mask_words(tl): the unmasked-key words
+        // (four threads per (graph, row)); mask_prefix(): their row prefix
+        // (warp 0, then a barrier)
         float *mask_s = stage_base + kComputeThreads * P;
         auto mask_copy = [&](int tl) {
             const int64_t g0 = (int64_t)tl * kGraphs;
@@ -682,9 +687,9 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                              : "memory");
             asm volatile("cp.async.commit_group;" ::: "memory");
         };
-        auto compact = [&](int tl) {
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            named_sync(1, kComputeThreads);  // every thread's mask copies landed
+        // (the words are built between the LayerNorm's two barriers: its first
+        // makes the mask copies visible, its second the words)
+        auto mask_words = [&](int tl) {
             {
                 // word r = tid / 4 (graph r / 32, row r % 32), keys
                 // [6 (tid % 4), 6 (tid % 4) + 6) from this thread, OR-ed over the 4
@@ -702,7 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 w |= __shfl_xor_sync(kFull, w, 2);
                 if (part == 0) um_s[r] = w;
             }
-            named_sync(1, kComputeThreads);
+        };
+        auto mask_prefix = [&]() {
             if (warp == 0) {
                 int cr[4], sum = 0;
 #pragma unroll
@@ -750,15 +756,16 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             asm volatile("cp.async.commit_group;" ::: "memory");
         };
 
-        // prologue: LayerNorm of the first tile; its relation-MLP prefetch
+        // prologue: LayerNorm of the first tile with its unmasked-pair words;
+        // its relation-MLP prefetch
         if (n_my > 0) {
             mask_copy(blockIdx.x);
-            compact(blockIdx.x);
-            if (128 * quad < rpre_s[128]) fetch_pairs(blockIdx.x, quad);
             mbar_wait(&br.nfull, 0, err);  // the first tile's node rows
-            layer_norm(p, nodes_s, red, rscale, gam, bet, tmem, col_a(0), blockIdx.x, warp, lane);
+            layer_norm(p, nodes_s, red, rscale, gam, bet, tmem, col_a(0), blockIdx.x, warp, lane,
+                       [&] { mask_words(blockIdx.x); });
             mbar_arrive(&br.xfull);
-            named_sync(1, kComputeThreads);  // statistics read: the bias region is free
+            mask_prefix();  // also: LayerNorm statistics read, the bias region is free
+            if (128 * quad < rpre_s[128]) fetch_pairs(blockIdx.x, quad);
         }
         uint32_t ph_ed = 0, ph_df = 0;
 
@@ -975,12 +982,13 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
             if (it + 1 < n_my) {
                 mbar_wait(&br.nfull, (uint32_t)(it + 1) & 1u, err);  // the next tile's node rows
+                // with the next tile's unmasked-pair words (this tile's attention
+                // has read the words), then their prefix and its first
+                // relation-MLP block
                 layer_norm(p, nodes_s, red, rscale, gam, bet, tmem, col_a(it + 1),
-                           tile + gridDim.x, warp, lane);
+                           tile + gridDim.x, warp, lane, [&] { mask_words(tile + gridDim.x); });
                 mbar_arrive(&br.xfull);
-                // the next tile's unmasked pairs (this tile's attention has read
-                // its words) and its first relation-MLP block
-                compact(tile + gridDim.x);
+                mask_prefix();
                 if (128 * quad < rpre_s[128]) fetch_pairs(tile + gridDim.x, quad);
             }
             mbar_wait(&br.ofull, ph_of, err);
