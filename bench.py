@@ -855,6 +855,36 @@ def bench_small(name, args):
         res["tensor_issue_frac_of_tf32_peak"] = 3 * tensor_flops / (ms * 1e-3) / 1e12 / tf32_peak
         res["tf32_peak_tflops"] = tf32_peak
         res["peak_kind"] = kind
+    if name in ("edge_softmax", "aggregate", "sddmm"):
+        # launch-bound at this size: the per-call events above include the
+        # host's time to issue the call. The same calls captured in a CUDA
+        # graph and replayed give the device time per call.
+        per_graph = 20
+        cs = torch.cuda.Stream()
+        cs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cs):
+            for _ in range(3):
+                fn()
+        torch.cuda.current_stream().wait_stream(cs)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(per_graph):
+                fn()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_replay = 20
+        ga.record()
+        for _ in range(n_replay):
+            graph.replay()
+        gb.record()
+        torch.cuda.synchronize()
+        g_ms = ga.elapsed_time(gb) / (n_replay * per_graph)
+        extra["graph_ms_per_call"] = g_ms
+        extra["graph_units_per_s"] = units / (g_ms * 1e-3)
+        extra["graph_note"] = f"{per_graph} calls captured in one CUDA graph, {n_replay} replays"
     res.update(extra)
     if "required_bytes" in extra:
         res["hbm_frac_required"] = extra["required_bytes"] / (ms * 1e-3) / 1e9 / hbm_peak

@@ -1333,15 +1333,12 @@ extern "C" gat_status_t gat_edge_softmax(const int32_t *row_ptr, int64_t n_rows,
         // the grid is exactly the resident blocks and batches are fetched
         // from the plan's counter
         auto kern = vec4 ? softmax_rows_kernel<4> : softmax_rows_kernel<1>;
-        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kSpanSmemBytes);
+        // the attribute and the resident-block count, once per device and kernel
+        static std::atomic<int> attr_done[2][kMaxDevices];
+        static std::atomic<int64_t> caps[2][kMaxDevices];
+        cudaError_t err = allow_dynamic_smem(attr_done[vec4 ? 1 : 0], kern, kSpanSmemBytes);
         if (err != cudaSuccess) return cuda_fail(err, "gat_edge_softmax: shared memory attribute");
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSoftmaxThreads,
-                                                          kSpanSmemBytes) != cudaSuccess ||
-            per_sm < 1)
-            per_sm = 1;
-        const int64_t cap = (int64_t)sm_count() * per_sm;
+        const int64_t cap = device_blocks(caps[vec4 ? 1 : 0], kern, kSoftmaxThreads, kSpanSmemBytes);
         const int64_t n_heavy = plan ? plan->n_heavy : 0;
         if (blocks > cap || (plan && n_heavy > 0)) blocks = cap;
         kern<<<(unsigned)blocks, kSoftmaxThreads, kSpanSmemBytes, s>>>(
