@@ -38,12 +38,16 @@
 //       next tile's LayerNorm); the same thread reads the hidden values back
 //       and applies b1, SiLU, W2, b2 (packed f32x2 FMAs), giving the bias of
 //       all heads;
-//   B (warp (g, h) = (w % 4, w / 4)): attention of head h in graph g, one
-//       thread per query node: Q row from TMEM, K and V rows staged in shared
-//       memory, scores + bias in log2 units (-inf for the query's masked
-//       keys, from its word), two-pass softmax with ex2,
-//       context (packed f32x2 FMAs); the context becomes the out-projection's
-//       A operand (scaled per graph by the largest |V|, which bounds it);
+//   B (warp (g, h) = (w % 4, w / 4)): attention of head h in graph g: V
+//       rows staged in shared memory, Q and K in 8-dim slices; scores and
+//       context as warp-level tensor-core MMAs (m16n8k8, tf32 operands
+//       split in two, three products per term) on the warp's 24 x 24
+//       products - a tcgen05 version would need 256 TMEM columns per head
+//       beside the projections' 512; bias in log2 units (-inf for the
+//       query's masked keys, from its word), softmax with ex2 over the
+//       quad of lanes sharing a row; the context becomes the
+//       out-projection's A operand (scaled per graph by the largest |V|,
+//       which bounds it);
 //   C: LayerNorm of tile t+1 into the other A region of TMEM (warp (g, k):
 //       columns [24k, 24k + 24) of graph g's rows, row statistics combined
 //       through shared memory), tile t+1's unmasked-pair words and prefix
@@ -284,6 +288,24 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     uint64_t r;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk2(a)), "l"(pk2(b)), "l"(pk2(c)));
     return up2(r);
+}
+
+// x as a tf32 part rounded to nearest (ties away) and its remainder, also
+// rounded: x = big + small up to ~2^-22 |x|
+__device__ __forceinline__ void split_tf32(float x, uint32_t &big, uint32_t &small) {
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(big) : "f"(x));
+    const float r = x - __uint_as_float(big);
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(small) : "f"(r));
+}
+
+// d += A B for one warp: A 16 x 8 (row-major fragment), B 8 x 8 (column-major
+// fragment), tf32 operands, fp32 accumulators
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -884,75 +906,182 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             const int sr = rscale[32 * g + n];
             float2 ctx[DH / 2];
             {
-                float *sk = stage_base + warp * 2 * N * DH;
-                float *sv = sk + N * DH;
+                // The warp's two staging slots: V rows in the second; the first
+                // holds 8-dim slices of the Q and K rows for one k-step of the
+                // scores at a time, then the normalised context.
+                float *s1 = stage_base + warp * 2 * N * DH;
+                float *sv = s1 + N * DH;
+                float *sq8 = s1, *sk8 = s1 + N * 8;
                 const float uq = exp2i(-sr) * exp2i(-sw_s[0]) * qk_scale,
                             uk = exp2i(-sr) * exp2i(-sw_s[1]), uv = exp2i(-sr) * exp2i(-sw_s[2]);
-                float qf[DH], kf[DH], vf[DH];
+                const int nq = b < p.B ? N : 0;  // the graph's rows (queries) and keys
+                float vm = 0.f;
 #pragma unroll
                 for (int c0 = 0; c0 < DH; c0 += 8) {
-                    tmem_ld8(tmem + lane_q + (uint32_t)(h * DH + c0), qf + c0);
-                    tmem_ld8(tmem + lane_q + (uint32_t)(D + h * DH + c0), kf + c0);
-                    tmem_ld8(tmem + lane_q + (uint32_t)(2 * D + h * DH + c0), vf + c0);
-                }
-                float vm = 0.f;
-                float2 q2[DH / 2];
+                    float vf[8];
+                    tmem_ld8(tmem + lane_q + (uint32_t)(2 * D + h * DH + c0), vf);
 #pragma unroll
-                for (int c = 0; c < DH / 2; ++c) q2[c] = make_float2(qf[2 * c] * uq, qf[2 * c + 1] * uq);
-                if (rvalid) {
-#pragma unroll
-                    for (int c = 0; c < DH; c += 4) {
-                        *reinterpret_cast<float4 *>(sk + n * DH + c) =
-                            make_float4(kf[c] * uk, kf[c + 1] * uk, kf[c + 2] * uk, kf[c + 3] * uk);
-                        const float4 v4 = make_float4(vf[c] * uv, vf[c + 1] * uv, vf[c + 2] * uv,
-                                                      vf[c + 3] * uv);
-                        *reinterpret_cast<float4 *>(sv + n * DH + c) = v4;
-                        vm = fmaxf(vm, fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)),
-                                             fmaxf(fabsf(v4.z), fabsf(v4.w))));
+                    for (int i = 0; i < 8; ++i) {
+                        vf[i] *= uv;
+                        vm = fmaxf(vm, fabsf(vf[i]));
+                    }
+                    if (rvalid) {
+                        *reinterpret_cast<float4 *>(sv + n * DH + c0) = make_float4(vf[0], vf[1], vf[2], vf[3]);
+                        *reinterpret_cast<float4 *>(sv + n * DH + c0 + 4) = make_float4(vf[4], vf[5], vf[6], vf[7]);
                     }
                 }
+                vm = rvalid ? vm : 0.f;
                 vm = warp_max(vm);
                 if (lane == 0) atomicMax(&vmax_s[g], __float_as_int(vm));
+                // Warp-level tensor-core MMAs (m16n8k8, tf32 operands split into
+                // a rounded part and its remainder, three products per term as
+                // the projections' split does): 32 query rows (2 row tiles) x
+                // 24 keys (3 tiles of 8), then x 24 dims. Fragment coordinates:
+                // row group tq, column pair / k slot tr.
+                const int tq = lane >> 2, tr = lane & 3;
+                float sacc[2][3][4];
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+#pragma unroll
+                    for (int t = 0; t < 3; ++t)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sacc[m][t][e] = 0.f;
+                // scores S = Q K^T (log2 units), k over the head's dims in 3 steps of 8
+#pragma unroll
+                for (int st = 0; st < DH / 8; ++st) {
+                    float qv[8], kv[8];
+                    tmem_ld8(tmem + lane_q + (uint32_t)(h * DH + 8 * st), qv);
+                    tmem_ld8(tmem + lane_q + (uint32_t)(D + h * DH + 8 * st), kv);
+                    __syncwarp();  // every lane is done with the previous slices
+                    if (rvalid) {
+                        *reinterpret_cast<float4 *>(sq8 + n * 8) =
+                            make_float4(qv[0] * uq, qv[1] * uq, qv[2] * uq, qv[3] * uq);
+                        *reinterpret_cast<float4 *>(sq8 + n * 8 + 4) =
+                            make_float4(qv[4] * uq, qv[5] * uq, qv[6] * uq, qv[7] * uq);
+                        *reinterpret_cast<float4 *>(sk8 + n * 8) =
+                            make_float4(kv[0] * uk, kv[1] * uk, kv[2] * uk, kv[3] * uk);
+                        *reinterpret_cast<float4 *>(sk8 + n * 8 + 4) =
+                            make_float4(kv[4] * uk, kv[5] * uk, kv[6] * uk, kv[7] * uk);
+                    }
+                    __syncwarp();
+                    uint32_t ab[2][4], as[2][4];
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        const int r0 = 16 * m + tq, r1 = r0 + 8;
+                        split_tf32(r0 < nq ? sq8[r0 * 8 + tr] : 0.f, ab[m][0], as[m][0]);
+                        split_tf32(r1 < nq ? sq8[r1 * 8 + tr] : 0.f, ab[m][1], as[m][1]);
+                        split_tf32(r0 < nq ? sq8[r0 * 8 + tr + 4] : 0.f, ab[m][2], as[m][2]);
+                        split_tf32(r1 < nq ? sq8[r1 * 8 + tr + 4] : 0.f, ab[m][3], as[m][3]);
+                    }
+#pragma unroll
+                    for (int t = 0; t < 3; ++t) {
+                        const int key = 8 * t + tq;
+                        uint32_t bb[2], bs[2];
+                        split_tf32(key < nq ? sk8[key * 8 + tr] : 0.f, bb[0], bs[0]);
+                        split_tf32(key < nq ? sk8[key * 8 + tr + 4] : 0.f, bb[1], bs[1]);
+#pragma unroll
+                        for (int m = 0; m < 2; ++m) {
+                            mma_tf32(sacc[m][t], as[m], bb);
+                            mma_tf32(sacc[m][t], ab[m], bs);
+                            mma_tf32(sacc[m][t], ab[m], bb);
+                        }
+                    }
+                }
+                // bias (log2 units) on the query's unmasked keys, -inf on the
+                // others and on keys past the graph's nodes; then the row softmax
+                // over the quad of lanes sharing a row (an all -inf row gives NaN,
+                // as the reference)
+                const float *bh = bias + (g * H + h) * N * NS;
+                float zr[2][2];
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int row = 16 * m + tq + 8 * i;
+                        const bool rv = row < nq;
+                        const uint32_t wr = rv ? um_s[32 * g + row] : 0xffffffffu;
+                        float mx = -INFINITY;
+#pragma unroll
+                        for (int t = 0; t < 3; ++t)
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int key = 8 * t + 2 * tr + e;
+                                const bool live = key < nq && ((wr >> key) & 1u);
+                                const float bv = live ? (rv ? bh[key * NS + row] : 0.f) : -INFINITY;
+                                const float sv2 = sacc[m][t][2 * i + e] + bv;
+                                sacc[m][t][2 * i + e] = sv2;
+                                mx = fmaxf(mx, sv2);
+                            }
+                        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+                        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+                        float z = 0.f;
+#pragma unroll
+                        for (int t = 0; t < 3; ++t)
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const float pe = ex2(sacc[m][t][2 * i + e] - mx);
+                                sacc[m][t][2 * i + e] = pe;
+                                z += pe;
+                            }
+                        z += __shfl_xor_sync(kFull, z, 1);
+                        z += __shfl_xor_sync(kFull, z, 2);
+                        zr[m][i] = z;
+                    }
+                // context = P V, k over the keys in 3 steps of 8, taken in the
+                // order 0 2 4 6 1 3 5 7 within a step: then P's accumulator
+                // fragment is its A fragment as it stands, and V's fragment
+                // follows the same order
+                float cacc[2][3][4];
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+#pragma unroll
+                    for (int t = 0; t < 3; ++t)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) cacc[m][t][e] = 0.f;
+#pragma unroll
+                for (int st = 0; st < 3; ++st) {
+                    uint32_t ab[2][4], as[2][4];
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        split_tf32(sacc[m][st][0], ab[m][0], as[m][0]);
+                        split_tf32(sacc[m][st][2], ab[m][1], as[m][1]);
+                        split_tf32(sacc[m][st][1], ab[m][2], as[m][2]);
+                        split_tf32(sacc[m][st][3], ab[m][3], as[m][3]);
+                    }
+                    const int k0 = 8 * st + 2 * tr, k1 = k0 + 1;
+#pragma unroll
+                    for (int t = 0; t < DH / 8; ++t) {
+                        const int dim = 8 * t + tq;
+                        uint32_t bb[2], bs[2];
+                        split_tf32(k0 < nq ? sv[k0 * DH + dim] : 0.f, bb[0], bs[0]);
+                        split_tf32(k1 < nq ? sv[k1 * DH + dim] : 0.f, bb[1], bs[1]);
+#pragma unroll
+                        for (int m = 0; m < 2; ++m) {
+                            mma_tf32(cacc[m][t], as[m], bb);
+                            mma_tf32(cacc[m][t], ab[m], bs);
+                            mma_tf32(cacc[m][t], ab[m], bb);
+                        }
+                    }
+                }
+                // normalised rows back to one row per lane through the first slot
+                __syncwarp();  // (every lane read its last Q / K slices before the softmax)
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int row = 16 * m + tq + 8 * i;
+                        if (row < nq) {
+                            const float inv = 1.0f / zr[m][i];
+#pragma unroll
+                            for (int t = 0; t < DH / 8; ++t)
+                                *reinterpret_cast<float2 *>(s1 + row * DH + 8 * t + 2 * tr) =
+                                    make_float2(cacc[m][t][2 * i] * inv, cacc[m][t][2 * i + 1] * inv);
+                        }
+                    }
                 __syncwarp();
-                // the score of (n, j) replaces its bias entry, which only this
-                // lane reads: the two softmax passes keep no score registers
-                float *brow = bias + (g * H + h) * N * NS + n;
-                const uint32_t unm = rvalid ? um_s[32 * g + n] : 0u;  // this query's unmasked keys
-                float m = -INFINITY;
-                const int nj = rvalid ? N : 0;  // lanes past the graph's nodes touch nothing
-#pragma unroll 2
-                for (int j = 0; j < nj; ++j) {
-                    float2 a = make_float2(0.f, 0.f), bb = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int c = 0; c < DH / 4; ++c) {
-                        const float4 k4 = *reinterpret_cast<const float4 *>(sk + j * DH + 4 * c);
-                        a = ffma2(q2[2 * c], make_float2(k4.x, k4.y), a);
-                        bb = ffma2(q2[2 * c + 1], make_float2(k4.z, k4.w), bb);
-                    }
-                    const float s = (unm >> j) & 1u ? ((a.x + a.y) + (bb.x + bb.y)) + brow[j * NS]
-                                                    : -INFINITY;
-                    brow[j * NS] = s;
-                    m = fmaxf(m, s);
-                }
-#pragma unroll
-                for (int c = 0; c < DH / 2; ++c) ctx[c] = make_float2(0.f, 0.f);
-                float z = 0.f;
-#pragma unroll 2
-                for (int j = 0; j < nj; ++j) {
-                    const float e = ex2(brow[j * NS] - m);  // all -inf row: NaN, as the reference
-                    z += e;
-                    const float2 ee = make_float2(e, e);
-#pragma unroll
-                    for (int c = 0; c < DH / 4; ++c) {
-                        const float4 v4 = *reinterpret_cast<const float4 *>(sv + j * DH + 4 * c);
-                        ctx[2 * c] = ffma2(ee, make_float2(v4.x, v4.y), ctx[2 * c]);
-                        ctx[2 * c + 1] = ffma2(ee, make_float2(v4.z, v4.w), ctx[2 * c + 1]);
-                    }
-                }
-                const float inv_z = rvalid ? 1.0f / z : 0.f;
 #pragma unroll
                 for (int c = 0; c < DH / 2; ++c)
-                    ctx[c] = rvalid ? make_float2(ctx[c].x * inv_z, ctx[c].y * inv_z)
+                    ctx[c] = rvalid ? *reinterpret_cast<const float2 *>(s1 + n * DH + 2 * c)
                                     : make_float2(0.f, 0.f);
             }
             named_sync(1, kComputeThreads);  // every graph's largest |V| known; staging free
