@@ -381,13 +381,16 @@ struct Smem {
         return b > lnred_bytes ? b : lnred_bytes;
     }
     __host__ __device__ static uint32_t stage(int N) { return bias + bias_bytes(N); }
-    // K / V staging of the attention, or (outside it) one prefetch slot of
-    // 16 features per compute thread and the next tile's mask values
-    __host__ __device__ static uint32_t stage_bytes(int N) {
-        const uint32_t kv = kComputeWarps * 2 * N * DH * 4,
-                       mlp = kComputeThreads * P * 4 + kGraphs * N * N * 4;
-        return kv > mlp ? kv : mlp;
+    // the attention's staging (per warp: 8-dim Q and K slices, then V rows,
+    // which the context replaces), or outside it one prefetch slot of 16
+    // features per compute thread; above both (float offset mask_off), the
+    // next tile's mask values, copied in during the attention
+    __host__ __device__ static uint32_t warp_stage(int N) { return 16 * N + N * DH; }
+    __host__ __device__ static uint32_t mask_off(int N) {
+        const uint32_t att = kComputeWarps * warp_stage(N), mlp = kComputeThreads * P;
+        return att > mlp ? att : mlp;
     }
+    __host__ __device__ static uint32_t stage_bytes(int N) { return (mask_off(N) + kGraphs * N * N) * 4; }
     __host__ __device__ static uint32_t nodes(int N) { return stage(N) + stage_bytes(N); }
     __host__ __device__ static uint32_t nodes_bytes(int N) { return kGraphs * N * kNodeStride * 4; }
     // W1 image (fp16 hi | lo, the MMA's B operand), b1, W2 transposed [u][h], b2,
@@ -479,11 +482,7 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
             }
             {
             const int pos = issued % kChunks, c = chunk_of(pos), s = issued % kRing;
-            if (!x_ok) {
-                x_ok = mbar_test(&br.xfull, (uint32_t)t & 1u);
-                // LayerNorm(t) has read the staged rows: the next tile's go there
-                if (x_ok && t + 1 < n_my) load_nodes(blockIdx.x + (t + 1) * gridDim.x);
-            }
+            if (!x_ok) x_ok = mbar_test(&br.xfull, (uint32_t)t & 1u);
             if (!e_ok) e_ok = mbar_test(&br.edone, (uint32_t)(t - 1) & 1u);
             if (c == kChunks - 1 && !c_ok) c_ok = mbar_test(&br.cfull, (uint32_t)t & 1u);
             const bool ready = c == kChunks - 1 ? c_ok : (c == 0 ? x_ok && e_ok : x_ok);
@@ -502,7 +501,12 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
                     mma_ts(d, al, dh, idesc, 1);
                 }
                 mma_commit(&br.wdone[s]);
-                if (c == 0) mma_commit(&br.qkv);  // Q, the last of the three
+                if (c == 0) {
+                    mma_commit(&br.qkv);  // Q, the last of the three
+                    // LayerNorm(t) has read the staged rows: the next tile's go
+                    // there, queued behind Q's weights (needed first)
+                    if (t + 1 < n_my) load_nodes(blockIdx.x + (t + 1) * gridDim.x);
+                }
                 if (c == kChunks - 1) mma_commit(&br.ofull);
                 ++issued;
                 progress = true;
@@ -695,11 +699,11 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         // the unmasked pairs of a tile are numbered in (graph, query, key)
         // order and taken in 128-pair blocks.
         // mask_copy(tl): tile tl's mask values into the staging region above
-        // the prefetch slots (cp.async, issued while the staging region is
-        // free and long before use); mask_words(tl): the unmasked-key words
+        // the prefetch slots and the attention's staging (cp.async, issued
+        // during the previous tile's attention); mask_words(tl): the unmasked-key words
         // (four threads per (graph, row)); mask_prefix(): their row prefix
         // (warp 0, then a barrier)
-        float *mask_s = stage_base + kComputeThreads * P;
+        float *mask_s = stage_base + Smem::mask_off(N);
         auto mask_copy = [&](int tl) {
             const int64_t g0 = (int64_t)tl * kGraphs;
             const int np = (int)((p.B - g0 < kGraphs ? p.B - g0 : kGraphs) * NN);
@@ -901,17 +905,18 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             mbar_wait(&br.qkv, ph_qkv, err);
             ph_qkv ^= 1u;
             fence_after();
+            // the next tile's mask values (its LayerNorm reads them)
+            if (it + 1 < n_my) mask_copy(tile + gridDim.x);
 
             // ======== phase B: attention of head h in graph g, thread = query node n
             const int sr = rscale[32 * g + n];
             float2 ctx[DH / 2];
             {
-                // The warp's two staging slots: V rows in the second; the first
-                // holds 8-dim slices of the Q and K rows for one k-step of the
-                // scores at a time, then the normalised context.
-                float *s1 = stage_base + warp * 2 * N * DH;
-                float *sv = s1 + N * DH;
-                float *sq8 = s1, *sk8 = s1 + N * 8;
+                // The warp's staging: 8-dim slices of the Q and K rows for one
+                // k-step of the scores at a time, then the V rows, which the
+                // normalised context replaces.
+                float *sq8 = stage_base + warp * Smem::warp_stage(N), *sk8 = sq8 + N * 8;
+                float *sv = sq8 + 16 * N;
                 const float uq = exp2i(-sr) * exp2i(-sw_s[0]) * qk_scale,
                             uk = exp2i(-sr) * exp2i(-sw_s[1]), uv = exp2i(-sr) * exp2i(-sw_s[2]);
                 const int nq = b < p.B ? N : 0;  // the graph's rows (queries) and keys
@@ -1063,8 +1068,8 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                         }
                     }
                 }
-                // normalised rows back to one row per lane through the first slot
-                __syncwarp();  // (every lane read its last Q / K slices before the softmax)
+                // normalised rows back to one row per lane through V's rows
+                __syncwarp();  // every lane is done reading V
 #pragma unroll
                 for (int m = 0; m < 2; ++m)
 #pragma unroll
@@ -1074,18 +1079,17 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                             const float inv = 1.0f / zr[m][i];
 #pragma unroll
                             for (int t = 0; t < DH / 8; ++t)
-                                *reinterpret_cast<float2 *>(s1 + row * DH + 8 * t + 2 * tr) =
+                                *reinterpret_cast<float2 *>(sv + row * DH + 8 * t + 2 * tr) =
                                     make_float2(cacc[m][t][2 * i] * inv, cacc[m][t][2 * i + 1] * inv);
                         }
                     }
                 __syncwarp();
 #pragma unroll
                 for (int c = 0; c < DH / 2; ++c)
-                    ctx[c] = rvalid ? *reinterpret_cast<const float2 *>(s1 + n * DH + 2 * c)
+                    ctx[c] = rvalid ? *reinterpret_cast<const float2 *>(sv + n * DH + 2 * c)
                                     : make_float2(0.f, 0.f);
             }
             named_sync(1, kComputeThreads);  // every graph's largest |V| known; staging free
-            if (it + 1 < n_my) mask_copy(tile + gridDim.x);  // read after the next LayerNorm
             // the context (|ctx| <= max |V| of the graph) as the out-projection's A operand
             const int sc_g = scale_exp(__int_as_float(vmax_s[g]));
             {
