@@ -79,6 +79,11 @@ constexpr uint32_t kW1Half = P * P * 2;           // W1 image, one of hi / lo
 // staged node rows: stride 100 floats, so the 16-byte loads of 8 lanes
 // (8 consecutive rows) fall in 8 distinct bank quads (one bulk copy per row)
 constexpr int kNodeStride = D + 4;
+// staged output rows: the same stride (8 consecutive rows' 16-byte stores in
+// 8 distinct bank quads)
+constexpr int kOutStride = D + 4;
+// residual / output float4s per thread of a graph's 128 (warps g, g + 4, ...)
+constexpr int kOutVec = (kMaxN * D / 4 + 127) / 128;
 // TMEM columns (32-bit): fp32 accumulators, or fp16 pairs for A operands
 // A operands (x_n, then the context) at column 288 (even tiles) or 384 (odd)
 // (hi: kAHalf columns of fp16 pairs for the D inputs, then lo)
@@ -384,13 +389,20 @@ struct Smem {
     // the attention's staging (per warp: 8-dim Q and K slices, then V rows,
     // which the context replaces), or outside it one prefetch slot of 16
     // features per compute thread; above both (float offset mask_off), the
-    // next tile's mask values, copied in during the attention
+    // next tile's mask values, copied in during the attention. The epilogue's
+    // output rows [graph][node][kOutStride] sit above the prefetch slots
+    // (float offset out_off), over the attention's staging and the mask
+    // values, both idle then.
     __host__ __device__ static uint32_t warp_stage(int N) { return 16 * N + N * DH; }
     __host__ __device__ static uint32_t mask_off(int N) {
         const uint32_t att = kComputeWarps * warp_stage(N), mlp = kComputeThreads * P;
         return att > mlp ? att : mlp;
     }
-    __host__ __device__ static uint32_t stage_bytes(int N) { return (mask_off(N) + kGraphs * N * N) * 4; }
+    static constexpr uint32_t out_off = kComputeThreads * P;
+    __host__ __device__ static uint32_t stage_bytes(int N) {
+        const uint32_t a = mask_off(N) + kGraphs * N * N, o = out_off + kGraphs * N * kOutStride;
+        return (a > o ? a : o) * 4;
+    }
     __host__ __device__ static uint32_t nodes(int N) { return stage(N) + stage_bytes(N); }
     __host__ __device__ static uint32_t nodes_bytes(int N) { return kGraphs * N * kNodeStride * 4; }
     // W1 image (fp16 hi | lo, the MMA's B operand), b1, W2 transposed [u][h], b2,
@@ -1107,47 +1119,65 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             mbar_arrive(&br.cfull);
 
             // ======== phase C: LayerNorm of the next tile, then out-projection + residual
-            const float *x = p.nodes + (b * N + n) * (int64_t)D + h * DH;
-            float4 xres[DH / 4];
-#pragma unroll
-            for (int c = 0; c < DH / 4; ++c)
-                xres[c] = rvalid ? __ldg(reinterpret_cast<const float4 *>(x) + c)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
             if (it + 1 < n_my) {
                 mbar_wait(&br.nfull, (uint32_t)(it + 1) & 1u, err);  // the next tile's node rows
                 // with the next tile's unmasked-pair words (this tile's attention
-                // has read the words), then their prefix and its first
-                // relation-MLP block
+                // has read the words)
                 layer_norm(p, nodes_s, red, rscale, gam, bet, tmem, col_a(it + 1),
                            tile + gridDim.x, warp, lane, [&] { mask_words(tile + gridDim.x); });
                 mbar_arrive(&br.xfull);
+            }
+            // The epilogue works per graph: its output block ([N][D], contiguous
+            // in global memory) is staged in shared memory by the four head
+            // warps of graph g, then written with its residual as consecutive
+            // float4s by the same 128 threads (float4 gt + 128 k). The residual
+            // and the error flag are loaded now, while the next tile's pair
+            // prefix and first relation-MLP block are set up.
+            const int gt = 32 * h + lane, nf4 = N * D / 4;
+            const bool gvalid = b < p.B;
+            const float4 *xg = reinterpret_cast<const float4 *>(p.nodes + b * N * (int64_t)D);
+            float4 xres[kOutVec];
+#pragma unroll
+            for (int k = 0; k < kOutVec; ++k)
+                xres[k] = gvalid && gt + 128 * k < nf4 ? __ldg(xg + gt + 128 * k)
+                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+            const bool failed = flag_set(err);
+            if (it + 1 < n_my) {
                 mask_prefix();
                 if (128 * quad < rpre_s[128]) fetch_pairs(tile + gridDim.x, quad);
             }
-            mbar_wait(&br.ofull, ph_of, err);
+            const bool o_ok = mbar_wait(&br.ofull, ph_of, err);
             ph_of ^= 1u;
             fence_after();
             {
-                const float fail = flag_set(err) ? NAN : 0.f;
                 const float uo = exp2i(-sc_g) * exp2i(-sw_s[3]);
-                float *o = p.out + (b * N + n) * (int64_t)D + h * DH;
+                float *os = stage_base + Smem::out_off + g * N * kOutStride;
 #pragma unroll
                 for (int c0 = 0; c0 < DH; c0 += 8) {
                     float v[8];
                     tmem_ld8(tmem + lane_q + (uint32_t)(h * DH + c0), v);
-                    if (rvalid) {
-                        const float4 x0 = xres[c0 / 4], x1 = xres[c0 / 4 + 1];
-                        reinterpret_cast<float4 *>(o + c0)[0] =
-                            make_float4(fmaf(v[0], uo, x0.x) + fail, fmaf(v[1], uo, x0.y) + fail,
-                                        fmaf(v[2], uo, x0.z) + fail, fmaf(v[3], uo, x0.w) + fail);
-                        reinterpret_cast<float4 *>(o + c0)[1] =
-                            make_float4(fmaf(v[4], uo, x1.x) + fail, fmaf(v[5], uo, x1.y) + fail,
-                                        fmaf(v[6], uo, x1.z) + fail, fmaf(v[7], uo, x1.w) + fail);
+                    if (n < N) {
+                        float4 *w = reinterpret_cast<float4 *>(os + n * kOutStride + h * DH + c0);
+                        w[0] = make_float4(v[0] * uo, v[1] * uo, v[2] * uo, v[3] * uo);
+                        w[1] = make_float4(v[4] * uo, v[5] * uo, v[6] * uo, v[7] * uo);
+                    }
+                }
+                fence_before();
+                mbar_arrive(&br.edone);  // this thread no longer reads columns [0, 288)
+                named_sync(6 + g, 128);  // graph g's output block staged
+                const float fail = failed || !o_ok ? NAN : 0.f;
+                float4 *og = reinterpret_cast<float4 *>(p.out + b * N * (int64_t)D);
+#pragma unroll
+                for (int k = 0; k < kOutVec; ++k) {
+                    const int f = gt + 128 * k;
+                    if (gvalid && f < nf4) {
+                        const int row = f / (D / 4), c4 = f - row * (D / 4);
+                        const float4 v = *reinterpret_cast<const float4 *>(os + row * kOutStride + 4 * c4);
+                        og[f] = make_float4(v.x + xres[k].x + fail, v.y + xres[k].y + fail,
+                                            v.z + xres[k].z + fail, v.w + xres[k].w + fail);
                     }
                 }
             }
-            fence_before();
-            mbar_arrive(&br.edone);  // this thread no longer reads columns [0, 288)
         }
     }
     fence_before();
