@@ -554,14 +554,14 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
 // w / 4) takes columns [24k, 24k + 24) of graph g's rows (thread = row), the
 // row statistics are summed over the four column quarters through `red`.
 // Writes the row scale exponents and returns after this thread's TMEM stores
-// are complete and fenced. Its first barrier also covers this thread's
-// cp.async copies (the tile's mask values), and `mid` runs between its two
-// barriers (whatever it writes is visible to all compute threads on return).
-template <typename Mid>
+// are complete and fenced. `mid` runs between its two barriers (whatever it
+// writes is visible to all compute threads after the second), `late` after
+// the second.
+template <typename Mid, typename Late>
 __device__ __forceinline__ void layer_norm(const Params &p, const float *nodes_s, float *red,
                                            int32_t *rscale, const float *gam, const float *bet,
                                            uint32_t tmem, uint32_t acol, int tile, int warp,
-                                           int lane, Mid &&mid) {
+                                           int lane, Mid &&mid, Late &&late) {
     const int g = warp & 3, k = warp >> 2, n = lane, N = p.N;
     const bool valid = (int64_t)tile * kGraphs + g < p.B && n < N;
     const int row = 32 * g + n;
@@ -574,7 +574,6 @@ __device__ __forceinline__ void layer_norm(const Params &p, const float *nodes_s
 #pragma unroll
     for (int c = 0; c < 6; ++c) s1 += (x[c].x + x[c].y) + (x[c].z + x[c].w);
     red[k * 128 + row] = s1;
-    asm volatile("cp.async.wait_all;" ::: "memory");
     named_sync(1, kComputeThreads);
     mid();
     const float mean = ((red[row] + red[128 + row]) + (red[256 + row] + red[384 + row])) / (float)D;
@@ -591,6 +590,7 @@ __device__ __forceinline__ void layer_norm(const Params &p, const float *nodes_s
     red[512 + k * 128 + row] = v2;
     red[1024 + k * 128 + row] = dm;
     named_sync(1, kComputeThreads);
+    late();
     const float var = ((red[512 + row] + red[640 + row]) + (red[768 + row] + red[896 + row])) / (float)D;
     const float dmax = fmaxf(fmaxf(red[1024 + row], red[1152 + row]), fmaxf(red[1280 + row], red[1408 + row]));
     const float rstd = 1.0f / sqrtf(var + p.ln_eps);
@@ -712,9 +712,10 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         // order and taken in 128-pair blocks.
         // mask_copy(tl): tile tl's mask values into the staging region above
         // the prefetch slots and the attention's staging (cp.async, issued
-        // during the previous tile's attention); mask_words(tl): the unmasked-key words
-        // (four threads per (graph, row)); mask_prefix(): their row prefix
-        // (warp 0, then a barrier)
+        // during the previous tile's attention); mask_words(tl), once the
+        // copies are complete and visible: the unmasked-key words (four
+        // threads per (graph, row)); mask_scan(): their row prefix (warp 0;
+        // visible after the next barrier)
         float *mask_s = stage_base + Smem::mask_off(N);
         auto mask_copy = [&](int tl) {
             const int64_t g0 = (int64_t)tl * kGraphs;
@@ -725,8 +726,6 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                              : "memory");
             asm volatile("cp.async.commit_group;" ::: "memory");
         };
-        // (the words are built between the LayerNorm's two barriers: its first
-        // makes the mask copies visible, its second the words)
         auto mask_words = [&](int tl) {
             {
                 // word r = tid / 4 (graph r / 32, row r % 32), keys
@@ -746,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 if (part == 0) um_s[r] = w;
             }
         };
-        auto mask_prefix = [&]() {
+        auto mask_scan = [&]() {
             if (warp == 0) {
                 int cr[4], sum = 0;
 #pragma unroll
@@ -768,7 +767,6 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 }
                 if (lane == 31) rpre_s[128] = incl;
             }
-            named_sync(1, kComputeThreads);
         };
         // the idx-th unmasked pair of the tile (idx < its count): the row by a
         // binary search of the prefix, the key as that row's k-th unmasked bit
@@ -780,30 +778,48 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             const int j = (int)__fns(um_s[r], 0, idx - rpre_s[r] + 1);
             return (r >> 5) * NN + (r & 31) * N + j;
         };
-        // this thread's relation-MLP prefetch slot: 16 features, quarter c at
-        // float4 index c * 512 + tid (a warp's 16-byte accesses consecutive)
-        const float4 *pslot = reinterpret_cast<const float4 *>(stage_base) + tid;
+        // relation-MLP prefetch slots: thread T's 16 features at float4
+        // 4 T + (c ^ (T / 2 % 4)) for quarter c (the swizzle keeps a warp's
+        // reads of one quarter and its copies of eight whole pairs free of
+        // bank conflicts)
+        float4 *slots = reinterpret_cast<float4 *>(stage_base);
+        const int swz = (tid >> 1) & 3;
+        const float4 *pslot = slots + 4 * tid;
+        // block blk of tile tl (warp-uniform call): the warp copies its own 32
+        // pairs, four lanes per pair (lane % 4 = the quarter), eight pairs per
+        // copy instruction, so that consecutive pairs give 512 consecutive bytes
         auto fetch_pairs = [&](int tl, int blk) {
             const int idx = 128 * blk + 32 * g + lane;
-            if (idx < rpre_s[128]) {
-                const int64_t pg = (int64_t)tl * kGraphs * NN + pair_of(idx);
+            const int pi = idx < rpre_s[128] ? pair_of(idx) : -1;
+            const float *src = p.pair + (int64_t)tl * kGraphs * NN * P + 4 * (lane & 3);
+            __syncwarp();  // every lane has read its slot (block blk - 4)
 #pragma unroll
-                for (int c = 0; c < P / 4; ++c)
-                    cp_async16(smem_u32(pslot + c * kComputeThreads), p.pair + pg * P + 4 * c);
+            for (int j = 0; j < 4; ++j) {
+                const int sl = 8 * j + (lane >> 2);
+                const int pj = __shfl_sync(kFull, pi, sl);
+                const int dt = 32 * warp + sl;
+                if (pj >= 0)
+                    cp_async16(smem_u32(slots + 4 * dt + ((lane & 3) ^ ((dt >> 1) & 3))),
+                               src + (int64_t)pj * P);
             }
             asm volatile("cp.async.commit_group;" ::: "memory");
         };
 
-        // prologue: LayerNorm of the first tile with its unmasked-pair words;
-        // its relation-MLP prefetch
+        // prologue: the first tile's unmasked-pair words, its LayerNorm with
+        // their prefix and its first relation-MLP blocks' prefetch
+        auto first_fetch = [&](int tl) {
+            if (128 * quad < rpre_s[128]) fetch_pairs(tl, quad);
+        };
         if (n_my > 0) {
             mask_copy(blockIdx.x);
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            named_sync(1, kComputeThreads);
+            mask_words(blockIdx.x);
             mbar_wait(&br.nfull, 0, err);  // the first tile's node rows
             layer_norm(p, nodes_s, red, rscale, gam, bet, tmem, col_a(0), blockIdx.x, warp, lane,
-                       [&] { mask_words(blockIdx.x); });
+                       mask_scan, [&] { first_fetch(blockIdx.x); });
             mbar_arrive(&br.xfull);
-            mask_prefix();  // also: LayerNorm statistics read, the bias region is free
-            if (128 * quad < rpre_s[128]) fetch_pairs(blockIdx.x, quad);
+            named_sync(1, kComputeThreads);  // LayerNorm statistics read, the bias region is free
         }
         uint32_t ph_ed = 0, ph_df = 0;
 
@@ -829,10 +845,11 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             auto split_issue = [&](int blk, int &sp) {
                 const bool valid = 128 * blk + 32 * g + lane < npairs;
                 asm volatile("cp.async.wait_all;" ::: "memory");
+                __syncwarp();  // the slots are filled by other lanes' copies
                 float pf[P];
 #pragma unroll
                 for (int c = 0; c < P / 4; ++c) {
-                    const float4 v = valid ? pslot[c * kComputeThreads] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 v = valid ? pslot[c ^ swz] : make_float4(0.f, 0.f, 0.f, 0.f);
                     pf[4 * c] = v.x;
                     pf[4 * c + 1] = v.y;
                     pf[4 * c + 2] = v.z;
@@ -1101,7 +1118,10 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                     ctx[c] = rvalid ? *reinterpret_cast<const float2 *>(sv + n * DH + 2 * c)
                                     : make_float2(0.f, 0.f);
             }
+            asm volatile("cp.async.wait_all;" ::: "memory");  // the next tile's mask values
             named_sync(1, kComputeThreads);  // every graph's largest |V| known; staging free
+            // the next tile's unmasked-pair words (this tile's are read)
+            if (it + 1 < n_my) mask_words(tile + gridDim.x);
             // the context (|ctx| <= max |V| of the graph) as the out-projection's A operand
             const int sc_g = scale_exp(__int_as_float(vmax_s[g]));
             {
@@ -1121,18 +1141,17 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             // ======== phase C: LayerNorm of the next tile, then out-projection + residual
             if (it + 1 < n_my) {
                 mbar_wait(&br.nfull, (uint32_t)(it + 1) & 1u, err);  // the next tile's node rows
-                // with the next tile's unmasked-pair words (this tile's attention
-                // has read the words)
+                // with the prefix of the next tile's unmasked-pair words, and the
+                // prefetch of its first relation-MLP blocks
                 layer_norm(p, nodes_s, red, rscale, gam, bet, tmem, col_a(it + 1),
-                           tile + gridDim.x, warp, lane, [&] { mask_words(tile + gridDim.x); });
+                           tile + gridDim.x, warp, lane, mask_scan,
+                           [&] { first_fetch(tile + gridDim.x); });
                 mbar_arrive(&br.xfull);
             }
             // The epilogue works per graph: its output block ([N][D], contiguous
             // in global memory) is staged in shared memory by the four head
             // warps of graph g, then written with its residual as consecutive
-            // float4s by the same 128 threads (float4 gt + 128 k). The residual
-            // and the error flag are loaded now, while the next tile's pair
-            // prefix and first relation-MLP block are set up.
+            // float4s by the same 128 threads (float4 gt + 128 k).
             const int gt = 32 * h + lane, nf4 = N * D / 4;
             const bool gvalid = b < p.B;
             const float4 *xg = reinterpret_cast<const float4 *>(p.nodes + b * N * (int64_t)D);
@@ -1142,10 +1161,6 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 xres[k] = gvalid && gt + 128 * k < nf4 ? __ldg(xg + gt + 128 * k)
                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
             const bool failed = flag_set(err);
-            if (it + 1 < n_my) {
-                mask_prefix();
-                if (128 * quad < rpre_s[128]) fetch_pairs(tile + gridDim.x, quad);
-            }
             const bool o_ok = mbar_wait(&br.ofull, ph_of, err);
             ph_of ^= 1u;
             fence_after();
