@@ -807,8 +807,33 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
 
         // prologue: the first tile's unmasked-pair words, its LayerNorm with
         // their prefix and its first relation-MLP blocks' prefetch
-        auto first_fetch = [&](int tl) {
-            if (128 * quad < rpre_s[128]) fetch_pairs(tl, quad);
+        auto first_fetch = [&](int tl) {  // (always one commit group)
+            if (128 * quad < rpre_s[128])
+                fetch_pairs(tl, quad);
+            else
+                asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        // The epilogue works per graph: its output block ([N][D], contiguous in
+        // global memory) is staged in shared memory, starting as the residual
+        // rows (copied in during the next tile's LayerNorm, one commit group);
+        // the four head warps of graph g add the out-projection there, then
+        // the same 128 threads write it as consecutive float4s (gt + 128 k).
+        const int gt = 32 * h + lane;
+        auto res_copy = [&](int tl) {
+            const int64_t bg = (int64_t)tl * kGraphs + g;
+            if (bg < p.B) {
+                const float4 *xg = reinterpret_cast<const float4 *>(p.nodes + bg * N * (int64_t)D);
+                float *os = stage_base + Smem::out_off + g * N * kOutStride;
+#pragma unroll
+                for (int k = 0; k < kOutVec; ++k) {
+                    const int f = gt + 128 * k;
+                    if (f < N * D / 4) {
+                        const int row = f / (D / 4), c4 = f - row * (D / 4);
+                        cp_async16(smem_u32(os + row * kOutStride + 4 * c4), xg + f);
+                    }
+                }
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
         };
         if (n_my > 0) {
             mask_copy(blockIdx.x);
@@ -1143,23 +1168,19 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 mbar_wait(&br.nfull, (uint32_t)(it + 1) & 1u, err);  // the next tile's node rows
                 // with the prefix of the next tile's unmasked-pair words, and the
                 // prefetch of its first relation-MLP blocks
+                // (the residual copies go in after its first barrier: every
+                // thread has read the mask values in the staging region then)
                 layer_norm(p, nodes_s, red, rscale, gam, bet, tmem, col_a(it + 1),
-                           tile + gridDim.x, warp, lane, mask_scan,
+                           tile + gridDim.x, warp, lane,
+                           [&] {
+                               mask_scan();
+                               res_copy(tile);
+                           },
                            [&] { first_fetch(tile + gridDim.x); });
                 mbar_arrive(&br.xfull);
+            } else {
+                res_copy(tile);
             }
-            // The epilogue works per graph: its output block ([N][D], contiguous
-            // in global memory) is staged in shared memory by the four head
-            // warps of graph g, then written with its residual as consecutive
-            // float4s by the same 128 threads (float4 gt + 128 k).
-            const int gt = 32 * h + lane, nf4 = N * D / 4;
-            const bool gvalid = b < p.B;
-            const float4 *xg = reinterpret_cast<const float4 *>(p.nodes + b * N * (int64_t)D);
-            float4 xres[kOutVec];
-#pragma unroll
-            for (int k = 0; k < kOutVec; ++k)
-                xres[k] = gvalid && gt + 128 * k < nf4 ? __ldg(xg + gt + 128 * k)
-                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
             const bool failed = flag_set(err);
             const bool o_ok = mbar_wait(&br.ofull, ph_of, err);
             ph_of ^= 1u;
@@ -1167,29 +1188,39 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             {
                 const float uo = exp2i(-sc_g) * exp2i(-sw_s[3]);
                 float *os = stage_base + Smem::out_off + g * N * kOutStride;
+                // this thread's residual copies (the prefetch's group may still
+                // be in flight), then the whole graph's
+                if (it + 1 < n_my)
+                    asm volatile("cp.async.wait_group 1;" ::: "memory");
+                else
+                    asm volatile("cp.async.wait_group 0;" ::: "memory");
+                named_sync(6 + g, 128);
 #pragma unroll
                 for (int c0 = 0; c0 < DH; c0 += 8) {
                     float v[8];
                     tmem_ld8(tmem + lane_q + (uint32_t)(h * DH + c0), v);
                     if (n < N) {
                         float4 *w = reinterpret_cast<float4 *>(os + n * kOutStride + h * DH + c0);
-                        w[0] = make_float4(v[0] * uo, v[1] * uo, v[2] * uo, v[3] * uo);
-                        w[1] = make_float4(v[4] * uo, v[5] * uo, v[6] * uo, v[7] * uo);
+                        const float4 x0 = w[0], x1 = w[1];
+                        w[0] = make_float4(fmaf(v[0], uo, x0.x), fmaf(v[1], uo, x0.y),
+                                           fmaf(v[2], uo, x0.z), fmaf(v[3], uo, x0.w));
+                        w[1] = make_float4(fmaf(v[4], uo, x1.x), fmaf(v[5], uo, x1.y),
+                                           fmaf(v[6], uo, x1.z), fmaf(v[7], uo, x1.w));
                     }
                 }
                 fence_before();
                 mbar_arrive(&br.edone);  // this thread no longer reads columns [0, 288)
-                named_sync(6 + g, 128);  // graph g's output block staged
+                named_sync(6 + g, 128);  // graph g's output block complete
                 const float fail = failed || !o_ok ? NAN : 0.f;
                 float4 *og = reinterpret_cast<float4 *>(p.out + b * N * (int64_t)D);
+                const int nf4 = N * D / 4;
 #pragma unroll
                 for (int k = 0; k < kOutVec; ++k) {
                     const int f = gt + 128 * k;
-                    if (gvalid && f < nf4) {
+                    if (b < p.B && f < nf4) {
                         const int row = f / (D / 4), c4 = f - row * (D / 4);
                         const float4 v = *reinterpret_cast<const float4 *>(os + row * kOutStride + 4 * c4);
-                        og[f] = make_float4(v.x + xres[k].x + fail, v.y + xres[k].y + fail,
-                                            v.z + xres[k].z + fail, v.w + xres[k].w + fail);
+                        og[f] = make_float4(v.x + fail, v.y + fail, v.z + fail, v.w + fail);
                     }
                 }
             }
