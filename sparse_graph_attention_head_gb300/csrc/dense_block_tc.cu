@@ -82,6 +82,10 @@ constexpr int kNodeStride = D + 4;
 // staged output rows: the same stride (8 consecutive rows' 16-byte stores in
 // 8 distinct bank quads)
 constexpr int kOutStride = D + 4;
+// row stride of the relation-MLP bias: at least N + 1 and 12 mod 16, so that
+// the attention's fragment reads (keys 2 apart in a quad of lanes, rows
+// consecutive) fall in distinct banks
+__host__ __device__ constexpr int bias_stride(int N) { return N + 1 + ((12 - (N + 1)) & 15); }
 // residual / output float4s per thread of a graph's 128 (warps g, g + 4, ...)
 constexpr int kOutVec = (kMaxN * D / 4 + 127) / 128;
 // TMEM columns (32-bit): fp32 accumulators, or fp16 pairs for A operands
@@ -377,12 +381,12 @@ struct Params {
 struct Smem {
     static constexpr uint32_t ring = 0;
     static constexpr uint32_t bias = ring + kRing * kChunkBytes;
-    // relation-MLP bias (and scores) [graph][head][j][node, padded to N + 1];
+    // relation-MLP bias (and scores) [graph][head][j][node, row stride bias_stride(N)];
     // between the attention and the next relation MLP it holds the LayerNorm
     // row statistics [sum | sum sq | max dev][4 column quarters][128 rows]
     static constexpr uint32_t lnred_bytes = 3 * 4 * 128 * 4;
     __host__ __device__ static uint32_t bias_bytes(int N) {
-        const uint32_t b = kGraphs * H * N * (N + 1) * 4;
+        const uint32_t b = kGraphs * H * N * bias_stride(N) * 4;
         return b > lnred_bytes ? b : lnred_bytes;
     }
     __host__ __device__ static uint32_t stage(int N) { return bias + bias_bytes(N); }
@@ -625,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
     __shared__ uint32_t tmem_slot;
     __shared__ int32_t sw_s[5];
     __shared__ int32_t vmax_s[kGraphs];
-    const int N = p.N, NN = N * N, NS = N + 1;
+    const int N = p.N, NN = N * N, NS = bias_stride(N);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const WsHeader *hd = reinterpret_cast<const WsHeader *>(p.ws);
     int32_t *err = const_cast<int32_t *>(&hd->err);
@@ -967,8 +971,10 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             float2 ctx[DH / 2];
             {
                 // The warp's staging: 8-dim slices of the Q and K rows for one
-                // k-step of the scores at a time, then the V rows, which the
-                // normalised context replaces.
+                // k-step of the scores at a time (rows with bit 2 set store their
+                // two halves swapped), then the V rows, which the normalised
+                // context replaces (row r rotated by 2 (r / 4 % 4) columns); the
+                // swizzles keep the fragment accesses free of bank conflicts.
                 float *sq8 = stage_base + warp * Smem::warp_stage(N), *sk8 = sq8 + N * 8;
                 float *sv = sq8 + 16 * N;
                 const float uq = exp2i(-sr) * exp2i(-sw_s[0]) * qk_scale,
@@ -1013,31 +1019,34 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                     tmem_ld8(tmem + lane_q + (uint32_t)(D + h * DH + 8 * st), kv);
                     __syncwarp();  // every lane is done with the previous slices
                     if (rvalid) {
-                        *reinterpret_cast<float4 *>(sq8 + n * 8) =
+                        const int s0 = n * 8 + (n & 4), s1 = n * 8 + ((n & 4) ^ 4);
+                        *reinterpret_cast<float4 *>(sq8 + s0) =
                             make_float4(qv[0] * uq, qv[1] * uq, qv[2] * uq, qv[3] * uq);
-                        *reinterpret_cast<float4 *>(sq8 + n * 8 + 4) =
+                        *reinterpret_cast<float4 *>(sq8 + s1) =
                             make_float4(qv[4] * uq, qv[5] * uq, qv[6] * uq, qv[7] * uq);
-                        *reinterpret_cast<float4 *>(sk8 + n * 8) =
+                        *reinterpret_cast<float4 *>(sk8 + s0) =
                             make_float4(kv[0] * uk, kv[1] * uk, kv[2] * uk, kv[3] * uk);
-                        *reinterpret_cast<float4 *>(sk8 + n * 8 + 4) =
+                        *reinterpret_cast<float4 *>(sk8 + s1) =
                             make_float4(kv[4] * uk, kv[5] * uk, kv[6] * uk, kv[7] * uk);
                     }
                     __syncwarp();
                     uint32_t ab[2][4], as[2][4];
+                    // (rows 16 m + tq, + 8 and keys 8 t + tq share bit 2 with tq)
+                    const int ka = tr ^ (tq & 4), kb = ka ^ 4;
 #pragma unroll
                     for (int m = 0; m < 2; ++m) {
                         const int r0 = 16 * m + tq, r1 = r0 + 8;
-                        split_tf32(r0 < nq ? sq8[r0 * 8 + tr] : 0.f, ab[m][0], as[m][0]);
-                        split_tf32(r1 < nq ? sq8[r1 * 8 + tr] : 0.f, ab[m][1], as[m][1]);
-                        split_tf32(r0 < nq ? sq8[r0 * 8 + tr + 4] : 0.f, ab[m][2], as[m][2]);
-                        split_tf32(r1 < nq ? sq8[r1 * 8 + tr + 4] : 0.f, ab[m][3], as[m][3]);
+                        split_tf32(r0 < nq ? sq8[r0 * 8 + ka] : 0.f, ab[m][0], as[m][0]);
+                        split_tf32(r1 < nq ? sq8[r1 * 8 + ka] : 0.f, ab[m][1], as[m][1]);
+                        split_tf32(r0 < nq ? sq8[r0 * 8 + kb] : 0.f, ab[m][2], as[m][2]);
+                        split_tf32(r1 < nq ? sq8[r1 * 8 + kb] : 0.f, ab[m][3], as[m][3]);
                     }
 #pragma unroll
                     for (int t = 0; t < 3; ++t) {
                         const int key = 8 * t + tq;
                         uint32_t bb[2], bs[2];
-                        split_tf32(key < nq ? sk8[key * 8 + tr] : 0.f, bb[0], bs[0]);
-                        split_tf32(key < nq ? sk8[key * 8 + tr + 4] : 0.f, bb[1], bs[1]);
+                        split_tf32(key < nq ? sk8[key * 8 + ka] : 0.f, bb[0], bs[0]);
+                        split_tf32(key < nq ? sk8[key * 8 + kb] : 0.f, bb[1], bs[1]);
 #pragma unroll
                         for (int m = 0; m < 2; ++m) {
                             mma_tf32(sacc[m][t], as[m], bb);
@@ -1131,17 +1140,25 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                         const int row = 16 * m + tq + 8 * i;
                         if (row < nq) {
                             const float inv = 1.0f / zr[m][i];
+                            const int rot = 2 * ((row >> 2) & 3);
 #pragma unroll
-                            for (int t = 0; t < DH / 8; ++t)
-                                *reinterpret_cast<float2 *>(sv + row * DH + 8 * t + 2 * tr) =
+                            for (int t = 0; t < DH / 8; ++t) {
+                                const int col = 8 * t + 2 * tr + rot;
+                                *reinterpret_cast<float2 *>(sv + row * DH + (col < DH ? col : col - DH)) =
                                     make_float2(cacc[m][t][2 * i] * inv, cacc[m][t][2 * i + 1] * inv);
+                            }
                         }
                     }
                 __syncwarp();
+                {
+                    const int rot = 2 * ((n >> 2) & 3);
 #pragma unroll
-                for (int c = 0; c < DH / 2; ++c)
-                    ctx[c] = rvalid ? *reinterpret_cast<const float2 *>(sv + n * DH + 2 * c)
-                                    : make_float2(0.f, 0.f);
+                    for (int c = 0; c < DH / 2; ++c) {
+                        const int col = 2 * c + rot;
+                        ctx[c] = rvalid ? *reinterpret_cast<const float2 *>(sv + n * DH + (col < DH ? col : col - DH))
+                                        : make_float2(0.f, 0.f);
+                    }
+                }
             }
             asm volatile("cp.async.wait_all;" ::: "memory");  // the next tile's mask values
             named_sync(1, kComputeThreads);  // every graph's largest |V| known; staging free
