@@ -789,12 +789,16 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         float4 *slots = reinterpret_cast<float4 *>(stage_base);
         const int swz = (tid >> 1) & 3;
         const float4 *pslot = slots + 4 * tid;
-        // block blk of tile tl (warp-uniform call): the warp copies its own 32
-        // pairs, four lanes per pair (lane % 4 = the quarter), eight pairs per
-        // copy instruction, so that consecutive pairs give 512 consecutive bytes
-        auto fetch_pairs = [&](int tl, int blk) {
+        // this thread's pair in block blk of the current words, or -1
+        auto pair_at = [&](int blk) -> int {
             const int idx = 128 * blk + 32 * g + lane;
-            const int pi = idx < rpre_s[128] ? pair_of(idx) : -1;
+            return idx < rpre_s[128] ? pair_of(idx) : -1;
+        };
+        // block blk of tile tl (warp-uniform call; pi = this thread's pair in
+        // it): the warp copies its own 32 pairs, four lanes per pair (lane % 4 =
+        // the quarter), eight pairs per copy instruction, so that consecutive
+        // pairs give 512 consecutive bytes
+        auto fetch_pairs = [&](int tl, int pi) {
             const float *src = p.pair + (int64_t)tl * kGraphs * NN * P + 4 * (lane & 3);
             __syncwarp();  // every lane has read its slot (block blk - 4)
 #pragma unroll
@@ -811,9 +815,14 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
 
         // prologue: the first tile's unmasked-pair words, its LayerNorm with
         // their prefix and its first relation-MLP blocks' prefetch
+        // (the pair of the quad's second block is found here too, beside the
+        // first's search, and kept for that block's prefetch)
+        int pi_second = -1;
         auto first_fetch = [&](int tl) {  // (always one commit group)
+            const int p0 = pair_at(quad);
+            pi_second = pair_at(quad + 4);
             if (128 * quad < rpre_s[128])
-                fetch_pairs(tl, quad);
+                fetch_pairs(tl, p0);
             else
                 asm volatile("cp.async.commit_group;" ::: "memory");
         };
@@ -884,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                     pf[4 * c + 2] = v.z;
                     pf[4 * c + 3] = v.w;
                 }
-                if (blk + 4 < nblk) fetch_pairs(tile, blk + 4);
+                if (blk + 4 < nblk) fetch_pairs(tile, blk == quad ? pi_second : pair_at(blk + 4));
                 float mx = 0.f;
 #pragma unroll
                 for (int u = 0; u < P; ++u) mx = fmaxf(mx, fabsf(pf[u]));
