@@ -423,16 +423,18 @@ struct Smem {
 };
 
 struct Barriers {
-    uint64_t wfull[kRing], wdone[kRing], dfull[4], nfull, xfull, edone, qkv, cfull, ofull, drain;
+    uint64_t wfull[kRing], wdone[kRing], dfull[4], nfull, xfull, edone, qk, vdone, cfull, ofull, drain;
 };
 
 // Control thread: weight ring and every MMA issue, driven by mbarriers.
-// Per tile the weight chunks stream as K, V, Q, O (workspace images 1, 2, 0,
-// 3): K and V (TMEM columns 96-287) go as soon as the tile's LayerNorm is in
-// TMEM, since the previous tile's attention - their only other reader - is
-// over by then; Q (columns 0-95) waits for the previous tile's epilogue to
-// read the out-projection there; O for the context.
-__host__ __device__ constexpr int chunk_of(int pos) { return pos == 0 ? 1 : pos == 1 ? 2 : pos == 2 ? 0 : 3; }
+// Per tile the weight chunks stream as K, Q, V, O (workspace images 1, 0, 2,
+// 3; ring slots 0, 1, 0, 1): K and V (TMEM columns 96-287) go as soon as the
+// tile's LayerNorm is in TMEM, since the previous tile's attention - their
+// only other reader - is over by then; Q (columns 0-95) waits for the
+// previous tile's epilogue to read the out-projection there, its weights
+// loaded long before into the slot the previous O freed; O for the context.
+// The scores wait for K and Q (one commit after Q), the context for V.
+__host__ __device__ constexpr int chunk_of(int pos) { return pos == 0 ? 1 : pos == 1 ? 0 : pos == 2 ? 2 : 3; }
 
 __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, uint32_t tmem,
                              int n_my, const float *nodes_s, int32_t *err) {
@@ -517,10 +519,11 @@ __device__ void control_loop(const Params &p, unsigned char *sm, Barriers &br, u
                     mma_ts(d, al, dh, idesc, 1);
                 }
                 mma_commit(&br.wdone[s]);
-                if (c == 0) {
-                    mma_commit(&br.qkv);  // Q, the last of the three
+                if (c == 0) mma_commit(&br.qk);  // Q, after K
+                if (c == 2) {
+                    mma_commit(&br.vdone);
                     // LayerNorm(t) has read the staged rows: the next tile's go
-                    // there, queued behind Q's weights (needed first)
+                    // there, queued behind the weights of this tile
                     if (t + 1 < n_my) load_nodes(blockIdx.x + (t + 1) * gridDim.x);
                 }
                 if (c == kChunks - 1) mma_commit(&br.ofull);
@@ -687,7 +690,8 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         mbar_init(&br.nfull, 1);
         mbar_init(&br.xfull, kComputeThreads);
         mbar_init(&br.edone, kComputeThreads);
-        mbar_init(&br.qkv, 1);
+        mbar_init(&br.qk, 1);
+        mbar_init(&br.vdone, 1);
         mbar_init(&br.cfull, kComputeThreads);
         mbar_init(&br.ofull, 1);
         mbar_init(&br.drain, 1);
@@ -708,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         const uint32_t lane_q = (uint32_t)(32 * g) << 16;
         const float qk_scale = kLog2e / sqrtf((float)DH);  // scores in log2 units
         const int quad = warp >> 2;                         // relation-MLP blocks quad, quad + 4, ...
-        uint32_t ph_qkv = 0, ph_of = 0;
+        uint32_t ph_qk = 0, ph_v = 0, ph_of = 0;
 
         // Relation-MLP pairs: only the unmasked ones. A masked pair's logit is
         // -inf whatever its relation MLP gives, so its features are never read;
@@ -969,8 +973,8 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 guard = false;
             }
             named_sync(1, kComputeThreads);  // every unmasked pair's bias written
-            mbar_wait(&br.qkv, ph_qkv, err);
-            ph_qkv ^= 1u;
+            mbar_wait(&br.qk, ph_qk, err);  // Q and K (V is waited for before its use)
+            ph_qk ^= 1u;
             fence_after();
             // the next tile's mask values (its LayerNorm reads them)
             if (it + 1 < n_my) mask_copy(tile + gridDim.x);
@@ -981,32 +985,14 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             {
                 // The warp's staging: 8-dim slices of the Q and K rows for one
                 // k-step of the scores at a time (rows with bit 2 set store their
-                // two halves swapped), then the V rows, which the normalised
-                // context replaces (row r rotated by 2 (r / 4 % 4) columns); the
+                // two halves swapped), and after the softmax the V rows, which
+                // the normalised context replaces (row r rotated by 2 (r / 4 % 4) columns); the
                 // swizzles keep the fragment accesses free of bank conflicts.
                 float *sq8 = stage_base + warp * Smem::warp_stage(N), *sk8 = sq8 + N * 8;
                 float *sv = sq8 + 16 * N;
                 const float uq = exp2i(-sr) * exp2i(-sw_s[0]) * qk_scale,
                             uk = exp2i(-sr) * exp2i(-sw_s[1]), uv = exp2i(-sr) * exp2i(-sw_s[2]);
                 const int nq = b < p.B ? N : 0;  // the graph's rows (queries) and keys
-                float vm = 0.f;
-#pragma unroll
-                for (int c0 = 0; c0 < DH; c0 += 8) {
-                    float vf[8];
-                    tmem_ld8(tmem + lane_q + (uint32_t)(2 * D + h * DH + c0), vf);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        vf[i] *= uv;
-                        vm = fmaxf(vm, fabsf(vf[i]));
-                    }
-                    if (rvalid) {
-                        *reinterpret_cast<float4 *>(sv + n * DH + c0) = make_float4(vf[0], vf[1], vf[2], vf[3]);
-                        *reinterpret_cast<float4 *>(sv + n * DH + c0 + 4) = make_float4(vf[4], vf[5], vf[6], vf[7]);
-                    }
-                }
-                vm = rvalid ? vm : 0.f;
-                vm = warp_max(vm);
-                if (lane == 0) atomicMax(&vmax_s[g], __float_as_int(vm));
                 // Warp-level tensor-core MMAs (m16n8k8, tf32 operands split into
                 // a rounded part and its remainder, three products per term as
                 // the projections' split does): 32 query rows (2 row tiles) x
@@ -1104,6 +1090,29 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                         z += __shfl_xor_sync(kFull, z, 2);
                         zr[m][i] = z;
                     }
+                // the V rows (scaled) into the warp's staging, and the graph's
+                // largest |V|
+                mbar_wait(&br.vdone, ph_v, err);
+                ph_v ^= 1u;
+                fence_after();
+                float vm = 0.f;
+#pragma unroll
+                for (int c0 = 0; c0 < DH; c0 += 8) {
+                    float vf[8];
+                    tmem_ld8(tmem + lane_q + (uint32_t)(2 * D + h * DH + c0), vf);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        vf[i] *= uv;
+                        vm = fmaxf(vm, fabsf(vf[i]));
+                    }
+                    if (rvalid) {
+                        *reinterpret_cast<float4 *>(sv + n * DH + c0) = make_float4(vf[0], vf[1], vf[2], vf[3]);
+                        *reinterpret_cast<float4 *>(sv + n * DH + c0 + 4) = make_float4(vf[4], vf[5], vf[6], vf[7]);
+                    }
+                }
+                vm = rvalid ? vm : 0.f;
+                vm = warp_max(vm);
+                if (lane == 0) atomicMax(&vmax_s[g], __float_as_int(vm));
                 // context = P V, k over the keys in 3 steps of 8, taken in the
                 // order 0 2 4 6 1 3 5 7 within a step: then P's accumulator
                 // fragment is its A fragment as it stands, and V's fragment
