@@ -820,13 +820,14 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
         // prologue: the first tile's unmasked-pair words, its LayerNorm with
         // their prefix and its first relation-MLP blocks' prefetch
         // (the pair of the quad's second block is found here too, beside the
-        // first's search, and kept for that block's prefetch)
-        int pi_second = -1;
+        // first's search; both are kept for the relation MLP: the second
+        // block's prefetch and the two blocks' bias writes)
+        int pi_first = -1, pi_second = -1;
         auto first_fetch = [&](int tl) {  // (always one commit group)
-            const int p0 = pair_at(quad);
+            pi_first = pair_at(quad);
             pi_second = pair_at(quad + 4);
             if (128 * quad < rpre_s[128])
-                fetch_pairs(tl, p0);
+                fetch_pairs(tl, pi_first);
             else
                 asm volatile("cp.async.commit_group;" ::: "memory");
         };
@@ -958,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                     guard = false;
                 }
                 if (valid) {
-                    const int pi = pair_of(idx);
+                    const int pi = blk == quad ? pi_first : (blk == quad + 4 ? pi_second : pair_of(idx));
                     const int gg = pi / NN, rem = pi - gg * NN, nn = rem / N, j = rem - nn * N;
                     float *bw = bias + (gg * H * N + j) * NS + nn;  // head stride N * NS
                     bw[0] = r01.x * kLog2e;
