@@ -317,6 +317,17 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+// d += A B for one warp: A 16 x 16 (row-major fragment), B 16 x 8
+// (column-major fragment), f16 operands (element pairs packed low first),
+// fp32 accumulators
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4],
+                                        const uint32_t (&b)[2]) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float r;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
@@ -1114,10 +1125,16 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 vm = rvalid ? vm : 0.f;
                 vm = warp_max(vm);
                 if (lane == 0) atomicMax(&vmax_s[g], __float_as_int(vm));
-                // context = P V, k over the keys in 3 steps of 8, taken in the
-                // order 0 2 4 6 1 3 5 7 within a step: then P's accumulator
-                // fragment is its A fragment as it stands, and V's fragment
-                // follows the same order
+                // context = P V on f16 MMAs (m16n8k16), each operand split into
+                // a rounded f16 part and its remainder as the projections' split
+                // does, three products per term; P scaled by 2^12 (P <= 1), V by
+                // this warp's 2^sv (its largest |V| to [2^12, 2^13)), both exact;
+                // k over the keys in 2 steps of 16 (the second half zero). P's
+                // accumulator fragment is its A fragment as it stands: keys
+                // 8 t + 2 tr, + 1 are registers (0, 1) of row tq and (2, 3) of
+                // row tq + 8.
+                const int sv_e = scale_exp(vm);
+                const float vsc = exp2i(sv_e), psc = 4096.f;
                 float cacc[2][3][4];
 #pragma unroll
                 for (int m = 0; m < 2; ++m)
@@ -1126,27 +1143,35 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) cacc[m][t][e] = 0.f;
 #pragma unroll
-                for (int st = 0; st < 3; ++st) {
-                    uint32_t ab[2][4], as[2][4];
+                for (int st = 0; st < 2; ++st) {
+                    uint32_t ah[2][4], al[2][4];
 #pragma unroll
                     for (int m = 0; m < 2; ++m) {
-                        split_tf32(sacc[m][st][0], ab[m][0], as[m][0]);
-                        split_tf32(sacc[m][st][2], ab[m][1], as[m][1]);
-                        split_tf32(sacc[m][st][1], ab[m][2], as[m][2]);
-                        split_tf32(sacc[m][st][3], ab[m][3], as[m][3]);
+                        split2(sacc[m][2 * st][0] * psc, sacc[m][2 * st][1] * psc, ah[m][0], al[m][0]);
+                        split2(sacc[m][2 * st][2] * psc, sacc[m][2 * st][3] * psc, ah[m][1], al[m][1]);
+                        if (st == 0) {
+                            split2(sacc[m][1][0] * psc, sacc[m][1][1] * psc, ah[m][2], al[m][2]);
+                            split2(sacc[m][1][2] * psc, sacc[m][1][3] * psc, ah[m][3], al[m][3]);
+                        } else {
+                            ah[m][2] = ah[m][3] = al[m][2] = al[m][3] = 0u;
+                        }
                     }
-                    const int k0 = 8 * st + 2 * tr, k1 = k0 + 1;
+                    const int k0 = 16 * st + 2 * tr;  // keys k0, k0 + 1, then k0 + 8, k0 + 9
 #pragma unroll
                     for (int t = 0; t < DH / 8; ++t) {
                         const int dim = 8 * t + tq;
-                        uint32_t bb[2], bs[2];
-                        split_tf32(k0 < nq ? sv[k0 * DH + dim] : 0.f, bb[0], bs[0]);
-                        split_tf32(k1 < nq ? sv[k1 * DH + dim] : 0.f, bb[1], bs[1]);
+                        const float v0 = k0 < nq ? sv[k0 * DH + dim] : 0.f;
+                        const float v1 = k0 + 1 < nq ? sv[(k0 + 1) * DH + dim] : 0.f;
+                        const float v2 = st == 0 && k0 + 8 < nq ? sv[(k0 + 8) * DH + dim] : 0.f;
+                        const float v3 = st == 0 && k0 + 9 < nq ? sv[(k0 + 9) * DH + dim] : 0.f;
+                        uint32_t bh[2], bl[2];
+                        split2(v0 * vsc, v1 * vsc, bh[0], bl[0]);
+                        split2(v2 * vsc, v3 * vsc, bh[1], bl[1]);
 #pragma unroll
                         for (int m = 0; m < 2; ++m) {
-                            mma_tf32(cacc[m][t], as[m], bb);
-                            mma_tf32(cacc[m][t], ab[m], bs);
-                            mma_tf32(cacc[m][t], ab[m], bb);
+                            mma_f16(cacc[m][t], al[m], bh);
+                            mma_f16(cacc[m][t], ah[m], bl);
+                            mma_f16(cacc[m][t], ah[m], bh);
                         }
                     }
                 }
@@ -1158,7 +1183,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                     for (int i = 0; i < 2; ++i) {
                         const int row = 16 * m + tq + 8 * i;
                         if (row < nq) {
-                            const float inv = 1.0f / zr[m][i];
+                            const float inv = exp2i(-12) * exp2i(-sv_e) * (1.0f / zr[m][i]);
                             const int rot = 2 * ((row >> 2) & 3);
 #pragma unroll
                             for (int t = 0; t < DH / 8; ++t) {
