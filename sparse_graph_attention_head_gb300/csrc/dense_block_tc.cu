@@ -251,6 +251,32 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 TMEM lanes x 8 columns (16x256b shape): thread t gets lane base + t / 4
+// at columns 2 (t % 4) and 2 (t % 4) + 1 (r[0], r[1]) and lane base + 8 + t / 4
+// at the same columns (r[2], r[3]); no wait (the tied waits below)
+__device__ __forceinline__ void tmem_ld16x8(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
+// the wait for this thread's TMEM loads, with the loads' registers tied to it
+// so that no use moves above it
+__device__ __forceinline__ void tmem_wait_tied(uint32_t *a, uint32_t *b) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(b[0]), "+r"(b[1]),
+                   "+r"(b[2]), "+r"(b[3])
+                 :
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_tied(uint32_t *a, uint32_t *b, uint32_t *c, uint32_t *d) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(b[0]), "+r"(b[1]),
+                   "+r"(b[2]), "+r"(b[3]), "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3]),
+                   "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+                 :
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
     uint32_t r[16];
     asm volatile(
@@ -297,24 +323,6 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     uint64_t r;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk2(a)), "l"(pk2(b)), "l"(pk2(c)));
     return up2(r);
-}
-
-// x as a tf32 part rounded to nearest (ties away) and its remainder, also
-// rounded: x = big + small up to ~2^-22 |x|
-__device__ __forceinline__ void split_tf32(float x, uint32_t &big, uint32_t &small) {
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(big) : "f"(x));
-    const float r = x - __uint_as_float(big);
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(small) : "f"(r));
-}
-
-// d += A B for one warp: A 16 x 8 (row-major fragment), B 8 x 8 (column-major
-// fragment), tf32 operands, fp32 accumulators
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
-                                         const uint32_t (&b)[2]) {
-    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
 // d += A B for one warp: A 16 x 16 (row-major fragment), B 16 x 8
@@ -401,14 +409,14 @@ struct Smem {
         return b > lnred_bytes ? b : lnred_bytes;
     }
     __host__ __device__ static uint32_t stage(int N) { return bias + bias_bytes(N); }
-    // the attention's staging (per warp: 8-dim Q and K slices, then V rows,
-    // which the context replaces), or outside it one prefetch slot of 16
+    // the attention's staging (per warp: the V rows, which the context
+    // replaces), or outside it one prefetch slot of 16
     // features per compute thread; above both (float offset mask_off), the
     // next tile's mask values, copied in during the attention. The epilogue's
     // output rows [graph][node][kOutStride] sit above the prefetch slots
     // (float offset out_off), over the attention's staging and the mask
     // values, both idle then.
-    __host__ __device__ static uint32_t warp_stage(int N) { return 16 * N + N * DH; }
+    __host__ __device__ static uint32_t warp_stage(int N) { return N * DH; }
     __host__ __device__ static uint32_t mask_off(int N) {
         const uint32_t att = kComputeWarps * warp_stage(N), mlp = kComputeThreads * P;
         return att > mlp ? att : mlp;
@@ -995,22 +1003,45 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             const int sr = rscale[32 * g + n];
             float2 ctx[DH / 2];
             {
-                // The warp's staging: 8-dim slices of the Q and K rows for one
-                // k-step of the scores at a time (rows with bit 2 set store their
-                // two halves swapped), and after the softmax the V rows, which
-                // the normalised context replaces (row r rotated by 2 (r / 4 % 4) columns); the
-                // swizzles keep the fragment accesses free of bank conflicts.
-                float *sq8 = stage_base + warp * Smem::warp_stage(N), *sk8 = sq8 + N * 8;
-                float *sv = sq8 + 16 * N;
-                const float uq = exp2i(-sr) * exp2i(-sw_s[0]) * qk_scale,
-                            uk = exp2i(-sr) * exp2i(-sw_s[1]), uv = exp2i(-sr) * exp2i(-sw_s[2]);
+                // The warp's staging: after the softmax the V rows, which the
+                // normalised context replaces (row r rotated by 2 (r / 4 % 4)
+                // columns, which keeps the context's accesses free of bank
+                // conflicts).
+                float *sv = stage_base + warp * Smem::warp_stage(N);
+                const float uv = exp2i(-sr) * exp2i(-sw_s[2]);
                 const int nq = b < p.B ? N : 0;  // the graph's rows (queries) and keys
-                // Warp-level tensor-core MMAs (m16n8k8, tf32 operands split into
-                // a rounded part and its remainder, three products per term as
-                // the projections' split does): 32 query rows (2 row tiles) x
-                // 24 keys (3 tiles of 8), then x 24 dims. Fragment coordinates:
-                // row group tq, column pair / k slot tr.
+                // Warp-level tensor-core MMAs (m16n8k16, f16 operands split into a
+                // rounded part and its remainder, three products per term as the
+                // projections' split does, each operand row scaled by a power of
+                // two into [2^12, 2^13) for the split): 32 query rows (2 row
+                // tiles) x 24 keys (3 tiles of 8), then x 24 dims. Fragment
+                // coordinates: row group tq, column pair tr.
                 const int tq = lane >> 2, tr = lane & 3;
+                // the row owner's ranges of its Q and K rows over the head's dims
+                int sq_n, sk_n;
+                {
+                    float mq = 0.f, mk = 0.f;
+#pragma unroll
+                    for (int c0 = 0; c0 < DH; c0 += 8) {
+                        float v[8];
+                        tmem_ld8(tmem + lane_q + (uint32_t)(h * DH + c0), v);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mq = fmaxf(mq, fabsf(v[i]));
+                        tmem_ld8(tmem + lane_q + (uint32_t)(D + h * DH + c0), v);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mk = fmaxf(mk, fabsf(v[i]));
+                    }
+                    sq_n = scale_exp(mq);
+                    sk_n = scale_exp(mk);
+                }
+                // fragment scales: rows 16 m + 8 i + tq, keys 8 t + tq
+                float aq[2][2], bk[3];
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) aq[m][i] = exp2i(__shfl_sync(kFull, sq_n, 16 * m + 8 * i + tq));
+#pragma unroll
+                for (int t = 0; t < 3; ++t) bk[t] = exp2i(__shfl_sync(kFull, sk_n, 8 * t + tq));
                 float sacc[2][3][4];
 #pragma unroll
                 for (int m = 0; m < 2; ++m)
@@ -1018,49 +1049,79 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                     for (int t = 0; t < 3; ++t)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) sacc[m][t][e] = 0.f;
-                // scores S = Q K^T (log2 units), k over the head's dims in 3 steps of 8
+                // scores S = Q K^T, k over the head's dims in 2 steps of 16 (the
+                // second half zero). The fragments come straight from TMEM
+                // (16x256b loads: lane (tq, tr) holds rows tq, tq + 8 of a
+                // 16-row half at columns 2 tr, 2 tr + 1 of an 8-column chunk).
+                // Padding rows and keys hold exact zeros (their LayerNorm rows
+                // are zero); their scores are masked or never stored.
 #pragma unroll
-                for (int st = 0; st < DH / 8; ++st) {
-                    float qv[8], kv[8];
-                    tmem_ld8(tmem + lane_q + (uint32_t)(h * DH + 8 * st), qv);
-                    tmem_ld8(tmem + lane_q + (uint32_t)(D + h * DH + 8 * st), kv);
-                    __syncwarp();  // every lane is done with the previous slices
-                    if (rvalid) {
-                        const int s0 = n * 8 + (n & 4), s1 = n * 8 + ((n & 4) ^ 4);
-                        *reinterpret_cast<float4 *>(sq8 + s0) =
-                            make_float4(qv[0] * uq, qv[1] * uq, qv[2] * uq, qv[3] * uq);
-                        *reinterpret_cast<float4 *>(sq8 + s1) =
-                            make_float4(qv[4] * uq, qv[5] * uq, qv[6] * uq, qv[7] * uq);
-                        *reinterpret_cast<float4 *>(sk8 + s0) =
-                            make_float4(kv[0] * uk, kv[1] * uk, kv[2] * uk, kv[3] * uk);
-                        *reinterpret_cast<float4 *>(sk8 + s1) =
-                            make_float4(kv[4] * uk, kv[5] * uk, kv[6] * uk, kv[7] * uk);
-                    }
-                    __syncwarp();
-                    uint32_t ab[2][4], as[2][4];
-                    // (rows 16 m + tq, + 8 and keys 8 t + tq share bit 2 with tq)
-                    const int ka = tr ^ (tq & 4), kb = ka ^ 4;
-#pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        const int r0 = 16 * m + tq, r1 = r0 + 8;
-                        split_tf32(r0 < nq ? sq8[r0 * 8 + ka] : 0.f, ab[m][0], as[m][0]);
-                        split_tf32(r1 < nq ? sq8[r1 * 8 + ka] : 0.f, ab[m][1], as[m][1]);
-                        split_tf32(r0 < nq ? sq8[r0 * 8 + kb] : 0.f, ab[m][2], as[m][2]);
-                        split_tf32(r1 < nq ? sq8[r1 * 8 + kb] : 0.f, ab[m][3], as[m][3]);
-                    }
+                for (int st = 0; st < 2; ++st) {
+                    const uint32_t cq = (uint32_t)(h * DH + 16 * st), ck = cq + (uint32_t)D;
+                    // keys: chunks 0 (dims 0-7 of the step) and 1 (8-15; unused in
+                    // the second step) of both 16-row halves
+                    uint32_t k00[4], k10[4], k01[4], k11[4];
+                    tmem_ld16x8(tmem + lane_q + ck, k00);
+                    tmem_ld16x8(tmem + lane_q + (16u << 16) + ck, k10);
+                    tmem_ld16x8(tmem + lane_q + ck + 8u, k01);
+                    tmem_ld16x8(tmem + lane_q + (16u << 16) + ck + 8u, k11);
+                    tmem_wait_tied(k00, k10, k01, k11);
+                    uint32_t bh[3][2], bl[3][2];
 #pragma unroll
                     for (int t = 0; t < 3; ++t) {
-                        const int key = 8 * t + tq;
-                        uint32_t bb[2], bs[2];
-                        split_tf32(key < nq ? sk8[key * 8 + ka] : 0.f, bb[0], bs[0]);
-                        split_tf32(key < nq ? sk8[key * 8 + kb] : 0.f, bb[1], bs[1]);
-#pragma unroll
-                        for (int m = 0; m < 2; ++m) {
-                            mma_tf32(sacc[m][t], as[m], bb);
-                            mma_tf32(sacc[m][t], ab[m], bs);
-                            mma_tf32(sacc[m][t], ab[m], bb);
+                        // key tile t: rows tq / tq + 8 of the first half, rows tq of the second
+                        const uint32_t *c0 = t < 2 ? k00 : k10, *c1 = t < 2 ? k01 : k11;
+                        const int o = t == 1 ? 2 : 0;
+                        split2(__uint_as_float(c0[o]) * bk[t], __uint_as_float(c0[o + 1]) * bk[t], bh[t][0], bl[t][0]);
+                        if (st == 0) {
+                            split2(__uint_as_float(c1[o]) * bk[t], __uint_as_float(c1[o + 1]) * bk[t], bh[t][1], bl[t][1]);
+                        } else {
+                            bh[t][1] = bl[t][1] = 0u;
                         }
                     }
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        uint32_t q0[4], q1[4];
+                        tmem_ld16x8(tmem + lane_q + ((uint32_t)(16 * m) << 16) + cq, q0);
+                        tmem_ld16x8(tmem + lane_q + ((uint32_t)(16 * m) << 16) + cq + 8u, q1);
+                        tmem_wait_tied(q0, q1);
+                        uint32_t ah[4], al[4];
+                        split2(__uint_as_float(q0[0]) * aq[m][0], __uint_as_float(q0[1]) * aq[m][0], ah[0], al[0]);
+                        split2(__uint_as_float(q0[2]) * aq[m][1], __uint_as_float(q0[3]) * aq[m][1], ah[1], al[1]);
+                        if (st == 0) {
+                            split2(__uint_as_float(q1[0]) * aq[m][0], __uint_as_float(q1[1]) * aq[m][0], ah[2], al[2]);
+                            split2(__uint_as_float(q1[2]) * aq[m][1], __uint_as_float(q1[3]) * aq[m][1], ah[3], al[3]);
+                        } else {
+                            ah[2] = ah[3] = al[2] = al[3] = 0u;
+                        }
+#pragma unroll
+                        for (int t = 0; t < 3; ++t) {
+                            mma_f16(sacc[m][t], al, bh[t]);
+                            mma_f16(sacc[m][t], ah, bl[t]);
+                            mma_f16(sacc[m][t], ah, bh[t]);
+                        }
+                    }
+                }
+                // back to log2 units: row r, key c by 2^-(sq_r + sk_c) times the
+                // projections' unscaling (and 1 / sqrt(head_dim) log2 e for Q)
+                {
+                    const float fq_n = exp2i(-sq_n) * exp2i(-sr) * exp2i(-sw_s[0]) * qk_scale;
+                    const float fk_n = exp2i(-sk_n) * exp2i(-sr) * exp2i(-sw_s[1]);
+                    float fq[2][2], fk[3][2];
+#pragma unroll
+                    for (int m = 0; m < 2; ++m)
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) fq[m][i] = __shfl_sync(kFull, fq_n, 16 * m + 8 * i + tq);
+#pragma unroll
+                    for (int t = 0; t < 3; ++t)
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) fk[t][j] = __shfl_sync(kFull, fk_n, 8 * t + 2 * tr + j);
+#pragma unroll
+                    for (int m = 0; m < 2; ++m)
+#pragma unroll
+                        for (int t = 0; t < 3; ++t)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) sacc[m][t][e] *= fq[m][e >> 1] * fk[t][e & 1];
                 }
                 // bias (log2 units) on the query's unmasked keys, -inf on the
                 // others and on keys past the graph's nodes; then the row softmax
