@@ -277,6 +277,13 @@ __device__ __forceinline__ void tmem_wait_tied(uint32_t *a, uint32_t *b, uint32_
                  : "memory");
 }
 
+// 16 TMEM lanes x 4 columns (16x128b shape): thread t writes lane
+// base + t / 4 at column t % 4 (a) and lane base + 8 + t / 4 there (b)
+__device__ __forceinline__ void tmem_st16x4(uint32_t taddr, uint32_t a, uint32_t b) {
+    asm volatile("tcgen05.st.sync.aligned.16x128b.x1.b32 [%0], {%1,%2};" ::"r"(taddr), "r"(a), "r"(b)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
     uint32_t r[16];
     asm volatile(
@@ -409,8 +416,8 @@ struct Smem {
         return b > lnred_bytes ? b : lnred_bytes;
     }
     __host__ __device__ static uint32_t stage(int N) { return bias + bias_bytes(N); }
-    // the attention's staging (per warp: the V rows, which the context
-    // replaces), or outside it one prefetch slot of 16
+    // the attention's staging (per warp: the V rows), or outside it one
+    // prefetch slot of 16
     // features per compute thread; above both (float offset mask_off), the
     // next tile's mask values, copied in during the attention. The epilogue's
     // output rows [graph][node][kOutStride] sit above the prefetch slots
@@ -1001,12 +1008,13 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
 
             // ======== phase B: attention of head h in graph g, thread = query node n
             const int sr = rscale[32 * g + n];
-            float2 ctx[DH / 2];
+            // the normalised context in the MMA accumulator layout: rows
+            // 16 m + tq + 8 i, dims 8 t + 2 tr + j at [m][t][2 i + j]
+            float cctx[2][3][4];
+            const int tq = lane >> 2, tr = lane & 3;
             {
-                // The warp's staging: after the softmax the V rows, which the
-                // normalised context replaces (row r rotated by 2 (r / 4 % 4)
-                // columns, which keeps the context's accesses free of bank
-                // conflicts).
+                // The warp's staging: after the softmax the V rows (the B
+                // operand of the context product).
                 float *sv = stage_base + warp * Smem::warp_stage(N);
                 const float uv = exp2i(-sr) * exp2i(-sw_s[2]);
                 const int nq = b < p.B ? N : 0;  // the graph's rows (queries) and keys
@@ -1016,7 +1024,6 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 // two into [2^12, 2^13) for the split): 32 query rows (2 row
                 // tiles) x 24 keys (3 tiles of 8), then x 24 dims. Fragment
                 // coordinates: row group tq, column pair tr.
-                const int tq = lane >> 2, tr = lane & 3;
                 // the row owner's ranges of its Q and K rows over the head's dims
                 int sq_n, sk_n;
                 {
@@ -1236,51 +1243,43 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                         }
                     }
                 }
-                // normalised rows back to one row per lane through V's rows
-                __syncwarp();  // every lane is done reading V
+                // normalised (rows past the graph's nodes: zero)
 #pragma unroll
                 for (int m = 0; m < 2; ++m)
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
                         const int row = 16 * m + tq + 8 * i;
-                        if (row < nq) {
-                            const float inv = exp2i(-12) * exp2i(-sv_e) * (1.0f / zr[m][i]);
-                            const int rot = 2 * ((row >> 2) & 3);
+                        const float inv = row < nq ? exp2i(-12) * exp2i(-sv_e) * (1.0f / zr[m][i]) : 0.f;
 #pragma unroll
-                            for (int t = 0; t < DH / 8; ++t) {
-                                const int col = 8 * t + 2 * tr + rot;
-                                *reinterpret_cast<float2 *>(sv + row * DH + (col < DH ? col : col - DH)) =
-                                    make_float2(cacc[m][t][2 * i] * inv, cacc[m][t][2 * i + 1] * inv);
-                            }
-                        }
-                    }
-                __syncwarp();
-                {
-                    const int rot = 2 * ((n >> 2) & 3);
+                        for (int t = 0; t < DH / 8; ++t)
 #pragma unroll
-                    for (int c = 0; c < DH / 2; ++c) {
-                        const int col = 2 * c + rot;
-                        ctx[c] = rvalid ? *reinterpret_cast<const float2 *>(sv + n * DH + (col < DH ? col : col - DH))
-                                        : make_float2(0.f, 0.f);
+                            for (int j = 0; j < 2; ++j)
+                                cctx[m][t][2 * i + j] = row < nq ? cacc[m][t][2 * i + j] * inv : 0.f;
                     }
-                }
             }
             asm volatile("cp.async.wait_all;" ::: "memory");  // the next tile's mask values
             named_sync(1, kComputeThreads);  // every graph's largest |V| known; staging free
             // the next tile's unmasked-pair words (this tile's are read)
             if (it + 1 < n_my) mask_words(tile + gridDim.x);
-            // the context (|ctx| <= max |V| of the graph) as the out-projection's A operand
+            // the context (|ctx| <= max |V| of the graph) as the out-projection's A
+            // operand, stored from the accumulator layout (16x128b: dims
+            // 8 t + 2 tr, + 1 are packed column h DH / 2 + 4 t + tr of rows tq,
+            // tq + 8 of each 16-row half)
             const int sc_g = scale_exp(__int_as_float(vmax_s[g]));
             {
                 const float sc = exp2i(sc_g);
-                uint32_t hi[DH / 2], lo[DH / 2];
 #pragma unroll
-                for (int c = 0; c < DH / 2; ++c) split2(ctx[c].x * sc, ctx[c].y * sc, hi[c], lo[c]);
+                for (int m = 0; m < 2; ++m)
 #pragma unroll
-                for (int c = 0; c < DH / 2; c += 4) {
-                    tmem_st4(tmem + lane_q + acol + (uint32_t)(h * DH / 2 + c), hi + c);
-                    tmem_st4(tmem + lane_q + acol + kAHalf + (uint32_t)(h * DH / 2 + c), lo + c);
-                }
+                    for (int t = 0; t < DH / 8; ++t) {
+                        uint32_t h0, l0, h1, l1;
+                        split2(cctx[m][t][0] * sc, cctx[m][t][1] * sc, h0, l0);
+                        split2(cctx[m][t][2] * sc, cctx[m][t][3] * sc, h1, l1);
+                        const uint32_t a = tmem + lane_q + ((uint32_t)(16 * m) << 16) + acol +
+                                           (uint32_t)(h * DH / 2 + 4 * t);
+                        tmem_st16x4(a, h0, h1);
+                        tmem_st16x4(a + kAHalf, l0, l1);
+                    }
             }
             tmem_st_done();
             mbar_arrive(&br.cfull);
