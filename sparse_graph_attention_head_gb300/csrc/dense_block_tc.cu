@@ -1289,15 +1289,15 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
                 mbar_wait(&br.nfull, (uint32_t)(it + 1) & 1u, err);  // the next tile's node rows
                 // with the prefix of the next tile's unmasked-pair words, and the
                 // prefetch of its first relation-MLP blocks
-                // (the residual copies go in after its first barrier: every
-                // thread has read the mask values in the staging region then)
+                // (the residual copies go in after the next tile's prefetch, which
+                // is needed first; every thread has read the mask values in the
+                // staging region by then)
                 layer_norm(p, nodes_s, red, rscale, gam, bet, tmem, col_a(it + 1),
-                           tile + gridDim.x, warp, lane,
+                           tile + gridDim.x, warp, lane, mask_scan,
                            [&] {
-                               mask_scan();
+                               first_fetch(tile + gridDim.x);
                                res_copy(tile);
-                           },
-                           [&] { first_fetch(tile + gridDim.x); });
+                           });
                 mbar_arrive(&br.xfull);
             } else {
                 res_copy(tile);
@@ -1309,12 +1309,9 @@ __global__ void __launch_bounds__(kThreads, 1) dense_tc_kernel(const Params p) {
             {
                 const float uo = exp2i(-sc_g) * exp2i(-sw_s[3]);
                 float *os = stage_base + Smem::out_off + g * N * kOutStride;
-                // this thread's residual copies (the prefetch's group may still
-                // be in flight), then the whole graph's
-                if (it + 1 < n_my)
-                    asm volatile("cp.async.wait_group 1;" ::: "memory");
-                else
-                    asm volatile("cp.async.wait_group 0;" ::: "memory");
+                // this thread's residual copies (committed last), then the whole
+                // graph's
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
                 named_sync(6 + g, 128);
 #pragma unroll
                 for (int c0 = 0; c0 < DH; c0 += 8) {
