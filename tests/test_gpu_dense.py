@@ -110,6 +110,24 @@ def test_dense_block_full_size_sampled_graphs(gat):
     assert np.isfinite(g).all()
 
 
+@pytest.mark.parametrize("N", [11, 12, 20, 23])
+def test_dense_block_tensor_core_several_tiles_per_cta(gat, N):
+    """1,301 graphs: 326 tiles of 4 over the 152 resident blocks, 2-3 tiles
+    each, so the cross-tile pipeline (the next tile's LayerNorm, mask words,
+    pair prefetch and residual rows overlapping this tile's work) runs at
+    node counts below 24; N = 11 and 12 sit on either side of the bias row
+    stride's step (12 -> 28 floats). Sampled graphs, the last partial tile
+    included, against the oracle."""
+    B = 1301
+    w = W.make_dense(seed=60 + N, B=B, N=N, wstd=0.05, affine_ln=True)
+    g = run(gat, w)
+    rng = np.random.default_rng(N)
+    sel = np.unique(np.concatenate([[0, 1, 607, 608, B - 2, B - 1], rng.integers(0, B, 40)]))
+    o, c = oracle.dense_block(w, graphs=sel, want_cond=True)
+    assert_fp32(g[sel], o, c, name=f"dense block B={B} N={N}")
+    assert np.isfinite(g).all()
+
+
 def test_dense_block_other_shapes_and_masked_row(gat):
     w = W.make_dense(seed=22, B=5, N=7, D=12, H=3, P=5, wstd=0.1, affine_ln=True)
     w["edge_mask"][1, 4, :] = 0.0  # node 4 of graph 1 attends to nothing -> NaN, as the reference
