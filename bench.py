@@ -804,11 +804,13 @@ def bench_small(name, args):
         attn = 2.0 * 2 * H_ * N_ * N_ * (D_ // H_)           # Q K^T and A V
         mlp = 2.0 * N_ * N_ * (P_ * P_ + H_ * P_)            # relation MLP
         flops = B_ * (proj + attn + mlp)
-        tensor_flops = B_ * proj
         # the kernel reads the pair features of unmasked pairs only (a masked
         # pair's logit is -inf whatever its relation-MLP bias): the bytes it
         # has to move on this mask, beside the nominal count above
         unmasked = int((g["edge_mask"] >= 0.5).sum())
+        # on the tensor cores: the projections, Q K^T and A V, and the relation
+        # MLP's first layer over the unmasked pairs
+        tensor_flops = B_ * (proj + attn) + 2.0 * P_ * P_ * unmasked
         need = B_ * 4 * (2 * N_ * D_ + N_ * N_) + 4 * P_ * unmasked + 4 * (4 * D_ * D_)
         extra["required_bytes"] = need
         extra["unmasked_pair_frac"] = unmasked / float(B_ * N_ * N_)
@@ -848,12 +850,12 @@ def bench_small(name, args):
     if flops:
         res["achieved_tflops"] = flops / (ms * 1e-3) / 1e12
     if tensor_flops:
-        # tf32 tensor peak = measured bf16 peak x nominal tf32/bf16 ratio (1.1/2.25);
-        # 3xTF32 issues three tensor products per useful one
-        tf32_peak = bf16_peak * (1.1 / 2.25)
-        res["projection_tflops_useful"] = tensor_flops / (ms * 1e-3) / 1e12
-        res["tensor_issue_frac_of_tf32_peak"] = 3 * tensor_flops / (ms * 1e-3) / 1e12 / tf32_peak
-        res["tf32_peak_tflops"] = tf32_peak
+        # f16 operands split in two terms: three tensor products per useful one
+        # (padding of the small attention tiles not counted); the f16 dense
+        # peak is the measured bf16 one
+        res["tensor_tflops_useful"] = tensor_flops / (ms * 1e-3) / 1e12
+        res["tensor_issue_frac_of_f16_peak"] = 3 * tensor_flops / (ms * 1e-3) / 1e12 / bf16_peak
+        res["f16_peak_tflops"] = bf16_peak
         res["peak_kind"] = kind
     if name in ("edge_softmax", "aggregate", "sddmm"):
         # launch-bound at this size: the per-call events above include the
