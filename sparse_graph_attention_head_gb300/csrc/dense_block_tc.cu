@@ -1,59 +1,62 @@
 // dense_block_tc.cu - the dense-masked attention block of the block page's
 // module shape (Kimi-K2.6 l2_p4, reference model: P = 16 pair features,
-// H = 4 heads of 24 dims, D = 96, up to 24 nodes), its four D x D projections
-// on the 5th-generation tensor cores (tcgen05, kind::f16, fp32 accumulators in
-// TMEM), everything else in fp32 on the CUDA cores.
+// H = 4 heads of 24 dims, D = 96, up to 24 nodes): the four D x D projections
+// and the relation MLP's first layer on the 5th-generation tensor cores
+// (tcgen05, kind::f16, fp32 accumulators in TMEM), the attention's Q K^T and
+// A V on warp-level f16 MMAs, the rest in fp32 on the CUDA cores.
 //
-// Projection precision: fp32 results from fp16 tensor-core products. Each
-// operand row (a normalised node row, a graph's context rows, a weight
-// matrix) is scaled by a power of two 2^s that brings its largest magnitude
-// into [2^12, 2^13), then split x 2^s = hi + lo, hi = fp16(x 2^s) and
-// lo = fp16(x 2^s - hi) (round to nearest even). A B ~ hi_A hi_B + hi_A lo_B +
-// lo_A hi_B: the dropped lo_A lo_B and lo's own rounding are ~2^-22 of the
-// row's largest term, the products accumulate in fp32, and the scales are
-// undone exactly afterwards. Three fp16 MMAs cost what 1.5 tf32 MMAs do, for
-// the accuracy of the 3xTF32 split.
+// Tensor-core precision: fp32 results from fp16 products. Each operand row (a
+// normalised node row, a Q / K / V / context row, a pair's features, a weight
+// matrix, the attention weights) is scaled by a power of two 2^s that brings
+// its largest magnitude into [2^12, 2^13), then split x 2^s = hi + lo,
+// hi = fp16(x 2^s) and lo = fp16(x 2^s - hi) (round to nearest even).
+// A B ~ hi_A hi_B + hi_A lo_B + lo_A hi_B: the dropped lo_A lo_B and lo's own
+// rounding are ~2^-22 of the row's largest term, the products accumulate in
+// fp32, and the scales are undone exactly afterwards. Three fp16 MMAs cost
+// what 1.5 tf32 MMAs do, for the accuracy of the 3xTF32 split.
 //
-// The A operands live in TMEM (written by tcgen05.st from the registers of
-// the threads owning the row), so the tensor cores read only the weights from
-// shared memory. A tile is 4 graphs padded to 32 rows: graph g owns TMEM lanes
-// 32g..32g+31, which warps g, g+4, g+8, g+12 may access. Every MMA is
-// 128 x 96 x 16 (a tcgen05 MMA costs ~47 cycles at any N up to 96, so wide
-// MMAs and few of them): Q, K, V and the out-projection are 18 MMAs each.
+// The projections' A operands live in TMEM (written by tcgen05.st from the
+// registers of the threads owning the row), so those tensor cores read only
+// the weights from shared memory. A tile is 4 graphs padded to 32 rows: graph
+// g owns TMEM lanes 32g..32g+31, which warps g, g+4, g+8, g+12 may access.
+// Every projection MMA is 128 x 96 x 16 (a tcgen05 MMA costs ~47 cycles at any
+// N up to 96, so wide MMAs and few of them): Q, K, V and the out-projection
+// are 18 MMAs each.
 //
 // 17 warps per CTA, one CTA per SM, persistent over tiles; per tile t:
-//   control warp (lane 0): streams the pre-split weight chunks (Q K V O,
-//       96 rows each) through a 2-slot shared-memory ring with bulk copies,
-//       issues Q|K|V once LayerNorm(t) is in TMEM and tile t-1's readers of
-//       those columns are done, each relation-MLP block once its features
-//       are in TMEM, and the out-projection once the context is;
+//   control warp (lane 0): streams the pre-split weight chunks (K Q V O, 96
+//       rows each) through a 2-slot shared-memory ring with bulk copies and
+//       issues them: K and V once LayerNorm(t) is in TMEM, Q once tile t-1's
+//       epilogue has read the out-projection from its columns, the
+//       out-projection once the context is; it also bulk-copies the next
+//       tile's node rows;
 //   A (quad q = warps 4q..4q+3): the relation MLP over the tile's unmasked
 //       pairs only (a masked pair's logit is -inf whatever its bias, so its
 //       features are never read): per (graph, query row) a word of unmasked
 //       keys and a prefix of their counts, built from the mask in shared
-//       memory the tile before; one thread per unmasked pair of 128-pair
-//       blocks q, q + 4, ...: the pair's 16 features (prefetched into shared
-//       memory by cp.async) go, split and scaled, to its TMEM lane as the A
-//       operand of W1 (128 x 16 x 16 MMAs, in TMEM columns idle until the
-//       next tile's LayerNorm); the same thread reads the hidden values back
-//       and applies b1, SiLU, W2, b2 (packed f32x2 FMAs), giving the bias of
-//       all heads;
-//   B (warp (g, h) = (w % 4, w / 4)): attention of head h in graph g: V
-//       rows staged in shared memory, Q and K in 8-dim slices; scores and
-//       context as warp-level tensor-core MMAs (m16n8k8, tf32 operands
-//       split in two, three products per term) on the warp's 24 x 24
-//       products - a tcgen05 version would need 256 TMEM columns per head
-//       beside the projections' 512; bias in log2 units (-inf for the
-//       query's masked keys, from its word), softmax with ex2 over the
-//       quad of lanes sharing a row; the context becomes the
-//       out-projection's A operand (scaled per graph by the largest |V|,
-//       which bounds it);
+//       memory during the tile before; one thread per unmasked pair of
+//       128-pair blocks q, q + 4, ...: the pair's 16 features (prefetched into
+//       shared memory by cp.async) go, split and scaled, to its TMEM lane as
+//       the A operand of W1 (128 x 16 x 16 MMAs the quad's first thread
+//       issues, in TMEM columns idle until the next tile's LayerNorm); the
+//       same thread reads the hidden values back and applies b1, SiLU, W2, b2
+//       (packed f32x2 FMAs), giving the bias of all heads;
+//   B (warp (g, h) = (w % 4, w / 4)): attention of head h in graph g on
+//       warp-level MMAs (m16n8k16, f16 operands split in two, three products
+//       per term): Q and K fragments loaded straight from TMEM (16x256b),
+//       each row scaled from its own range; bias in log2 units (-inf for the
+//       query's masked keys, from its word), softmax with ex2 over the quad
+//       of lanes sharing a row; A V with V staged in shared memory; the
+//       context stored from the fragments (16x128b) as the out-projection's A
+//       operand (scaled per graph by the largest |V|, which bounds it); the
+//       next tile's mask (copied in during B) becomes its unmasked-pair words;
 //   C: LayerNorm of tile t+1 into the other A region of TMEM (warp (g, k):
 //       columns [24k, 24k + 24) of graph g's rows, row statistics combined
-//       through shared memory), tile t+1's unmasked-pair words and prefix
-//       (its mask copied in by cp.async since the end of B) and its first
-//       relation-MLP prefetch, then out-projection columns [24h, 24h + 24)
-//       + the residual.
+//       through shared memory) with tile t+1's pair prefix, its first
+//       relation-MLP prefetches and tile t's residual rows copied in; then
+//       the epilogue per graph: the four head warps add their out-projection
+//       columns to the staged residual block, and its 128 threads store the
+//       block as consecutive float4s.
 // Every mbarrier wait is bounded; a wait that gives up sets the call's error
 // flag in the workspace (readable with gat_dense_masked_attention_status) and
 // the outputs of the remaining tiles are written as NaN, never as garbage.
