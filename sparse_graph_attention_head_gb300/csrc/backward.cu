@@ -30,6 +30,7 @@
 // dv += a dout[i], dk += ds q[i]; dk is scaled at the end.
 // Shapes outside the vector lanes take the scalar kernels at the end.
 #include <climits>
+#include <type_traits>
 
 #include "row_engine.cuh"
 
@@ -81,11 +82,32 @@ __device__ __forceinline__ float bexp2(float x) {
 // HL = H / HG whole heads, G lanes each.
 constexpr float kRescale = 8.f;  // the running max is moved only by more than this (log2 units)
 
+// <a, b> over 8 bf16 pairs (16-byte vectors) with mixed-precision FMAs: each
+// bf16 x bf16 product is exact in fp32 and each sum rounded once, as fmaf on
+// the converted values; two partial sums (elements 0, 2, .. and 1, 3, ..)
+__device__ __forceinline__ float dot_bf16x8(const uint4 &a, const uint4 &b) {
+    float s0 = 0.f, s1 = 0.f;
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"
+        "mov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %6;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t"
+        "mov.b32 {a0, a1}, %3;\n\tmov.b32 {b0, b1}, %7;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t"
+        "mov.b32 {a0, a1}, %4;\n\tmov.b32 {b0, b1}, %8;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t"
+        "mov.b32 {a0, a1}, %5;\n\tmov.b32 {b0, b1}, %9;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w));
+    return s0 + s1;
+}
+
 template <typename T, int U>
 struct BwdRow {
+    static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     using L = Lanes<T, 1, 32>;
     static constexpr int VE = L::VE;
     float qf[VE], gf[VE];  // q * qscale and dout of the row's group
+    uint4 gpk;             // dout as stored (bf16: <dout, v> on the packed pairs)
     float A[VE], B[VE];
     float m, l, S;
 
@@ -100,7 +122,10 @@ struct BwdRow {
 
     __device__ __forceinline__ void begin(const BwdParams &p, const uint4 &qr, const uint4 &gr) {
         Vec<T>::unpack(qr, qf);
-        Vec<T>::unpack(gr, gf);
+        if (kBf16)
+            gpk = gr;
+        else
+            Vec<T>::unpack(gr, gf);
 #pragma unroll
         for (int t = 0; t < VE; ++t) {
             qf[t] *= p.qscale;
@@ -138,14 +163,18 @@ struct BwdRow {
                 float sc[U], da[U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    float kf[VE], vf[VE];
+                    float kf[VE];
                     Vec<T>::unpack(kr[u], kf);
-                    Vec<T>::unpack(vr[u], vf);
                     float a = 0.f, b = 0.f;
 #pragma unroll
-                    for (int t = 0; t < VE; ++t) {
-                        a = fmaf(qf[t], kf[t], a);
-                        b = fmaf(gf[t], vf[t], b);
+                    for (int t = 0; t < VE; ++t) a = fmaf(qf[t], kf[t], a);
+                    if constexpr (kBf16) {
+                        b = dot_bf16x8(gpk, vr[u]);
+                    } else {
+                        float vf[VE];
+                        Vec<T>::unpack(vr[u], vf);
+#pragma unroll
+                        for (int t = 0; t < VE; ++t) b = fmaf(gf[t], vf[t], b);
                     }
                     sc[u] = a;
                     da[u] = b;
