@@ -107,7 +107,7 @@ struct BwdRow {
     using L = Lanes<T, 1, 32>;
     static constexpr int VE = L::VE;
     float qf[VE], gf[VE];  // q * qscale and dout of the row's group
-    uint4 gpk;             // dout as stored (bf16: <dout, v> on the packed pairs)
+    uint4 qpk, gpk;        // q and dout as stored (bf16: the dot products on the packed pairs)
     float A[VE], B[VE];
     float m, l, S;
 
@@ -121,16 +121,17 @@ struct BwdRow {
     }
 
     __device__ __forceinline__ void begin(const BwdParams &p, const uint4 &qr, const uint4 &gr) {
-        Vec<T>::unpack(qr, qf);
-        if (kBf16)
+        if (kBf16) {
+            qpk = qr;
             gpk = gr;
-        else
+        } else {
+            Vec<T>::unpack(qr, qf);
             Vec<T>::unpack(gr, gf);
 #pragma unroll
-        for (int t = 0; t < VE; ++t) {
-            qf[t] *= p.qscale;
-            A[t] = B[t] = 0.f;
+            for (int t = 0; t < VE; ++t) qf[t] *= p.qscale;
         }
+#pragma unroll
+        for (int t = 0; t < VE; ++t) A[t] = B[t] = 0.f;
         m = -INFINITY;
         l = 0.f;
         S = 0.f;
@@ -163,18 +164,19 @@ struct BwdRow {
                 float sc[U], da[U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    float kf[VE];
-                    Vec<T>::unpack(kr[u], kf);
                     float a = 0.f, b = 0.f;
-#pragma unroll
-                    for (int t = 0; t < VE; ++t) a = fmaf(qf[t], kf[t], a);
                     if constexpr (kBf16) {
+                        a = dot_bf16x8(qpk, kr[u]);  // scaled after the head's sum
                         b = dot_bf16x8(gpk, vr[u]);
                     } else {
-                        float vf[VE];
+                        float kf[VE], vf[VE];
+                        Vec<T>::unpack(kr[u], kf);
                         Vec<T>::unpack(vr[u], vf);
 #pragma unroll
-                        for (int t = 0; t < VE; ++t) b = fmaf(gf[t], vf[t], b);
+                        for (int t = 0; t < VE; ++t) {
+                            a = fmaf(qf[t], kf[t], a);
+                            b = fmaf(gf[t], vf[t], b);
+                        }
                     }
                     sc[u] = a;
                     da[u] = b;
@@ -186,6 +188,9 @@ struct BwdRow {
                         da[u] += __shfl_xor_sync(kFull, da[u], o);
                     }
                 }
+                if (kBf16)
+#pragma unroll
+                    for (int u = 0; u < U; ++u) sc[u] *= p.qscale;
                 // the head's first lane records the edge's score and da
                 if (leader)
 #pragma unroll
