@@ -101,6 +101,16 @@ __device__ __forceinline__ float dot_bf16x8(const uint4 &a, const uint4 &b) {
     return s0 + s1;
 }
 
+// packed fp32 FMA on a pair, (a.x b.x + c.x, a.y b.y + c.y), each rounded once
+__device__ __forceinline__ float2 fma_x2(float2 a, float2 b, float2 c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)),
+          "l"(*reinterpret_cast<uint64_t *>(&c)));
+    return *reinterpret_cast<float2 *>(&r);
+}
+
 template <typename T, int U>
 struct BwdRow {
     static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -222,10 +232,16 @@ struct BwdRow {
                     S += pd;
                     float kf[VE];
                     Vec<T>::unpack(kr[u], kf);
+                    const float2 pd2 = make_float2(pd, pd), pe2 = make_float2(pe, pe);
 #pragma unroll
-                    for (int t = 0; t < VE; ++t) {
-                        A[t] = fmaf(pd, kf[t], A[t]);
-                        B[t] = fmaf(pe, kf[t], B[t]);
+                    for (int t = 0; t < VE; t += 2) {
+                        const float2 k2 = make_float2(kf[t], kf[t + 1]);
+                        const float2 a2 = fma_x2(pd2, k2, make_float2(A[t], A[t + 1]));
+                        const float2 b2 = fma_x2(pe2, k2, make_float2(B[t], B[t + 1]));
+                        A[t] = a2.x;
+                        A[t + 1] = a2.y;
+                        B[t] = b2.x;
+                        B[t + 1] = b2.y;
                     }
                 }
             }
