@@ -82,25 +82,6 @@ __device__ __forceinline__ float bexp2(float x) {
 // HL = H / HG whole heads, G lanes each.
 constexpr float kRescale = 8.f;  // the running max is moved only by more than this (log2 units)
 
-// <a, b> over 8 bf16 pairs (16-byte vectors) with mixed-precision FMAs: each
-// bf16 x bf16 product is exact in fp32 and each sum rounded once, as fmaf on
-// the converted values; two partial sums (elements 0, 2, .. and 1, 3, ..)
-__device__ __forceinline__ float dot_bf16x8(const uint4 &a, const uint4 &b) {
-    float s0 = 0.f, s1 = 0.f;
-    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"
-        "mov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %6;\n\t"
-        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t"
-        "mov.b32 {a0, a1}, %3;\n\tmov.b32 {b0, b1}, %7;\n\t"
-        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t"
-        "mov.b32 {a0, a1}, %4;\n\tmov.b32 {b0, b1}, %8;\n\t"
-        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t"
-        "mov.b32 {a0, a1}, %5;\n\tmov.b32 {b0, b1}, %9;\n\t"
-        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t}"
-        : "+f"(s0), "+f"(s1)
-        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w));
-    return s0 + s1;
-}
-
 // packed fp32 FMA on a pair, (a.x b.x + c.x, a.y b.y + c.y), each rounded once
 __device__ __forceinline__ float2 fma_x2(float2 a, float2 b, float2 c) {
     uint64_t r;

@@ -1,6 +1,7 @@
 // common.cuh - internal helpers shared by the libgat translation units.
 #pragma once
 
+#include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -130,6 +131,25 @@ struct Vec<__nv_bfloat16> {
         return make_uint4(w[0], w[1], w[2], w[3]);
     }
 };
+
+// <a, b> over 8 bf16 pairs (16-byte vectors) with mixed-precision FMAs: each
+// bf16 x bf16 product is exact in fp32 and each sum rounded once, as fmaf on
+// the converted values; two partial sums (elements 0, 2, .. and 1, 3, ..)
+__device__ __forceinline__ float dot_bf16x8(const uint4 &a, const uint4 &b) {
+    float s0 = 0.f, s1 = 0.f;
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"
+        "mov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %6;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t"
+        "mov.b32 {a0, a1}, %3;\n\tmov.b32 {b0, b1}, %7;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t"
+        "mov.b32 {a0, a1}, %4;\n\tmov.b32 {b0, b1}, %8;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t"
+        "mov.b32 {a0, a1}, %5;\n\tmov.b32 {b0, b1}, %9;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w));
+    return s0 + s1;
+}
 
 // Scalar element access for the non-vector kernels.
 __device__ __forceinline__ float load_elem(const float *p, int64_t i) { return __ldg(p + i); }

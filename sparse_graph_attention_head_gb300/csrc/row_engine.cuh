@@ -132,7 +132,9 @@ struct FusedRow {
     using L = Lanes<T, V, LE>;
     static constexpr int VE = L::VE;
     static constexpr int ES = L::ES;
-    float qf[V][VE];
+    static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    float qf[V][VE];  // q * qscale (bf16: q as stored in qpk, scaled after the dot)
+    uint4 qpk[V];
     float acc[V][VE];
     float m[V], l[V];
 
@@ -141,9 +143,13 @@ struct FusedRow {
 #pragma unroll
         for (int s = 0; s < V; ++s) {
             uint4 u = ld_stream16(qrow + ln.vi[s] * 16);
-            Vec<T>::unpack(u, qf[s]);
+            if (kBf16) {
+                qpk[s] = u;
+            } else {
+                Vec<T>::unpack(u, qf[s]);
 #pragma unroll
-            for (int t = 0; t < VE; ++t) qf[s][t] *= p.qscale;
+                for (int t = 0; t < VE; ++t) qf[s][t] *= p.qscale;
+            }
         }
     }
 
@@ -216,12 +222,16 @@ struct FusedRow {
                     for (int u = 0; u < U; ++u)
 #pragma unroll
                         for (int s = 0; s < V; ++s) {
-                            float kf[VE];
-                            Vec<T>::unpack(kr[u][s], kf);
-                            float d = 0.f;
+                            if constexpr (kBf16) {
+                                sc[u][s] = dot_bf16x8(qpk[s], kr[u][s]);
+                            } else {
+                                float kf[VE];
+                                Vec<T>::unpack(kr[u][s], kf);
+                                float d = 0.f;
 #pragma unroll
-                            for (int t = 0; t < VE; ++t) d = fmaf(qf[s][t], kf[t], d);
-                            sc[u][s] = d;
+                                for (int t = 0; t < VE; ++t) d = fmaf(qf[s][t], kf[t], d);
+                                sc[u][s] = d;
+                            }
                         }
                     // per-head sums over the head's G lanes (uniform across the warp)
                     for (int o = 1; o < ln.G; o <<= 1) {
@@ -231,6 +241,11 @@ struct FusedRow {
                             for (int s = 0; s < V; ++s)
                                 sc[u][s] += __shfl_xor_sync(kFull, sc[u][s], o);
                     }
+                    if (kBf16)
+#pragma unroll
+                        for (int u = 0; u < U; ++u)
+#pragma unroll
+                            for (int s = 0; s < V; ++s) sc[u][s] *= p.qscale;
                 }
 #pragma unroll
                 for (int s = 0; s < V; ++s) {
