@@ -110,12 +110,21 @@ sddmm_rows_kernel(const int32_t *__restrict__ row_ptr, const int32_t *__restrict
             ++r;
             rend = __ldg(row_ptr + r + 1);
         }
+        // the row's b vectors: as stored for bf16 (the dot on the packed pairs,
+        // scaled after the head's sum), else unpacked and scaled
+        constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
         float qf[V][VE];
+        uint4 qpk[V];
 #pragma unroll
         for (int s = 0; s < V; ++s) {
-            Vec<T>::unpack(ld_stream16(bb + r * row_bytes + (s * 32 + lane) * 16), qf[s]);
+            const uint4 u = ld_stream16(bb + r * row_bytes + (s * 32 + lane) * 16);
+            if (kBf16) {
+                qpk[s] = u;
+            } else {
+                Vec<T>::unpack(u, qf[s]);
 #pragma unroll
-            for (int t = 0; t < VE; ++t) qf[s][t] *= scale;
+                for (int t = 0; t < VE; ++t) qf[s][t] *= scale;
+            }
         }
         const int64_t seg_end = rend < e_end ? rend : e_end;
         for (int64_t base = e; base < seg_end; base += 32) {
@@ -137,17 +146,24 @@ sddmm_rows_kernel(const int32_t *__restrict__ row_ptr, const int32_t *__restrict
                     float part[V];
 #pragma unroll
                     for (int s = 0; s < V; ++s) {
-                        float kf[VE];
-                        Vec<T>::unpack(kr[u][s], kf);
-                        float acc = 0.f;
+                        if constexpr (kBf16) {
+                            part[s] = dot_bf16x8(qpk[s], kr[u][s]);
+                        } else {
+                            float kf[VE];
+                            Vec<T>::unpack(kr[u][s], kf);
+                            float acc = 0.f;
 #pragma unroll
-                        for (int t = 0; t < VE; ++t) acc = fmaf(qf[s][t], kf[t], acc);
-                        part[s] = acc;
+                            for (int t = 0; t < VE; ++t) acc = fmaf(qf[s][t], kf[t], acc);
+                            part[s] = acc;
+                        }
                     }
                     for (int o = 1; o < G; o <<= 1) {
 #pragma unroll
                         for (int s = 0; s < V; ++s) part[s] += __shfl_xor_sync(kFull, part[s], o);
                     }
+                    if (kBf16)
+#pragma unroll
+                        for (int s = 0; s < V; ++s) part[s] *= scale;
                     if (j0 + u < n && my_slot < V) {
                         float val = part[0];
 #pragma unroll
