@@ -17,9 +17,10 @@
 //     than the resident limit are read twice (fold, then normalise);
 //   phase 2: batches of 32 consecutive rows, fetched from a second counter
 //     (static stride without a plan). A warp stages runs of consecutive rows
-//     (up to 2048 scores, cp.async with every copy in flight), computes them
-//     in shared memory / registers and writes each run back with one bulk
-//     copy (TMA engine).
+//     (up to 2048 scores: one bulk copy in, on the warp's mbarrier, with
+//     W = 4; cp.async with every copy in flight otherwise), computes them in
+//     shared memory / registers and writes each run back with one bulk copy
+//     (TMA engine).
 // Threads work on W consecutive heads at once: W = 4 (16-byte accesses) when
 // H % 4 == 0 and the pointers are 16-byte aligned, else W = 1 with 4-byte
 // copies and plain stores. With W = 4 and Q = H/4 a power of two, a light
@@ -293,6 +294,35 @@ __device__ __forceinline__ void bulk_wait_read() {
 }
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// one bulk copy (TMA engine) of `bytes` (a multiple of 16, both addresses
+// 16-byte aligned) global -> shared, completing on the mbarrier `bar`, which
+// the calling thread arms with the byte count
+__device__ __forceinline__ void bulk_load(float *dst, const float *src, unsigned bytes, uint64_t *bar) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+    const unsigned b = (unsigned)__cvta_generic_to_shared(bar);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(d),
+        "l"(src), "r"(bytes), "r"(b)
+        : "memory");
+}
+// wait for the phase of parity `ph` of `bar` (bounded: 2^30 polls, far beyond
+// any copy; the data is then used as it stands)
+__device__ __forceinline__ void mbar_wait_bounded(uint64_t *bar, unsigned ph) {
+    const unsigned b = (unsigned)__cvta_generic_to_shared(bar);
+    for (unsigned it = 0; it < (1u << 30); ++it) {
+        unsigned done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(b), "r"(ph)
+            : "memory");
+        if (done) return;
+    }
 }
 
 // start copying n floats global -> shared with the calling threads (t of nt)
@@ -1039,8 +1069,8 @@ __device__ __forceinline__ void softmax_heavy_ring(const int32_t *__restrict__ r
 // when there is a plan (so blocks that had more heavy work take fewer
 // batches), else by a static stride. Consecutive light rows of a batch own
 // one contiguous run of scores; the warp stages such a run (at most
-// kSpanFloats scores) into its buffer, computes it and writes it back with
-// one bulk copy. W = 4 with Q = H/4 a power of two: rows go to register
+// kSpanFloats scores) into its buffer (one bulk copy with W = 4), computes
+// it and writes it back with one bulk copy. W = 4 with Q = H/4 a power of two: rows go to register
 // tiers (up to 4 or 8 float4s per lane) or, past 8 per lane, to the
 // whole-warp shared-memory routine, and a row beyond the buffer that the
 // plan does not call heavy streams through the warp's buffer twice;
@@ -1058,7 +1088,15 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
     __shared__ int32_t h_e0[kHeavyUnit], h_deg[kHeavyUnit];
     __shared__ int hcount;
     __shared__ int32_t s_unit;
+    __shared__ __align__(8) uint64_t wbar[kSoftmaxThreads / 32];  // light runs' bulk loads
     const int t = threadIdx.x, lane = t & 31;
+    if (W == 4 && lane == 0) {
+        const unsigned b = (unsigned)__cvta_generic_to_shared(&wbar[t >> 5]);
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    unsigned wph = 0;
     const int32_t cap_e = kSpanFloats / H;  // edges per warp buffer
     // light rows the buffer does not hold are the warps' (two passes through
     // the buffer with W = 4 and Q a power of two, else straight from global);
@@ -1104,6 +1142,9 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
             __syncthreads();
         }
         if (W == 4 && t == 0) bulk_wait_read();  // the shared buffer is the warps' again
+        // this thread's generic accesses to the buffer come before the bulk
+        // loads that overwrite it
+        if (W == 4) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
     }
     float *sb = span_smem + (t >> 5) * kSpanFloats;
@@ -1156,8 +1197,17 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
             if (n > 0) {
                 // the buffer's last bulk store has read it
                 if (W == 4 && lane == 0) bulk_wait_read();
+                if (W == 4) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                stage_in<W>(sb, scores + x0, n, lane, 32);
+                if (W == 4) {
+                    // the run is contiguous and 16-byte aligned (H a multiple of
+                    // 4): one bulk copy, on the warp's mbarrier
+                    if (lane == 0) bulk_load(sb, scores + x0, (unsigned)n * 4u, &wbar[t >> 5]);
+                    mbar_wait_bounded(&wbar[t >> 5], wph);
+                    wph ^= 1u;
+                } else {
+                    stage_in<W>(sb, scores + x0, n, lane, 32);
+                }
                 __syncwarp();
                 const unsigned run_mask =
                     (i1 - i0 == 32 ? 0xffffffffu : ((1u << (i1 - i0)) - 1u)) << i0;
