@@ -1105,6 +1105,9 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
     if (n_heavy > 0 && tiers && H <= 32) {
         softmax_heavy_ring(row_ptr, heavy_rows, n_heavy, H, cap_e, scores, out, span_smem, red);
         cp_async_wait_all();
+        // this thread's generic accesses to the buffer come before the bulk
+        // loads that overwrite it
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();  // the buffer is the warps' again
     } else if (n_heavy > 0) {
         // units of kHeavyUnit list entries from the plan's second counter;
