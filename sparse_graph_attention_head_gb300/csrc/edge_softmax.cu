@@ -1166,6 +1166,10 @@ softmax_rows_kernel(const int32_t *__restrict__ row_ptr, int64_t n_rows, int32_t
     while (b < n_batches) {
         // the next batch's index is fetched now and used after this one
         const int64_t b_next = dyn ? fetch() : b + n_warps;
+        if (b_next < n_batches) {  // the next batch's 33 row offsets into L2
+            const int64_t rn = b_next * 32 + lane;
+            if (rn <= n_rows) asm volatile("prefetch.global.L2 [%0];" ::"l"(row_ptr + rn));
+        }
         const int64_t r0 = b * 32;
         const int nb = n_rows - r0 < 32 ? (int)(n_rows - r0) : 32;
         const int32_t e0_lane = row_ptr[r0 + (lane < nb ? lane : nb - 1)];
